@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the Gated DeltaNet recurrence library on GB300.
+
+One step = one gdn_forward call over the decode workload (D_k = D_v = 128,
+n_k_heads = 16, n_v_heads = 32, n_tokens = 1, n_seqs = 64, f32; seeded
+synthetic inputs), updating the state in place.  Prints ONE JSON line.
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs of C-ABI calls, bracketed by a barrier and a device synchronize, timed
+with CUDA events on the launching stream; the maximum over ranks is taken.
+Steps rotate over 4 independent input/state sets, so about 1.1 GB is touched
+between two uses of the same buffer (more than 8x the L2).
+
+Also reported: the end-to-end number through the public API from pinned host
+buffers (copies inside the timed region), the HBM roofline of the kernel, the
+CPU oracle as a baseline, SM clocks sampled during the timed region, and
+quick timings of the other workloads (wide-GQA decode, capture, prefill).
+
+``--impl reference`` times the double-precision CPU oracle on the same
+workload and metric instead (a bounded sample of heads per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode us/call + state HBM GB/s (% of 8 TB/s); prefill tokens/s"
+WORKLOAD_TEXT = ("decode: D_k=D_v=128, n_k_heads=16, n_v_heads=32, n_tokens=1, n_seqs=64, f32, "
+                 "in-place state update")
+N_SETS = 4
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+# ---------------------------------------------------------------- helpers
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, t["source"])
+    try:
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return t["dram_bytes_per_launch"] if h == t["source_sha256"] else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local: int):
+        self.index = self.smi_id(local)
+        self.proc = None
+        self.file = None
+
+    @staticmethod
+    def smi_id(local: int) -> str:
+        """nvidia-smi ignores CUDA_VISIBLE_DEVICES, so name the GPU by UUID."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(local).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(local)
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (each rank's elapsed time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, elapsed_s: float, world: int, device=None):
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    t = max_over_ranks(elapsed_s, world, device)
+    return per_rank_units * world / t, t
+
+
+# ---------------------------------------------------------------- our arm
+
+def make_sets(torch, w, n_sets, device, capture=False):
+    from serving_gdn_decode_gb300.workloads import make_inputs
+    sets = []
+    for i in range(n_sets):
+        x = make_inputs(w, seed=i)
+        d = {k: torch.from_numpy(v).to(device) for k, v in x.items()}
+        d["output"] = torch.empty(w.v_elems, dtype=torch.float32, device=device)
+        d["state"] = d.pop("state_in")  # updated in place
+        if capture:
+            d["capture"] = torch.empty(w.capture_elems, dtype=torch.float32, device=device)
+        sets.append(d)
+    return sets
+
+
+def call(nat, d, params, capture):
+    if capture:
+        nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], d["output"],
+                                d["state"], params, d["capture"])
+    else:
+        nat.gdn_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], d["output"],
+                        d["state"], params)
+
+
+def time_graphed(torch, nat, sets, params, steps, warmup, capture=False, world=1, clocks=None):
+    """Exactly `steps` calls (rotating over `sets`) from CUDA graphs; returns
+    (elapsed seconds on the device, max over ranks)."""
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            call(nat, sets[i % len(sets)], params, capture)
+    torch.cuda.synchronize()
+    chunk = max(1, min(steps, 64 * len(sets)))
+    graphs = []
+
+    def graph_of(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                call(nat, sets[i % len(sets)], params, capture)
+        return g
+
+    full, rest = divmod(steps, chunk)
+    g_full = graph_of(chunk) if full else None
+    g_rest = graph_of(rest) if rest else None
+    if g_full is not None:
+        graphs += [g_full] * full
+    if g_rest is not None:
+        graphs.append(g_rest)
+    # one untimed replay of each graph (first replay uploads the graph)
+    with torch.cuda.stream(stream):
+        for g in {id(x): x for x in graphs}.values():
+            g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for g in graphs:
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks is not None else None
+    return start.elapsed_time(end) / 1e3, clk
+
+
+def time_e2e(torch, nat, w, params, steps, device):
+    """End to end through the public API: every step copies its inputs from
+    pinned host memory, calls gdn_forward, and reads output and state back."""
+    from serving_gdn_decode_gb300.workloads import make_inputs
+    x = make_inputs(w, seed=100)
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_d = torch.empty(w.v_elems, dtype=torch.float32, device=device)
+    st_d = torch.empty(w.state_elems, dtype=torch.float32, device=device)
+    out_h = torch.empty(w.v_elems, dtype=torch.float32).pin_memory()
+    st_h = torch.empty(w.state_elems, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+
+    def step():
+        for k in ("q", "k", "v", "g", "beta", "state_in"):
+            dev[k].copy_(host[k], non_blocking=True)
+        nat.gdn_forward(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["state_in"], out_d,
+                        st_d, params)
+        out_h.copy_(out_d, non_blocking=True)
+        st_h.copy_(st_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * 4 + st_h.numel() * 4
+    return start.elapsed_time(end) / 1e3 / steps, h2d, d2h
+
+
+def extras(torch, nat, peak_gbs, device):
+    from serving_gdn_decode_gb300.params import PATH_SCAN
+    from serving_gdn_decode_gb300.workloads import WORKLOADS
+    res = {}
+
+    def hbm_case(key, w, params, capture, n_sets, steps):
+        sets = make_sets(torch, w, n_sets, device, capture)
+        t, _ = time_graphed(torch, nat, sets, params, steps, 5, capture)
+        us = t / steps * 1e6
+        gbs = w.algorithmic_bytes() / (t / steps) / 1e9
+        res[key] = {"path": nat.gdn_path_name(params, capture), "us_per_call": round(us, 2),
+                    "GB_s": round(gbs, 1), "hbm_frac": round(gbs / peak_gbs, 3)}
+        del sets
+        torch.cuda.empty_cache()
+
+    wg = WORKLOADS["decode_wide_gqa"]
+    hbm_case("decode_wide_gqa_mod", wg, wg.params(), False, 3, 60)
+    hbm_case("decode_wide_gqa_div", wg, wg.params(khead_div=True), False, 3, 60)
+    wc = WORKLOADS["spec_capture"]
+    hbm_case("spec_capture_s32", wc, wc.params(), True, 4, 200)
+    wc64 = wc.with_(n_seqs=64)
+    hbm_case("spec_capture_s64", wc64, wc64.params(), True, 3, 120)
+
+    wp = WORKLOADS["long_prefill"]
+    for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),):
+        sets = make_sets(torch, wp, 1, device)
+        steps = 5
+        t, _ = time_graphed(torch, nat, sets, params, steps, 2)
+        s = t / steps
+        res[key] = {"path": nat.gdn_path_name(params), "ms_per_call": round(s * 1e3, 3),
+                    "tokens_per_s": round(wp.n_tokens * wp.n_seqs / s, 1),
+                    "head_tokens_per_s": round(wp.n_tokens * wp.n_seqs * wp.n_v_heads / s, 1),
+                    "fp32_tflops": round(wp.flops() / s / 1e12, 2)}
+        del sets
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(w, budget_s=2.0):
+    """The oracle as it stands, on all host cores, over whole decode calls."""
+    import oracle
+    from serving_gdn_decode_gb300.workloads import make_inputs
+    x = make_inputs(w, seed=0)
+    p = w.params()
+    cores = oracle.default_threads()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(p, **x, n_threads=cores)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per = el / n
+    return {"value": round(w.algorithmic_bytes() / per / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} whole decode call(s) of the oracle (all {w.heads} heads), "
+                      f"{per * 1e3:.1f} ms each"}
+
+
+def run_ours(args):
+    import torch
+
+    from serving_gdn_decode_gb300 import _native as nat
+    from serving_gdn_decode_gb300 import build as native_build
+    from serving_gdn_decode_gb300.workloads import WORKLOADS
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    native_build.build()
+    nat.lib()
+    peaks, peak_kind = load_peaks()
+    peak_gbs = float(peaks["hbm_gbs"])
+
+    w = WORKLOADS["decode"]
+    params = w.params()
+    kernel = nat.gdn_path_name(params)
+    sets = make_sets(torch, w, N_SETS, device)
+    clocks = ClockSampler(local)
+    elapsed, clk = time_graphed(torch, nat, sets, params, args.steps, args.warmup, world=world,
+                                clocks=clocks)
+    bytes_per_call = w.algorithmic_bytes()
+    value_bps, t_max = aggregate(bytes_per_call * args.steps, elapsed, world, device)
+    per_call_s = elapsed / args.steps
+    achieved = bytes_per_call / per_call_s / 1e9
+    del sets
+    torch.cuda.empty_cache()
+
+    e2e_s, h2d, d2h = time_e2e(torch, nat, w, params, min(args.steps, 30), device)
+    e2e_val, _ = aggregate(bytes_per_call, e2e_s, world, device)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value_bps / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 5),
+        "us_per_call": round(per_call_s * 1e6, 2),
+        "hbm_frac_of_8TBs": round(achieved / 8000.0, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded: q,k ~N(0,1) L2-normalised, v ~N(0,1), g ~U[0,0.5), "
+                "beta ~U[0,1), state ~N(0,0.1))",
+        "config": {"workload": WORKLOAD_TEXT, "kernel": kernel,
+                   "l2": f"{N_SETS} rotating input/state sets, "
+                         f"{N_SETS * bytes_per_call / 1e9:.2f} GB touched between reuses",
+                   "timing": "CUDA graphs of C-ABI calls, CUDA events on the launching stream",
+                   "parallelism": f"replicas: each of {world} rank(s) runs the whole workload"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs,
+                     "unit": "GB/s", "frac": round(achieved / peak_gbs, 3),
+                     "peak_kind": f"of {peak_kind} ({'hbm_gbs, MEASURED_PEAKS.json' if peak_kind == 'measured' else 'recipe fallback'})",
+                     "bytes_per_launch": bytes_per_call,
+                     "traffic": kernel_traffic(kernel)},
+        "e2e": {"value": round(e2e_val / 1e9, 2), "unit": "GB/s",
+                "us_per_call": round(e2e_s * 1e6, 1), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "pinned host -> device copies of all inputs, gdn_forward, device -> "
+                       "pinned host copies of output and state, per step"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if not args.no_extras and rank == 0:
+        line["other_workloads"] = extras(torch, nat, peak_gbs, device)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from serving_gdn_decode_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS["decode"]
+    x = make_inputs(w, seed=0)
+    p = w.params()
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.forward_heads(p, **x, heads=np.arange(w.heads, dtype=np.uint32), n_threads=cores)
+    t_full = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    n_heads = int(max(1, min(w.heads, w.heads * budget / max(t_full, 1e-6))))
+    heads = [np.arange(i * n_heads, (i + 1) * n_heads) % w.heads for i in range(4)]
+    for i in range(args.warmup):
+        oracle.forward_heads(p, **x, heads=heads[i % 4], n_threads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.forward_heads(p, **x, heads=heads[i % 4], n_threads=cores)
+    el = time.perf_counter() - t0
+    bytes_per_step = w.algorithmic_bytes() * n_heads / w.heads
+    value = bytes_per_step * args.steps / el / 1e9
+    sample = (f"{n_heads} of {w.heads} (seq, value-head) pairs of the decode workload per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT, "kernel": "CPU oracle (double precision)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

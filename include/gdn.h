@@ -1,0 +1,153 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet recurrence library
+ *          (libgdn_gb300.so).
+ *
+ * The operation.  For every sequence s and value head vh, with the D_v x D_k
+ * f32 state S of that pair (row i = d_v index, column j = d_k index) and for
+ * tokens t = 0 .. n_tokens-1 in order:
+ *
+ *     alpha    = exp(-g_t)
+ *     S        = alpha * S                       (decay-first, flags bit0 = 0)
+ *     sk[i]    = sum_j S[i][j] * k_t[j]
+ *     delta[i] = (v_t[i] - sk[i]) * beta_t
+ *     S[i][j] += delta[i] * k_t[j]
+ *     y_t[i]   = q_scale * sum_j S[i][j] * q_t[j]
+ *
+ * This is the step order of the kernel body of
+ * "gated_delta_net_decode_capture.metal" (mlx-native 0.9.2), steps
+ * "decay + partial s_k" and "state update + output partial".  With flags
+ * bit0 = 1 the state is decayed after S@k instead, as in the recurrence of
+ * the module doc of "gated_delta_net.rs" (mlx-native 0.4.0):
+ * S' = alpha*S + beta*outer(v - S@k, k), y = S'@q.
+ *
+ * k_head, the key/query head read by value head vh ("GQA broadcast",
+ * gated_delta_net.rs): vh % n_k_heads (flags bit1 = 0, the capture kernel's
+ * head setup) or vh / (n_v_heads / n_k_heads) (flags bit1 = 1).
+ *
+ * Layouts, innermost (fastest) dimension first, all f32, densely packed
+ * ("Memory layouts" table of gated_delta_net.rs; "Memory layout for
+ * state_capture" section of the capture kernel page):
+ *     q, k            [D_k, n_k_heads, n_tokens, n_seqs]
+ *     v, output       [D_v, n_v_heads, n_tokens, n_seqs]
+ *     g, beta         [n_v_heads, n_tokens, n_seqs]
+ *     state_in/out    [D_k, D_v, n_v_heads, n_seqs]
+ *     state_capture   [D_k, D_v, n_v_heads, n_tokens, n_seqs]
+ *
+ * Parameters: a HOST array of at least 9 uint32 ("Buffer bindings" section of
+ * the capture kernel page; "Buffer / params contract" of
+ * gated_delta_net_decode.rs, mlx-native 0.21.1):
+ *     params[0..5] = D_k, D_v, n_k_heads, n_v_heads, n_tokens, n_seqs
+ *     params[6]    = flags (the pages always write 0 here; see GDN_FLAG_*)
+ *     params[7]    = reserved, must be 0
+ *     params[8]    = q_scale_bits: the f32 bit pattern of q_scale, applied to
+ *                    y at writeback; 0 means q_scale = 1.0.
+ *
+ * Ownership and lifetime.  Every buffer pointer is a DEVICE pointer owned by
+ * the caller; the library allocates no memory, keeps no state between calls
+ * and never synchronises.  All work is enqueued on `stream` (NULL = the
+ * legacy default stream) and is asynchronous: buffers must stay valid until
+ * the stream reaches the call.  Calls on different streams with disjoint
+ * buffers may run concurrently.
+ *
+ * Errors.  Arguments are checked on the host before anything is enqueued; a
+ * failed check returns GDN_ERR_INVALID_ARGUMENT or GDN_ERR_UNSUPPORTED and
+ * enqueues nothing.  A failed launch returns GDN_ERR_CUDA.  Faults during
+ * kernel execution surface through the stream like any CUDA error.  After a
+ * non-OK status, gdn_last_error() gives a message (per calling thread).
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as CUDA's cudaStream_t / CUstream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARGUMENT = 1, /* the pages' InvalidArgument cases, and ours */
+  GDN_ERR_UNSUPPORTED = 2,      /* valid for the method, no kernel for it here */
+  GDN_ERR_CUDA = 3              /* a CUDA runtime call failed */
+} gdn_status;
+
+#define GDN_N_PARAMS 9
+
+/* params[6] flag bits.  0 selects the behaviour of the pages' kernel. */
+#define GDN_FLAG_DECAY_AFTER 0x1u /* decay after S@k (gated_delta_net.rs)  */
+#define GDN_FLAG_KHEAD_DIV 0x2u   /* k_head = vh / (n_v/n_k)               */
+#define GDN_PATH_SHIFT 2u         /* bits 2-3: path choice                 */
+#define GDN_PATH_MASK 0xCu
+#define GDN_PATH_AUTO 0u          /* the library picks by shape            */
+#define GDN_PATH_SCAN 1u          /* token-by-token scan kernel            */
+#define GDN_PATH_CHUNKED 2u       /* chunked tensor-core prefill           */
+
+/*
+ * gdn_forward -- run the recurrence over n_tokens tokens for every
+ * (seq, value head) pair, write y to `output` and the final state to
+ * `state_out`.  Follows dispatch_gated_delta_net_decode
+ * (gated_delta_net_decode.rs, mlx-native 0.21.1) and dispatch_gated_delta_net
+ * (gated_delta_net.rs, mlx-native 0.4.0); buffer order is the pages' buffer
+ * slots 0-8.
+ *
+ * Checks (mirroring `validate` and `validate_params_buf` of
+ * gated_delta_net_decode.rs):
+ *   INVALID_ARGUMENT: params == NULL or n_params < 9; any of D_k, D_v,
+ *     n_k_heads, n_v_heads, n_tokens, n_seqs == 0; n_v_heads % n_k_heads != 0;
+ *     D_k % 32 != 0 or D_k > 128; D_v % (D_k/32) != 0; params[7] != 0;
+ *     unknown flag bits or path 3; a NULL buffer; q, k, state_in or state_out
+ *     not 16-byte aligned, or v, g, beta, output not 4-byte aligned;
+ *     state_in and state_out overlapping without being the same pointer
+ *     (state_in == state_out, an in-place update, is allowed); output
+ *     overlapping any other buffer.
+ *   UNSUPPORTED: D_k = 96 (D_k/32 = 3 has no kernel, as on the pages);
+ *     the chunked path forced for a shape it does not cover.
+ * Buffer sizes cannot be checked through raw pointers: each buffer must hold
+ * the element count its layout above gives.
+ */
+gdn_status gdn_forward(const float *q, const float *k, const float *v, const float *g,
+                       const float *beta, const float *state_in, float *output,
+                       float *state_out, const uint32_t *params, size_t n_params,
+                       gdn_stream_t stream);
+
+/*
+ * gdn_forward_capture -- gdn_forward, plus the state after every token
+ * written to `state_capture` (slot 9 of the capture kernel page):
+ * state_capture[:, :, vh, t, s] = S after token t.  Slice n_tokens-1 is
+ * bit-identical to state_out (the "Determinism contract" of
+ * dispatch_gated_delta_net_decode_with_capture).  For speculative-decode
+ * rollback the caller takes slice `accepted_idx` as the new state.
+ *
+ * Extra checks (dispatch_gated_delta_net_decode_with_capture):
+ *   INVALID_ARGUMENT: state_capture == NULL or not 16-byte aligned, or
+ *     overlapping any other buffer; state_capture_elems !=
+ *     n_tokens*D_k*D_v*n_v_heads*n_seqs when n_seqs > 1, or smaller than it
+ *     when n_seqs == 1 (elements past that count are left untouched).
+ *   UNSUPPORTED: the chunked path forced (it keeps no per-token state).
+ */
+gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, const float *g,
+                               const float *beta, const float *state_in, float *output,
+                               float *state_out, const uint32_t *params, size_t n_params,
+                               float *state_capture, size_t state_capture_elems,
+                               gdn_stream_t stream);
+
+/* Message for the last non-OK status returned on the calling thread ("" if
+ * none).  The pointer stays valid until the thread's next call. */
+const char *gdn_last_error(void);
+
+/* The kernel path the library would run for `params` (with or without
+ * capture): on GDN_OK, *name points to a static string such as
+ * "token_loop_decode".  Runs the same params checks as gdn_forward and returns
+ * the same status for invalid params.  Host-only: enqueues nothing. */
+gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
+                         const char **name);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

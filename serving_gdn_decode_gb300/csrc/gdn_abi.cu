@@ -1,0 +1,250 @@
+// C-ABI entry points of libgdn_gb300.so: argument checks, path choice and
+// dispatch.  The checks mirror `validate`, `validate_params_buf` and the
+// capture-size rule of gated_delta_net_decode.rs (mlx-native 0.21.1); the
+// alias and alignment rules are this library's own (the pages are silent).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+gdn_status fail(gdn_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+// Largest n_tokens that runs on the decode launch shape under GDN_PATH_AUTO.
+constexpr uint32_t kDecodeMaxTokens = 16;
+// Upper bound on any buffer's element count (keeps byte counts far from
+// 64-bit overflow).
+constexpr unsigned long long kMaxElems = 1ull << 60;
+
+bool mul_ok(unsigned long long a, unsigned long long b, unsigned long long *out) {
+  const unsigned __int128 r = static_cast<unsigned __int128>(a) * b;
+  if (r > kMaxElems) return false;
+  *out = static_cast<unsigned long long>(r);
+  return true;
+}
+
+struct Span {
+  const void *p;
+  unsigned long long bytes;
+  const char *name;
+};
+
+bool overlap(const Span &a, const Span &b) {
+  const auto a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+struct Decoded {
+  gdn::Problem prob;
+  unsigned long long qk_elems, v_elems, sc_elems, state_elems, capture_elems;
+  uint32_t path;
+};
+
+// Params block checks (no buffers).
+gdn_status decode_params(const uint32_t *params, size_t n_params, Decoded *d) {
+  if (params == nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: params is NULL");
+  if (n_params < GDN_N_PARAMS)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: params has %zu u32, expected >= 9 (index 8 = q_scale_bits)", n_params);
+  gdn::Problem &p = d->prob;
+  std::memset(&p, 0, sizeof p);
+  p.dk = params[0]; p.dv = params[1]; p.nk = params[2]; p.nv = params[3];
+  p.nt = params[4]; p.ns = params[5];
+  const uint32_t flags = params[6];
+  if (p.dk == 0 || p.dv == 0 || p.nk == 0 || p.nv == 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: dims must all be > 0");
+  if (p.nt == 0 || p.ns == 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: n_tokens and n_seqs must be > 0");
+  if (p.nv % p.nk != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: n_v_heads (%u) must be a multiple of n_k_heads (%u)", p.nv, p.nk);
+  if (p.dk % 32 != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: D_k (%u) must be a multiple of 32", p.dk);
+  if (p.dk > 128)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: D_k (%u) must be <= 128 (D_k/32 <= 4)", p.dk);
+  if (p.dk == 96)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn: D_k = 96 (D_k/32 = 3) has no kernel; use 32, 64 or 128");
+  const uint32_t nsg = p.dk / 32;
+  if (p.dv % nsg != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: D_v (%u) must be a multiple of D_k/32 (%u)", p.dv,
+                nsg);
+  if (params[7] != 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: params[7] is reserved and must be 0 (got %u)",
+                params[7]);
+  if (flags & ~(GDN_FLAG_DECAY_AFTER | GDN_FLAG_KHEAD_DIV | GDN_PATH_MASK))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: unknown flag bits 0x%x in params[6]", flags);
+  d->path = (flags & GDN_PATH_MASK) >> GDN_PATH_SHIFT;
+  if (d->path > GDN_PATH_CHUNKED)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: path %u in params[6] does not exist", d->path);
+  p.decay_after = (flags & GDN_FLAG_DECAY_AFTER) != 0;
+  p.khead_div = (flags & GDN_FLAG_KHEAD_DIV) != 0;
+  if (params[8] == 0) {
+    p.q_scale = 1.0f;
+  } else {
+    std::memcpy(&p.q_scale, &params[8], sizeof(float));
+  }
+  unsigned long long x;
+  if (!mul_ok(p.dk, p.nk, &x) || !mul_ok(x, p.nt, &x) || !mul_ok(x, p.ns, &d->qk_elems) ||
+      !mul_ok(p.dv, p.nv, &x) || !mul_ok(x, p.nt, &x) || !mul_ok(x, p.ns, &d->v_elems) ||
+      !mul_ok(p.nv, p.nt, &x) || !mul_ok(x, p.ns, &d->sc_elems) ||
+      !mul_ok(p.dk, p.dv, &x) || !mul_ok(x, p.nv, &x) || !mul_ok(x, p.ns, &d->state_elems) ||
+      !mul_ok(d->state_elems, p.nt, &d->capture_elems))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: buffer sizes overflow");
+  return GDN_OK;
+}
+
+enum class Path { kDecode, kScan };
+
+gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
+  switch (d.path) {
+    case GDN_PATH_SCAN:
+      *out = Path::kScan;
+      return GDN_OK;
+    case GDN_PATH_CHUNKED:
+      if (capture)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path keeps no per-token state (capture)");
+      return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked prefill path is not available");
+    default:
+      *out = d.prob.nt <= kDecodeMaxTokens ? Path::kDecode : Path::kScan;
+      return GDN_OK;
+  }
+}
+
+gdn_status check_buffers(const Decoded &d, const float *q, const float *k, const float *v,
+                         const float *g, const float *beta, const float *state_in, float *output,
+                         float *state_out, float *capture, size_t capture_elems, bool with_capture) {
+  const Span in[] = {{q, d.qk_elems * 4, "q"},       {k, d.qk_elems * 4, "k"},
+                     {v, d.v_elems * 4, "v"},        {g, d.sc_elems * 4, "g"},
+                     {beta, d.sc_elems * 4, "beta"}, {state_in, d.state_elems * 4, "state_in"}};
+  for (const Span &s : in)
+    if (s.p == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s is NULL", s.name);
+  if (output == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output is NULL");
+  if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out is NULL");
+  if (with_capture && capture == nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture is NULL");
+
+  const struct { const void *p; uintptr_t a; const char *name; } al[] = {
+      {q, 16, "q"}, {k, 16, "k"}, {state_in, 16, "state_in"}, {state_out, 16, "state_out"},
+      {v, 4, "v"}, {g, 4, "g"}, {beta, 4, "beta"}, {output, 4, "output"}};
+  for (const auto &x : al)
+    if (!aligned(x.p, x.a))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s must be %u-byte aligned", x.name,
+                  static_cast<unsigned>(x.a));
+  if (with_capture && !aligned(capture, 16))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture must be 16-byte aligned");
+
+  if (with_capture) {
+    if (d.prob.ns > 1 && capture_elems != d.capture_elems)
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "gdn: state_capture element count %zu != required %llu (n_tokens x state "
+                  "elements); equality is required when n_seqs > 1",
+                  capture_elems, d.capture_elems);
+    if (d.prob.ns == 1 && capture_elems < d.capture_elems)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture element count %zu < required %llu",
+                  capture_elems, d.capture_elems);
+  }
+
+  const Span st_out{state_out, d.state_elems * 4, "state_out"};
+  if (state_out != state_in && overlap(st_out, in[5]))
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: state_in and state_out overlap without being the same buffer");
+  const Span out{output, d.v_elems * 4, "output"};
+  for (const Span &s : in)
+    if (overlap(out, s)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps %s", s.name);
+  if (overlap(out, st_out)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps state_out");
+  for (int i = 0; i < 5; ++i)
+    if (overlap(st_out, in[i]))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out overlaps %s", in[i].name);
+  if (with_capture) {
+    const Span cap{capture, d.capture_elems * 4, "state_capture"};
+    for (const Span &s : in)
+      if (overlap(cap, s))
+        return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture overlaps %s", s.name);
+    if (overlap(cap, out) || overlap(cap, st_out))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture overlaps an output buffer");
+  }
+  return GDN_OK;
+}
+
+gdn_status run(const float *q, const float *k, const float *v, const float *g, const float *beta,
+               const float *state_in, float *output, float *state_out, const uint32_t *params,
+               size_t n_params, float *capture, size_t capture_elems, bool with_capture,
+               gdn_stream_t stream) {
+  g_last_error[0] = '\0';
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  st = check_buffers(d, q, k, v, g, beta, state_in, output, state_out, capture, capture_elems,
+                     with_capture);
+  if (st != GDN_OK) return st;
+  Path path;
+  st = choose_path(d, with_capture, &path);
+  if (st != GDN_OK) return st;
+
+  gdn::Problem &p = d.prob;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_in = state_in;
+  p.output = output; p.state_out = state_out; p.capture = with_capture ? capture : nullptr;
+  const cudaError_t err = gdn::launch_token_loop(
+      p, path == Path::kDecode ? gdn::LoopGeometry::kDecode : gdn::LoopGeometry::kScan,
+      reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_forward(const float *q, const float *k, const float *v, const float *g,
+                       const float *beta, const float *state_in, float *output, float *state_out,
+                       const uint32_t *params, size_t n_params, gdn_stream_t stream) {
+  return run(q, k, v, g, beta, state_in, output, state_out, params, n_params, nullptr, 0, false,
+             stream);
+}
+
+gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, const float *g,
+                               const float *beta, const float *state_in, float *output,
+                               float *state_out, const uint32_t *params, size_t n_params,
+                               float *state_capture, size_t state_capture_elems,
+                               gdn_stream_t stream) {
+  return run(q, k, v, g, beta, state_in, output, state_out, params, n_params, state_capture,
+             state_capture_elems, true, stream);
+}
+
+const char *gdn_last_error(void) { return g_last_error; }
+
+gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
+                         const char **name) {
+  g_last_error[0] = '\0';
+  if (name == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: name is NULL");
+  *name = nullptr;
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  Path path;
+  st = choose_path(d, capture != 0, &path);
+  if (st != GDN_OK) return st;
+  *name = gdn::token_loop_name(
+      path == Path::kDecode ? gdn::LoopGeometry::kDecode : gdn::LoopGeometry::kScan,
+      capture != 0);
+  return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,360 @@
+// Token-loop kernels for the Gated DeltaNet recurrence on sm_103a: decode,
+// multi-token windows with per-token state capture, and the sequential-scan
+// prefill.
+//
+// Work decomposition.  The D_v rows of a (seq, value head) state are
+// independent (each row i only meets v_t[i] and the shared k_t, q_t), so a
+// warp owns R consecutive rows and a CTA owns WARPS*R rows of one pair.
+// Lane l keeps the D_k/32 contiguous f32 cells [l*NSG, l*NSG+NSG) of each of
+// its R rows in registers for the whole token range (NSG = D_k/32), as the
+// capture kernel of "gated_delta_net_decode_capture.metal" (mlx-native 0.9.2)
+// keeps NSG cells per lane; state therefore crosses HBM once in and once out
+// per call whatever n_tokens is ("Threading" section of gated_delta_net.rs,
+// mlx-native 0.4.0).  Loads and stores of state are coalesced 128-bit
+// (D_k = 128) streaming accesses.
+//
+// Per token (decay-first; the kernel body's steps "decay + partial s_k" and
+// "state update + output partial"):
+//     S *= alpha;  sk = S@k;  delta = (v - sk)*beta;  S += delta k^T;  y = S@q
+// The two row reductions (S@k, S@q) are warp reductions over the 32 lanes.
+// Reducing R rows at once uses a transpose-reduce: at each of log2(R)
+// butterfly stages a lane keeps half of its remaining row partials and
+// trades the other half with its partner, so R rows cost R-1+5-log2(R)
+// shuffles instead of 5R; lane l ends with the total of row l/(32/R).
+//
+// k_t, q_t (shared by every row of the CTA), v_t for the CTA's rows, g_t and
+// beta_t are staged into shared memory with cp.async, in chunks of `tc`
+// tokens, double-buffered so the next chunk loads while this one computes.
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct LoopArgs {
+  const float *__restrict__ q;
+  const float *__restrict__ k;
+  const float *__restrict__ v;
+  const float *__restrict__ g;
+  const float *__restrict__ beta;
+  const float *state_in;  // may be the same buffer as state_out
+  float *__restrict__ output;
+  float *state_out;
+  float *__restrict__ capture;
+  uint32_t dv, nk, nv, nt, group, khead_div;
+  float q_scale;
+  uint32_t row_blocks;  // CTAs per (seq, value head) pair
+  uint32_t tc;          // tokens per staged chunk
+};
+
+// ---- small PTX helpers (cp.async into shared memory)
+
+__device__ __forceinline__ void cp_async_16(float *smem, const float *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(float *smem, const float *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---- NSG contiguous floats per lane: streaming global and plain shared I/O
+
+template <int NSG>
+struct Cells;
+template <>
+struct Cells<4> {
+  static __device__ __forceinline__ void load_cs(const float *p, float (&c)[4]) {
+    const float4 x = __ldcs(reinterpret_cast<const float4 *>(p));
+    c[0] = x.x; c[1] = x.y; c[2] = x.z; c[3] = x.w;
+  }
+  static __device__ __forceinline__ void store_cs(float *p, const float (&c)[4]) {
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(c[0], c[1], c[2], c[3]));
+  }
+  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[4]) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    c[0] = x.x; c[1] = x.y; c[2] = x.z; c[3] = x.w;
+  }
+};
+template <>
+struct Cells<2> {
+  static __device__ __forceinline__ void load_cs(const float *p, float (&c)[2]) {
+    const float2 x = __ldcs(reinterpret_cast<const float2 *>(p));
+    c[0] = x.x; c[1] = x.y;
+  }
+  static __device__ __forceinline__ void store_cs(float *p, const float (&c)[2]) {
+    __stcs(reinterpret_cast<float2 *>(p), make_float2(c[0], c[1]));
+  }
+  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[2]) {
+    const float2 x = *reinterpret_cast<const float2 *>(p);
+    c[0] = x.x; c[1] = x.y;
+  }
+};
+template <>
+struct Cells<1> {
+  static __device__ __forceinline__ void load_cs(const float *p, float (&c)[1]) { c[0] = __ldcs(p); }
+  static __device__ __forceinline__ void store_cs(float *p, const float (&c)[1]) { __stcs(p, c[0]); }
+  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[1]) { c[0] = *p; }
+};
+
+// Transpose-reduce R per-lane partials over the warp.  Returns, in every
+// lane l, the warp-wide total of row l / (32/R).
+template <int R>
+__device__ __forceinline__ float reduce_rows(float (&a)[R], int lane) {
+#pragma unroll
+  for (int m = R, o = 16; m > 1; m >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < m / 2; ++i) {
+      const float send = upper ? a[i] : a[i + m / 2];
+      const float keep = upper ? a[i + m / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+  }
+  float x = a[0];
+#pragma unroll
+  for (int o = 16 / R; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+template <int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER>
+__global__ void __launch_bounds__(WARPS * 32)
+    gdn_token_loop_kernel(const LoopArgs a) {
+  constexpr int DK = 32 * NSG;
+  constexpr int ROWS = WARPS * R;  // rows per CTA
+  constexpr int LPR = 32 / R;      // lanes that end up holding one row's total
+  static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+
+  extern __shared__ __align__(16) float smem[];
+  const int tc = static_cast<int>(a.tc);
+  // One staging buffer: k[tc][DK] q[tc][DK] v[tc][ROWS] g[tc] beta[tc],
+  // padded to a multiple of 4 floats so both buffers start 16-byte aligned.
+  const int buf_floats = (tc * (2 * DK + ROWS + 2) + 3) & ~3;
+
+  const uint32_t rb = blockIdx.x % a.row_blocks;
+  const uint32_t head = blockIdx.x / a.row_blocks;  // = s * nv + vh
+  const uint32_t vh = head % a.nv;
+  const uint32_t s = head / a.nv;
+  const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const uint32_t row_cta0 = rb * ROWS;
+  const uint32_t row0 = row_cta0 + static_cast<uint32_t>(warp * R);
+  const uint32_t nt = a.nt;
+
+  // 1. Issue the state loads first: they are the bulk of the HBM traffic.
+  const size_t state_head = static_cast<size_t>(head) * a.dv * DK;
+  float st[R][NSG];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (row0 + r < a.dv) {
+      Cells<NSG>::load_cs(a.state_in + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
+                          st[r]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NSG; ++j) st[r][j] = 0.f;
+    }
+  }
+
+  // 2. Staging of per-token inputs.
+  const size_t kq_tok = static_cast<size_t>(a.nk) * DK;
+  const size_t kq_first = (static_cast<size_t>(s) * nt * a.nk + kh) * DK;
+  const size_t v_tok = static_cast<size_t>(a.nv) * a.dv;
+  const size_t v_first = (static_cast<size_t>(s) * nt * a.nv + vh) * a.dv + row_cta0;
+  const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;  // token stride nv
+
+  auto stage = [&](uint32_t chunk, int buf) {
+    float *ks = smem + buf * buf_floats;
+    float *qs = ks + tc * DK;
+    float *vs = qs + tc * DK;
+    float *gs = vs + tc * ROWS;
+    float *bs = gs + tc;
+    const uint32_t t0 = chunk * static_cast<uint32_t>(tc);
+    const int n = static_cast<int>(min(static_cast<uint32_t>(tc), nt - t0));
+    for (int i = threadIdx.x; i < n * (DK / 4); i += WARPS * 32) {
+      const int t = i / (DK / 4), e = 4 * (i % (DK / 4));
+      const size_t src = kq_first + (t0 + t) * kq_tok + e;
+      cp_async_16(ks + t * DK + e, a.k + src);
+      cp_async_16(qs + t * DK + e, a.q + src);
+    }
+    for (int i = threadIdx.x; i < n * ROWS; i += WARPS * 32) {
+      const int t = i / ROWS, r = i % ROWS;
+      if (row_cta0 + r < a.dv)
+        cp_async_4(vs + t * ROWS + r, a.v + v_first + (t0 + t) * v_tok + r);
+      else
+        vs[t * ROWS + r] = 0.f;
+    }
+    for (int i = threadIdx.x; i < n; i += WARPS * 32) {
+      const size_t src = sc_first + static_cast<size_t>(t0 + i) * a.nv;
+      cp_async_4(gs + i, a.g + src);
+      cp_async_4(bs + i, a.beta + src);
+    }
+    cp_async_commit();
+  };
+
+  const uint32_t nchunks = (nt + tc - 1) / tc;
+  const int my_r = lane / LPR;  // the row whose totals this lane ends up holding
+  const uint32_t my_row = row0 + my_r;
+
+  stage(0, 0);
+  for (uint32_t c = 0; c < nchunks; ++c) {
+    if (c + 1 < nchunks) {
+      stage(c + 1, (c + 1) & 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+
+    const float *ks = smem + (c & 1) * buf_floats;
+    const float *qs = ks + tc * DK;
+    const float *vs = qs + tc * DK;
+    const float *gs = vs + tc * ROWS;
+    const float *bs = gs + tc;
+    const int n = static_cast<int>(min(static_cast<uint32_t>(tc), nt - c * tc));
+
+    for (int tt = 0; tt < n; ++tt) {
+      const uint32_t t = c * tc + tt;
+      float kk[NSG], qq[NSG];
+      Cells<NSG>::load_smem(ks + tt * DK + lane * NSG, kk);
+      Cells<NSG>::load_smem(qs + tt * DK + lane * NSG, qq);
+      const float alpha = expf(-gs[tt]);
+      const float b = bs[tt];
+
+      // S@k (on the decayed state for decay-first, the old one for decay-after)
+      float part[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        part[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NSG; ++j) {
+          if (!DECAY_AFTER) st[r][j] *= alpha;
+          part[r] = fmaf(st[r][j], kk[j], part[r]);
+        }
+      }
+      const float sk = reduce_rows<R>(part, lane);
+      const float d = (vs[tt * ROWS + warp * R + my_r] - sk) * b;
+
+      // rank-1 update and S@q
+      float py[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float dr = __shfl_sync(kFull, d, r * LPR);
+        py[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NSG; ++j) {
+          if (DECAY_AFTER)
+            st[r][j] = fmaf(alpha, st[r][j], dr * kk[j]);
+          else
+            st[r][j] = fmaf(dr, kk[j], st[r][j]);
+          py[r] = fmaf(st[r][j], qq[j], py[r]);
+        }
+      }
+      const float y = reduce_rows<R>(py, lane);
+      const size_t tok_head = (static_cast<size_t>(s) * nt + t) * a.nv + vh;
+      if ((lane % LPR) == 0 && my_row < a.dv) a.output[tok_head * a.dv + my_row] = y * a.q_scale;
+
+      if (CAPTURE) {
+        float *cap = a.capture + tok_head * a.dv * DK;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (row0 + r < a.dv)
+            Cells<NSG>::store_cs(cap + static_cast<size_t>(row0 + r) * DK + lane * NSG, st[r]);
+      }
+    }
+    __syncthreads();  // this buffer is refilled by the stage() of chunk c+2
+  }
+
+  // 3. Final state, from the same registers as the last capture slice.
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (row0 + r < a.dv)
+      Cells<NSG>::store_cs(a.state_out + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
+                           st[r]);
+}
+
+// ---- launch shapes
+
+struct Shape {
+  int r, warps, tc_max;
+};
+
+// Decode: several rows per warp so each SM keeps tens of KB of state loads
+// in flight.  Scan: fewer rows per CTA so the ~D_v*n_v*S row chains spread
+// over all SMs.
+template <int NSG>
+constexpr Shape shape_for(LoopGeometry geo) {
+  return geo == LoopGeometry::kDecode ? Shape{16 / NSG, 8, 8} : Shape{16 / NSG, 4, 16};
+}
+
+template <int NSG, int R, int WARPS, bool CAPTURE, bool DA>
+cudaError_t launch_one(const Problem &p, int tc_max, cudaStream_t stream) {
+  constexpr int ROWS = WARPS * R;
+  constexpr int DK = 32 * NSG;
+  LoopArgs a;
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
+  a.state_in = p.state_in; a.output = p.output; a.state_out = p.state_out; a.capture = p.capture;
+  a.dv = p.dv; a.nk = p.nk; a.nv = p.nv; a.nt = p.nt;
+  a.group = p.nv / p.nk;
+  a.khead_div = p.khead_div ? 1u : 0u;
+  a.q_scale = p.q_scale;
+  a.row_blocks = (p.dv + ROWS - 1) / ROWS;
+  a.tc = static_cast<uint32_t>(p.nt < static_cast<uint32_t>(tc_max) ? p.nt : tc_max);
+  const unsigned long long blocks =
+      static_cast<unsigned long long>(a.row_blocks) * p.nv * static_cast<unsigned long long>(p.ns);
+  if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  const int buf_floats = (static_cast<int>(a.tc) * (2 * DK + ROWS + 2) + 3) & ~3;
+  const size_t smem = 2u * static_cast<size_t>(buf_floats) * sizeof(float);
+  gdn_token_loop_kernel<NSG, R, WARPS, CAPTURE, DA>
+      <<<static_cast<unsigned>(blocks), WARPS * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int NSG, bool CAPTURE, bool DA>
+cudaError_t launch_geo(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
+  if (geo == LoopGeometry::kDecode) {
+    constexpr Shape sh = shape_for<NSG>(LoopGeometry::kDecode);
+    return launch_one<NSG, sh.r, sh.warps, CAPTURE, DA>(p, sh.tc_max, stream);
+  }
+  constexpr Shape sh = shape_for<NSG>(LoopGeometry::kScan);
+  return launch_one<NSG, sh.r, sh.warps, CAPTURE, DA>(p, sh.tc_max, stream);
+}
+
+template <int NSG>
+cudaError_t launch_nsg(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
+  const bool cap = p.capture != nullptr;
+  if (cap)
+    return p.decay_after ? launch_geo<NSG, true, true>(p, geo, stream)
+                         : launch_geo<NSG, true, false>(p, geo, stream);
+  return p.decay_after ? launch_geo<NSG, false, true>(p, geo, stream)
+                       : launch_geo<NSG, false, false>(p, geo, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_token_loop(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
+  switch (p.dk) {
+    case 32: return launch_nsg<1>(p, geo, stream);
+    case 64: return launch_nsg<2>(p, geo, stream);
+    case 128: return launch_nsg<4>(p, geo, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+const char *token_loop_name(LoopGeometry geo, bool capture) {
+  static const char *names[2][2] = {{"token_loop_decode", "token_loop_decode_capture"},
+                                    {"token_loop_scan", "token_loop_scan_capture"}};
+  return names[geo == LoopGeometry::kScan ? 1 : 0][capture ? 1 : 0];
+}
+
+}  // namespace gdn

@@ -1,0 +1,101 @@
+"""Shared helpers of the GPU tests: run the CUDA path through the C ABI on
+seeded inputs, run the oracle on the same inputs, compare.
+
+Tolerances (the parity bar):
+* n_tokens <= 8: max|gpu - ref| <= 1e-4 * max|ref|, separately for output,
+  state_out and state_capture;
+* longer windows (the 4096-token prefill, and the 9..4095-token windows of
+  the ragged-chunk tests): ||gpu - ref||_2 / ||ref||_2 <= 1e-3 for output,
+  state_out and state_capture, and, as a guard against a few wild elements
+  hiding in the L2 norm, max|gpu - ref| <= 1e-2 * max|ref|.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MAXABS_TOL = 1e-4
+RELL2_TOL = 1e-3
+
+
+LONG_MAXABS_GUARD = 1e-2
+
+
+def to_dev(x):
+    import torch
+    return {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in x.items()}
+
+
+def run_gpu(w, x, params, capture=False, in_place=False, stream=None, dev=None):
+    """Run the CUDA path.  Returns numpy (output, state_out, capture|None)."""
+    import torch
+
+    from serving_gdn_decode_gb300 import _native as nat
+    d = dev if dev is not None else to_dev(x)
+    out = torch.empty(w.v_elems, dtype=torch.float32, device="cuda")
+    if in_place:
+        st = d["state_in"].clone()
+        st_in = st
+    else:
+        st = torch.empty(w.state_elems, dtype=torch.float32, device="cuda")
+        st_in = d["state_in"]
+    if capture:
+        cap = torch.empty(w.capture_elems, dtype=torch.float32, device="cuda")
+        nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params,
+                                cap, stream=stream)
+    else:
+        cap = None
+        nat.gdn_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params,
+                        stream=stream)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy(), st.cpu().numpy(), None if cap is None else cap.cpu().numpy())
+
+
+def max_abs_rel(gpu, ref) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(np.asarray(gpu, dtype=np.float64) - ref)) / max(den, 1e-300))
+
+
+def rel_l2(gpu, ref) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    d = np.asarray(gpu, dtype=np.float64) - ref
+    return float(np.sqrt(np.sum(d * d)) / max(np.sqrt(np.sum(ref * ref)), 1e-300))
+
+
+def assert_close(name, gpu, ref, n_tokens):
+    assert np.all(np.isfinite(gpu)), f"{name}: non-finite GPU values"
+    if n_tokens > 8:
+        e = rel_l2(gpu, ref)
+        assert e <= RELL2_TOL, f"{name}: rel-L2 {e:.3e} > {RELL2_TOL}"
+        m = max_abs_rel(gpu, ref)
+        assert m <= LONG_MAXABS_GUARD, f"{name}: max-abs/max|ref| {m:.3e} > {LONG_MAXABS_GUARD}"
+    else:
+        e = max_abs_rel(gpu, ref)
+        assert e <= MAXABS_TOL, f"{name}: max-abs/max|ref| {e:.3e} > {MAXABS_TOL}"
+    return e
+
+
+def sample_heads(w, n: int, seed: int = 0) -> np.ndarray:
+    """First and last head plus n-2 spread over the rest (head = s*n_v + vh)."""
+    H = w.heads
+    if H <= n:
+        return np.arange(H, dtype=np.uint32)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, H - 1), size=n - 2, replace=False)
+    return np.sort(np.concatenate([[0, H - 1], mid])).astype(np.uint32)
+
+
+def gather_heads(w, out, st, cap, heads):
+    """Pick the listed heads out of full-layout GPU results, in the oracle's
+    compact per-head order."""
+    o = out.reshape(w.n_seqs, w.n_tokens, w.n_v_heads, w.d_v)
+    s = st.reshape(w.n_seqs, w.n_v_heads, w.d_v, w.d_k)
+    c = None if cap is None else cap.reshape(w.n_seqs, w.n_tokens, w.n_v_heads, w.d_v, w.d_k)
+    oh, sh, ch = [], [], []
+    for h in heads:
+        si, vh = divmod(int(h), w.n_v_heads)
+        oh.append(o[si, :, vh])
+        sh.append(s[si, vh])
+        if c is not None:
+            ch.append(c[si, :, vh])
+    return np.stack(oh), np.stack(sh), (np.stack(ch) if c is not None else None)

@@ -1,0 +1,218 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+* the library loads and exports every function include/gdn.h declares;
+* argument checks return the documented status before anything is enqueued.
+
+Buffer-check cases pass made-up device addresses, so each of them has
+exactly one invalid argument and must be rejected on the host.  They are
+skipped where a CUDA device is visible: there a wrongly accepted call would
+launch a kernel on those addresses.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from serving_gdn_decode_gb300 import _native as nat
+from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN, pack_params
+from serving_gdn_decode_gb300.workloads import WORKLOADS
+
+
+@pytest.fixture(scope="module")
+def L():
+    from serving_gdn_decode_gb300 import build
+    build.build()
+    return nat.lib()
+
+
+def _has_cuda_device():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+no_device = pytest.mark.skipif(_has_cuda_device(), reason="fake-address cases run only without a GPU")
+
+
+def test_exports_every_declared_function(L):
+    names = nat.header_functions()
+    assert {"gdn_forward", "gdn_forward_capture", "gdn_last_error", "gdn_path_name"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/gdn.h but not exported"
+
+
+def test_header_constants_match_binding():
+    text = open(nat.HEADER_PATH).read()
+    for name, val in (("GDN_OK", 0), ("GDN_ERR_INVALID_ARGUMENT", 1), ("GDN_ERR_UNSUPPORTED", 2),
+                      ("GDN_ERR_CUDA", 3)):
+        assert f"{name} = {val}" in text
+    assert "#define GDN_N_PARAMS 9" in text
+    assert "#define GDN_FLAG_DECAY_AFTER 0x1u" in text and "#define GDN_FLAG_KHEAD_DIV 0x2u" in text
+
+
+# ---------------------------------------------------------------- params-only checks
+
+def _path(p, capture=False):
+    return nat.gdn_path_name(p, capture)
+
+
+def test_path_choice(L):
+    assert _path(WORKLOADS["decode"].params()) == "token_loop_decode"
+    assert _path(WORKLOADS["decode_wide_gqa"].params(khead_div=True)) == "token_loop_decode"
+    assert _path(WORKLOADS["spec_capture"].params(), True) == "token_loop_decode_capture"
+    assert _path(WORKLOADS["long_prefill"].params(path=PATH_SCAN)) == "token_loop_scan"
+    assert _path(WORKLOADS["tiny"].params(path=PATH_SCAN), True) == "token_loop_scan_capture"
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: p[:8], nat.GDN_ERR_INVALID_ARGUMENT),                 # fewer than 9 u32
+    (lambda p: _set(p, 0, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # D_k = 0
+    (lambda p: _set(p, 1, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # D_v = 0
+    (lambda p: _set(p, 2, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # n_k = 0
+    (lambda p: _set(p, 3, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # n_v = 0
+    (lambda p: _set(p, 4, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # n_tokens = 0
+    (lambda p: _set(p, 5, 0), nat.GDN_ERR_INVALID_ARGUMENT),         # n_seqs = 0
+    (lambda p: _set(p, 3, 24), nat.GDN_ERR_INVALID_ARGUMENT),        # n_v % n_k != 0
+    (lambda p: _set(p, 0, 48), nat.GDN_ERR_INVALID_ARGUMENT),        # D_k % 32 != 0
+    (lambda p: _set(p, 0, 160), nat.GDN_ERR_INVALID_ARGUMENT),       # D_k/32 > 4
+    (lambda p: _set(p, 0, 96), nat.GDN_ERR_UNSUPPORTED),             # D_k/32 = 3
+    (lambda p: _set(p, 1, 126), nat.GDN_ERR_INVALID_ARGUMENT),       # D_v % (D_k/32) != 0
+    (lambda p: _set(p, 7, 1), nat.GDN_ERR_INVALID_ARGUMENT),         # reserved slot
+    (lambda p: _set(p, 6, 0x10), nat.GDN_ERR_INVALID_ARGUMENT),      # unknown flag bit
+    (lambda p: _set(p, 6, 0xC), nat.GDN_ERR_INVALID_ARGUMENT),       # path 3
+])
+def test_params_rejected(L, mutate, status):
+    p = mutate(WORKLOADS["decode"].params())
+    with pytest.raises(nat.GdnError) as e:
+        _path(p)
+    assert e.value.status == status
+    assert nat.gdn_last_error() != ""
+
+
+def _set(p, i, val):
+    p = p.copy()
+    p[i] = val
+    return p
+
+
+def test_chunked_forced_with_capture_is_unsupported(L):
+    with pytest.raises(nat.GdnError) as e:
+        _path(WORKLOADS["spec_capture"].params(path=PATH_CHUNKED), capture=True)
+    assert e.value.status == nat.GDN_ERR_UNSUPPORTED
+
+
+def test_supported_head_dims(L):
+    for dk in (32, 64, 128):
+        nsg = dk // 32
+        for dv in (nsg, 3 * nsg, 128, 200 - 200 % nsg):
+            assert _path(pack_params(dk, dv, 2, 6, 3, 2)) == "token_loop_decode"
+
+
+# ---------------------------------------------------------------- buffer checks (fake addresses)
+
+GAP = 1 << 32
+
+
+class Fake:
+    """Disjoint, 256-byte aligned made-up device addresses for each buffer."""
+
+    def __init__(self, w, capture=False):
+        self.w = w
+        names = ["q", "k", "v", "g", "beta", "state_in", "output", "state_out", "state_capture"]
+        self.addr = {n: (i + 1) * GAP for i, n in enumerate(names)}
+        self.cap_elems = w.capture_elems
+
+    def call(self, params=None, capture=False, **over):
+        a = dict(self.addr, **over)
+        p = self.w.params() if params is None else params
+        args = [a[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+        if capture:
+            return nat.forward_capture_raw(*args, p, a["state_capture"],
+                                           over.get("cap_elems", self.cap_elems))
+        return nat.forward_raw(*args, p)
+
+
+SMALL = WORKLOADS["decode"].with_(n_seqs=2, n_tokens=3)
+SMALL1 = WORKLOADS["decode"].with_(n_seqs=1, n_tokens=3)
+
+
+@no_device
+@pytest.mark.parametrize("name", ["q", "k", "v", "g", "beta", "state_in", "output", "state_out"])
+def test_null_buffer(L, name):
+    f = Fake(SMALL)
+    assert f.call(**{name: 0}) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert name in nat.gdn_last_error()
+
+
+@no_device
+@pytest.mark.parametrize("name,off", [("q", 4), ("k", 8), ("state_in", 4), ("state_out", 12),
+                                      ("v", 2), ("g", 1), ("beta", 3), ("output", 2)])
+def test_misaligned_buffer(L, name, off):
+    f = Fake(SMALL)
+    assert f.call(**{name: f.addr[name] + off}) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "aligned" in nat.gdn_last_error()
+
+
+@no_device
+def test_partial_state_alias_rejected(L):
+    f = Fake(SMALL)
+    assert f.call(state_out=f.addr["state_in"] + 16) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "overlap" in nat.gdn_last_error()
+
+
+@no_device
+@pytest.mark.parametrize("victim", ["q", "v", "state_in", "state_out"])
+def test_output_overlap_rejected(L, victim):
+    f = Fake(SMALL)
+    assert f.call(output=f.addr[victim] + 16) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_state_out_overlapping_input_rejected(L):
+    f = Fake(SMALL)
+    assert f.call(state_out=f.addr["k"]) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_capture_size_rules(L):
+    f = Fake(SMALL, capture=True)
+    need = SMALL.capture_elems
+    # n_seqs > 1: exact size only
+    assert f.call(capture=True, cap_elems=need + 4) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(capture=True, cap_elems=need - 4) == nat.GDN_ERR_INVALID_ARGUMENT
+    # n_seqs == 1: smaller is rejected (larger is accepted; not called here)
+    f1 = Fake(SMALL1, capture=True)
+    assert f1.call(capture=True, cap_elems=SMALL1.capture_elems - 1) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(capture=True, state_capture=0) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(capture=True, state_capture=f.addr["state_capture"] + 4) == \
+        nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(capture=True, state_capture=f.addr["state_out"]) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(capture=True, state_capture=f.addr["v"] + 64) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_invalid_params_through_forward(L):
+    f = Fake(SMALL)
+    p = SMALL.params()
+    p[3] = 17
+    assert f.call(params=p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert f.call(params=SMALL.params()[:8]) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.lib().gdn_forward(*([GAP] * 8), None, 9, None) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_capture_memory_cost_matches_pages():
+    """'Memory cost' section of gated_delta_net_decode_capture.metal: D_k = D_v =
+    128, n_v = 8, n_seqs = 1, K+1 = 4 tokens -> 128*128*8*4*4 bytes = 2 MB per
+    linear-attention layer."""
+    w = WORKLOADS["spec_capture"].with_(n_v_heads=8, n_seqs=1, n_tokens=4)
+    assert w.capture_elems * 4 == 2 * 1024 * 1024
+    assert WORKLOADS["spec_capture"].capture_elems * 4 == 256 * 1024 * 1024
+
+
+def test_binding_rejects_before_calling():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4)
+    with pytest.raises(nat.GdnError):
+        nat.gdn_forward(x, x, x, x, x, x, x, x, pack_params(32, 32, 1, 1, 1, 1))
