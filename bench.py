@@ -262,41 +262,31 @@ def time_graphed(torch, nat, sets, params, steps, warmup, capture=False, world=1
 
 
 def time_e2e(torch, nat, w, params, steps, device):
-    """End to end through the public API: every step copies its inputs from
-    pinned host memory, calls gdn_forward, and reads output and state back."""
+    """End to end through the public API from pinned host memory: each step
+    copies all inputs in and output + state out (HostPipeline overlaps the
+    two copy directions and the kernel over groups of sequences)."""
     from serving_gdn_decode_gb300.workloads import make_inputs
     x = make_inputs(w, seed=100)
     host = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
-    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    out_d = torch.empty(w.v_elems, dtype=torch.float32, device=device)
-    st_d = torch.empty(w.state_elems, dtype=torch.float32, device=device)
     out_h = torch.empty(w.v_elems, dtype=torch.float32).pin_memory()
     st_h = torch.empty(w.state_elems, dtype=torch.float32).pin_memory()
-    stream = torch.cuda.Stream()
+    pipe = nat.HostPipeline(params, max_group=max(1, w.n_seqs // 8), device=device)
 
     def step():
-        for k in ("q", "k", "v", "g", "beta", "state_in"):
-            dev[k].copy_(host[k], non_blocking=True)
-        nat.gdn_forward(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["state_in"], out_d,
-                        st_d, params)
-        out_h.copy_(out_d, non_blocking=True)
-        st_h.copy_(st_d, non_blocking=True)
+        pipe(host["q"], host["k"], host["v"], host["g"], host["beta"], host["state_in"], out_h,
+             st_h)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+    for _ in range(3):
+        step()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(steps):
-            step()
-        end.record(stream)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
     torch.cuda.synchronize()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * 4 + st_h.numel() * 4
-    return start.elapsed_time(end) / 1e3 / steps, h2d, d2h
+    return start.elapsed_time(end) / 1e3 / steps, pipe.h2d_bytes(), pipe.d2h_bytes()
 
 
 def extras(torch, nat, peak_gbs, device):
@@ -321,6 +311,38 @@ def extras(torch, nat, peak_gbs, device):
     hbm_case("spec_capture_s32", wc, wc.params(), True, 4, 200)
     wc64 = wc.with_(n_seqs=64)
     hbm_case("spec_capture_s64", wc64, wc64.params(), True, 3, 120)
+
+    # speculative-decode rollback commit: gathers one captured state per sequence
+    import numpy as np
+    sets = make_sets(torch, wc, 3, device, capture=True)
+    for d in sets:
+        d["idx"] = torch.from_numpy(
+            np.random.default_rng(1).integers(0, wc.n_tokens, wc.n_seqs).astype(np.int32)).to(device)
+    stream = torch.cuda.Stream()
+    steps = 300
+    with torch.cuda.stream(stream):
+        for i in range(10):
+            d = sets[i % 3]
+            nat.gdn_commit_capture(d["capture"], d["idx"], d["state"], wc.params())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                d = sets[i % 3]
+                nat.gdn_commit_capture(d["capture"], d["idx"], d["state"], wc.params())
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    nbytes = 2 * wc.state_elems * 4 + wc.n_seqs * 4
+    res["commit_capture_s32"] = {"us_per_call": round(t * 1e6, 2), "GB_s": round(nbytes / t / 1e9, 1),
+                                 "hbm_frac": round(nbytes / t / 1e9 / peak_gbs, 3)}
+    del sets, g
+    torch.cuda.empty_cache()
 
     wp = WORKLOADS["long_prefill"]
     for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),):
@@ -420,8 +442,9 @@ def run_ours(args):
         "e2e": {"value": round(e2e_val / 1e9, 2), "unit": "GB/s",
                 "us_per_call": round(e2e_s * 1e6, 1), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "pinned host -> device copies of all inputs, gdn_forward, device -> "
-                       "pinned host copies of output and state, per step"},
+                "how": "HostPipeline: per step, pinned host -> device copies of all inputs, "
+                       "gdn_forward, device -> pinned host copies of output and state, "
+                       "overlapped over 8 groups of sequences on 3 streams"},
         "gpu_launches": args.steps,
         "clocks": clk,
     }

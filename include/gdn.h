@@ -135,6 +135,32 @@ gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, c
                                float *state_capture, size_t state_capture_elems,
                                gdn_stream_t stream);
 
+/*
+ * gdn_commit_capture -- speculative-decode rollback.  After gdn_forward_capture
+ * verified n_tokens tokens, make the state after each sequence's last
+ * accepted token the active state:
+ *     for every s with 0 <= accepted_idx[s] < n_tokens:
+ *         state[:, :, :, s] = state_capture[:, :, :, accepted_idx[s], s]
+ * Sequences with an index outside [0, n_tokens) (e.g. -1: nothing accepted)
+ * keep their state.  The pages leave this step to the caller
+ * (dispatch_gated_delta_net_decode_with_capture, gated_delta_net_decode.rs:
+ * "the caller reads state_capture[..., accepted_idx, ...] as the new active
+ * state"); here it is one launch that reads the indices on the device.
+ *
+ * state_capture: DEVICE, [D_k, D_v, n_v_heads, n_tokens, n_seqs] f32 as written by
+ *   gdn_forward_capture with the same params; state_capture_elems as there.
+ * accepted_idx:  DEVICE, n_seqs int32.
+ * state:         DEVICE, [D_k, D_v, n_v_heads, n_seqs] f32, updated in place.
+ * params:        HOST, the same 9-u32 block as the capture call (n_k_heads and
+ *   the flags are checked but not used).
+ * Checks: the params checks of gdn_forward; NULL pointers; state_capture and
+ *   state 16-byte aligned, accepted_idx 4-byte aligned; the capture size rule
+ *   of gdn_forward_capture; state overlapping state_capture or accepted_idx.
+ */
+gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_elems,
+                              const int32_t *accepted_idx, float *state, const uint32_t *params,
+                              size_t n_params, gdn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the thread's next call. */
 const char *gdn_last_error(void);

@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_last_error.restype = ctypes.c_char_p
             L.gdn_path_name.argtypes = [u32p, sz, ctypes.c_int, ctypes.POINTER(ctypes.c_char_p)]
             L.gdn_path_name.restype = ctypes.c_int
+            L.gdn_commit_capture.argtypes = [vp, sz, vp, vp, u32p, sz, vp]
+            L.gdn_commit_capture.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -100,6 +102,14 @@ def forward_capture_raw(q, k, v, g, beta, state_in, output, state_out, params, s
     p, pp, n = _params_arg(params)
     return lib().gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, pp, n,
                                      state_capture, state_capture_elems, stream)
+
+
+def commit_capture_raw(state_capture, state_capture_elems, accepted_idx, state, params,
+                       stream=0) -> int:
+    """Call gdn_commit_capture with integer device addresses; returns the status."""
+    p, pp, n = _params_arg(params)
+    return lib().gdn_commit_capture(state_capture, state_capture_elems, accepted_idx, state, pp, n,
+                                    stream)
 
 
 # ---------------------------------------------------------------- torch tensors
@@ -169,3 +179,110 @@ def gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, params, s
                              _stream(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
+
+
+def gdn_commit_capture(state_capture, accepted_idx, state, params, stream=None) -> None:
+    """Speculative-decode rollback on torch CUDA tensors: for every sequence s
+    with 0 <= accepted_idx[s] < n_tokens, state[.., s] = state_capture[.., accepted_idx[s], s];
+    other sequences keep their state.  ``accepted_idx`` is an int32 CUDA tensor
+    of n_seqs entries (read on the device)."""
+    import torch
+    s = _sizes(params)
+    cap = _check("state_capture", state_capture, s["state"] * s["nt"], allow_larger=s["ns"] == 1)
+    stp = _check("state", state, s["state"])
+    if (not isinstance(accepted_idx, torch.Tensor) or accepted_idx.dtype != torch.int32
+            or not accepted_idx.is_cuda or not accepted_idx.is_contiguous()
+            or accepted_idx.numel() != s["ns"]):
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                       "accepted_idx must be a contiguous int32 CUDA tensor of n_seqs entries")
+    st = commit_capture_raw(cap, state_capture.numel(), accepted_idx.data_ptr(), stp, params,
+                            _stream(stream, state.device))
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+
+
+# ---------------------------------------------------------------- host buffers
+
+class HostPipeline:
+    """Run gdn_forward on PINNED HOST tensors, end to end.
+
+    Sequences are independent and n_seqs is the outermost dimension of every
+    buffer, so the batch is cut into groups of sequences; group i's inputs
+    are copied in on one stream while group i-1 runs and group i-2's output
+    and state are copied out on a third stream.  Device staging buffers are
+    allocated once (by torch) at construction for `max_group` sequences and
+    reused, double-buffered, by every call.
+    """
+
+    def __init__(self, params, max_group: int | None = None, device=None):
+        import torch
+        p = np.asarray(params, dtype=np.uint32).reshape(-1)
+        self.params = p.copy()
+        dk, dv, nk, nv, nt, ns = (int(x) for x in p[:6])
+        self.ns = ns
+        self.group = max(1, min(ns, max_group or max(1, ns // 8)))
+        self.per_seq = dict(q=dk * nk * nt, k=dk * nk * nt, v=dv * nv * nt, g=nv * nt,
+                            beta=nv * nt, state_in=dk * dv * nv, output=dv * nv * nt,
+                            state_out=dk * dv * nv)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.device = dev
+        self.bufs = [{k: torch.empty(n * self.group, dtype=torch.float32, device=dev)
+                      for k, n in self.per_seq.items()} for _ in range(2)]
+        self.s_in = torch.cuda.Stream(dev)
+        self.s_run = torch.cuda.Stream(dev)
+        self.s_out = torch.cuda.Stream(dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_run = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def h2d_bytes(self) -> int:
+        return 4 * self.ns * sum(self.per_seq[k] for k in ("q", "k", "v", "g", "beta", "state_in"))
+
+    def d2h_bytes(self) -> int:
+        return 4 * self.ns * (self.per_seq["output"] + self.per_seq["state_out"])
+
+    def __call__(self, q, k, v, g, beta, state_in, output, state_out, stream=None):
+        """Inputs and outputs: flat f32 pinned host tensors in the layouts of
+        include/gdn.h.  Work is enqueued after `stream` (default: the current
+        stream), which waits for all of it before returning control on the
+        GPU; the host does not block."""
+        import torch
+        host = dict(q=q, k=k, v=v, g=g, beta=beta, state_in=state_in, output=output,
+                    state_out=state_out)
+        for name, t in host.items():
+            if t.is_cuda or not t.is_pinned() or t.dtype != torch.float32 or not t.is_contiguous():
+                raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                               f"{name} must be a contiguous f32 pinned host tensor")
+            if t.numel() != self.per_seq[name] * self.ns:
+                raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                               f"{name} element count {t.numel()} != {self.per_seq[name] * self.ns}")
+        base = torch.cuda.current_stream(self.device) if stream is None else stream
+        for s in (self.s_in, self.s_run, self.s_out):
+            s.wait_stream(base)
+        groups = [(s0, min(self.group, self.ns - s0)) for s0 in range(0, self.ns, self.group)]
+        for i, (s0, n) in enumerate(groups):
+            b = i & 1
+            buf = self.bufs[b]
+            p = self.params.copy()
+            p[5] = n
+            with torch.cuda.stream(self.s_in):
+                if i >= 2:
+                    self.s_in.wait_event(self.ev_out[b])  # buffer b's previous output copied out
+                for name in ("q", "k", "v", "g", "beta", "state_in"):
+                    m = self.per_seq[name]
+                    buf[name][: m * n].copy_(host[name][s0 * m:(s0 + n) * m], non_blocking=True)
+                self.ev_in[b].record(self.s_in)
+            with torch.cuda.stream(self.s_run):
+                self.s_run.wait_event(self.ev_in[b])
+                gdn_forward(*(buf[x][: self.per_seq[x] * n] for x in
+                              ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")),
+                            p, stream=self.s_run)
+                self.ev_run[b].record(self.s_run)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(self.ev_run[b])
+                for name in ("output", "state_out"):
+                    m = self.per_seq[name]
+                    host[name][s0 * m:(s0 + n) * m].copy_(buf[name][: m * n], non_blocking=True)
+                self.ev_out[b].record(self.s_out)
+        for s in (self.s_in, self.s_run, self.s_out):
+            base.wait_stream(s)

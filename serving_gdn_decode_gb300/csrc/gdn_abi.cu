@@ -111,6 +111,13 @@ gdn_status decode_params(const uint32_t *params, size_t n_params, Decoded *d) {
 
 enum class Path { kDecode, kScan };
 
+const char *path_name(Path path, bool capture) {
+  switch (path) {
+    case Path::kDecode: return capture ? "token_loop_decode_capture" : "token_loop_decode";
+    default: return capture ? "scan_capture" : "scan";
+  }
+}
+
 gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
   switch (d.path) {
     case GDN_PATH_SCAN:
@@ -200,9 +207,9 @@ gdn_status run(const float *q, const float *k, const float *v, const float *g, c
   gdn::Problem &p = d.prob;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_in = state_in;
   p.output = output; p.state_out = state_out; p.capture = with_capture ? capture : nullptr;
-  const cudaError_t err = gdn::launch_token_loop(
-      p, path == Path::kDecode ? gdn::LoopGeometry::kDecode : gdn::LoopGeometry::kScan,
-      reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t err =
+      path == Path::kDecode ? gdn::launch_token_loop(p, cs) : gdn::launch_scan(p, cs);
   if (err != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
   return GDN_OK;
@@ -228,6 +235,42 @@ gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, c
              state_capture_elems, true, stream);
 }
 
+gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_elems,
+                              const int32_t *accepted_idx, float *state, const uint32_t *params,
+                              size_t n_params, gdn_stream_t stream) {
+  g_last_error[0] = '\0';
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  if (state_capture == nullptr || accepted_idx == nullptr || state == nullptr)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: NULL buffer");
+  if (!aligned(state_capture, 16) || !aligned(state, 16) || !aligned(accepted_idx, 4))
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: state_capture and state must be 16-byte aligned, accepted_idx 4-byte");
+  if (d.prob.ns > 1 && state_capture_elems != d.capture_elems)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture element count %zu != required %llu",
+                state_capture_elems, d.capture_elems);
+  if (d.prob.ns == 1 && state_capture_elems < d.capture_elems)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture element count %zu < required %llu",
+                state_capture_elems, d.capture_elems);
+  const Span cap{state_capture, d.capture_elems * 4, "state_capture"};
+  const Span stt{state, d.state_elems * 4, "state"};
+  const Span idx{accepted_idx, static_cast<unsigned long long>(d.prob.ns) * 4, "accepted_idx"};
+  if (overlap(stt, cap) || overlap(stt, idx))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state overlaps state_capture or accepted_idx");
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const cudaError_t err = gdn::launch_commit(
+      state_capture, accepted_idx, state, d.prob.nt, d.prob.ns,
+      static_cast<uint64_t>(d.prob.dk) * d.prob.dv * d.prob.nv, sms,
+      reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn: commit launch failed: %s", cudaGetErrorString(err));
+  return GDN_OK;
+}
+
 const char *gdn_last_error(void) { return g_last_error; }
 
 gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
@@ -241,9 +284,7 @@ gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
   Path path;
   st = choose_path(d, capture != 0, &path);
   if (st != GDN_OK) return st;
-  *name = gdn::token_loop_name(
-      path == Path::kDecode ? gdn::LoopGeometry::kDecode : gdn::LoopGeometry::kScan,
-      capture != 0);
+  *name = path_name(path, capture != 0);
   return GDN_OK;
 }
 

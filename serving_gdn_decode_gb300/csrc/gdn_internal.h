@@ -19,13 +19,18 @@ struct Problem {
   float q_scale;
 };
 
-// Token-loop kernels: the state rows of every (seq, value head) pair stay in
-// registers across the whole token range.  `geometry` picks the decode
-// launch shape (few tokens, HBM-bound) or the scan shape (many tokens).
-enum class LoopGeometry { kDecode, kScan };
-cudaError_t launch_token_loop(const Problem &p, LoopGeometry geometry, cudaStream_t stream);
+// Decode / multi-token-window kernel (token_loop.cu): every (seq, value head)
+// state row stays in registers across the call; shaped for HBM throughput.
+cudaError_t launch_token_loop(const Problem &p, cudaStream_t stream);
 
-// Kernel name of the token-loop launch that `launch_token_loop` would use.
-const char *token_loop_name(LoopGeometry geometry, bool capture);
+// Sequential-scan kernel for long token ranges (scan.cu): two lanes per row,
+// lazy decay; shaped for FP32 issue throughput.
+cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
+
+// Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
+// every sequence whose accepted index lies in [0, nt).
+cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,
+                          uint32_t nt, uint32_t ns, uint64_t slice_elems, int sm_count,
+                          cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,6 +1,6 @@
-// Token-loop kernels for the Gated DeltaNet recurrence on sm_103a: decode,
-// multi-token windows with per-token state capture, and the sequential-scan
-// prefill.
+// Token-loop kernel for the Gated DeltaNet recurrence on sm_103a: decode and
+// short multi-token windows, with optional per-token state capture.  Long
+// token ranges use the scan kernel (scan.cu) instead.
 //
 // Work decomposition.  The D_v rows of a (seq, value head) state are
 // independent (each row i only meets v_t[i] and the shared k_t, q_t), so a
@@ -283,23 +283,17 @@ __global__ void __launch_bounds__(WARPS * 32)
                            st[r]);
 }
 
-// ---- launch shapes
+// ---- launch shape: several rows per warp (R = 16/NSG, 64 B of state per
+// lane) and 8 warps per CTA, so each SM keeps tens of KB of state loads in
+// flight; tokens are staged 8 at a time.
 
-struct Shape {
-  int r, warps, tc_max;
-};
+constexpr int kWarps = 8;
+constexpr int kTcMax = 8;
 
-// Decode: several rows per warp so each SM keeps tens of KB of state loads
-// in flight.  Scan: fewer rows per CTA so the ~D_v*n_v*S row chains spread
-// over all SMs.
-template <int NSG>
-constexpr Shape shape_for(LoopGeometry geo) {
-  return geo == LoopGeometry::kDecode ? Shape{16 / NSG, 8, 8} : Shape{16 / NSG, 4, 16};
-}
-
-template <int NSG, int R, int WARPS, bool CAPTURE, bool DA>
-cudaError_t launch_one(const Problem &p, int tc_max, cudaStream_t stream) {
-  constexpr int ROWS = WARPS * R;
+template <int NSG, bool CAPTURE, bool DA>
+cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
+  constexpr int R = 16 / NSG;
+  constexpr int ROWS = kWarps * R;
   constexpr int DK = 32 * NSG;
   LoopArgs a;
   a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
@@ -309,52 +303,36 @@ cudaError_t launch_one(const Problem &p, int tc_max, cudaStream_t stream) {
   a.khead_div = p.khead_div ? 1u : 0u;
   a.q_scale = p.q_scale;
   a.row_blocks = (p.dv + ROWS - 1) / ROWS;
-  a.tc = static_cast<uint32_t>(p.nt < static_cast<uint32_t>(tc_max) ? p.nt : tc_max);
+  a.tc = static_cast<uint32_t>(p.nt < static_cast<uint32_t>(kTcMax) ? p.nt : kTcMax);
   const unsigned long long blocks =
       static_cast<unsigned long long>(a.row_blocks) * p.nv * static_cast<unsigned long long>(p.ns);
   if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   const int buf_floats = (static_cast<int>(a.tc) * (2 * DK + ROWS + 2) + 3) & ~3;
   const size_t smem = 2u * static_cast<size_t>(buf_floats) * sizeof(float);
-  gdn_token_loop_kernel<NSG, R, WARPS, CAPTURE, DA>
-      <<<static_cast<unsigned>(blocks), WARPS * 32, smem, stream>>>(a);
+  gdn_token_loop_kernel<NSG, R, kWarps, CAPTURE, DA>
+      <<<static_cast<unsigned>(blocks), kWarps * 32, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <int NSG, bool CAPTURE, bool DA>
-cudaError_t launch_geo(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
-  if (geo == LoopGeometry::kDecode) {
-    constexpr Shape sh = shape_for<NSG>(LoopGeometry::kDecode);
-    return launch_one<NSG, sh.r, sh.warps, CAPTURE, DA>(p, sh.tc_max, stream);
-  }
-  constexpr Shape sh = shape_for<NSG>(LoopGeometry::kScan);
-  return launch_one<NSG, sh.r, sh.warps, CAPTURE, DA>(p, sh.tc_max, stream);
-}
-
 template <int NSG>
-cudaError_t launch_nsg(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
+cudaError_t launch_nsg(const Problem &p, cudaStream_t stream) {
   const bool cap = p.capture != nullptr;
   if (cap)
-    return p.decay_after ? launch_geo<NSG, true, true>(p, geo, stream)
-                         : launch_geo<NSG, true, false>(p, geo, stream);
-  return p.decay_after ? launch_geo<NSG, false, true>(p, geo, stream)
-                       : launch_geo<NSG, false, false>(p, geo, stream);
+    return p.decay_after ? launch_one<NSG, true, true>(p, stream)
+                         : launch_one<NSG, true, false>(p, stream);
+  return p.decay_after ? launch_one<NSG, false, true>(p, stream)
+                       : launch_one<NSG, false, false>(p, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_token_loop(const Problem &p, LoopGeometry geo, cudaStream_t stream) {
+cudaError_t launch_token_loop(const Problem &p, cudaStream_t stream) {
   switch (p.dk) {
-    case 32: return launch_nsg<1>(p, geo, stream);
-    case 64: return launch_nsg<2>(p, geo, stream);
-    case 128: return launch_nsg<4>(p, geo, stream);
+    case 32: return launch_nsg<1>(p, stream);
+    case 64: return launch_nsg<2>(p, stream);
+    case 128: return launch_nsg<4>(p, stream);
     default: return cudaErrorInvalidValue;
   }
-}
-
-const char *token_loop_name(LoopGeometry geo, bool capture) {
-  static const char *names[2][2] = {{"token_loop_decode", "token_loop_decode_capture"},
-                                    {"token_loop_scan", "token_loop_scan_capture"}};
-  return names[geo == LoopGeometry::kScan ? 1 : 0][capture ? 1 : 0];
 }
 
 }  // namespace gdn

@@ -62,8 +62,11 @@ def test_path_choice(L):
     assert _path(WORKLOADS["decode"].params()) == "token_loop_decode"
     assert _path(WORKLOADS["decode_wide_gqa"].params(khead_div=True)) == "token_loop_decode"
     assert _path(WORKLOADS["spec_capture"].params(), True) == "token_loop_decode_capture"
-    assert _path(WORKLOADS["long_prefill"].params(path=PATH_SCAN)) == "token_loop_scan"
-    assert _path(WORKLOADS["tiny"].params(path=PATH_SCAN), True) == "token_loop_scan_capture"
+    assert _path(WORKLOADS["long_prefill"].params()) == "scan"
+    assert _path(WORKLOADS["long_prefill"].params(path=PATH_SCAN)) == "scan"
+    assert _path(WORKLOADS["tiny"].params(path=PATH_SCAN), True) == "scan_capture"
+    assert _path(WORKLOADS["decode"].with_(n_tokens=16).params()) == "token_loop_decode"
+    assert _path(WORKLOADS["decode"].with_(n_tokens=17).params()) == "scan"
 
 
 @pytest.mark.parametrize("mutate,status", [
@@ -216,3 +219,25 @@ def test_binding_rejects_before_calling():
     x = torch.zeros(4)
     with pytest.raises(nat.GdnError):
         nat.gdn_forward(x, x, x, x, x, x, x, x, pack_params(32, 32, 1, 1, 1, 1))
+
+
+# ---------------------------------------------------------------- rollback commit checks
+
+@no_device
+def test_commit_checks(L):
+    w = SMALL
+    cap, idx, st = 1 * GAP, 2 * GAP, 3 * GAP
+    p = w.params()
+    ok_elems = w.capture_elems
+    assert nat.commit_capture_raw(0, ok_elems, idx, st, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, 0, st, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, idx, 0, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap + 8, ok_elems, idx, st, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, idx + 2, st, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems + 4, idx, st, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, idx, cap + 64, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, idx, idx, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.commit_capture_raw(cap, ok_elems, idx, st, p[:8]) == nat.GDN_ERR_INVALID_ARGUMENT
+    w1 = SMALL1
+    assert nat.commit_capture_raw(cap, w1.capture_elems - 1, idx, st, w1.params()) == \
+        nat.GDN_ERR_INVALID_ARGUMENT

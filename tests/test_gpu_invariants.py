@@ -1,8 +1,10 @@
 """GPU invariants, edge cases and ragged shapes, through the C ABI.
 
 * bitwise properties that need no oracle: capture's last slice equals
-  state_out; chained calls equal one call on the same path; doubling
-  (state_in, v) doubles every result; in-place equals out-of-place;
+  state_out; chained calls equal one call on the decode path (the scan path
+  folds its lazy decay at chunk boundaries counted from the call's first
+  token, so there chaining holds within tolerance); doubling (state_in, v)
+  doubles every result; in-place equals out-of-place;
 * no write outside the caller's buffers (guard bands), and the unused tail of
   an oversized capture buffer (allowed when n_seqs == 1) stays untouched;
 * ragged shapes (several CTAs with a partial last one, token chunks with a
@@ -35,8 +37,9 @@ def _cut(w, x, t0, t1):
             "beta": cut(x["beta"], w.n_v_heads), "state_in": x["state_in"]}
 
 
-@pytest.mark.parametrize("path,nt,split", [(0, 12, 5), (PATH_SCAN, 40, 17), (PATH_SCAN, 9, 1)])
-def test_chained_equals_one_call_bitwise(torch, path, nt, split):
+@pytest.mark.parametrize("path,nt,split", [(0, 12, 5), (0, 16, 1), (PATH_SCAN, 40, 17),
+                                           (PATH_SCAN, 9, 1)])
+def test_chained_equals_one_call(torch, path, nt, split):
     w = Workload("chain", 128, 64, 2, 4, nt, 3)
     x = make_inputs(w, 5)
     out, st, _ = run_gpu(w, x, w.params(path=path))
@@ -47,6 +50,11 @@ def test_chained_equals_one_call_bitwise(torch, path, nt, split):
     xb["state_in"] = sa
     ob, sb, _ = run_gpu(wb, xb, wb.params(path=path))
     o = out.reshape(w.n_seqs, nt, -1)
+    if path == PATH_SCAN:
+        assert_close("output", oa, o[:, :split].reshape(-1).astype(np.float64), split)
+        assert_close("output", ob, o[:, split:].reshape(-1).astype(np.float64), nt - split)
+        assert_close("state_out", sb, st.astype(np.float64), nt)
+        return
     np.testing.assert_array_equal(o[:, :split].reshape(-1), oa)
     np.testing.assert_array_equal(o[:, split:].reshape(-1), ob)
     np.testing.assert_array_equal(st, sb)
@@ -159,6 +167,33 @@ def test_ragged_shapes_vs_oracle(torch, oracle_mod, shape, flags, capture):
     assert_close("state_out", st, rs, nt)
     if capture:
         assert_close("state_capture", cap, rc, nt)
+
+
+@pytest.mark.parametrize("gate", ["large", "negative", "mixed"])
+@pytest.mark.parametrize("decay_after", [False, True])
+@pytest.mark.parametrize("capture", [False, True], ids=["plain", "capture"])
+def test_scan_extreme_gates_vs_oracle(torch, oracle_mod, gate, decay_after, capture):
+    """Gates far outside U[0, 0.5): the scan kernel's lazy decay must fall back
+    to explicit decay in chunks where the running log-scale leaves [-40, 40]."""
+    w = Workload("gates", 128, 64, 2, 4, 70, 2)
+    x = make_inputs(w, 41)
+    rng = np.random.default_rng(43)
+    if gate == "large":
+        x["g"] = rng.uniform(0.0, 8.0, w.scalar_elems).astype(np.float32)
+    elif gate == "negative":
+        x["g"] = rng.uniform(-0.12, 0.0, w.scalar_elems).astype(np.float32)
+    else:  # some chunks lazy, some explicit, some tokens with alpha underflowing to 0
+        g = rng.uniform(0.0, 0.5, w.scalar_elems).astype(np.float32)
+        g[::7] = 60.0
+        g[5::23] = 200.0
+        x["g"] = g
+    p = w.params(path=PATH_SCAN, decay_after=decay_after)
+    out, st, cap = run_gpu(w, x, p, capture=capture)
+    ro, rs, rc = oracle_mod.forward(p, **x, capture=capture)
+    assert_close("output", out, ro, w.n_tokens)
+    assert_close("state_out", st, rs, w.n_tokens)
+    if capture:
+        assert_close("state_capture", cap, rc, w.n_tokens)
 
 
 def test_decode_and_scan_shapes_agree(torch):
