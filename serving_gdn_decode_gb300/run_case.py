@@ -25,6 +25,8 @@ def main(argv=None):
     ap.add_argument("--capture", action="store_true", help="use gdn_forward_capture")
     ap.add_argument("--decay-after", action="store_true")
     ap.add_argument("--khead-div", action="store_true")
+    ap.add_argument("--commit", action="store_true",
+                    help="after each capture call, commit a random accepted token per sequence")
     a = ap.parse_args(argv)
 
     import torch
@@ -43,10 +45,18 @@ def main(argv=None):
     st = torch.empty(w.state_elems, dtype=torch.float32, device=dev)
     cap = torch.empty(w.capture_elems, dtype=torch.float32, device=dev) if capture else None
     p = w.params(decay_after=a.decay_after, khead_div=a.khead_div, path=PATHS[a.path])
+    if a.commit:
+        import numpy as np
+        capture = True
+        cap = torch.empty(w.capture_elems, dtype=torch.float32, device=dev)
+        idx = torch.from_numpy(np.random.default_rng(0).integers(0, w.n_tokens, w.n_seqs)
+                               .astype(np.int32)).to(dev)
     for _ in range(a.calls):
         if capture:
             nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], out,
                                     st, p, cap)
+            if a.commit:
+                nat.gdn_commit_capture(cap, idx, st, p)
         else:
             nat.gdn_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], out, st, p)
     torch.cuda.synchronize()
