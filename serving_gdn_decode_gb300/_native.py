@@ -207,45 +207,44 @@ class HostPipeline:
     """Run gdn_forward on PINNED HOST tensors, end to end.
 
     Sequences are independent and n_seqs is the outermost dimension of every
-    buffer, so the batch is cut into groups of sequences; group i's inputs
-    are copied in on one stream while group i-1 runs and group i-2's output
-    and state are copied out on a third stream.  Device staging buffers are
-    allocated once (by torch) at construction for `max_group` sequences and
-    reused, double-buffered, by every call.
+    buffer.  q, k, v, g, beta (small) are copied in with one copy each; the
+    state, which dominates the bytes, is cut into `groups` groups of sequences
+    so that group i's state is copied in on one stream while group i-1 runs
+    and group i-2's new state is copied out on a third stream (the two copy
+    directions overlap).  Device buffers of the full problem size are
+    allocated once (by torch) at construction and reused by every call.
     """
 
-    def __init__(self, params, max_group: int | None = None, device=None):
+    SMALL_INPUTS = ("q", "k", "v", "g", "beta")
+
+    def __init__(self, params, groups: int = 4, device=None):
         import torch
         p = np.asarray(params, dtype=np.uint32).reshape(-1)
         self.params = p.copy()
         dk, dv, nk, nv, nt, ns = (int(x) for x in p[:6])
         self.ns = ns
-        self.group = max(1, min(ns, max_group or max(1, ns // 8)))
+        self.group = max(1, -(-ns // max(1, groups)))
         self.per_seq = dict(q=dk * nk * nt, k=dk * nk * nt, v=dv * nv * nt, g=nv * nt,
                             beta=nv * nt, state_in=dk * dv * nv, output=dv * nv * nt,
                             state_out=dk * dv * nv)
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         self.device = dev
-        self.bufs = [{k: torch.empty(n * self.group, dtype=torch.float32, device=dev)
-                      for k, n in self.per_seq.items()} for _ in range(2)]
+        self.buf = {k: torch.empty(n * ns, dtype=torch.float32, device=dev)
+                    for k, n in self.per_seq.items()}
         self.s_in = torch.cuda.Stream(dev)
         self.s_run = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
-        self.ev_in = [torch.cuda.Event() for _ in range(2)]
-        self.ev_run = [torch.cuda.Event() for _ in range(2)]
-        self.ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def h2d_bytes(self) -> int:
-        return 4 * self.ns * sum(self.per_seq[k] for k in ("q", "k", "v", "g", "beta", "state_in"))
+        return 4 * self.ns * sum(self.per_seq[k] for k in self.SMALL_INPUTS + ("state_in",))
 
     def d2h_bytes(self) -> int:
         return 4 * self.ns * (self.per_seq["output"] + self.per_seq["state_out"])
 
     def __call__(self, q, k, v, g, beta, state_in, output, state_out, stream=None):
         """Inputs and outputs: flat f32 pinned host tensors in the layouts of
-        include/gdn.h.  Work is enqueued after `stream` (default: the current
-        stream), which waits for all of it before returning control on the
-        GPU; the host does not block."""
+        include/gdn.h.  Work is ordered after `stream` (default: the current
+        stream), and `stream` waits for all of it; the host does not block."""
         import torch
         host = dict(q=q, k=k, v=v, g=g, beta=beta, state_in=state_in, output=output,
                     state_out=state_out)
@@ -259,30 +258,32 @@ class HostPipeline:
         base = torch.cuda.current_stream(self.device) if stream is None else stream
         for s in (self.s_in, self.s_run, self.s_out):
             s.wait_stream(base)
-        groups = [(s0, min(self.group, self.ns - s0)) for s0 in range(0, self.ns, self.group)]
-        for i, (s0, n) in enumerate(groups):
-            b = i & 1
-            buf = self.bufs[b]
-            p = self.params.copy()
-            p[5] = n
+        buf = self.buf
+        with torch.cuda.stream(self.s_in):
+            for name in self.SMALL_INPUTS:
+                buf[name].copy_(host[name], non_blocking=True)
+        m_st = self.per_seq["state_in"]
+        for s0 in range(0, self.ns, self.group):
+            n = min(self.group, self.ns - s0)
+            sl = slice(s0 * m_st, (s0 + n) * m_st)
             with torch.cuda.stream(self.s_in):
-                if i >= 2:
-                    self.s_in.wait_event(self.ev_out[b])  # buffer b's previous output copied out
-                for name in ("q", "k", "v", "g", "beta", "state_in"):
-                    m = self.per_seq[name]
-                    buf[name][: m * n].copy_(host[name][s0 * m:(s0 + n) * m], non_blocking=True)
-                self.ev_in[b].record(self.s_in)
+                buf["state_in"][sl].copy_(host["state_in"][sl], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(self.s_in)
             with torch.cuda.stream(self.s_run):
-                self.s_run.wait_event(self.ev_in[b])
-                gdn_forward(*(buf[x][: self.per_seq[x] * n] for x in
-                              ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")),
-                            p, stream=self.s_run)
-                self.ev_run[b].record(self.s_run)
+                self.s_run.wait_event(ev_in)
+                p = self.params.copy()
+                p[5] = n
+                args = [buf[x][s0 * self.per_seq[x]:(s0 + n) * self.per_seq[x]] for x in
+                        ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+                gdn_forward(*args, p, stream=self.s_run)
+                ev_run = torch.cuda.Event()
+                ev_run.record(self.s_run)
             with torch.cuda.stream(self.s_out):
-                self.s_out.wait_event(self.ev_run[b])
-                for name in ("output", "state_out"):
-                    m = self.per_seq[name]
-                    host[name][s0 * m:(s0 + n) * m].copy_(buf[name][: m * n], non_blocking=True)
-                self.ev_out[b].record(self.s_out)
+                self.s_out.wait_event(ev_run)
+                host["state_out"][sl].copy_(buf["state_out"][sl], non_blocking=True)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_stream(self.s_run)
+            host["output"].copy_(buf["output"], non_blocking=True)
         for s in (self.s_in, self.s_run, self.s_out):
             base.wait_stream(s)

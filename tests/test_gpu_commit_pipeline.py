@@ -59,8 +59,8 @@ def test_commit_gathers_accepted_slice(torch, oracle_mod, name, ns):
                  np.stack([rc[s, idx[s]] for s in sel]), w.n_tokens)
 
 
-@pytest.mark.parametrize("group", [1, 3, 8, 64])
-def test_host_pipeline_equals_device_call(torch, group):
+@pytest.mark.parametrize("groups", [1, 3, 4, 19, 64])
+def test_host_pipeline_equals_device_call(torch, groups):
     from serving_gdn_decode_gb300 import _native as nat
     w = Workload("pipe", 128, 128, 4, 8, 2, 19)
     x = make_inputs(w, 7)
@@ -69,7 +69,7 @@ def test_host_pipeline_equals_device_call(torch, group):
     host = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
     out = torch.zeros(w.v_elems, dtype=torch.float32).pin_memory()
     st = torch.zeros(w.state_elems, dtype=torch.float32).pin_memory()
-    pipe = nat.HostPipeline(p, max_group=group)
+    pipe = nat.HostPipeline(p, groups=groups)
     for _ in range(2):  # buffers are reused across calls
         pipe(host["q"], host["k"], host["v"], host["g"], host["beta"], host["state_in"], out, st)
         torch.cuda.synchronize()
