@@ -290,7 +290,7 @@ def time_e2e(torch, nat, w, params, steps, device):
 
 
 def extras(torch, nat, peak_gbs, device):
-    from serving_gdn_decode_gb300.params import PATH_SCAN
+    from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN
     from serving_gdn_decode_gb300.workloads import WORKLOADS
     res = {}
 
@@ -345,7 +345,8 @@ def extras(torch, nat, peak_gbs, device):
     torch.cuda.empty_cache()
 
     wp = WORKLOADS["long_prefill"]
-    for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),):
+    for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),
+                        ("long_prefill_chunked", wp.params(path=PATH_CHUNKED))):
         sets = make_sets(torch, wp, 1, device)
         steps = 5
         t, _ = time_graphed(torch, nat, sets, params, steps, 2)

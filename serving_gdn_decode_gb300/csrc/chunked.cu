@@ -1,0 +1,727 @@
+// Chunked (WY / UT-transform) prefill of the Gated DeltaNet recurrence on the
+// 5th-generation tensor cores of sm_103a (tcgen05.mma kind::tf32, TMEM
+// accumulators), for D_k = D_v = 128.
+//
+// The recurrence is the token-by-token one of the capture kernel page
+// ("gated_delta_net_decode_capture.metal", mlx-native 0.9.2, decay-first) or
+// of the module doc of "gated_delta_net.rs" (mlx-native 0.4.0, decay-after).
+// Over a chunk of C = 64 tokens it is rewritten exactly (up to rounding) in
+// matrix form.  With S the state entering the chunk (D_v x D_k, row = d_v),
+// G_r = sum_{tau<=r} g_tau, gamma_r = exp(-G_r), Gam_{r,i} = exp(G_i - G_r):
+//
+//   A_{r,i}  = beta_r * Gam_{r,i} * (k_r . k_i)       (i < r; decay-after:
+//              Gam_{r-1,i} and gamma_{r-1} below)      T = (I + A)^-1
+//   U        = T diag(beta) V  -  T diag(beta gamma) K S^T       (C x D_v)
+//   Y        = q_scale [diag(gamma) Q S^T + (Q K^T o Gam)_{i<=r} U]
+//   S_next   = gamma_C S + U^T diag(Gam_{C,.}) K
+//
+// (the pseudo-values U are the per-token delta's; substituting the recurrence
+// into itself gives exactly these sums).  Every product with a dimension of
+// 128 runs on the tensor cores with M = 128 (D_v or the stacked [K;Q]):
+//
+//   G   = [K;Q] K^T              (Gram: rows 0..63 = K K^T, 64..127 = Q K^T)
+//   Ut  = V^T  T''^T              T''= T diag(beta)        (A = V^T from TMEM)
+//   X   = S K^T                                           (A = S from TMEM)
+//   Ut += X (-T')^T               T' = c T diag(beta gamma) (A = X from TMEM)
+//   Yt  = S Q'^T                  Q' = c q_scale diag(gamma) Q
+//   Yt += Ut P'^T                 P' = q_scale (Q K^T o Gam)  (A = Ut from TMEM)
+//   S  += Ut K'^T                 K' = diag(Gam_C / c_next) K
+//
+// where Ut = U^T, Yt = Y^T (D_v x C) live in TMEM, and S is kept lazily as
+// c * S (c = product of the chunk decays since the last fold), so the decay
+// never needs a read-modify-write of TMEM; c is folded into S when it leaves
+// [2^-30, 2^30], and a chunk whose |G| exceeds 40 (extreme gates) folds its
+// decay into S before the update instead.  Operands are rounded to TF32
+// (round-to-nearest) when staged in shared memory; accumulation is f32.
+// The triangular inverse (64 x 64) runs on the CUDA cores, blocked 16 x 16.
+//
+// One CTA (8 warps) owns one (seq, value head) for the whole token range;
+// TMEM: S 128 cols, X 64, Ut 64, Yt 64, G 64, V^T 64 (512 allocated).
+// Shared-memory operands use the canonical K-major no-swizzle layout:
+// 8-row x 16-byte core matrices, cores adjacent along K (LBO = 128 B), core
+// rows SBO = (K/4)*128 B apart.  Every mbarrier wait is bounded; on a timeout
+// the CTA writes NaN to its state_out, frees its TMEM and returns.
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int C = 64;     // tokens per chunk
+constexpr int D = 128;    // D_k = D_v
+constexpr int NTH = 256;  // threads per CTA
+constexpr int LD = 68;    // row stride (floats) of the plain 64 x 64 work matrices
+constexpr float kMaxLogScale = 40.f;
+constexpr float kRenormLo = 9.3132257e-10f;  // 2^-30
+constexpr float kRenormHi = 1.0737418e+09f;  // 2^30
+
+// TMEM columns
+constexpr uint32_t TM_S = 0, TM_X = 128, TM_U = 192, TM_Y = 256, TM_G = 320, TM_V = 384;
+constexpr uint32_t TM_COLS = 512;
+
+// shared memory map (bytes)
+constexpr uint32_t SM_STACK = 0;                     // [K;Q] 128 x 128 canonical, 64 KB
+constexpr uint32_t SM_KT = SM_STACK + 65536;         // K'^T 128 x 64 canonical, 32 KB
+constexpr uint32_t SM_P = SM_KT + 32768;             // P'   64 x 64 canonical, 16 KB
+constexpr uint32_t SM_A = SM_P + 16384;              // A plain 64 x LD; then -T' (canonical)
+constexpr uint32_t SM_T = SM_A + 64 * LD * 4;        // T plain 64 x LD; then T'' (canonical)
+constexpr uint32_t SM_M = SM_T + 64 * LD * 4;        // block products, 3 x 256 f32
+constexpr uint32_t SM_SC = SM_M + 3 * 256 * 4;       // per-token scalars
+constexpr int NSC = 11;                              // scalar arrays of 64
+constexpr uint32_t SM_MISC = SM_SC + NSC * 64 * 4;   // mbarrier, tmem base, flags
+constexpr int LDS = 132;                             // staging row stride (floats): 528 B, so the
+                                                     // 8 rows of a core matrix hit distinct banks
+constexpr uint32_t SM_KS = SM_MISC + 64;             // next chunk's K rows (natural), 64 x LDS
+constexpr uint32_t SM_VS = SM_KS + 64 * LDS * 4;     // next chunk's V rows (natural), 64 x LDS
+constexpr uint32_t SMEM_BYTES = SM_VS + 64 * LDS * 4;
+constexpr uint32_t SM_TP = SM_A;                     // -T' canonical (16 KB) over the dead A
+constexpr uint32_t SM_TPP = SM_T;                    // T''  canonical (16 KB) over the dead T
+
+// scalar array slots
+enum { SC_G = 0, SC_GAM, SC_GAMP, SC_BETA, SC_KTS, SC_TPS, SC_QS, SC_GPREV, SC_EG, SC_GRAW, SC_BRAW };
+
+struct ChunkArgs {
+  const float *__restrict__ q;
+  const float *__restrict__ k;
+  const float *__restrict__ v;
+  const float *__restrict__ g;
+  const float *__restrict__ beta;
+  const float *state_in;
+  float *__restrict__ output;
+  float *state_out;
+  uint32_t nk, nv, nt, group, khead_div;
+  float q_scale;
+};
+
+struct Misc {
+  unsigned long long mbar;
+  uint32_t tmem_base;
+  int failed;
+  float c_renorm;   // factor folded into S at the chunk start (if do_renorm)
+  float c_fold;     // factor folded into S before the update (if do_fold)
+  float c_next;     // scale after this chunk
+  int do_renorm;
+  int do_fold;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+// canonical K-major no-swizzle byte offset of element (row, k) in a matrix
+// whose K extent is KE elements
+__device__ __forceinline__ uint32_t canon(int row, int kk, int KE) {
+  return static_cast<uint32_t>(((row >> 3) * (KE >> 2) + (kk >> 2)) * 128 + (row & 7) * 16 + (kk & 3) * 4);
+}
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+               :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(mbar) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void cta_sync() {
+  fence_before();
+  __syncthreads();
+  fence_after();
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase: about a second of clock at most.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t done;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.u32 %0, 1, 0, p;\n}\n" : "=r"(done) : "r"(mbar), "r"(phase) : "memory");
+    if (done) return true;
+    if (clock64() - t0 > 2000000000LL) return false;
+  }
+}
+
+#define GDN_TMEM_LD32(taddr, v)                                                                \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11," \
+               "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"   \
+               "%31}, [%32];\n"                                                                 \
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),        \
+                 "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),      \
+                 "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),  \
+                 "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),  \
+                 "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),  \
+                 "=r"(v[30]), "=r"(v[31])                                                       \
+               : "r"(taddr))
+#define GDN_TMEM_ST32(taddr, v)                                                                 \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10," \
+               "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"  \
+               "%30,%31,%32};\n"                                                               \
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), \
+                  "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),          \
+                  "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),      \
+                  "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),      \
+                  "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),      \
+                  "r"(v[30]), "r"(v[31]))
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Scale the 64 TMEM columns [col, col+64) of this warp's 32 lanes by f.
+__device__ __forceinline__ void tmem_scale64(uint32_t taddr, float f) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[32];
+    GDN_TMEM_LD32(taddr + 32 * h, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+    GDN_TMEM_ST32(taddr + 32 * h, v);
+  }
+  tmem_wait_st();
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 A (plain, row stride LD), with
+// 16 x 16 blocks: the diagonal blocks by forward substitution (one thread per
+// column), then T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj level by level
+// (i - j = 1, 2, 3), one warp per block, each lane a 2 x 4 register tile.
+// M is 3 x 256 floats of per-warp scratch.
+__device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
+  // the six blocks above the diagonal stay zero
+  for (int e = tid; e < 6 * 256; e += NTH) {
+    const int b = e >> 8, rr = (e & 255) >> 4, cc = e & 15;
+    const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2), bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+    T[(16 * bi + rr) * LD + 16 * bj + cc] = 0.f;
+  }
+  if (tid < 64) {
+    const int base = 16 * (tid >> 4), cl = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+      for (int i = 0; i < r; ++i) acc = fmaf(-A[(base + r) * LD + base + i], x[i], acc);
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) T[(base + r) * LD + base + cl] = x[r];
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);  // this lane's 2 x 4 tile of a block
+  for (int d = 1; d <= 3; ++d) {
+    if (warp < 4 - d) {
+      const int j = warp, i = j + d;
+      float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kb = j; kb < i; ++kb) {
+        const float *a0 = A + (16 * i + tr) * LD + 16 * kb;
+        const float *tb = T + (16 * kb) * LD + 16 * j + tc;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float x0 = a0[q], x1 = a0[LD + q];
+          const float4 b = *reinterpret_cast<const float4 *>(tb + q * LD);
+          m0[0] = fmaf(x0, b.x, m0[0]); m0[1] = fmaf(x0, b.y, m0[1]);
+          m0[2] = fmaf(x0, b.z, m0[2]); m0[3] = fmaf(x0, b.w, m0[3]);
+          m1[0] = fmaf(x1, b.x, m1[0]); m1[1] = fmaf(x1, b.y, m1[1]);
+          m1[2] = fmaf(x1, b.z, m1[2]); m1[3] = fmaf(x1, b.w, m1[3]);
+        }
+      }
+      float *mw = M + warp * 256;
+      *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
+      *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
+      __syncwarp();
+      // T_ij = -T_ii M: T_ii is lower triangular (its upper entries are stored zeros)
+      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+      const float *li = T + (16 * i + tr) * LD + 16 * i;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q <= tr + 1) {
+          const float l0 = li[q], l1 = li[LD + q];
+          const float4 mm = *reinterpret_cast<const float4 *>(mw + q * 16 + tc);
+          t0[0] = fmaf(l0, mm.x, t0[0]); t0[1] = fmaf(l0, mm.y, t0[1]);
+          t0[2] = fmaf(l0, mm.z, t0[2]); t0[3] = fmaf(l0, mm.w, t0[3]);
+          t1[0] = fmaf(l1, mm.x, t1[0]); t1[1] = fmaf(l1, mm.y, t1[1]);
+          t1[2] = fmaf(l1, mm.z, t1[2]); t1[3] = fmaf(l1, mm.w, t1[3]);
+        }
+      }
+      float *to = T + (16 * i + tr) * LD + 16 * j + tc;
+      *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
+      *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
+    }
+    __syncthreads();
+  }
+}
+
+// Asynchronous copies of one chunk's Q rows into the stack's Q half
+// (canonical layout, rows 64..127), and of its gates and betas into the
+// scalar area; tokens past the chunk's end are zero-filled.
+__device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const float *qbase, size_t kq_tok,
+                                                        const float *g, const float *beta, size_t sc0,
+                                                        size_t nv, int nc, int tid) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int cc = tid + NTH * it;        // 16-byte chunk within the Q half
+    const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
+    cp_async16(sbase + SM_STACK + 32768 + cc * 16, qbase + (r < nc ? r : 0) * kq_tok + 4 * c4,
+               r < nc ? 16u : 0u);
+  }
+  if (tid < 128) {
+    const int i = tid & 63;
+    const size_t src = sc0 + static_cast<size_t>(i < nc ? i : 0) * nv;
+    cp_async4(sbase + SM_SC + ((tid < 64 ? SC_GRAW : SC_BRAW) * 64 + i) * 4,
+              (tid < 64 ? g : beta) + src, i < nc ? 4u : 0u);
+  }
+  cp_async_commit();
+}
+
+// Asynchronous copies of one chunk's K and V rows (natural layout: 64 rows
+// of 512 bytes each) into the staging buffers; rows past the end are zeros.
+__device__ __forceinline__ void stage_kv_async(uint32_t sbase, const float *kbase, size_t kq_tok,
+                                               const float *vbase, size_t v_tok, int nc, int tid) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int ci = tid + NTH * it;        // 16-byte chunk: row ci/32, float4 ci%32
+    const int r = ci >> 5, c4 = ci & 31;
+    const uint32_t n = r < nc ? 16u : 0u;
+    const int rr = r < nc ? r : 0;
+    const uint32_t dst = static_cast<uint32_t>((r * LDS + 4 * c4) * 4);
+    cp_async16(sbase + SM_KS + dst, kbase + rr * kq_tok + 4 * c4, n);
+    cp_async16(sbase + SM_VS + dst, vbase + rr * v_tok + 4 * c4, n);
+  }
+  cp_async_commit();
+}
+
+template <bool DECAY_AFTER>
+__global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *sA = reinterpret_cast<float *>(smem + SM_A);
+  float *sT = reinterpret_cast<float *>(smem + SM_T);
+  float *sM = reinterpret_cast<float *>(smem + SM_M);
+  float *sc = reinterpret_cast<float *>(smem + SM_SC);
+  const float *sKS = reinterpret_cast<const float *>(smem + SM_KS);
+  const float *sVS = reinterpret_cast<const float *>(smem + SM_VS);
+  Misc *misc = reinterpret_cast<Misc *>(smem + SM_MISC);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t mbar = smem_addr(&misc->mbar);
+
+  const int tid = static_cast<int>(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;          // TMEM lane of this thread (= d_v or a Gram row)
+  const int half = tid >> 7;          // which half of a 64-column group this thread handles
+  const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+  const uint32_t head = blockIdx.x;   // = s * nv + vh
+  const uint32_t vh = head % a.nv, s = head / a.nv;
+  const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
+  const uint32_t nt = a.nt;
+  const size_t state_head = static_cast<size_t>(head) * D * D;
+  const size_t kq_tok = static_cast<size_t>(a.nk) * D;
+  const size_t v_tok = static_cast<size_t>(a.nv) * D;
+  const float *kseq = a.k + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;  // token 0 of this seq
+  const float *qseq = a.q + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
+  const float *vseq = a.v + ((static_cast<size_t>(s) * nt) * a.nv + vh) * D;
+  const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
+  const uint32_t nchunks = (nt + C - 1) / C;
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    misc->failed = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(&misc->tmem_base)), "r"(TM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // chunk 0's inputs start arriving while the state is loaded
+  {
+    const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
+    stage_kv_async(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
+    stage_q_and_gates_async(sbase, qseq, kq_tok, a.g, a.beta, sc_first, a.nv, nc0, tid);
+  }
+  cta_sync();
+  const uint32_t tmem = misc->tmem_base;
+  const uint32_t tl = tmem + lane_field;  // this warp's lane quarter
+
+  // S <- state_in (c = 1).  Thread: row d_v, columns [64*half, 64*half + 64).
+  {
+    const float4 *src = reinterpret_cast<const float4 *>(a.state_in + state_head + row * D + 64 * half);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = __ldcs(src + 8 * h + j);
+        v[4 * j] = __float_as_uint(x.x); v[4 * j + 1] = __float_as_uint(x.y);
+        v[4 * j + 2] = __float_as_uint(x.z); v[4 * j + 3] = __float_as_uint(x.w);
+      }
+      GDN_TMEM_ST32(tl + TM_S + 64 * half + 32 * h, v);
+    }
+    tmem_wait_st();
+  }
+
+  float c = 1.f;          // S = c * (TMEM S)
+  uint32_t phase = 0;
+  bool failed = false;
+
+  for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
+    const uint32_t t0 = ch * C;
+    const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
+
+    // ---- 0. this chunk's staged inputs (K, V rows, Q half, gates) have landed
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- 1. per-token scalars (warp 0): prefix sums of g, decays, scalings
+    if (warp == 0) {
+      float g0 = sc[SC_GRAW * 64 + lane], g1 = sc[SC_GRAW * 64 + lane + 32];
+      const float b0 = sc[SC_BRAW * 64 + lane], b1 = sc[SC_BRAW * 64 + lane + 32];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, g0, o), u1 = __shfl_up_sync(0xffffffffu, g1, o);
+        if (lane >= o) { g0 += u0; g1 += u1; }
+      }
+      g1 += __shfl_sync(0xffffffffu, g0, 31);
+      const float G0 = g0, G1 = g1;               // inclusive prefix sums, tokens lane, lane+32
+      const float GC = __shfl_sync(0xffffffffu, G1, 31);  // = G of the last (or padded) token
+      float Gp0 = __shfl_up_sync(0xffffffffu, G0, 1);
+      if (lane == 0) Gp0 = 0.f;
+      float Gp1 = __shfl_up_sync(0xffffffffu, G1, 1);
+      const float G0_last = __shfl_sync(0xffffffffu, G0, 31);  // every lane takes part
+      if (lane == 0) Gp1 = G0_last;
+      const bool extreme = __any_sync(0xffffffffu, fabsf(G0) > kMaxLogScale || fabsf(G1) > kMaxLogScale);
+      // fold c into S at the chunk start if it left [2^-30, 2^30]
+      float cc = c, renorm = 1.f;
+      const bool do_renorm = cc < kRenormLo || cc > kRenormHi;
+      if (do_renorm) { renorm = cc; cc = 1.f; }
+      const float gamC = __expf(-GC);
+      float cnext, fold = 1.f;
+      if (extreme) { fold = cc * gamC; cnext = 1.f; }
+      else { cnext = cc * gamC; }
+      const float gam0 = __expf(-G0), gam1 = __expf(-G1);
+      const float gp0 = __expf(-Gp0), gp1 = __expf(-Gp1);
+      sc[SC_G * 64 + lane] = G0; sc[SC_G * 64 + lane + 32] = G1;
+      sc[SC_GPREV * 64 + lane] = Gp0; sc[SC_GPREV * 64 + lane + 32] = Gp1;
+      sc[SC_GAM * 64 + lane] = gam0; sc[SC_GAM * 64 + lane + 32] = gam1;
+      sc[SC_GAMP * 64 + lane] = gp0; sc[SC_GAMP * 64 + lane + 32] = gp1;
+      sc[SC_BETA * 64 + lane] = b0; sc[SC_BETA * 64 + lane + 32] = b1;
+      // e^{G_i} (only used when |G| <= 40, where it cannot overflow)
+      sc[SC_EG * 64 + lane] = __expf(G0); sc[SC_EG * 64 + lane + 32] = __expf(G1);
+      // K' row scale: Gam_{C,i} / c_next (lazy) or Gam_{C,i} (after a fold)
+      sc[SC_KTS * 64 + lane] = __expf(G0 - GC) / cnext;
+      sc[SC_KTS * 64 + lane + 32] = __expf(G1 - GC) / cnext;
+      // -T' column scale: -c beta_i gamma_i (decay-after: gamma_{i-1})
+      sc[SC_TPS * 64 + lane] = -cc * b0 * (DECAY_AFTER ? gp0 : gam0);
+      sc[SC_TPS * 64 + lane + 32] = -cc * b1 * (DECAY_AFTER ? gp1 : gam1);
+      // Q' row scale: c q_scale gamma_r
+      sc[SC_QS * 64 + lane] = cc * a.q_scale * gam0;
+      sc[SC_QS * 64 + lane + 32] = cc * a.q_scale * gam1;
+      if (lane == 0) {
+        misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext;
+        misc->do_renorm = do_renorm; misc->do_fold = extreme;
+      }
+    }
+    __syncthreads();
+    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
+    const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
+
+    // ---- 2. fold c into S if needed (no MMA in flight here)
+    if (do_renorm) tmem_scale64(tl + TM_S + 64 * half, c_renorm);
+
+    // ---- 3. operands from the staged rows: the stack's K half (canonical,
+    // TF32), the Q half rounded in place, K'^T (smem), V^T (TMEM)
+    {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int ci = tid + NTH * it;        // 16-byte chunk of the K half
+        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
+        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
+        x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
+        *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
+        float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
+        float4 y = *pq;
+        y.x = tf32_rna(y.x); y.y = tf32_rna(y.y); y.z = tf32_rna(y.z); y.w = tf32_rna(y.w);
+        *pq = y;
+      }
+      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
+      const float *kts = sc + SC_KTS * 64;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = 32 * half + 4 * j;
+        *reinterpret_cast<float4 *>(smem + SM_KT + canon(row, i, 64)) =
+            make_float4(tf32_rna(sKS[(i + 0) * LDS + row] * kts[i + 0]),
+                        tf32_rna(sKS[(i + 1) * LDS + row] * kts[i + 1]),
+                        tf32_rna(sKS[(i + 2) * LDS + row] * kts[i + 2]),
+                        tf32_rna(sKS[(i + 3) * LDS + row] * kts[i + 3]));
+      }
+      // V^T -> TMEM (lane d_v = row, columns = tokens [32*half, +32))
+      uint32_t vv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * LDS + row]));
+      GDN_TMEM_ST32(tl + TM_V + 32 * half, vv);
+      tmem_wait_st();
+    }
+    fence_async_smem();
+    cta_sync();
+    // the staging buffers are free: start the next chunk's K and V rows
+    if (ch + 1 < nchunks) {
+      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+      stage_kv_async(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
+    }
+
+    // ---- 4. Gram [K;Q] K^T -> TMEM G
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks) {
+        const uint64_t d = sdesc(sbase + SM_STACK + ks * 256, 4096);
+        mma_ss(tmem + TM_G, d, d, idesc_tf32(128, 64), ks > 0);
+      }
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+
+    // ---- 5. A (plain), P' (canonical), Q' (in place)
+    {
+      uint32_t gv[32];
+      GDN_TMEM_LD32(tl + TM_G + 32 * half, gv);
+      tmem_wait_ld();
+      const float *G = sc + SC_G * 64, *eG = sc + SC_EG * 64;
+      if (row < 64) {
+        const int r = row;
+        const float br = sc[SC_BETA * 64 + r];
+        // Gam_{r,i} = e^{G_i - G_r} (decay-after: G_{r-1}); products of e^{G_i}
+        // and e^{-G_r} when |G| <= 40, exponentials of differences otherwise
+        const float Gr = DECAY_AFTER ? sc[SC_GPREV * 64 + r] : G[r];
+        const float bgr = br * (DECAY_AFTER ? sc[SC_GAMP * 64 + r] : sc[SC_GAM * 64 + r]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 32 * half + 4 * j + u;
+            const float gam = do_fold ? br * __expf(G[i] - Gr) : bgr * eG[i];
+            e[u] = i < r ? gam * __uint_as_float(gv[4 * j + u]) : 0.f;
+          }
+          *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
+        }
+      } else {
+        const int r = row - 64;
+        const float Gr = G[r];
+        const float qgr = a.q_scale * sc[SC_GAM * 64 + r];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 32 * half + 4 * j + u;
+            const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+            e[u] = i <= r ? tf32_rna(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+          }
+          *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
+              make_float4(e[0], e[1], e[2], e[3]);
+        }
+      }
+      // Q' = c q_scale gamma_r Q, in place in the stack's Q half (rows 64..127)
+      const float *qs = sc + SC_QS * 64;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int cc = tid + NTH * it;        // chunk within the Q half
+        const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7);
+        float4 *p = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + cc * 16);
+        float4 x = *p;
+        const float f = qs[r];
+        x.x = tf32_rna(x.x * f); x.y = tf32_rna(x.y * f); x.z = tf32_rna(x.z * f); x.w = tf32_rna(x.w * f);
+        *p = x;
+      }
+    }
+    cta_sync();
+
+    // ---- 6. T = (I + A)^-1, then -T' (over A) and T'' (over T), canonical
+    tri_inverse(sA, sT, sM, tid);
+    {
+      const float *tps = sc + SC_TPS * 64, *bet = sc + SC_BETA * 64;
+      float4 t[4];
+      int ci[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        ci[it] = tid + NTH * it;              // 16-byte chunk of a 64 x 64 canonical image
+        const int core = ci[it] >> 3, r = (core >> 4) * 8 + (ci[it] & 7), i0 = 4 * (core & 15);
+        t[it] = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+      }
+      __syncthreads();                        // every thread has read T before it is overwritten
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int i0 = 4 * ((ci[it] >> 3) & 15);
+        *reinterpret_cast<float4 *>(smem + SM_TP + ci[it] * 16) =
+            make_float4(tf32_rna(t[it].x * tps[i0]), tf32_rna(t[it].y * tps[i0 + 1]),
+                        tf32_rna(t[it].z * tps[i0 + 2]), tf32_rna(t[it].w * tps[i0 + 3]));
+        *reinterpret_cast<float4 *>(smem + SM_TPP + ci[it] * 16) =
+            make_float4(tf32_rna(t[it].x * bet[i0]), tf32_rna(t[it].y * bet[i0 + 1]),
+                        tf32_rna(t[it].z * bet[i0 + 2]), tf32_rna(t[it].w * bet[i0 + 3]));
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+    if (misc->failed) { failed = true; break; }
+
+    // ---- 7. the state-dependent products.  Batch 1 builds U^T and the
+    // inter-chunk output; then U^T is rounded to TF32 (nearest) in place -- the
+    // tensor core would otherwise truncate it as an A operand -- and, for an
+    // extreme-gate chunk, the chunk's decay is folded into S; batch 2 adds the
+    // intra-chunk output and updates S.
+    if (tid == 0) {
+      const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
+        mma_ts(tmem + TM_U, tmem + TM_V + 8 * ks, sdesc(sbase + SM_TPP + ks * 256, 2048), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
+        mma_ts(tmem + TM_X, tmem + TM_S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
+        mma_ts(tmem + TM_U, tmem + TM_X + 8 * ks, sdesc(sbase + SM_TP + ks * 256, 2048), i64, 1);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
+        mma_ts(tmem + TM_Y, tmem + TM_S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
+               ks > 0);
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+    __syncthreads();
+    if (misc->failed) { failed = true; break; }
+    // the stack's Q half is free now: start the next chunk's Q rows and gates
+    if (ch + 1 < nchunks) {
+      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+      stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                              sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+    }
+    {
+      uint32_t uv[32];
+      GDN_TMEM_LD32(tl + TM_U + 32 * half, uv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rna(__uint_as_float(uv[j])));
+      GDN_TMEM_ST32(tl + TM_U + 32 * half, uv);
+      tmem_wait_st();
+    }
+    if (do_fold) tmem_scale64(tl + TM_S + 64 * half, c_fold);  // extreme gates: decay S now
+    cta_sync();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)   // Yt += Ut P'^T
+        mma_ts(tmem + TM_Y, tmem + TM_U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048),
+               idesc_tf32(128, 64), 1);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)   // S += Ut K'^T
+        mma_ts(tmem + TM_S, tmem + TM_U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
+               idesc_tf32(128, 128), 1);
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+
+    // ---- 8. outputs: thread = d_v, tokens [32*half, +32)
+    {
+      uint32_t yv[32];
+      GDN_TMEM_LD32(tl + TM_Y + 32 * half, yv);
+      tmem_wait_ld();
+      float *obase = a.output + ((static_cast<size_t>(s) * nt + t0) * a.nv + vh) * D + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int i = 32 * half + j;
+        if (i < nc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      }
+    }
+    c = misc->c_next;
+    cta_sync();
+    if (misc->failed) failed = true;
+  }
+
+  cp_async_wait_all();  // no copy may still be landing in shared memory at exit
+
+  // ---- state_out = c * S (or NaN if a wait timed out)
+  {
+    float4 *dst = reinterpret_cast<float4 *>(a.state_out + state_head + row * D + 64 * half);
+    const float f = failed ? __int_as_float(0x7fc00000) : c;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+      GDN_TMEM_LD32(tl + TM_S + 64 * half + 32 * h, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        __stcs(dst + 8 * h + j, make_float4(__uint_as_float(v[4 * j]) * f, __uint_as_float(v[4 * j + 1]) * f,
+                                            __uint_as_float(v[4 * j + 2]) * f, __uint_as_float(v[4 * j + 3]) * f));
+    }
+  }
+  cta_sync();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TM_COLS));
+}
+
+template <bool DA>
+cudaError_t launch(const Problem &p, cudaStream_t stream) {
+  ChunkArgs a;
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
+  a.state_in = p.state_in; a.output = p.output; a.state_out = p.state_out;
+  a.nk = p.nk; a.nv = p.nv; a.nt = p.nt;
+  a.group = p.nv / p.nk;
+  a.khead_div = p.khead_div ? 1u : 0u;
+  a.q_scale = p.q_scale;
+  const unsigned long long blocks = static_cast<unsigned long long>(p.nv) * p.ns;
+  if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  auto kern = gdn_chunked_kernel<DA>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(blocks), NTH, SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunked_supported(const Problem &p) { return p.dk == 128 && p.dv == 128 && p.capture == nullptr; }
+
+cudaError_t launch_chunked(const Problem &p, cudaStream_t stream) {
+  if (!chunked_supported(p)) return cudaErrorInvalidValue;
+  return p.decay_after ? launch<true>(p, stream) : launch<false>(p, stream);
+}
+
+}  // namespace gdn

@@ -109,11 +109,12 @@ gdn_status decode_params(const uint32_t *params, size_t n_params, Decoded *d) {
   return GDN_OK;
 }
 
-enum class Path { kDecode, kScan };
+enum class Path { kDecode, kScan, kChunked };
 
 const char *path_name(Path path, bool capture) {
   switch (path) {
     case Path::kDecode: return capture ? "token_loop_decode_capture" : "token_loop_decode";
+    case Path::kChunked: return "chunked";
     default: return capture ? "scan_capture" : "scan";
   }
 }
@@ -126,7 +127,10 @@ gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
     case GDN_PATH_CHUNKED:
       if (capture)
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path keeps no per-token state (capture)");
-      return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked prefill path is not available");
+      if (d.prob.dk != 128 || d.prob.dv != 128)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path needs D_k = D_v = 128");
+      *out = Path::kChunked;
+      return GDN_OK;
     default:
       *out = d.prob.nt <= kDecodeMaxTokens ? Path::kDecode : Path::kScan;
       return GDN_OK;
@@ -208,8 +212,9 @@ gdn_status run(const float *q, const float *k, const float *v, const float *g, c
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_in = state_in;
   p.output = output; p.state_out = state_out; p.capture = with_capture ? capture : nullptr;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t err =
-      path == Path::kDecode ? gdn::launch_token_loop(p, cs) : gdn::launch_scan(p, cs);
+  const cudaError_t err = path == Path::kDecode    ? gdn::launch_token_loop(p, cs)
+                          : path == Path::kChunked ? gdn::launch_chunked(p, cs)
+                                                   : gdn::launch_scan(p, cs);
   if (err != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
   return GDN_OK;

@@ -27,6 +27,10 @@ cudaError_t launch_token_loop(const Problem &p, cudaStream_t stream);
 // lazy decay; shaped for FP32 issue throughput.
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 
+// Chunked tensor-core prefill (chunked.cu): D_k = D_v = 128, no capture.
+bool chunked_supported(const Problem &p);
+cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
+
 // Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
 // every sequence whose accepted index lies in [0, nt).
 cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,

@@ -106,6 +106,14 @@ def test_chunked_forced_with_capture_is_unsupported(L):
     assert e.value.status == nat.GDN_ERR_UNSUPPORTED
 
 
+def test_chunked_path_shapes(L):
+    assert _path(WORKLOADS["long_prefill"].params(path=PATH_CHUNKED)) == "chunked"
+    for dk, dv in ((64, 64), (128, 64), (32, 32)):
+        with pytest.raises(nat.GdnError) as e:
+            _path(pack_params(dk, dv, 1, 2, 100, 1, path=PATH_CHUNKED))
+        assert e.value.status == nat.GDN_ERR_UNSUPPORTED
+
+
 def test_supported_head_dims(L):
     for dk in (32, 64, 128):
         nsg = dk // 32

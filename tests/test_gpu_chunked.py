@@ -1,0 +1,114 @@
+"""GPU parity of the chunked tensor-core prefill path (forced with path bits
+= 2) against the oracle.
+
+The chunked path rewrites the recurrence in matrix form over 64-token chunks
+and runs its products on tcgen05 with TF32 operands, so it is held to the
+long-window bar (rel-L2 <= 1e-3, plus the max-abs guard) and is used for
+windows of more than 8 tokens only.  Cases: single partial chunk, exact
+chunks, ragged tails, both decay orders and k_head mappings, gates that make
+the kernel fold its lazy scale (large, negative, underflowing), chaining
+calls, and the long-prefill workload at full size on sampled heads.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_close, gather_heads, run_gpu, sample_heads, to_dev
+from serving_gdn_decode_gb300.params import PATH_CHUNKED
+from serving_gdn_decode_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    assert t.cuda.is_available(), "GPU tests need a CUDA device"
+    from serving_gdn_decode_gb300 import build
+    build.build()
+    return t
+
+
+SHAPES = [  # (n_k, n_v, n_tokens, n_seqs)
+    (2, 4, 9, 2),      # one partial chunk
+    (1, 2, 64, 1),     # exactly one chunk
+    (2, 6, 65, 2),     # one chunk + 1 token
+    (4, 8, 200, 2),    # ragged tail
+    (16, 48, 256, 1),  # wide GQA, 4 chunks
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+@pytest.mark.parametrize("flags", [dict(), dict(decay_after=True), dict(khead_div=True),
+                                   dict(decay_after=True, khead_div=True)],
+                         ids=["first-mod", "after-mod", "first-div", "after-div"])
+def test_chunked_vs_oracle(torch, oracle_mod, shape, flags):
+    nk, nv, nt, ns = shape
+    w = Workload("chunked", 128, 128, nk, nv, nt, ns)
+    x = make_inputs(w, 51)
+    p = w.params(path=PATH_CHUNKED, **flags)
+    out, st, _ = run_gpu(w, x, p)
+    ro, rs, _ = oracle_mod.forward(p, **x)
+    assert_close("output", out, ro, max(nt, 9))
+    assert_close("state_out", st, rs, max(nt, 9))
+
+
+@pytest.mark.parametrize("gate", ["large", "negative", "mixed", "zero"])
+@pytest.mark.parametrize("decay_after", [False, True])
+def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after):
+    w = Workload("gates", 128, 128, 2, 4, 300, 2)
+    x = make_inputs(w, 53)
+    rng = np.random.default_rng(55)
+    if gate == "large":
+        x["g"] = rng.uniform(0.0, 4.0, w.scalar_elems).astype(np.float32)
+    elif gate == "negative":
+        # alpha > 1: the state grows (about e^1.5 over the window); TF32
+        # rounding errors grow with it, so the growth is kept mild here (the
+        # FP32 scan path is the one for strongly growing states)
+        x["g"] = rng.uniform(-0.01, 0.0, w.scalar_elems).astype(np.float32)
+    elif gate == "mixed":
+        g = rng.uniform(0.0, 0.5, w.scalar_elems).astype(np.float32)
+        g[::37] = 60.0
+        g[11::101] = 300.0
+        x["g"] = g
+    else:
+        x["g"] = np.zeros(w.scalar_elems, dtype=np.float32)
+    p = w.params(path=PATH_CHUNKED, decay_after=decay_after)
+    out, st, _ = run_gpu(w, x, p)
+    ro, rs, _ = oracle_mod.forward(p, **x)
+    assert_close("output", out, ro, w.n_tokens)
+    assert_close("state_out", st, rs, w.n_tokens)
+
+
+def test_chunked_chaining(torch):
+    w = Workload("chain", 128, 128, 2, 4, 160, 2)
+    x = make_inputs(w, 57)
+    out, st, _ = run_gpu(w, x, w.params(path=PATH_CHUNKED))
+
+    def cut(a, inner, t0, t1):
+        return np.ascontiguousarray(a.reshape(w.n_seqs, w.n_tokens, inner)[:, t0:t1]).reshape(-1)
+
+    def part(t0, t1, state):
+        return {"q": cut(x["q"], w.n_k_heads * w.d_k, t0, t1), "k": cut(x["k"], w.n_k_heads * w.d_k, t0, t1),
+                "v": cut(x["v"], w.n_v_heads * w.d_v, t0, t1), "g": cut(x["g"], w.n_v_heads, t0, t1),
+                "beta": cut(x["beta"], w.n_v_heads, t0, t1), "state_in": state}
+    wa, wb = w.with_(n_tokens=100), w.with_(n_tokens=60)
+    oa, sa, _ = run_gpu(wa, part(0, 100, x["state_in"]), wa.params(path=PATH_CHUNKED))
+    ob, sb, _ = run_gpu(wb, part(100, 160, sa), wb.params(path=PATH_CHUNKED))
+    o = out.reshape(w.n_seqs, w.n_tokens, -1)
+    assert_close("output", oa, o[:, :100].reshape(-1).astype(np.float64), 100)
+    assert_close("output", ob, o[:, 100:].reshape(-1).astype(np.float64), 60)
+    assert_close("state_out", sb, st.astype(np.float64), 160)
+
+
+@pytest.mark.parametrize("flags", [dict(), dict(decay_after=True, khead_div=True)],
+                         ids=["first-mod", "after-div"])
+def test_long_prefill_chunked_sampled(torch, oracle_mod, flags):
+    w = WORKLOADS["long_prefill"]
+    x = make_inputs(w, 0)
+    p = w.params(path=PATH_CHUNKED, **flags)
+    out, st, _ = run_gpu(w, x, p)
+    heads = sample_heads(w, 8, seed=3)
+    ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
+    go, gs, _ = gather_heads(w, out, st, None, heads)
+    assert_close("output", go, ro, w.n_tokens)
+    assert_close("state_out", gs, rs, w.n_tokens)
