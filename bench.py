@@ -31,6 +31,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -344,6 +346,12 @@ def extras(torch, nat, peak_gbs, device):
     del sets, g
     torch.cuda.empty_cache()
 
+    # 32 linear-attention layers of single-token decode: one launch per layer
+    # vs one gdn_forward_layers launch for all of them
+    for S in (1, 8):
+        res[f"decode_32_layers_s{S}"] = layers_case(torch, nat, WORKLOADS["decode"].with_(n_seqs=S),
+                                                    32, peak_gbs, device)
+
     wp = WORKLOADS["long_prefill"]
     for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),
                         ("long_prefill_chunked", wp.params(path=PATH_CHUNKED))):
@@ -358,6 +366,62 @@ def extras(torch, nat, peak_gbs, device):
         del sets
         torch.cuda.empty_cache()
     return res
+
+
+def layers_case(torch, nat, w, n_layers, peak_gbs, device):
+    params = w.params()
+    n_sets = max(2, int(np.ceil(4 * 130e6 / (w.algorithmic_bytes() * n_layers))))
+    sets = []
+    for i in range(n_sets):
+        layers = []
+        for l in range(n_layers):
+            x = make_small_inputs(w, 1000 * i + l)
+            d = {k: torch.from_numpy(v).to(device) for k, v in x.items()}
+            d["output"] = torch.empty(w.v_elems, dtype=torch.float32, device=device)
+            d["state_out"] = d["state_in"]
+            layers.append(d)
+        sets.append(layers)
+    stream = torch.cuda.Stream()
+
+    def per_layer(layers):
+        for d in layers:
+            nat.gdn_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], d["output"],
+                            d["state_out"], params)
+
+    def batched(layers):
+        nat.gdn_forward_layers(layers, params)
+
+    out = {}
+    for name, fn in (("per_layer_launches", per_layer), ("one_launch", batched)):
+        with torch.cuda.stream(stream):
+            for layers in sets:
+                fn(layers)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for layers in sets:
+                    fn(layers)
+            g.replay()
+        torch.cuda.synchronize()
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / (reps * n_sets)   # one forward = all layers of one set
+        gbs = w.algorithmic_bytes() * n_layers / t / 1e9
+        out[name] = {"us_per_forward": round(t * 1e6, 2), "GB_s": round(gbs, 1),
+                     "hbm_frac": round(gbs / peak_gbs, 3)}
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def make_small_inputs(w, seed):
+    from serving_gdn_decode_gb300.workloads import make_inputs
+    return make_inputs(w, seed)
 
 
 def cpu_baseline(w, budget_s=2.0):

@@ -135,6 +135,35 @@ gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, c
                                float *state_capture, size_t state_capture_elems,
                                gdn_stream_t stream);
 
+/* The buffers of one problem (e.g. one linear-attention layer) for
+ * gdn_forward_layers; every pointer is a DEVICE pointer, as in gdn_forward. */
+typedef struct gdn_layer_buffers {
+  const float *q, *k, *v, *g, *beta, *state_in;
+  float *output, *state_out;
+  float *state_capture; /* read only when with_capture != 0 */
+} gdn_layer_buffers;
+
+/*
+ * gdn_forward_layers -- gdn_forward (or gdn_forward_capture when with_capture
+ * != 0) on n_layers problems of the same shape and flags (`params`), such as
+ * the linear-attention layers of one forward pass, which the pages run one
+ * dispatch per layer ("Memory cost" of gated_delta_net_decode_capture.metal:
+ * 30+ linear-attention layers per forward).  On the decode path (n_tokens <=
+ * 16, automatic path) all layers run in one launch per 64 layers, so a
+ * small-batch decode step is not paid for in launch latency; otherwise the
+ * layers are launched one after another.  `layers` is a HOST array of
+ * n_layers entries (1 <= n_layers <= 1024) that the call reads before it
+ * returns.
+ *
+ * Checks: those of gdn_forward / gdn_forward_capture for every layer (the
+ * message names the layer), plus INVALID_ARGUMENT when a layer's output,
+ * state_out or state_capture overlaps any buffer of another layer.
+ * Results are bit-identical to calling gdn_forward once per layer.
+ */
+gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
+                              const uint32_t *params, size_t n_params, int with_capture,
+                              size_t state_capture_elems, gdn_stream_t stream);
+
 /*
  * gdn_commit_capture -- speculative-decode rollback.  After gdn_forward_capture
  * verified n_tokens tokens, make the state after each sequence's last

@@ -30,6 +30,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+class LayerBuffers(ctypes.Structure):
+    """Mirror of gdn_layer_buffers (include/gdn.h)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "beta", "state_in", "output",
+                                                "state_out", "state_capture")]
+
+
 class GdnError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -58,6 +64,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_path_name.restype = ctypes.c_int
             L.gdn_commit_capture.argtypes = [vp, sz, vp, vp, u32p, sz, vp]
             L.gdn_commit_capture.restype = ctypes.c_int
+            L.gdn_forward_layers.argtypes = [ctypes.POINTER(LayerBuffers), sz, u32p, sz, ctypes.c_int,
+                                             sz, vp]
+            L.gdn_forward_layers.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -102,6 +111,16 @@ def forward_capture_raw(q, k, v, g, beta, state_in, output, state_out, params, s
     p, pp, n = _params_arg(params)
     return lib().gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, pp, n,
                                      state_capture, state_capture_elems, stream)
+
+
+def forward_layers_raw(layers, params, with_capture=False, state_capture_elems=0, stream=0) -> int:
+    """Call gdn_forward_layers with per-layer tuples of 9 integer device
+    addresses (q, k, v, g, beta, state_in, output, state_out, state_capture);
+    returns the status."""
+    p, pp, n = _params_arg(params)
+    arr = (LayerBuffers * max(1, len(layers)))(*[LayerBuffers(*lay) for lay in layers])
+    return lib().gdn_forward_layers(arr if layers else None, len(layers), pp, n,
+                                    1 if with_capture else 0, state_capture_elems, stream)
 
 
 def commit_capture_raw(state_capture, state_capture_elems, accepted_idx, state, params,
@@ -197,6 +216,41 @@ def gdn_commit_capture(state_capture, accepted_idx, state, params, stream=None) 
                        "accepted_idx must be a contiguous int32 CUDA tensor of n_seqs entries")
     st = commit_capture_raw(cap, state_capture.numel(), accepted_idx.data_ptr(), stp, params,
                             _stream(stream, state.device))
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+
+
+def gdn_forward_layers(layers, params, with_capture: bool = False, stream=None) -> None:
+    """gdn_forward (or gdn_forward_capture) on several problems of one shape,
+    such as the linear-attention layers of a forward pass: ``layers`` is a list
+    of dicts with torch CUDA tensors under the keys q, k, v, g, beta, state_in,
+    output, state_out (and state_capture when ``with_capture``).  On the decode
+    path all layers run in one launch (per 64 layers)."""
+    s = _sizes(params)
+    rows, cap_elems = [], 0
+    dev = None
+    for i, L in enumerate(layers):
+        ptrs = [_check(f"layers[{i}].q", L["q"], s["qk"]), _check(f"layers[{i}].k", L["k"], s["qk"]),
+                _check(f"layers[{i}].v", L["v"], s["v"]), _check(f"layers[{i}].g", L["g"], s["sc"]),
+                _check(f"layers[{i}].beta", L["beta"], s["sc"]),
+                _check(f"layers[{i}].state_in", L["state_in"], s["state"]),
+                _check(f"layers[{i}].output", L["output"], s["v"]),
+                _check(f"layers[{i}].state_out", L["state_out"], s["state"])]
+        if with_capture:
+            c = L["state_capture"]
+            ptrs.append(_check(f"layers[{i}].state_capture", c, s["state"] * s["nt"],
+                               allow_larger=s["ns"] == 1))
+            if i == 0:
+                cap_elems = c.numel()
+            elif c.numel() != cap_elems:
+                raise GdnError(GDN_ERR_INVALID_ARGUMENT, "state_capture sizes differ between layers")
+        else:
+            ptrs.append(None)
+        rows.append(ptrs)
+        dev = L["q"].device
+    if not rows:
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT, "no layers")
+    st = forward_layers_raw(rows, params, with_capture, cap_elems, _stream(stream, dev))
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 

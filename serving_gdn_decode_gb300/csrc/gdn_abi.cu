@@ -28,6 +28,9 @@ constexpr uint32_t kDecodeMaxTokens = 16;
 // Upper bound on any buffer's element count (keeps byte counts far from
 // 64-bit overflow).
 constexpr unsigned long long kMaxElems = 1ull << 60;
+// Most layers one gdn_forward_layers call takes (the cross-layer overlap check
+// is quadratic in it).
+constexpr size_t kMaxLayers = 1024;
 
 bool mul_ok(unsigned long long a, unsigned long long b, unsigned long long *out) {
   const unsigned __int128 r = static_cast<unsigned __int128>(a) * b;
@@ -238,6 +241,79 @@ gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, c
                                gdn_stream_t stream) {
   return run(q, k, v, g, beta, state_in, output, state_out, params, n_params, state_capture,
              state_capture_elems, true, stream);
+}
+
+gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
+                              const uint32_t *params, size_t n_params, int with_capture,
+                              size_t state_capture_elems, gdn_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (layers == nullptr || n_layers == 0)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: layers is NULL or n_layers is 0");
+  if (n_layers > kMaxLayers)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: n_layers %zu > %zu", n_layers, kMaxLayers);
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  const bool cap = with_capture != 0;
+  Path path;
+  st = choose_path(d, cap, &path);
+  if (st != GDN_OK) return st;
+  for (size_t i = 0; i < n_layers; ++i) {
+    const gdn_layer_buffers &L = layers[i];
+    st = check_buffers(d, L.q, L.k, L.v, L.g, L.beta, L.state_in, L.output, L.state_out,
+                       L.state_capture, state_capture_elems, cap);
+    if (st != GDN_OK) {
+      char msg[sizeof g_last_error];
+      std::snprintf(msg, sizeof msg, "%s", g_last_error);
+      return fail(st, "%s (layer %zu)", msg, i);
+    }
+  }
+  // No layer may write where another layer reads or writes.
+  for (size_t i = 0; i < n_layers; ++i) {
+    const gdn_layer_buffers &A = layers[i];
+    const Span outs[3] = {{A.output, d.v_elems * 4, "output"},
+                          {A.state_out, d.state_elems * 4, "state_out"},
+                          {cap ? A.state_capture : nullptr, cap ? d.capture_elems * 4 : 0,
+                           "state_capture"}};
+    for (size_t j = 0; j < n_layers; ++j) {
+      if (j == i) continue;
+      const gdn_layer_buffers &B = layers[j];
+      const Span all[9] = {{B.q, d.qk_elems * 4, "q"},          {B.k, d.qk_elems * 4, "k"},
+                           {B.v, d.v_elems * 4, "v"},           {B.g, d.sc_elems * 4, "g"},
+                           {B.beta, d.sc_elems * 4, "beta"},    {B.state_in, d.state_elems * 4, "state_in"},
+                           {B.output, d.v_elems * 4, "output"}, {B.state_out, d.state_elems * 4, "state_out"},
+                           {cap ? B.state_capture : nullptr, cap ? d.capture_elems * 4 : 0, "state_capture"}};
+      for (const Span &o : outs) {
+        if (o.p == nullptr) continue;
+        for (const Span &b : all)
+          if (b.p != nullptr && overlap(o, b))
+            return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s of layer %zu overlaps %s of layer %zu",
+                        o.name, i, b.name, j);
+      }
+    }
+  }
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  gdn::Problem batch[gdn::kMaxLayersPerLaunch];
+  for (size_t i0 = 0; i0 < n_layers; i0 += gdn::kMaxLayersPerLaunch) {
+    const size_t n = n_layers - i0 < gdn::kMaxLayersPerLaunch ? n_layers - i0 : gdn::kMaxLayersPerLaunch;
+    for (size_t i = 0; i < n; ++i) {
+      const gdn_layer_buffers &L = layers[i0 + i];
+      gdn::Problem &p = batch[i];
+      p = d.prob;
+      p.q = L.q; p.k = L.k; p.v = L.v; p.g = L.g; p.beta = L.beta; p.state_in = L.state_in;
+      p.output = L.output; p.state_out = L.state_out; p.capture = cap ? L.state_capture : nullptr;
+    }
+    cudaError_t err = cudaSuccess;
+    if (path == Path::kDecode) {
+      err = gdn::launch_token_loop_layers(batch, static_cast<uint32_t>(n), cs);
+    } else {
+      for (size_t i = 0; i < n && err == cudaSuccess; ++i)
+        err = path == Path::kChunked ? gdn::launch_chunked(batch[i], cs) : gdn::launch_scan(batch[i], cs);
+    }
+    if (err != cudaSuccess)
+      return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
+  }
+  return GDN_OK;
 }
 
 gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_elems,

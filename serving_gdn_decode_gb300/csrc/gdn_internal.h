@@ -23,6 +23,12 @@ struct Problem {
 // state row stays in registers across the call; shaped for HBM throughput.
 cudaError_t launch_token_loop(const Problem &p, cudaStream_t stream);
 
+// The same kernel over several problems of one shape (the layers of a
+// forward pass) in ceil(n / kMaxLayersPerLaunch) launches; layers[i] share
+// every field but the buffer pointers.
+constexpr uint32_t kMaxLayersPerLaunch = 64;
+cudaError_t launch_token_loop_layers(const Problem *layers, uint32_t n_layers, cudaStream_t stream);
+
 // Sequential-scan kernel for long token ranges (scan.cu): two lanes per row,
 // lazy decay; shaped for FP32 issue throughput.
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);

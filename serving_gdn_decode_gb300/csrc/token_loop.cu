@@ -34,20 +34,17 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+struct LayerPtrs {
+  const float *q, *k, *v, *g, *beta, *state_in;
+  float *output, *state_out, *capture;
+};
+
 struct LoopArgs {
-  const float *__restrict__ q;
-  const float *__restrict__ k;
-  const float *__restrict__ v;
-  const float *__restrict__ g;
-  const float *__restrict__ beta;
-  const float *state_in;  // may be the same buffer as state_out
-  float *__restrict__ output;
-  float *state_out;
-  float *__restrict__ capture;
   uint32_t dv, nk, nv, nt, group, khead_div;
   float q_scale;
-  uint32_t row_blocks;  // CTAs per (seq, value head) pair
-  uint32_t tc;          // tokens per staged chunk
+  uint32_t row_blocks;    // CTAs per (seq, value head) pair
+  uint32_t layer_blocks;  // CTAs per layer = row_blocks * nv * ns
+  uint32_t tc;            // tokens per staged chunk
 };
 
 // ---- small PTX helpers (cp.async into shared memory)
@@ -127,9 +124,20 @@ __device__ __forceinline__ float reduce_rows(float (&a)[R], int lane) {
   return x;
 }
 
-template <int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER>
-__global__ void __launch_bounds__(WARPS * 32)
-    gdn_token_loop_kernel(const LoopArgs a) {
+// Up to MAXL problems of the same shape (e.g. the linear-attention layers of
+// one forward pass) in one launch: CTA blocks are layer-major, and each CTA
+// reads its layer's buffers from this table in the kernel parameters.
+template <int MAXL>
+struct LayerTable {
+  LayerPtrs l[MAXL];
+};
+
+// Single-layer launches leave the register count to the compiler (48 at
+// D_k = 128: five 8-warp CTAs per SM); multi-layer launches are held to 64.
+template <int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER, int MAXL>
+__global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
+    gdn_token_loop_kernel(const LoopArgs a, const LayerPtrs one,
+                          const __grid_constant__ LayerTable<MAXL> tab) {
   constexpr int DK = 32 * NSG;
   constexpr int ROWS = WARPS * R;  // rows per CTA
   constexpr int LPR = 32 / R;      // lanes that end up holding one row's total
@@ -141,8 +149,13 @@ __global__ void __launch_bounds__(WARPS * 32)
   // padded to a multiple of 4 floats so both buffers start 16-byte aligned.
   const int buf_floats = (tc * (2 * DK + ROWS + 2) + 3) & ~3;
 
-  const uint32_t rb = blockIdx.x % a.row_blocks;
-  const uint32_t head = blockIdx.x / a.row_blocks;  // = s * nv + vh
+  const uint32_t layer = MAXL == 1 ? 0u : blockIdx.x / a.layer_blocks;
+  const uint32_t bid = blockIdx.x - layer * a.layer_blocks;
+  // Buffer pointers: `one` when the launch has a single layer, else this
+  // CTA's entry of the table.
+#define GDN_LAYER(field) (MAXL == 1 ? one.field : tab.l[layer].field)
+  const uint32_t rb = bid % a.row_blocks;
+  const uint32_t head = bid / a.row_blocks;  // = s * nv + vh
   const uint32_t vh = head % a.nv;
   const uint32_t s = head / a.nv;
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
@@ -158,7 +171,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (row0 + r < a.dv) {
-      Cells<NSG>::load_cs(a.state_in + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
+      Cells<NSG>::load_cs(GDN_LAYER(state_in) + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
                           st[r]);
     } else {
 #pragma unroll
@@ -184,20 +197,20 @@ __global__ void __launch_bounds__(WARPS * 32)
     for (int i = threadIdx.x; i < n * (DK / 4); i += WARPS * 32) {
       const int t = i / (DK / 4), e = 4 * (i % (DK / 4));
       const size_t src = kq_first + (t0 + t) * kq_tok + e;
-      cp_async_16(ks + t * DK + e, a.k + src);
-      cp_async_16(qs + t * DK + e, a.q + src);
+      cp_async_16(ks + t * DK + e, GDN_LAYER(k) + src);
+      cp_async_16(qs + t * DK + e, GDN_LAYER(q) + src);
     }
     for (int i = threadIdx.x; i < n * ROWS; i += WARPS * 32) {
       const int t = i / ROWS, r = i % ROWS;
       if (row_cta0 + r < a.dv)
-        cp_async_4(vs + t * ROWS + r, a.v + v_first + (t0 + t) * v_tok + r);
+        cp_async_4(vs + t * ROWS + r, GDN_LAYER(v) + v_first + (t0 + t) * v_tok + r);
       else
         vs[t * ROWS + r] = 0.f;
     }
     for (int i = threadIdx.x; i < n; i += WARPS * 32) {
       const size_t src = sc_first + static_cast<size_t>(t0 + i) * a.nv;
-      cp_async_4(gs + i, a.g + src);
-      cp_async_4(bs + i, a.beta + src);
+      cp_async_4(gs + i, GDN_LAYER(g) + src);
+      cp_async_4(bs + i, GDN_LAYER(beta) + src);
     }
     cp_async_commit();
   };
@@ -262,10 +275,10 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
       const float y = reduce_rows<R>(py, lane);
       const size_t tok_head = (static_cast<size_t>(s) * nt + t) * a.nv + vh;
-      if ((lane % LPR) == 0 && my_row < a.dv) a.output[tok_head * a.dv + my_row] = y * a.q_scale;
+      if ((lane % LPR) == 0 && my_row < a.dv) GDN_LAYER(output)[tok_head * a.dv + my_row] = y * a.q_scale;
 
       if (CAPTURE) {
-        float *cap = a.capture + tok_head * a.dv * DK;
+        float *cap = GDN_LAYER(capture) + tok_head * a.dv * DK;
 #pragma unroll
         for (int r = 0; r < R; ++r)
           if (row0 + r < a.dv)
@@ -279,8 +292,9 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
   for (int r = 0; r < R; ++r)
     if (row0 + r < a.dv)
-      Cells<NSG>::store_cs(a.state_out + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
+      Cells<NSG>::store_cs(GDN_LAYER(state_out) + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
                            st[r]);
+#undef GDN_LAYER
 }
 
 // ---- launch shape: several rows per warp (R = 16/NSG, 64 B of state per
@@ -290,49 +304,70 @@ __global__ void __launch_bounds__(WARPS * 32)
 constexpr int kWarps = 8;
 constexpr int kTcMax = 8;
 
-template <int NSG, bool CAPTURE, bool DA>
-cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
+template <int NSG, bool CAPTURE, bool DA, int MAXL>
+cudaError_t launch_layers(const Problem &p, const Problem *layers, uint32_t n_layers,
+                          cudaStream_t stream) {
   constexpr int R = 16 / NSG;
   constexpr int ROWS = kWarps * R;
   constexpr int DK = 32 * NSG;
   LoopArgs a;
-  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
-  a.state_in = p.state_in; a.output = p.output; a.state_out = p.state_out; a.capture = p.capture;
   a.dv = p.dv; a.nk = p.nk; a.nv = p.nv; a.nt = p.nt;
   a.group = p.nv / p.nk;
   a.khead_div = p.khead_div ? 1u : 0u;
   a.q_scale = p.q_scale;
   a.row_blocks = (p.dv + ROWS - 1) / ROWS;
   a.tc = static_cast<uint32_t>(p.nt < static_cast<uint32_t>(kTcMax) ? p.nt : kTcMax);
-  const unsigned long long blocks =
+  const unsigned long long per_layer =
       static_cast<unsigned long long>(a.row_blocks) * p.nv * static_cast<unsigned long long>(p.ns);
-  if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  if (per_layer == 0 || per_layer * n_layers > 0x7fffffffull || n_layers == 0 || n_layers > MAXL)
+    return cudaErrorInvalidConfiguration;
+  a.layer_blocks = static_cast<uint32_t>(per_layer);
+  LayerTable<MAXL> t;
+  for (uint32_t i = 0; i < n_layers; ++i) {
+    const Problem &x = layers[i];
+    t.l[i] = LayerPtrs{x.q, x.k, x.v, x.g, x.beta, x.state_in, x.output, x.state_out, x.capture};
+  }
+  const LayerPtrs one = t.l[0];
   const int buf_floats = (static_cast<int>(a.tc) * (2 * DK + ROWS + 2) + 3) & ~3;
   const size_t smem = 2u * static_cast<size_t>(buf_floats) * sizeof(float);
-  gdn_token_loop_kernel<NSG, R, kWarps, CAPTURE, DA>
-      <<<static_cast<unsigned>(blocks), kWarps * 32, smem, stream>>>(a);
+  gdn_token_loop_kernel<NSG, R, kWarps, CAPTURE, DA, MAXL>
+      <<<static_cast<unsigned>(per_layer * n_layers), kWarps * 32, smem, stream>>>(a, one, t);
   return cudaGetLastError();
 }
 
-template <int NSG>
-cudaError_t launch_nsg(const Problem &p, cudaStream_t stream) {
+template <int NSG, int MAXL>
+cudaError_t launch_nsg(const Problem &p, const Problem *layers, uint32_t n, cudaStream_t stream) {
   const bool cap = p.capture != nullptr;
   if (cap)
-    return p.decay_after ? launch_one<NSG, true, true>(p, stream)
-                         : launch_one<NSG, true, false>(p, stream);
-  return p.decay_after ? launch_one<NSG, false, true>(p, stream)
-                       : launch_one<NSG, false, false>(p, stream);
+    return p.decay_after ? launch_layers<NSG, true, true, MAXL>(p, layers, n, stream)
+                         : launch_layers<NSG, true, false, MAXL>(p, layers, n, stream);
+  return p.decay_after ? launch_layers<NSG, false, true, MAXL>(p, layers, n, stream)
+                       : launch_layers<NSG, false, false, MAXL>(p, layers, n, stream);
+}
+
+template <int MAXL>
+cudaError_t launch_dk(const Problem &p, const Problem *layers, uint32_t n, cudaStream_t stream) {
+  switch (p.dk) {
+    case 32: return launch_nsg<1, MAXL>(p, layers, n, stream);
+    case 64: return launch_nsg<2, MAXL>(p, layers, n, stream);
+    case 128: return launch_nsg<4, MAXL>(p, layers, n, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_token_loop(const Problem &p, cudaStream_t stream) {
-  switch (p.dk) {
-    case 32: return launch_nsg<1>(p, stream);
-    case 64: return launch_nsg<2>(p, stream);
-    case 128: return launch_nsg<4>(p, stream);
-    default: return cudaErrorInvalidValue;
+  return launch_dk<1>(p, &p, 1, stream);
+}
+
+cudaError_t launch_token_loop_layers(const Problem *layers, uint32_t n_layers, cudaStream_t stream) {
+  for (uint32_t i = 0; i < n_layers; i += kMaxLayersPerLaunch) {
+    const uint32_t n = n_layers - i < kMaxLayersPerLaunch ? n_layers - i : kMaxLayersPerLaunch;
+    const cudaError_t e = launch_dk<kMaxLayersPerLaunch>(layers[i], layers + i, n, stream);
+    if (e != cudaSuccess) return e;
   }
+  return cudaSuccess;
 }
 
 }  // namespace gdn

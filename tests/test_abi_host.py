@@ -249,3 +249,38 @@ def test_commit_checks(L):
     w1 = SMALL1
     assert nat.commit_capture_raw(cap, w1.capture_elems - 1, idx, st, w1.params()) == \
         nat.GDN_ERR_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------- multi-layer checks
+
+def _layer_rows(n, base=1 << 36):
+    names = ["q", "k", "v", "g", "beta", "state_in", "output", "state_out", "state_capture"]
+    return [[base + (9 * i + j) * GAP for j in range(len(names))] for i in range(n)]
+
+
+@no_device
+def test_layers_checks(L):
+    p = SMALL.params()
+    assert nat.forward_layers_raw([], p) == nat.GDN_ERR_INVALID_ARGUMENT
+    rows = _layer_rows(3)
+    rows[1][0] = 0                                     # layer 1: q is NULL
+    assert nat.forward_layers_raw(rows, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "layer 1" in nat.gdn_last_error()
+    rows = _layer_rows(3)
+    rows[2][6] = rows[0][1] + 64                       # layer 2's output inside layer 0's k
+    assert nat.forward_layers_raw(rows, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "layer 2" in nat.gdn_last_error() and "layer 0" in nat.gdn_last_error()
+    rows = _layer_rows(2)
+    rows[1][7] = rows[0][7]                            # two layers write the same state
+    assert nat.forward_layers_raw(rows, p) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_layers_raw(_layer_rows(2), p[:8]) == nat.GDN_ERR_INVALID_ARGUMENT
+    rows = _layer_rows(2)
+    assert nat.forward_layers_raw(rows, p, with_capture=True,
+                                  state_capture_elems=SMALL.capture_elems - 4) == \
+        nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_layers_count_limit(L):
+    rows = _layer_rows(1025, base=1 << 40)
+    assert nat.forward_layers_raw(rows, SMALL.params()) == nat.GDN_ERR_INVALID_ARGUMENT
