@@ -339,13 +339,9 @@ gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_e
   const Span idx{accepted_idx, static_cast<unsigned long long>(d.prob.ns) * 4, "accepted_idx"};
   if (overlap(stt, cap) || overlap(stt, idx))
     return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state overlaps state_capture or accepted_idx");
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 0;
   const cudaError_t err = gdn::launch_commit(
       state_capture, accepted_idx, state, d.prob.nt, d.prob.ns,
-      static_cast<uint64_t>(d.prob.dk) * d.prob.dv * d.prob.nv, sms,
+      static_cast<uint64_t>(d.prob.dk) * d.prob.dv * d.prob.nv,
       reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn: commit launch failed: %s", cudaGetErrorString(err));

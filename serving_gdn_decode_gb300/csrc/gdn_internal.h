@@ -40,7 +40,6 @@ cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 // Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
 // every sequence whose accepted index lies in [0, nt).
 cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,
-                          uint32_t nt, uint32_t ns, uint64_t slice_elems, int sm_count,
-                          cudaStream_t stream);
+                          uint32_t nt, uint32_t ns, uint64_t slice_elems, cudaStream_t stream);
 
 }  // namespace gdn
