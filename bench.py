@@ -193,13 +193,16 @@ def aggregate(per_rank_units: float, elapsed_s: float, world: int, device=None):
 
 # ---------------------------------------------------------------- our arm
 
-def make_sets(torch, w, n_sets, device, capture=False):
+def make_sets(torch, w, n_sets, device, capture=False, act="f32"):
     from serving_gdn_decode_gb300.workloads import make_inputs
     sets = []
+    adt = torch.bfloat16 if act == "bf16" else torch.float32
     for i in range(n_sets):
-        x = make_inputs(w, seed=i)
+        x = make_inputs(w, seed=i, act=act)
         d = {k: torch.from_numpy(v).to(device) for k, v in x.items()}
-        d["output"] = torch.empty(w.v_elems, dtype=torch.float32, device=device)
+        for k in ("q", "k", "v"):
+            d[k] = d[k].to(adt)
+        d["output"] = torch.empty(w.v_elems, dtype=adt, device=device)
         d["state"] = d.pop("state_in")  # updated in place
         if capture:
             d["capture"] = torch.empty(w.capture_elems, dtype=torch.float32, device=device)
@@ -264,9 +267,15 @@ def time_graphed(torch, nat, sets, params, steps, warmup, capture=False, world=1
 
 
 def time_e2e(torch, nat, w, params, steps, device):
-    """End to end through the public API from pinned host memory: each step
-    copies all inputs in and output + state out (HostPipeline overlaps the
-    two copy directions and the kernel over groups of sequences)."""
+    """End to end through the public API from pinned host memory, two ways.
+
+    zero_copy (the reported e2e): every step is one gdn_forward_host call on
+    pinned host buffers -- the kernel reads all inputs from host memory and
+    writes output and state back to host memory over the CPU-GPU link.
+    copy_engines: HostPipeline -- per step, copies of all inputs to device
+    buffers, gdn_forward, copies of output and state back, overlapped over 4
+    groups of sequences.  Both move the same bytes across the link per step.
+    """
     from serving_gdn_decode_gb300.workloads import make_inputs
     x = make_inputs(w, seed=100)
     host = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
@@ -274,21 +283,28 @@ def time_e2e(torch, nat, w, params, steps, device):
     st_h = torch.empty(w.state_elems, dtype=torch.float32).pin_memory()
     pipe = nat.HostPipeline(params, groups=4, device=device)
 
-    def step():
+    def zero_copy():
+        nat.gdn_forward_host(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                             host["state_in"], out_h, st_h, params, device=device)
+
+    def copy_engines():
         pipe(host["q"], host["k"], host["v"], host["g"], host["beta"], host["state_in"], out_h,
              st_h)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
-    torch.cuda.synchronize()
-    return start.elapsed_time(end) / 1e3 / steps, pipe.h2d_bytes(), pipe.d2h_bytes()
+    res = {}
+    for name, step in (("zero_copy", zero_copy), ("copy_engines", copy_engines)):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(steps):
+            step()
+        end.record()
+        torch.cuda.synchronize()
+        res[name] = start.elapsed_time(end) / 1e3 / steps
+    return res, pipe.h2d_bytes(), pipe.d2h_bytes()
 
 
 def extras(torch, nat, peak_gbs, device):
@@ -296,11 +312,11 @@ def extras(torch, nat, peak_gbs, device):
     from serving_gdn_decode_gb300.workloads import WORKLOADS
     res = {}
 
-    def hbm_case(key, w, params, capture, n_sets, steps):
-        sets = make_sets(torch, w, n_sets, device, capture)
+    def hbm_case(key, w, params, capture, n_sets, steps, act="f32"):
+        sets = make_sets(torch, w, n_sets, device, capture, act=act)
         t, _ = time_graphed(torch, nat, sets, params, steps, 5, capture)
         us = t / steps * 1e6
-        gbs = w.algorithmic_bytes() / (t / steps) / 1e9
+        gbs = w.algorithmic_bytes(act) / (t / steps) / 1e9
         res[key] = {"path": nat.gdn_path_name(params, capture), "us_per_call": round(us, 2),
                     "GB_s": round(gbs, 1), "hbm_frac": round(gbs / peak_gbs, 3)}
         del sets
@@ -313,6 +329,10 @@ def extras(torch, nat, peak_gbs, device):
     hbm_case("spec_capture_s32", wc, wc.params(), True, 4, 200)
     wc64 = wc.with_(n_seqs=64)
     hbm_case("spec_capture_s64", wc64, wc64.params(), True, 3, 120)
+    # bf16 activations (q, k, v, output), f32 state
+    wd = WORKLOADS["decode"]
+    hbm_case("decode_bf16", wd, wd.params(), False, 4, 400, act="bf16")
+    hbm_case("spec_capture_s32_bf16", wc, wc.params(), True, 4, 200, act="bf16")
 
     # speculative-decode rollback commit: gathers one captured state per sequence
     import numpy as np
@@ -353,9 +373,10 @@ def extras(torch, nat, peak_gbs, device):
                                                     32, peak_gbs, device)
 
     wp = WORKLOADS["long_prefill"]
-    for key, params in (("long_prefill_scan", wp.params(path=PATH_SCAN)),
-                        ("long_prefill_chunked", wp.params(path=PATH_CHUNKED))):
-        sets = make_sets(torch, wp, 1, device)
+    for key, params, act in (("long_prefill_scan", wp.params(path=PATH_SCAN), "f32"),
+                             ("long_prefill_chunked", wp.params(path=PATH_CHUNKED), "f32"),
+                             ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16")):
+        sets = make_sets(torch, wp, 1, device, act=act)
         steps = 5
         t, _ = time_graphed(torch, nat, sets, params, steps, 2)
         s = t / steps
@@ -475,7 +496,8 @@ def run_ours(args):
     del sets
     torch.cuda.empty_cache()
 
-    e2e_s, h2d, d2h = time_e2e(torch, nat, w, params, min(args.steps, 30), device)
+    e2e_t, h2d, d2h = time_e2e(torch, nat, w, params, min(args.steps, 30), device)
+    e2e_s = e2e_t["zero_copy"]
     e2e_val, _ = aggregate(bytes_per_call, e2e_s, world, device)
 
     line = {
@@ -507,9 +529,14 @@ def run_ours(args):
         "e2e": {"value": round(e2e_val / 1e9, 2), "unit": "GB/s",
                 "us_per_call": round(e2e_s * 1e6, 1), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "HostPipeline: per step, pinned host -> device copies of all inputs, "
-                       "gdn_forward, device -> pinned host copies of output and state; the "
-                       "state moves in 4 groups of sequences so both copy directions overlap"},
+                "how": "gdn_forward_host (zero-copy): per step one C-ABI call on pinned host "
+                       "buffers; the kernel reads every input from host memory and writes output "
+                       "and state to host memory over the CPU-GPU link",
+                "copy_engines": {"value": round(bytes_per_call / e2e_t["copy_engines"] / 1e9, 2),
+                                 "us_per_call": round(e2e_t["copy_engines"] * 1e6, 1),
+                                 "how": "HostPipeline: copies of all inputs in and of output and "
+                                        "state out around gdn_forward, overlapped over 4 groups "
+                                        "of sequences"}},
         "gpu_launches": args.steps,
         "clocks": clk,
     }

@@ -190,6 +190,49 @@ gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_e
                               const int32_t *accepted_idx, float *state, const uint32_t *params,
                               size_t n_params, gdn_stream_t stream);
 
+/*
+ * bf16 activations with f32 state.  The prefill page ("Dtype / precision" of
+ * gated_delta_net.rs, mlx-native 0.4.0) keeps all accumulation in f32 and
+ * names bf16 inputs and outputs as a later variant.  These entry points are
+ * that variant: q, k, v and output hold bfloat16 (the upper half of an f32
+ * bit pattern, as torch.bfloat16 / __nv_bfloat16), in the same layouts as
+ * above; g, beta, state_in, state_out and state_capture stay f32.  Each
+ * bf16 value is widened exactly to f32 on load, every product and sum is f32
+ * as in gdn_forward, and y is rounded once, to nearest-even bf16, when it is
+ * stored.  Results for the same widened inputs therefore equal gdn_forward's
+ * up to that final rounding of y (state and capture are bit-identical).
+ *
+ * Extra checks: v 4-byte aligned and output 2-byte aligned (q and k stay
+ * 16-byte); UNSUPPORTED when D_v is odd (v is staged two rows at a time) or
+ * when the chunked path is forced.
+ */
+typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
+
+gdn_status gdn_forward_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                            const float *g, const float *beta, const float *state_in,
+                            gdn_bf16 *output, float *state_out, const uint32_t *params,
+                            size_t n_params, gdn_stream_t stream);
+
+gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                    const float *g, const float *beta, const float *state_in,
+                                    gdn_bf16 *output, float *state_out, const uint32_t *params,
+                                    size_t n_params, float *state_capture,
+                                    size_t state_capture_elems, gdn_stream_t stream);
+
+/* gdn_layer_buffers with bf16 q, k, v and output. */
+typedef struct gdn_layer_buffers_bf16 {
+  const gdn_bf16 *q, *k, *v;
+  const float *g, *beta, *state_in;
+  gdn_bf16 *output;
+  float *state_out;
+  float *state_capture; /* read only when with_capture != 0 */
+} gdn_layer_buffers_bf16;
+
+/* gdn_forward_layers on bf16 activations (gdn_forward_bf16 per layer). */
+gdn_status gdn_forward_layers_bf16(const gdn_layer_buffers_bf16 *layers, size_t n_layers,
+                                   const uint32_t *params, size_t n_params, int with_capture,
+                                   size_t state_capture_elems, gdn_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the thread's next call. */
 const char *gdn_last_error(void);

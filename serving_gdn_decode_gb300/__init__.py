@@ -10,15 +10,17 @@ from .params import (FLAG_DECAY_AFTER, FLAG_KHEAD_DIV, N_PARAMS, PATH_AUTO, PATH
 
 __all__ = ["FLAG_DECAY_AFTER", "FLAG_KHEAD_DIV", "N_PARAMS", "PATH_AUTO", "PATH_CHUNKED",
            "PATH_SCAN", "pack_params", "q_scale_bits", "gdn_forward", "gdn_forward_capture",
-           "gdn_last_error", "gdn_path_name", "gdn_commit_capture", "gdn_forward_layers", "HostPipeline",
-           "GdnError"]
+           "gdn_last_error", "gdn_path_name", "gdn_commit_capture", "gdn_forward_layers",
+           "gdn_forward_host", "HostPipeline", "GdnError"]
+
+_NATIVE = ("gdn_forward", "gdn_forward_capture", "gdn_last_error", "gdn_path_name",
+           "gdn_commit_capture", "gdn_forward_layers", "gdn_forward_host", "HostPipeline", "GdnError")
 
 
 def __getattr__(name):
     # The native binding loads on first use, so importing the package (for
     # the parameter packer or the input generator) needs no GPU library.
-    if name in ("gdn_forward", "gdn_forward_capture", "gdn_last_error", "gdn_path_name",
-                "gdn_commit_capture", "gdn_forward_layers", "HostPipeline", "GdnError"):
+    if name in _NATIVE:
         from . import _native
         return getattr(_native, name)
     raise AttributeError(name)

@@ -31,7 +31,8 @@ _lib = None
 
 
 class LayerBuffers(ctypes.Structure):
-    """Mirror of gdn_layer_buffers (include/gdn.h)."""
+    """Mirror of gdn_layer_buffers and gdn_layer_buffers_bf16 (include/gdn.h):
+    nine pointers in the same order in both."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "beta", "state_in", "output",
                                                 "state_out", "state_capture")]
 
@@ -67,6 +68,12 @@ def lib() -> ctypes.CDLL:
             L.gdn_forward_layers.argtypes = [ctypes.POINTER(LayerBuffers), sz, u32p, sz, ctypes.c_int,
                                              sz, vp]
             L.gdn_forward_layers.restype = ctypes.c_int
+            L.gdn_forward_bf16.argtypes = L.gdn_forward.argtypes
+            L.gdn_forward_bf16.restype = ctypes.c_int
+            L.gdn_forward_capture_bf16.argtypes = L.gdn_forward_capture.argtypes
+            L.gdn_forward_capture_bf16.restype = ctypes.c_int
+            L.gdn_forward_layers_bf16.argtypes = L.gdn_forward_layers.argtypes
+            L.gdn_forward_layers_bf16.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -99,28 +106,35 @@ def gdn_path_name(params, capture: bool = False) -> str:
 
 # ---------------------------------------------------------------- raw calls
 
-def forward_raw(q, k, v, g, beta, state_in, output, state_out, params, stream=0) -> int:
-    """Call gdn_forward with integer device addresses; returns the status."""
+def forward_raw(q, k, v, g, beta, state_in, output, state_out, params, stream=0,
+                bf16=False) -> int:
+    """Call gdn_forward (gdn_forward_bf16 when ``bf16``) with integer device
+    addresses; returns the status."""
     p, pp, n = _params_arg(params)
-    return lib().gdn_forward(q, k, v, g, beta, state_in, output, state_out, pp, n, stream)
+    fn = lib().gdn_forward_bf16 if bf16 else lib().gdn_forward
+    return fn(q, k, v, g, beta, state_in, output, state_out, pp, n, stream)
 
 
 def forward_capture_raw(q, k, v, g, beta, state_in, output, state_out, params, state_capture,
-                        state_capture_elems, stream=0) -> int:
-    """Call gdn_forward_capture with integer device addresses; returns the status."""
+                        state_capture_elems, stream=0, bf16=False) -> int:
+    """Call gdn_forward_capture (gdn_forward_capture_bf16 when ``bf16``) with
+    integer device addresses; returns the status."""
     p, pp, n = _params_arg(params)
-    return lib().gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, pp, n,
-                                     state_capture, state_capture_elems, stream)
+    fn = lib().gdn_forward_capture_bf16 if bf16 else lib().gdn_forward_capture
+    return fn(q, k, v, g, beta, state_in, output, state_out, pp, n, state_capture,
+              state_capture_elems, stream)
 
 
-def forward_layers_raw(layers, params, with_capture=False, state_capture_elems=0, stream=0) -> int:
-    """Call gdn_forward_layers with per-layer tuples of 9 integer device
-    addresses (q, k, v, g, beta, state_in, output, state_out, state_capture);
-    returns the status."""
+def forward_layers_raw(layers, params, with_capture=False, state_capture_elems=0, stream=0,
+                       bf16=False) -> int:
+    """Call gdn_forward_layers (gdn_forward_layers_bf16 when ``bf16``) with
+    per-layer tuples of 9 integer device addresses (q, k, v, g, beta,
+    state_in, output, state_out, state_capture); returns the status."""
     p, pp, n = _params_arg(params)
     arr = (LayerBuffers * max(1, len(layers)))(*[LayerBuffers(*lay) for lay in layers])
-    return lib().gdn_forward_layers(arr if layers else None, len(layers), pp, n,
-                                    1 if with_capture else 0, state_capture_elems, stream)
+    fn = lib().gdn_forward_layers_bf16 if bf16 else lib().gdn_forward_layers
+    return fn(arr if layers else None, len(layers), pp, n, 1 if with_capture else 0,
+              state_capture_elems, stream)
 
 
 def commit_capture_raw(state_capture, state_capture_elems, accepted_idx, state, params,
@@ -133,12 +147,19 @@ def commit_capture_raw(state_capture, state_capture_elems, accepted_idx, state, 
 
 # ---------------------------------------------------------------- torch tensors
 
-def _check(name, t, expect_numel, allow_larger=False):
+def _dtype_name(dtype) -> str:
+    import torch
+    return "bf16" if dtype == torch.bfloat16 else "f32"
+
+
+def _check(name, t, expect_numel, allow_larger=False, dtype=None):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.float32:
-        raise GdnError(GDN_ERR_INVALID_ARGUMENT, f"{name} must be f32 (got {t.dtype})")
+    dtype = torch.float32 if dtype is None else dtype
+    if t.dtype != dtype:
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                       f"{name} must be {_dtype_name(dtype)} (got {t.dtype})")
     if not t.is_cuda:
         raise GdnError(GDN_ERR_INVALID_ARGUMENT, f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
@@ -148,6 +169,44 @@ def _check(name, t, expect_numel, allow_larger=False):
         raise GdnError(GDN_ERR_INVALID_ARGUMENT,
                        f"{name} element count {n} != expected {expect_numel}")
     return t.data_ptr()
+
+
+def _act_dtype(q):
+    """Activation dtype of a call, taken from q: f32 (gdn_forward) or bf16
+    (gdn_forward_bf16); k, v and output must match it."""
+    import torch
+    if isinstance(q, torch.Tensor) and q.dtype in (torch.float32, torch.bfloat16):
+        return q.dtype
+    raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                   f"q must be an f32 or bf16 torch.Tensor (got {getattr(q, 'dtype', type(q))})")
+
+
+def _check_dtypes(prefix, act, k, v, g, beta, state_in, output, state_out):
+    """Every buffer's dtype, before any other check, so that a mixed-dtype
+    call is reported as such."""
+    import torch
+    f32 = torch.float32
+    for name, t, want in (("k", k, act), ("v", v, act), ("g", g, f32), ("beta", beta, f32),
+                          ("state_in", state_in, f32), ("output", output, act),
+                          ("state_out", state_out, f32)):
+        if isinstance(t, torch.Tensor) and t.dtype != want:
+            raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                           f"{prefix}{name} must be {_dtype_name(want)} (got {t.dtype})")
+
+
+def _act_ptrs(prefix, q, k, v, g, beta, state_in, output, state_out, s):
+    """Checked device addresses of the eight buffers of one call, and whether
+    the activations (q, k, v, output) are bf16."""
+    import torch
+    act = _act_dtype(q)
+    _check_dtypes(prefix, act, k, v, g, beta, state_in, output, state_out)
+    ptrs = [_check(prefix + "q", q, s["qk"], dtype=act), _check(prefix + "k", k, s["qk"], dtype=act),
+            _check(prefix + "v", v, s["v"], dtype=act), _check(prefix + "g", g, s["sc"]),
+            _check(prefix + "beta", beta, s["sc"]),
+            _check(prefix + "state_in", state_in, s["state"]),
+            _check(prefix + "output", output, s["v"], dtype=act),
+            _check(prefix + "state_out", state_out, s["state"])]
+    return ptrs, act == torch.bfloat16
 
 
 def _sizes(params):
@@ -169,16 +228,15 @@ def _stream(stream, device):
 
 
 def gdn_forward(q, k, v, g, beta, state_in, output, state_out, params, stream=None) -> None:
-    """Run gdn_forward on torch CUDA tensors (flat f32, the layouts of
-    include/gdn.h).  Checks dtype, device, contiguity and element counts
-    (the per-buffer checks of `validate` in gated_delta_net_decode.rs), then
-    hands the device pointers to the C ABI.  Raises GdnError on failure."""
+    """Run gdn_forward on torch CUDA tensors (flat, the layouts of
+    include/gdn.h).  q, k, v and output are all f32, or all bf16 (then
+    gdn_forward_bf16 runs); g, beta and the states are f32.  Checks dtype,
+    device, contiguity and element counts (the per-buffer checks of
+    `validate` in gated_delta_net_decode.rs), then hands the device pointers
+    to the C ABI.  Raises GdnError on failure."""
     s = _sizes(params)
-    ptrs = [_check("q", q, s["qk"]), _check("k", k, s["qk"]), _check("v", v, s["v"]),
-            _check("g", g, s["sc"]), _check("beta", beta, s["sc"]),
-            _check("state_in", state_in, s["state"]), _check("output", output, s["v"]),
-            _check("state_out", state_out, s["state"])]
-    st = forward_raw(*ptrs, params, _stream(stream, q.device))
+    ptrs, bf16 = _act_ptrs("", q, k, v, g, beta, state_in, output, state_out, s)
+    st = forward_raw(*ptrs, params, _stream(stream, q.device), bf16=bf16)
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 
@@ -189,13 +247,10 @@ def gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, params, s
     ([D_k, D_v, n_v, n_tokens, n_seqs]; may be larger than needed when
     n_seqs == 1, as dispatch_gated_delta_net_decode_with_capture allows)."""
     s = _sizes(params)
-    ptrs = [_check("q", q, s["qk"]), _check("k", k, s["qk"]), _check("v", v, s["v"]),
-            _check("g", g, s["sc"]), _check("beta", beta, s["sc"]),
-            _check("state_in", state_in, s["state"]), _check("output", output, s["v"]),
-            _check("state_out", state_out, s["state"])]
+    ptrs, bf16 = _act_ptrs("", q, k, v, g, beta, state_in, output, state_out, s)
     cap = _check("state_capture", state_capture, s["state"] * s["nt"], allow_larger=s["ns"] == 1)
     st = forward_capture_raw(*ptrs, params, cap, state_capture.numel(),
-                             _stream(stream, q.device))
+                             _stream(stream, q.device), bf16=bf16)
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 
@@ -225,17 +280,18 @@ def gdn_forward_layers(layers, params, with_capture: bool = False, stream=None) 
     such as the linear-attention layers of a forward pass: ``layers`` is a list
     of dicts with torch CUDA tensors under the keys q, k, v, g, beta, state_in,
     output, state_out (and state_capture when ``with_capture``).  On the decode
-    path all layers run in one launch (per 64 layers)."""
+    path all layers run in one launch (per 64 layers).  Activations are f32
+    or bf16, the same for every layer."""
     s = _sizes(params)
     rows, cap_elems = [], 0
     dev = None
+    bf16 = None
     for i, L in enumerate(layers):
-        ptrs = [_check(f"layers[{i}].q", L["q"], s["qk"]), _check(f"layers[{i}].k", L["k"], s["qk"]),
-                _check(f"layers[{i}].v", L["v"], s["v"]), _check(f"layers[{i}].g", L["g"], s["sc"]),
-                _check(f"layers[{i}].beta", L["beta"], s["sc"]),
-                _check(f"layers[{i}].state_in", L["state_in"], s["state"]),
-                _check(f"layers[{i}].output", L["output"], s["v"]),
-                _check(f"layers[{i}].state_out", L["state_out"], s["state"])]
+        ptrs, b = _act_ptrs(f"layers[{i}].", L["q"], L["k"], L["v"], L["g"], L["beta"],
+                            L["state_in"], L["output"], L["state_out"], s)
+        if bf16 is not None and b != bf16:
+            raise GdnError(GDN_ERR_INVALID_ARGUMENT, "activation dtypes differ between layers")
+        bf16 = b
         if with_capture:
             c = L["state_capture"]
             ptrs.append(_check(f"layers[{i}].state_capture", c, s["state"] * s["nt"],
@@ -250,12 +306,63 @@ def gdn_forward_layers(layers, params, with_capture: bool = False, stream=None) 
         dev = L["q"].device
     if not rows:
         raise GdnError(GDN_ERR_INVALID_ARGUMENT, "no layers")
-    st = forward_layers_raw(rows, params, with_capture, cap_elems, _stream(stream, dev))
+    st = forward_layers_raw(rows, params, with_capture, cap_elems, _stream(stream, dev), bf16=bf16)
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 
 
 # ---------------------------------------------------------------- host buffers
+
+def _check_host(name, t, expect_numel, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda or not t.is_pinned() or not t.is_contiguous() or t.dtype != dtype:
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                       f"{name} must be a contiguous {_dtype_name(dtype)} pinned host tensor")
+    if t.numel() != expect_numel:
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT,
+                       f"{name} element count {t.numel()} != expected {expect_numel}")
+    return t.data_ptr()
+
+
+def gdn_forward_host(q, k, v, g, beta, state_in, output, state_out, params, state_capture=None,
+                     stream=None, device=None) -> None:
+    """gdn_forward (gdn_forward_capture when ``state_capture`` is given) on
+    PINNED HOST tensors, zero-copy: the kernel reads the inputs from host
+    memory and writes output, state and capture back to host memory itself,
+    over the CPU-GPU link, with no staging copy.  Pinned host memory is
+    device-accessible, and under CUDA's unified addressing (every 64-bit
+    platform) its device address is its host address, so the host pointers
+    go to the C ABI unchanged.  Same dtype rules as gdn_forward (q, k, v and
+    output f32 or all bf16).  Runs on ``stream`` (default: the current stream
+    of ``device``, default the current device) and does not block the host:
+    synchronise before reading the results."""
+    import torch
+    s = _sizes(params)
+    act = _act_dtype(q)
+    f32 = torch.float32
+    _check_dtypes("", act, k, v, g, beta, state_in, output, state_out)
+    ptrs = [_check_host("q", q, s["qk"], act), _check_host("k", k, s["qk"], act),
+            _check_host("v", v, s["v"], act), _check_host("g", g, s["sc"], f32),
+            _check_host("beta", beta, s["sc"], f32),
+            _check_host("state_in", state_in, s["state"], f32),
+            _check_host("output", output, s["v"], act),
+            _check_host("state_out", state_out, s["state"], f32)]
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    strm = _stream(stream, dev)
+    bf16 = act == torch.bfloat16
+    if state_capture is None:
+        st = forward_raw(*ptrs, params, strm, bf16=bf16)
+    else:
+        need = s["state"] * s["nt"]
+        n_cap = state_capture.numel() if isinstance(state_capture, torch.Tensor) else -1
+        cap = _check_host("state_capture", state_capture,
+                          max(n_cap, need) if s["ns"] == 1 else need, f32)
+        st = forward_capture_raw(*ptrs, params, cap, state_capture.numel(), strm, bf16=bf16)
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+
 
 class HostPipeline:
     """Run gdn_forward on PINNED HOST tensors, end to end.

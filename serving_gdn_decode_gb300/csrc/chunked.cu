@@ -699,8 +699,9 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 template <bool DA>
 cudaError_t launch(const Problem &p, cudaStream_t stream) {
   ChunkArgs a;
-  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
-  a.state_in = p.state_in; a.output = p.output; a.state_out = p.state_out;
+  a.q = static_cast<const float *>(p.q); a.k = static_cast<const float *>(p.k);
+  a.v = static_cast<const float *>(p.v); a.g = p.g; a.beta = p.beta;
+  a.state_in = p.state_in; a.output = static_cast<float *>(p.output); a.state_out = p.state_out;
   a.nk = p.nk; a.nv = p.nv; a.nt = p.nt;
   a.group = p.nv / p.nk;
   a.khead_div = p.khead_div ? 1u : 0u;
@@ -717,7 +718,9 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
 
 }  // namespace
 
-bool chunked_supported(const Problem &p) { return p.dk == 128 && p.dv == 128 && p.capture == nullptr; }
+bool chunked_supported(const Problem &p) {
+  return p.dk == 128 && p.dv == 128 && p.capture == nullptr && !p.io_bf16;
+}
 
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream) {
   if (!chunked_supported(p)) return cudaErrorInvalidValue;

@@ -122,7 +122,9 @@ const char *path_name(Path path, bool capture) {
   }
 }
 
-gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
+gdn_status choose_path(const Decoded &d, bool capture, bool bf16, Path *out) {
+  if (bf16 && d.prob.dv % 2 != 0)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn: bf16 activations need an even D_v (got %u)", d.prob.dv);
   switch (d.path) {
     case GDN_PATH_SCAN:
       *out = Path::kScan;
@@ -132,6 +134,8 @@ gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path keeps no per-token state (capture)");
       if (d.prob.dk != 128 || d.prob.dv != 128)
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path needs D_k = D_v = 128");
+      if (bf16)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path takes f32 activations only");
       *out = Path::kChunked;
       return GDN_OK;
     default:
@@ -140,27 +144,58 @@ gdn_status choose_path(const Decoded &d, bool capture, Path *out) {
   }
 }
 
-gdn_status check_buffers(const Decoded &d, const float *q, const float *k, const float *v,
-                         const float *g, const float *beta, const float *state_in, float *output,
-                         float *state_out, float *capture, size_t capture_elems, bool with_capture) {
-  const Span in[] = {{q, d.qk_elems * 4, "q"},       {k, d.qk_elems * 4, "k"},
-                     {v, d.v_elems * 4, "v"},        {g, d.sc_elems * 4, "g"},
-                     {beta, d.sc_elems * 4, "beta"}, {state_in, d.state_elems * 4, "state_in"}};
-  for (const Span &s : in)
+// The buffers of one call, in slot order; q, k, v and output hold f32 or bf16.
+struct Buffers {
+  const void *q, *k, *v;
+  const float *g, *beta, *state_in;
+  void *output;
+  float *state_out, *capture;
+};
+
+template <typename L>
+Buffers buffers_of(const L &x, bool with_capture) {
+  return Buffers{x.q, x.k, x.v, x.g, x.beta, x.state_in, x.output, x.state_out,
+                 with_capture ? x.state_capture : nullptr};
+}
+
+// Byte spans of every buffer of one call (capture: zero bytes when absent).
+struct Spans {
+  Span in[6];  // q, k, v, g, beta, state_in
+  Span output, state_out, capture;
+};
+
+Spans spans_of(const Decoded &d, const Buffers &b, bool bf16) {
+  const unsigned long long io = bf16 ? 2 : 4;
+  return Spans{{{b.q, d.qk_elems * io, "q"},
+                {b.k, d.qk_elems * io, "k"},
+                {b.v, d.v_elems * io, "v"},
+                {b.g, d.sc_elems * 4, "g"},
+                {b.beta, d.sc_elems * 4, "beta"},
+                {b.state_in, d.state_elems * 4, "state_in"}},
+               {b.output, d.v_elems * io, "output"},
+               {b.state_out, d.state_elems * 4, "state_out"},
+               {b.capture, b.capture ? d.capture_elems * 4 : 0, "state_capture"}};
+}
+
+gdn_status check_buffers(const Decoded &d, const Buffers &b, size_t capture_elems,
+                         bool with_capture, bool bf16) {
+  const Spans sp = spans_of(d, b, bf16);
+  for (const Span &s : sp.in)
     if (s.p == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s is NULL", s.name);
-  if (output == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output is NULL");
-  if (state_out == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out is NULL");
-  if (with_capture && capture == nullptr)
+  if (b.output == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output is NULL");
+  if (b.state_out == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out is NULL");
+  if (with_capture && b.capture == nullptr)
     return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture is NULL");
 
   const struct { const void *p; uintptr_t a; const char *name; } al[] = {
-      {q, 16, "q"}, {k, 16, "k"}, {state_in, 16, "state_in"}, {state_out, 16, "state_out"},
-      {v, 4, "v"}, {g, 4, "g"}, {beta, 4, "beta"}, {output, 4, "output"}};
+      {b.q, 16, "q"},        {b.k, 16, "k"},         {b.state_in, 16, "state_in"},
+      {b.state_out, 16, "state_out"}, {b.v, 4, "v"}, {b.g, 4, "g"},
+      {b.beta, 4, "beta"},   {b.output, bf16 ? 2u : 4u, "output"}};
   for (const auto &x : al)
     if (!aligned(x.p, x.a))
       return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s must be %u-byte aligned", x.name,
                   static_cast<unsigned>(x.a));
-  if (with_capture && !aligned(capture, 16))
+  if (with_capture && !aligned(b.capture, 16))
     return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture must be 16-byte aligned");
 
   if (with_capture) {
@@ -174,46 +209,46 @@ gdn_status check_buffers(const Decoded &d, const float *q, const float *k, const
                   capture_elems, d.capture_elems);
   }
 
-  const Span st_out{state_out, d.state_elems * 4, "state_out"};
-  if (state_out != state_in && overlap(st_out, in[5]))
+  if (b.state_out != b.state_in && overlap(sp.state_out, sp.in[5]))
     return fail(GDN_ERR_INVALID_ARGUMENT,
                 "gdn: state_in and state_out overlap without being the same buffer");
-  const Span out{output, d.v_elems * 4, "output"};
-  for (const Span &s : in)
-    if (overlap(out, s)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps %s", s.name);
-  if (overlap(out, st_out)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps state_out");
+  for (const Span &s : sp.in)
+    if (overlap(sp.output, s)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps %s", s.name);
+  if (overlap(sp.output, sp.state_out))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: output overlaps state_out");
   for (int i = 0; i < 5; ++i)
-    if (overlap(st_out, in[i]))
-      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out overlaps %s", in[i].name);
+    if (overlap(sp.state_out, sp.in[i]))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_out overlaps %s", sp.in[i].name);
   if (with_capture) {
-    const Span cap{capture, d.capture_elems * 4, "state_capture"};
-    for (const Span &s : in)
-      if (overlap(cap, s))
+    for (const Span &s : sp.in)
+      if (overlap(sp.capture, s))
         return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture overlaps %s", s.name);
-    if (overlap(cap, out) || overlap(cap, st_out))
+    if (overlap(sp.capture, sp.output) || overlap(sp.capture, sp.state_out))
       return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: state_capture overlaps an output buffer");
   }
   return GDN_OK;
 }
 
-gdn_status run(const float *q, const float *k, const float *v, const float *g, const float *beta,
-               const float *state_in, float *output, float *state_out, const uint32_t *params,
-               size_t n_params, float *capture, size_t capture_elems, bool with_capture,
-               gdn_stream_t stream) {
+void fill_problem(gdn::Problem &p, const Buffers &b, bool bf16) {
+  p.q = b.q; p.k = b.k; p.v = b.v; p.g = b.g; p.beta = b.beta; p.state_in = b.state_in;
+  p.output = b.output; p.state_out = b.state_out; p.capture = b.capture;
+  p.io_bf16 = bf16;
+}
+
+gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t capture_elems,
+               bool with_capture, bool bf16, gdn_stream_t stream) {
   g_last_error[0] = '\0';
   Decoded d;
   gdn_status st = decode_params(params, n_params, &d);
   if (st != GDN_OK) return st;
-  st = check_buffers(d, q, k, v, g, beta, state_in, output, state_out, capture, capture_elems,
-                     with_capture);
+  st = check_buffers(d, b, capture_elems, with_capture, bf16);
   if (st != GDN_OK) return st;
   Path path;
-  st = choose_path(d, with_capture, &path);
+  st = choose_path(d, with_capture, bf16, &path);
   if (st != GDN_OK) return st;
 
   gdn::Problem &p = d.prob;
-  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state_in = state_in;
-  p.output = output; p.state_out = state_out; p.capture = with_capture ? capture : nullptr;
+  fill_problem(p, b, bf16);
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t err = path == Path::kDecode    ? gdn::launch_token_loop(p, cs)
                           : path == Path::kChunked ? gdn::launch_chunked(p, cs)
@@ -223,29 +258,12 @@ gdn_status run(const float *q, const float *k, const float *v, const float *g, c
   return GDN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-gdn_status gdn_forward(const float *q, const float *k, const float *v, const float *g,
-                       const float *beta, const float *state_in, float *output, float *state_out,
-                       const uint32_t *params, size_t n_params, gdn_stream_t stream) {
-  return run(q, k, v, g, beta, state_in, output, state_out, params, n_params, nullptr, 0, false,
-             stream);
-}
-
-gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, const float *g,
-                               const float *beta, const float *state_in, float *output,
-                               float *state_out, const uint32_t *params, size_t n_params,
-                               float *state_capture, size_t state_capture_elems,
-                               gdn_stream_t stream) {
-  return run(q, k, v, g, beta, state_in, output, state_out, params, n_params, state_capture,
-             state_capture_elems, true, stream);
-}
-
-gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
-                              const uint32_t *params, size_t n_params, int with_capture,
-                              size_t state_capture_elems, gdn_stream_t stream) {
+// gdn_forward_layers and its bf16 twin: L is gdn_layer_buffers or
+// gdn_layer_buffers_bf16 (same field names).
+template <typename L>
+gdn_status run_layers(const L *layers, size_t n_layers, const uint32_t *params, size_t n_params,
+                      int with_capture, size_t state_capture_elems, bool bf16,
+                      gdn_stream_t stream) {
   g_last_error[0] = '\0';
   if (layers == nullptr || n_layers == 0)
     return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: layers is NULL or n_layers is 0");
@@ -256,12 +274,10 @@ gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
   if (st != GDN_OK) return st;
   const bool cap = with_capture != 0;
   Path path;
-  st = choose_path(d, cap, &path);
+  st = choose_path(d, cap, bf16, &path);
   if (st != GDN_OK) return st;
   for (size_t i = 0; i < n_layers; ++i) {
-    const gdn_layer_buffers &L = layers[i];
-    st = check_buffers(d, L.q, L.k, L.v, L.g, L.beta, L.state_in, L.output, L.state_out,
-                       L.state_capture, state_capture_elems, cap);
+    st = check_buffers(d, buffers_of(layers[i], cap), state_capture_elems, cap, bf16);
     if (st != GDN_OK) {
       char msg[sizeof g_last_error];
       std::snprintf(msg, sizeof msg, "%s", g_last_error);
@@ -270,25 +286,19 @@ gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
   }
   // No layer may write where another layer reads or writes.
   for (size_t i = 0; i < n_layers; ++i) {
-    const gdn_layer_buffers &A = layers[i];
-    const Span outs[3] = {{A.output, d.v_elems * 4, "output"},
-                          {A.state_out, d.state_elems * 4, "state_out"},
-                          {cap ? A.state_capture : nullptr, cap ? d.capture_elems * 4 : 0,
-                           "state_capture"}};
+    const Spans A = spans_of(d, buffers_of(layers[i], cap), bf16);
+    const Span outs[3] = {A.output, A.state_out, A.capture};
     for (size_t j = 0; j < n_layers; ++j) {
       if (j == i) continue;
-      const gdn_layer_buffers &B = layers[j];
-      const Span all[9] = {{B.q, d.qk_elems * 4, "q"},          {B.k, d.qk_elems * 4, "k"},
-                           {B.v, d.v_elems * 4, "v"},           {B.g, d.sc_elems * 4, "g"},
-                           {B.beta, d.sc_elems * 4, "beta"},    {B.state_in, d.state_elems * 4, "state_in"},
-                           {B.output, d.v_elems * 4, "output"}, {B.state_out, d.state_elems * 4, "state_out"},
-                           {cap ? B.state_capture : nullptr, cap ? d.capture_elems * 4 : 0, "state_capture"}};
+      const Spans B = spans_of(d, buffers_of(layers[j], cap), bf16);
+      const Span all[9] = {B.in[0], B.in[1], B.in[2], B.in[3], B.in[4], B.in[5],
+                           B.output, B.state_out, B.capture};
       for (const Span &o : outs) {
         if (o.p == nullptr) continue;
-        for (const Span &b : all)
-          if (b.p != nullptr && overlap(o, b))
+        for (const Span &x : all)
+          if (x.p != nullptr && overlap(o, x))
             return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: %s of layer %zu overlaps %s of layer %zu",
-                        o.name, i, b.name, j);
+                        o.name, i, x.name, j);
       }
     }
   }
@@ -297,11 +307,8 @@ gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
   for (size_t i0 = 0; i0 < n_layers; i0 += gdn::kMaxLayersPerLaunch) {
     const size_t n = n_layers - i0 < gdn::kMaxLayersPerLaunch ? n_layers - i0 : gdn::kMaxLayersPerLaunch;
     for (size_t i = 0; i < n; ++i) {
-      const gdn_layer_buffers &L = layers[i0 + i];
-      gdn::Problem &p = batch[i];
-      p = d.prob;
-      p.q = L.q; p.k = L.k; p.v = L.v; p.g = L.g; p.beta = L.beta; p.state_in = L.state_in;
-      p.output = L.output; p.state_out = L.state_out; p.capture = cap ? L.state_capture : nullptr;
+      batch[i] = d.prob;
+      fill_problem(batch[i], buffers_of(layers[i0 + i], cap), bf16);
     }
     cudaError_t err = cudaSuccess;
     if (path == Path::kDecode) {
@@ -314,6 +321,57 @@ gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
       return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
   }
   return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_forward(const float *q, const float *k, const float *v, const float *g,
+                       const float *beta, const float *state_in, float *output, float *state_out,
+                       const uint32_t *params, size_t n_params, gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, nullptr}, params, n_params, 0,
+             false, false, stream);
+}
+
+gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, const float *g,
+                               const float *beta, const float *state_in, float *output,
+                               float *state_out, const uint32_t *params, size_t n_params,
+                               float *state_capture, size_t state_capture_elems,
+                               gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, state_capture}, params,
+             n_params, state_capture_elems, true, false, stream);
+}
+
+gdn_status gdn_forward_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                            const float *g, const float *beta, const float *state_in,
+                            gdn_bf16 *output, float *state_out, const uint32_t *params,
+                            size_t n_params, gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, nullptr}, params, n_params, 0,
+             false, true, stream);
+}
+
+gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                    const float *g, const float *beta, const float *state_in,
+                                    gdn_bf16 *output, float *state_out, const uint32_t *params,
+                                    size_t n_params, float *state_capture,
+                                    size_t state_capture_elems, gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, state_capture}, params,
+             n_params, state_capture_elems, true, true, stream);
+}
+
+gdn_status gdn_forward_layers(const gdn_layer_buffers *layers, size_t n_layers,
+                              const uint32_t *params, size_t n_params, int with_capture,
+                              size_t state_capture_elems, gdn_stream_t stream) {
+  return run_layers(layers, n_layers, params, n_params, with_capture, state_capture_elems, false,
+                    stream);
+}
+
+gdn_status gdn_forward_layers_bf16(const gdn_layer_buffers_bf16 *layers, size_t n_layers,
+                                   const uint32_t *params, size_t n_params, int with_capture,
+                                   size_t state_capture_elems, gdn_stream_t stream) {
+  return run_layers(layers, n_layers, params, n_params, with_capture, state_capture_elems, true,
+                    stream);
 }
 
 gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_elems,
@@ -359,7 +417,7 @@ gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
   gdn_status st = decode_params(params, n_params, &d);
   if (st != GDN_OK) return st;
   Path path;
-  st = choose_path(d, capture != 0, &path);
+  st = choose_path(d, capture != 0, false, &path);
   if (st != GDN_OK) return st;
   *name = path_name(path, capture != 0);
   return GDN_OK;

@@ -9,13 +9,17 @@
 namespace gdn {
 
 // One validated problem.  Pointers are device pointers in the layouts of
-// gdn.h; sizes are the decoded params.
+// gdn.h; sizes are the decoded params.  q, k, v and output hold f32, or
+// bf16 when io_bf16 is set; every other buffer is f32.
 struct Problem {
-  const float *q, *k, *v, *g, *beta, *state_in;
-  float *output, *state_out, *capture;  // capture == nullptr: no capture
+  const void *q, *k, *v;
+  const float *g, *beta, *state_in;
+  void *output;
+  float *state_out, *capture;  // capture == nullptr: no capture
   uint32_t dk, dv, nk, nv, nt, ns;
   bool decay_after;
   bool khead_div;
+  bool io_bf16;
   float q_scale;
 };
 
@@ -33,7 +37,7 @@ cudaError_t launch_token_loop_layers(const Problem *layers, uint32_t n_layers, c
 // lazy decay; shaped for FP32 issue throughput.
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 
-// Chunked tensor-core prefill (chunked.cu): D_k = D_v = 128, no capture.
+// Chunked tensor-core prefill (chunked.cu): D_k = D_v = 128, f32 I/O, no capture.
 bool chunked_supported(const Problem &p);
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 

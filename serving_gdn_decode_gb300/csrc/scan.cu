@@ -27,9 +27,15 @@
 //   1/c could overflow), that chunk runs with the decay applied explicitly.
 //
 // * k, q, v (the CTA's rows), g and beta are staged into shared memory with
-//   cp.async in chunks of TC tokens, double-buffered.
+//   cp.async in chunks of TC tokens, double-buffered.  q, k, v and output
+//   are f32 or bf16 (IO).  bf16 k and q are widened once per chunk into an
+//   f32 copy in shared memory (every lane pair of a warp reads all of them,
+//   so widening on each read would repeat the work 32/P times); v is widened
+//   on its one read per row, and y is rounded once on store.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "device_io.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -40,33 +46,19 @@ constexpr int TC = 16;            // tokens per staged chunk (<= 32: one lane pe
 constexpr float kMaxLogScale = 40.f;
 
 struct ScanArgs {
-  const float *__restrict__ q;
-  const float *__restrict__ k;
-  const float *__restrict__ v;
+  const void *__restrict__ q;
+  const void *__restrict__ k;
+  const void *__restrict__ v;
   const float *__restrict__ g;
   const float *__restrict__ beta;
   const float *state_in;  // may be the same buffer as state_out
-  float *__restrict__ output;
+  void *__restrict__ output;
   float *state_out;
   float *__restrict__ capture;
   uint32_t dv, nk, nv, nt, group, khead_div;
   float q_scale;
   uint32_t row_blocks;
 };
-
-__device__ __forceinline__ void cp_async_16(float *smem, const float *gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_4(float *smem, const float *gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ float dot4(const float4 a, const float4 b, float acc) {
   acc = fmaf(a.x, b.x, acc);
@@ -83,23 +75,49 @@ __device__ __forceinline__ void axpy4(float a, const float4 x, float4 &y) {
 __device__ __forceinline__ void scale4(float a, float4 &y) {
   y.x *= a; y.y *= a; y.z *= a; y.w *= a;
 }
+// Pairwise sum of N partials (N a power of two): ((a0 + a1) + (a2 + a3)) ...
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&a)[N]) {
+#pragma unroll
+  for (int h = N / 2; h >= 1; h >>= 1) {
+#pragma unroll
+    for (int i = 0; i < h; ++i) a[i] = a[2 * i] + a[2 * i + 1];
+  }
+  return a[0];
+}
 
-#ifndef GDN_SCAN_P
-#define GDN_SCAN_P 2
-#endif
-constexpr int kScanP = GDN_SCAN_P;  // lanes per state row
+constexpr int kScanP = 2;    // lanes per state row (4 measured slower at D_k = 128)
+constexpr int kScanAcc = 4;  // independent partial sums per dot product
 
-template <int NSG, int P, int WARPS, bool CAPTURE, bool DECAY_AFTER>
+// Bytes of one staging buffer: k[TC][DK] q[TC][DK] v[TC][ROWS] (IO), then
+// g[TC] beta[TC] (f32); a multiple of 16 for every DK and ROWS used here.
+template <typename IO, int DK, int ROWS>
+constexpr int scan_staging_bytes() {
+  return TC * ((2 * DK + ROWS) * static_cast<int>(sizeof(IO)) + 8);
+}
+// Bytes of the f32 copy of one chunk's k and q (bf16 activations only).
+template <typename IO, int DK>
+constexpr int scan_widened_bytes() {
+  return sizeof(IO) == sizeof(float) ? 0 : TC * 2 * DK * static_cast<int>(sizeof(float));
+}
+
+template <typename IO, int NSG, int P, int WARPS, bool CAPTURE, bool DECAY_AFTER>
 __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(const ScanArgs a) {
   constexpr int DK = 32 * NSG;
-  constexpr int NC = DK / (4 * P);      // float4 chunks per lane (each lane holds DK/P cells)
+  constexpr int NC = DK / (4 * P);      // 4-cell chunks per lane (each lane holds DK/P cells)
+  constexpr int NA = NC < kScanAcc ? NC : kScanAcc;  // accumulators per dot product
   constexpr int RPW = 32 / P;           // rows per warp
   constexpr int ROWS = WARPS * RPW;     // rows per CTA
+  constexpr int E16 = 16 / static_cast<int>(sizeof(IO));  // elements per 16-byte copy
+  constexpr int E4 = Act<IO>::kPer4B;                      // elements per 4-byte copy
   static_assert(P == 2 || P == 4, "two or four lanes per row");
-  constexpr int BUF = TC * (2 * DK + ROWS + 2);  // floats per staging buffer (multiple of 4)
-  static_assert(BUF % 4 == 0, "staging buffers must stay 16-byte aligned");
+  constexpr int BUF = scan_staging_bytes<IO, DK, ROWS>();
+  static_assert(BUF % 16 == 0, "staging buffers must stay 16-byte aligned");
+  static_assert(DK % E16 == 0 && ROWS % E4 == 0, "staging granularity");
+  constexpr bool WIDEN = sizeof(IO) != sizeof(float);
 
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(16) unsigned char smem[];
+  float *const kq32 = reinterpret_cast<float *>(smem + 2 * BUF);  // WIDEN: k[TC][DK] q[TC][DK]
   const uint32_t rb = blockIdx.x % a.row_blocks;
   const uint32_t head = blockIdx.x / a.row_blocks;  // = s * nv + vh
   const uint32_t vh = head % a.nv;
@@ -128,26 +146,34 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
   const size_t v_first = (static_cast<size_t>(s) * nt * a.nv + vh) * a.dv + row_cta0;
   const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
 
+  const IO *gk = static_cast<const IO *>(a.k);
+  const IO *gq = static_cast<const IO *>(a.q);
+  const IO *gv = static_cast<const IO *>(a.v);
+  IO *gout = static_cast<IO *>(a.output);
+
   auto stage = [&](uint32_t chunk, int buf) {
-    float *ks = smem + buf * BUF;
-    float *qs = ks + TC * DK;
-    float *vs = qs + TC * DK;
-    float *gs = vs + TC * ROWS;
+    IO *ks = reinterpret_cast<IO *>(smem + buf * BUF);
+    IO *qs = ks + TC * DK;
+    IO *vs = qs + TC * DK;
+    float *gs = reinterpret_cast<float *>(vs + TC * ROWS);
     float *bs = gs + TC;
     const uint32_t t0 = chunk * TC;
     const int n = static_cast<int>(min(static_cast<uint32_t>(TC), nt - t0));
-    for (int i = threadIdx.x; i < n * (DK / 4); i += WARPS * 32) {
-      const int t = i / (DK / 4), e = 4 * (i % (DK / 4));
+    for (int i = threadIdx.x; i < n * (DK / E16); i += WARPS * 32) {
+      const int t = i / (DK / E16), e = E16 * (i % (DK / E16));
       const size_t src = kq_first + (t0 + t) * kq_tok + e;
-      cp_async_16(ks + t * DK + e, a.k + src);
-      cp_async_16(qs + t * DK + e, a.q + src);
+      cp_async_16(ks + t * DK + e, gk + src);
+      cp_async_16(qs + t * DK + e, gq + src);
     }
-    for (int i = threadIdx.x; i < n * ROWS; i += WARPS * 32) {
-      const int t = i / ROWS, r = i % ROWS;
-      if (row_cta0 + r < a.dv)
-        cp_async_4(vs + t * ROWS + r, a.v + v_first + (t0 + t) * v_tok + r);
-      else
-        vs[t * ROWS + r] = 0.f;
+    // v in 4-byte units (one f32 or two bf16 rows; D_v is even for bf16)
+    for (int i = threadIdx.x; i < n * (ROWS / E4); i += WARPS * 32) {
+      const int t = i / (ROWS / E4), r = E4 * (i % (ROWS / E4));
+      if (row_cta0 + r < a.dv) {
+        cp_async_4(vs + t * ROWS + r, gv + v_first + (t0 + t) * v_tok + r);
+      } else {
+#pragma unroll
+        for (int u = 0; u < E4; ++u) Act<IO>::put(vs + t * ROWS + r + u, 0.f);
+      }
     }
     for (int i = threadIdx.x; i < n; i += WARPS * 32) {
       const size_t src = sc_first + static_cast<size_t>(t0 + i) * a.nv;
@@ -168,13 +194,30 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
     }
     __syncthreads();
 
-    const float *ks = smem + (c & 1) * BUF;
-    const float *qs = ks + TC * DK;
-    const float *vs = qs + TC * DK;
-    const float *gs = vs + TC * ROWS;
+    const IO *ks = reinterpret_cast<const IO *>(smem + (c & 1) * BUF);
+    const IO *qs = ks + TC * DK;
+    const IO *vs = qs + TC * DK;
+    const float *gs = reinterpret_cast<const float *>(vs + TC * ROWS);
     const float *bs = gs + TC;
     const uint32_t t0 = c * TC;
     const int n = static_cast<int>(min(static_cast<uint32_t>(TC), nt - t0));
+
+    const float *kf;  // this chunk's k and q as f32
+    const float *qf;
+    if constexpr (WIDEN) {
+      // k and q are adjacent in the staging buffer and in kq32
+      for (int i = threadIdx.x; i < 2 * TC * DK / 4; i += WARPS * 32) {
+        float c4[4];
+        Act<IO>::template get_n<4>(ks + 4 * i, c4);
+        *reinterpret_cast<float4 *>(kq32 + 4 * i) = make_float4(c4[0], c4[1], c4[2], c4[3]);
+      }
+      __syncthreads();
+      kf = kq32;
+      qf = kq32 + TC * DK;
+    } else {
+      kf = reinterpret_cast<const float *>(ks);
+      qf = reinterpret_cast<const float *>(qs);
+    }
 
     // Per-token scalars of this chunk: lane t holds those of token t.
     const float gl = lane < n ? gs[lane] : 0.f;
@@ -198,8 +241,8 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
       const float c_t = __shfl_sync(kFull, cl, tt);
       const float csk = __shfl_sync(kFull, csk_l, tt);
       const float binv = __shfl_sync(kFull, binv_l, tt);
-      const float4 *kr = reinterpret_cast<const float4 *>(ks + tt * DK + 4 * part);
-      const float4 *qr = reinterpret_cast<const float4 *>(qs + tt * DK + 4 * part);
+      const float4 *kr = reinterpret_cast<const float4 *>(kf + tt * DK + 4 * part);
+      const float4 *qr = reinterpret_cast<const float4 *>(qf + tt * DK + 4 * part);
       float4 kk[NC];
 #pragma unroll
       for (int i = 0; i < NC; ++i) kk[i] = kr[P * i];
@@ -208,15 +251,12 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
 #pragma unroll
         for (int i = 0; i < NC; ++i) scale4(at, st[i]);
       }
-      float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+      float pa[NA];
 #pragma unroll
-      for (int i = 0; i < NC; i += 4) {
-        p0 = dot4(st[i], kk[i], p0);
-        if (i + 1 < NC) p1 = dot4(st[i + 1], kk[i + 1], p1);
-        if (i + 2 < NC) p2 = dot4(st[i + 2], kk[i + 2], p2);
-        if (i + 3 < NC) p3 = dot4(st[i + 3], kk[i + 3], p3);
-      }
-      float x = (p0 + p1) + (p2 + p3);
+      for (int j = 0; j < NA; ++j) pa[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < NC; ++i) pa[i % NA] = dot4(st[i], kk[i], pa[i % NA]);
+      float x = tree_sum<NA>(pa);
 #pragma unroll
       for (int o = 1; o < P; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
       if (direct && DECAY_AFTER) {
@@ -224,21 +264,20 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
 #pragma unroll
         for (int i = 0; i < NC; ++i) scale4(at, st[i]);
       }
-      const float d = (vs[tt * ROWS + row_in_cta] - csk * x) * binv;
-      float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+      const float d = (Act<IO>::get(vs + tt * ROWS + row_in_cta) - csk * x) * binv;
+      float ya[NA];
 #pragma unroll
-      for (int i = 0; i < NC; i += 4) {
+      for (int j = 0; j < NA; ++j) ya[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
         axpy4(d, kk[i], st[i]);
-        y0 = dot4(st[i], qr[P * i], y0);
-        if (i + 1 < NC) { axpy4(d, kk[i + 1], st[i + 1]); y1 = dot4(st[i + 1], qr[P * (i + 1)], y1); }
-        if (i + 2 < NC) { axpy4(d, kk[i + 2], st[i + 2]); y2 = dot4(st[i + 2], qr[P * (i + 2)], y2); }
-        if (i + 3 < NC) { axpy4(d, kk[i + 3], st[i + 3]); y3 = dot4(st[i + 3], qr[P * (i + 3)], y3); }
+        ya[i % NA] = dot4(st[i], qr[P * i], ya[i % NA]);
       }
-      float y = (y0 + y1) + (y2 + y3);
+      float y = tree_sum<NA>(ya);
 #pragma unroll
       for (int o = 1; o < P; o <<= 1) y += __shfl_xor_sync(kFull, y, o);
       const size_t tok_head = (static_cast<size_t>(s) * nt + t0 + tt) * a.nv + vh;
-      if (part == 0 && row_ok) a.output[tok_head * a.dv + row] = y * (c_t * a.q_scale);
+      if (part == 0 && row_ok) Act<IO>::put(gout + tok_head * a.dv + row, y * (c_t * a.q_scale));
       if (CAPTURE && row_ok) {
         float *cap = a.capture + (tok_head * a.dv + row) * DK + 4 * part;
 #pragma unroll
@@ -265,7 +304,7 @@ __global__ void __launch_bounds__(WARPS * 32, P == 2 ? 3 : 5) gdn_scan_kernel(co
 
 constexpr int kScanWarps = 4;
 
-template <int NSG, bool CAPTURE, bool DA>
+template <typename IO, int NSG, bool CAPTURE, bool DA>
 cudaError_t launch(const Problem &p, cudaStream_t stream) {
   constexpr int DK = 32 * NSG;
   constexpr int ROWS = kScanWarps * (32 / kScanP);
@@ -280,8 +319,8 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
   const unsigned long long blocks =
       static_cast<unsigned long long>(a.row_blocks) * p.nv * static_cast<unsigned long long>(p.ns);
   if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  const size_t smem = 2u * TC * (2 * DK + ROWS + 2) * sizeof(float);
-  auto kern = gdn_scan_kernel<NSG, kScanP, kScanWarps, CAPTURE, DA>;
+  const size_t smem = 2u * scan_staging_bytes<IO, DK, ROWS>() + scan_widened_bytes<IO, DK>();
+  auto kern = gdn_scan_kernel<IO, NSG, kScanP, kScanWarps, CAPTURE, DA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -289,22 +328,32 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int NSG>
+template <typename IO, int NSG>
 cudaError_t launch_nsg(const Problem &p, cudaStream_t stream) {
   const bool cap = p.capture != nullptr;
-  if (cap) return p.decay_after ? launch<NSG, true, true>(p, stream) : launch<NSG, true, false>(p, stream);
-  return p.decay_after ? launch<NSG, false, true>(p, stream) : launch<NSG, false, false>(p, stream);
+  if (cap)
+    return p.decay_after ? launch<IO, NSG, true, true>(p, stream) : launch<IO, NSG, true, false>(p, stream);
+  return p.decay_after ? launch<IO, NSG, false, true>(p, stream) : launch<IO, NSG, false, false>(p, stream);
+}
+
+template <typename IO>
+cudaError_t launch_io(const Problem &p, cudaStream_t stream) {
+  switch (p.dk) {
+    case 32: return launch_nsg<IO, 1>(p, stream);
+    case 64: return launch_nsg<IO, 2>(p, stream);
+    case 128: return launch_nsg<IO, 4>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream) {
-  switch (p.dk) {
-    case 32: return launch_nsg<1>(p, stream);
-    case 64: return launch_nsg<2>(p, stream);
-    case 128: return launch_nsg<4>(p, stream);
-    default: return cudaErrorInvalidValue;
+  if (p.io_bf16) {
+    if (p.dv % 2 != 0) return cudaErrorInvalidValue;  // v is staged two bf16 rows at a time
+    return launch_io<__nv_bfloat16>(p, stream);
   }
+  return launch_io<float>(p, stream);
 }
 
 }  // namespace gdn

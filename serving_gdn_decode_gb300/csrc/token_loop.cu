@@ -25,8 +25,12 @@
 // k_t, q_t (shared by every row of the CTA), v_t for the CTA's rows, g_t and
 // beta_t are staged into shared memory with cp.async, in chunks of `tc`
 // tokens, double-buffered so the next chunk loads while this one computes.
+// q, k, v and output are f32 or bf16 (IO); staging keeps the stored type and
+// widens to f32 on the shared-memory read, and y is rounded once on store.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "device_io.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -35,8 +39,10 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 struct LayerPtrs {
-  const float *q, *k, *v, *g, *beta, *state_in;
-  float *output, *state_out, *capture;
+  const void *q, *k, *v;
+  const float *g, *beta, *state_in;
+  void *output;
+  float *state_out, *capture;
 };
 
 struct LoopArgs {
@@ -46,24 +52,6 @@ struct LoopArgs {
   uint32_t layer_blocks;  // CTAs per layer = row_blocks * nv * ns
   uint32_t tc;            // tokens per staged chunk
 };
-
-// ---- small PTX helpers (cp.async into shared memory)
-
-__device__ __forceinline__ void cp_async_16(float *smem, const float *gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_4(float *smem, const float *gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 // ---- NSG contiguous floats per lane: streaming global and plain shared I/O
 
@@ -78,10 +66,6 @@ struct Cells<4> {
   static __device__ __forceinline__ void store_cs(float *p, const float (&c)[4]) {
     __stcs(reinterpret_cast<float4 *>(p), make_float4(c[0], c[1], c[2], c[3]));
   }
-  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[4]) {
-    const float4 x = *reinterpret_cast<const float4 *>(p);
-    c[0] = x.x; c[1] = x.y; c[2] = x.z; c[3] = x.w;
-  }
 };
 template <>
 struct Cells<2> {
@@ -92,16 +76,11 @@ struct Cells<2> {
   static __device__ __forceinline__ void store_cs(float *p, const float (&c)[2]) {
     __stcs(reinterpret_cast<float2 *>(p), make_float2(c[0], c[1]));
   }
-  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[2]) {
-    const float2 x = *reinterpret_cast<const float2 *>(p);
-    c[0] = x.x; c[1] = x.y;
-  }
 };
 template <>
 struct Cells<1> {
   static __device__ __forceinline__ void load_cs(const float *p, float (&c)[1]) { c[0] = __ldcs(p); }
   static __device__ __forceinline__ void store_cs(float *p, const float (&c)[1]) { __stcs(p, c[0]); }
-  static __device__ __forceinline__ void load_smem(const float *p, float (&c)[1]) { c[0] = *p; }
 };
 
 // Transpose-reduce R per-lane partials over the warp.  Returns, in every
@@ -132,22 +111,30 @@ struct LayerTable {
   LayerPtrs l[MAXL];
 };
 
+// Bytes of one staging buffer: k[tc][DK] q[tc][DK] v[tc][ROWS] (IO) then
+// g[tc] beta[tc] (f32), padded so both buffers start 16-byte aligned.
+template <typename IO, int DK, int ROWS>
+__host__ __device__ constexpr int staging_bytes(int tc) {
+  return (tc * ((2 * DK + ROWS) * static_cast<int>(sizeof(IO)) + 8) + 15) & ~15;
+}
+
 // Single-layer launches leave the register count to the compiler (48 at
 // D_k = 128: five 8-warp CTAs per SM); multi-layer launches are held to 64.
-template <int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER, int MAXL>
+template <typename IO, int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER, int MAXL>
 __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
     gdn_token_loop_kernel(const LoopArgs a, const LayerPtrs one,
                           const __grid_constant__ LayerTable<MAXL> tab) {
   constexpr int DK = 32 * NSG;
   constexpr int ROWS = WARPS * R;  // rows per CTA
   constexpr int LPR = 32 / R;      // lanes that end up holding one row's total
+  constexpr int E16 = 16 / static_cast<int>(sizeof(IO));  // elements per 16-byte copy
+  constexpr int E4 = Act<IO>::kPer4B;                      // elements per 4-byte copy
   static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+  static_assert(DK % E16 == 0 && ROWS % E4 == 0, "staging granularity");
 
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(16) unsigned char smem[];
   const int tc = static_cast<int>(a.tc);
-  // One staging buffer: k[tc][DK] q[tc][DK] v[tc][ROWS] g[tc] beta[tc],
-  // padded to a multiple of 4 floats so both buffers start 16-byte aligned.
-  const int buf_floats = (tc * (2 * DK + ROWS + 2) + 3) & ~3;
+  const int buf_bytes = staging_bytes<IO, DK, ROWS>(tc);
 
   const uint32_t layer = MAXL == 1 ? 0u : blockIdx.x / a.layer_blocks;
   const uint32_t bid = blockIdx.x - layer * a.layer_blocks;
@@ -186,26 +173,35 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
   const size_t v_first = (static_cast<size_t>(s) * nt * a.nv + vh) * a.dv + row_cta0;
   const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;  // token stride nv
 
+  const IO *gk = static_cast<const IO *>(GDN_LAYER(k));
+  const IO *gq = static_cast<const IO *>(GDN_LAYER(q));
+  const IO *gv = static_cast<const IO *>(GDN_LAYER(v));
+  IO *gout = static_cast<IO *>(GDN_LAYER(output));
+
   auto stage = [&](uint32_t chunk, int buf) {
-    float *ks = smem + buf * buf_floats;
-    float *qs = ks + tc * DK;
-    float *vs = qs + tc * DK;
-    float *gs = vs + tc * ROWS;
+    IO *ks = reinterpret_cast<IO *>(smem + buf * buf_bytes);
+    IO *qs = ks + tc * DK;
+    IO *vs = qs + tc * DK;
+    float *gs = reinterpret_cast<float *>(vs + tc * ROWS);
     float *bs = gs + tc;
     const uint32_t t0 = chunk * static_cast<uint32_t>(tc);
     const int n = static_cast<int>(min(static_cast<uint32_t>(tc), nt - t0));
-    for (int i = threadIdx.x; i < n * (DK / 4); i += WARPS * 32) {
-      const int t = i / (DK / 4), e = 4 * (i % (DK / 4));
+    for (int i = threadIdx.x; i < n * (DK / E16); i += WARPS * 32) {
+      const int t = i / (DK / E16), e = E16 * (i % (DK / E16));
       const size_t src = kq_first + (t0 + t) * kq_tok + e;
-      cp_async_16(ks + t * DK + e, GDN_LAYER(k) + src);
-      cp_async_16(qs + t * DK + e, GDN_LAYER(q) + src);
+      cp_async_16(ks + t * DK + e, gk + src);
+      cp_async_16(qs + t * DK + e, gq + src);
     }
-    for (int i = threadIdx.x; i < n * ROWS; i += WARPS * 32) {
-      const int t = i / ROWS, r = i % ROWS;
-      if (row_cta0 + r < a.dv)
-        cp_async_4(vs + t * ROWS + r, GDN_LAYER(v) + v_first + (t0 + t) * v_tok + r);
-      else
-        vs[t * ROWS + r] = 0.f;
+    // v in 4-byte units (one f32 or two bf16 rows; D_v is even for bf16, so a
+    // unit is either wholly inside the head or wholly past its last row)
+    for (int i = threadIdx.x; i < n * (ROWS / E4); i += WARPS * 32) {
+      const int t = i / (ROWS / E4), r = E4 * (i % (ROWS / E4));
+      if (row_cta0 + r < a.dv) {
+        cp_async_4(vs + t * ROWS + r, gv + v_first + (t0 + t) * v_tok + r);
+      } else {
+#pragma unroll
+        for (int u = 0; u < E4; ++u) Act<IO>::put(vs + t * ROWS + r + u, 0.f);
+      }
     }
     for (int i = threadIdx.x; i < n; i += WARPS * 32) {
       const size_t src = sc_first + static_cast<size_t>(t0 + i) * a.nv;
@@ -229,18 +225,18 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
     }
     __syncthreads();
 
-    const float *ks = smem + (c & 1) * buf_floats;
-    const float *qs = ks + tc * DK;
-    const float *vs = qs + tc * DK;
-    const float *gs = vs + tc * ROWS;
+    const IO *ks = reinterpret_cast<const IO *>(smem + (c & 1) * buf_bytes);
+    const IO *qs = ks + tc * DK;
+    const IO *vs = qs + tc * DK;
+    const float *gs = reinterpret_cast<const float *>(vs + tc * ROWS);
     const float *bs = gs + tc;
     const int n = static_cast<int>(min(static_cast<uint32_t>(tc), nt - c * tc));
 
     for (int tt = 0; tt < n; ++tt) {
       const uint32_t t = c * tc + tt;
       float kk[NSG], qq[NSG];
-      Cells<NSG>::load_smem(ks + tt * DK + lane * NSG, kk);
-      Cells<NSG>::load_smem(qs + tt * DK + lane * NSG, qq);
+      Act<IO>::template get_n<NSG>(ks + tt * DK + lane * NSG, kk);
+      Act<IO>::template get_n<NSG>(qs + tt * DK + lane * NSG, qq);
       const float alpha = expf(-gs[tt]);
       const float b = bs[tt];
 
@@ -256,7 +252,7 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
         }
       }
       const float sk = reduce_rows<R>(part, lane);
-      const float d = (vs[tt * ROWS + warp * R + my_r] - sk) * b;
+      const float d = (Act<IO>::get(vs + tt * ROWS + warp * R + my_r) - sk) * b;
 
       // rank-1 update and S@q
       float py[R];
@@ -275,7 +271,7 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
       }
       const float y = reduce_rows<R>(py, lane);
       const size_t tok_head = (static_cast<size_t>(s) * nt + t) * a.nv + vh;
-      if ((lane % LPR) == 0 && my_row < a.dv) GDN_LAYER(output)[tok_head * a.dv + my_row] = y * a.q_scale;
+      if ((lane % LPR) == 0 && my_row < a.dv) Act<IO>::put(gout + tok_head * a.dv + my_row, y * a.q_scale);
 
       if (CAPTURE) {
         float *cap = GDN_LAYER(capture) + tok_head * a.dv * DK;
@@ -304,7 +300,7 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 4)
 constexpr int kWarps = 8;
 constexpr int kTcMax = 8;
 
-template <int NSG, bool CAPTURE, bool DA, int MAXL>
+template <typename IO, int NSG, bool CAPTURE, bool DA, int MAXL>
 cudaError_t launch_layers(const Problem &p, const Problem *layers, uint32_t n_layers,
                           cudaStream_t stream) {
   constexpr int R = 16 / NSG;
@@ -328,31 +324,39 @@ cudaError_t launch_layers(const Problem &p, const Problem *layers, uint32_t n_la
     t.l[i] = LayerPtrs{x.q, x.k, x.v, x.g, x.beta, x.state_in, x.output, x.state_out, x.capture};
   }
   const LayerPtrs one = t.l[0];
-  const int buf_floats = (static_cast<int>(a.tc) * (2 * DK + ROWS + 2) + 3) & ~3;
-  const size_t smem = 2u * static_cast<size_t>(buf_floats) * sizeof(float);
-  gdn_token_loop_kernel<NSG, R, kWarps, CAPTURE, DA, MAXL>
+  const size_t smem = 2u * static_cast<size_t>(staging_bytes<IO, DK, ROWS>(static_cast<int>(a.tc)));
+  gdn_token_loop_kernel<IO, NSG, R, kWarps, CAPTURE, DA, MAXL>
       <<<static_cast<unsigned>(per_layer * n_layers), kWarps * 32, smem, stream>>>(a, one, t);
   return cudaGetLastError();
 }
 
-template <int NSG, int MAXL>
+template <typename IO, int NSG, int MAXL>
 cudaError_t launch_nsg(const Problem &p, const Problem *layers, uint32_t n, cudaStream_t stream) {
   const bool cap = p.capture != nullptr;
   if (cap)
-    return p.decay_after ? launch_layers<NSG, true, true, MAXL>(p, layers, n, stream)
-                         : launch_layers<NSG, true, false, MAXL>(p, layers, n, stream);
-  return p.decay_after ? launch_layers<NSG, false, true, MAXL>(p, layers, n, stream)
-                       : launch_layers<NSG, false, false, MAXL>(p, layers, n, stream);
+    return p.decay_after ? launch_layers<IO, NSG, true, true, MAXL>(p, layers, n, stream)
+                         : launch_layers<IO, NSG, true, false, MAXL>(p, layers, n, stream);
+  return p.decay_after ? launch_layers<IO, NSG, false, true, MAXL>(p, layers, n, stream)
+                       : launch_layers<IO, NSG, false, false, MAXL>(p, layers, n, stream);
+}
+
+template <typename IO, int MAXL>
+cudaError_t launch_io(const Problem &p, const Problem *layers, uint32_t n, cudaStream_t stream) {
+  switch (p.dk) {
+    case 32: return launch_nsg<IO, 1, MAXL>(p, layers, n, stream);
+    case 64: return launch_nsg<IO, 2, MAXL>(p, layers, n, stream);
+    case 128: return launch_nsg<IO, 4, MAXL>(p, layers, n, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int MAXL>
 cudaError_t launch_dk(const Problem &p, const Problem *layers, uint32_t n, cudaStream_t stream) {
-  switch (p.dk) {
-    case 32: return launch_nsg<1, MAXL>(p, layers, n, stream);
-    case 64: return launch_nsg<2, MAXL>(p, layers, n, stream);
-    case 128: return launch_nsg<4, MAXL>(p, layers, n, stream);
-    default: return cudaErrorInvalidValue;
+  if (p.io_bf16) {
+    if (p.dv % 2 != 0) return cudaErrorInvalidValue;  // v is staged two bf16 rows at a time
+    return launch_io<__nv_bfloat16, MAXL>(p, layers, n, stream);
   }
+  return launch_io<float, MAXL>(p, layers, n, stream);
 }
 
 }  // namespace

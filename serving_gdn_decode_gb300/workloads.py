@@ -79,14 +79,15 @@ class Workload:
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
 
-    def algorithmic_bytes(self) -> int:
+    def algorithmic_bytes(self, act: str = "f32") -> int:
         """Bytes the method must move once per call: every input read once,
         every output written once (q and k counted once although several value
-        heads read them)."""
+        heads read them).  ``act="bf16"``: q, k, v and output take 2 bytes."""
         f = 4
+        a = 2 if act == "bf16" else 4
         b = 2 * self.state_elems * f            # state_in read + state_out write
-        b += 2 * self.qk_elems * f              # q, k
-        b += 2 * self.v_elems * f               # v, output
+        b += 2 * self.qk_elems * a              # q, k
+        b += 2 * self.v_elems * a               # v, output
         b += 2 * self.scalar_elems * f          # g, beta
         if self.capture:
             b += self.capture_elems * f         # state_capture write
@@ -112,13 +113,27 @@ def _unit_rows(rng: np.random.Generator, n_vec: int, dim: int) -> np.ndarray:
     return x.astype(np.float32).reshape(-1)
 
 
-def make_inputs(w: Workload, seed: int = 0) -> dict[str, np.ndarray]:
-    """Draw the seeded inputs of ``w`` as flat float32 arrays."""
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even), returned
+    as float32 arrays holding exactly those values.  Finite inputs only."""
+    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def make_inputs(w: Workload, seed: int = 0, act: str = "f32") -> dict[str, np.ndarray]:
+    """Draw the seeded inputs of ``w`` as flat float32 arrays.  With
+    ``act="bf16"`` q, k and v are rounded to bfloat16 values (still stored as
+    float32 here, so they widen exactly on either side of a comparison)."""
+    if act not in ("f32", "bf16"):
+        raise ValueError(f"act must be 'f32' or 'bf16', not {act!r}")
     rng = np.random.default_rng(seed)
     n_vec = w.n_k_heads * w.n_tokens * w.n_seqs
     q = _unit_rows(rng, n_vec, w.d_k)
     k = _unit_rows(rng, n_vec, w.d_k)
     v = rng.standard_normal(w.v_elems, dtype=np.float32)
+    if act == "bf16":
+        q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
     g = (rng.random(w.scalar_elems, dtype=np.float32) * np.float32(0.5)).astype(np.float32)
     beta = rng.random(w.scalar_elems, dtype=np.float32)
     if w.zero_state:

@@ -135,14 +135,14 @@ class Fake:
         self.addr = {n: (i + 1) * GAP for i, n in enumerate(names)}
         self.cap_elems = w.capture_elems
 
-    def call(self, params=None, capture=False, **over):
+    def call(self, params=None, capture=False, bf16=False, **over):
         a = dict(self.addr, **over)
         p = self.w.params() if params is None else params
         args = [a[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
         if capture:
             return nat.forward_capture_raw(*args, p, a["state_capture"],
-                                           over.get("cap_elems", self.cap_elems))
-        return nat.forward_raw(*args, p)
+                                           over.get("cap_elems", self.cap_elems), bf16=bf16)
+        return nat.forward_raw(*args, p, bf16=bf16)
 
 
 SMALL = WORKLOADS["decode"].with_(n_seqs=2, n_tokens=3)
@@ -284,3 +284,87 @@ def test_layers_checks(L):
 def test_layers_count_limit(L):
     rows = _layer_rows(1025, base=1 << 40)
     assert nat.forward_layers_raw(rows, SMALL.params()) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------- bf16 activations
+
+@no_device
+@pytest.mark.parametrize("name,off", [("q", 8), ("k", 2), ("v", 2), ("output", 1), ("g", 2),
+                                      ("state_in", 8)])
+def test_bf16_misaligned_buffer(L, name, off):
+    f = Fake(SMALL)
+    assert f.call(bf16=True, **{name: f.addr[name] + off}) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "aligned" in nat.gdn_last_error()
+
+
+@no_device
+def test_bf16_spans_are_two_bytes(L):
+    """With bf16 activations, v and output take 2 bytes per element: an output
+    placed right after v's bf16 extent passes every host check (the launch
+    then fails here for want of a device), while the same placement overlaps
+    v's f32 extent."""
+    f = Fake(SMALL)
+    after_v = f.addr["v"] + SMALL.v_elems * 2
+    assert f.call(bf16=True, output=after_v) == nat.GDN_ERR_CUDA
+    assert f.call(output=after_v) == nat.GDN_ERR_INVALID_ARGUMENT
+    # 2-byte aligned output is enough for bf16, not for f32
+    assert f.call(bf16=True, output=f.addr["output"] + 2) == nat.GDN_ERR_CUDA
+    assert f.call(output=f.addr["output"] + 2) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_bf16_unsupported_shapes(L):
+    odd = WORKLOADS["tiny"].with_(d_v=33)
+    assert Fake(odd).call(bf16=True) == nat.GDN_ERR_UNSUPPORTED
+    assert "even D_v" in nat.gdn_last_error()
+    assert Fake(odd).call() != nat.GDN_ERR_UNSUPPORTED       # f32 takes odd D_v
+    w = WORKLOADS["long_prefill"].with_(n_tokens=64, n_seqs=1)
+    assert Fake(w).call(params=w.params(path=PATH_CHUNKED), bf16=True) == nat.GDN_ERR_UNSUPPORTED
+    assert "f32 activations" in nat.gdn_last_error()
+
+
+@no_device
+def test_bf16_layers_checks(L):
+    p = SMALL.params()
+    rows = _layer_rows(2)
+    rows[1][2] += 2                                    # layer 1: v only 2-byte aligned
+    assert nat.forward_layers_raw(rows, p, bf16=True) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "layer 1" in nat.gdn_last_error()
+    rows = _layer_rows(2)
+    rows[1][6] = rows[0][2] + SMALL.v_elems * 2 - 2    # layer 1's output on layer 0's last v
+    assert nat.forward_layers_raw(rows, p, bf16=True) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+def test_binding_bf16_dtype_rules():
+    torch = pytest.importorskip("torch")
+    w = WORKLOADS["tiny"]
+    p = w.params()
+    bf, f32 = torch.bfloat16, torch.float32
+    t = {n: torch.zeros(getattr(w, f"{e}_elems"), dtype=d) for n, e, d in (
+        ("q", "qk", bf), ("k", "qk", bf), ("v", "v", bf), ("g", "scalar", f32),
+        ("beta", "scalar", f32), ("state_in", "state", f32), ("output", "v", bf),
+        ("state_out", "state", f32))}
+    with pytest.raises(nat.GdnError, match="k must be bf16"):
+        nat.gdn_forward(**dict(t, k=t["k"].float()), params=p)
+    with pytest.raises(nat.GdnError, match="g must be f32"):
+        nat.gdn_forward(**dict(t, g=t["g"].to(bf)), params=p)
+    with pytest.raises(nat.GdnError, match="q must be an f32 or bf16"):
+        nat.gdn_forward(**dict(t, q=t["q"].half()), params=p)
+    with pytest.raises(nat.GdnError, match="CUDA tensor"):   # all dtypes right: device check
+        nat.gdn_forward(**t, params=p)
+    with pytest.raises(nat.GdnError, match="pinned host"):   # zero-copy call: pageable memory
+        nat.gdn_forward_host(**t, params=p)
+
+
+def test_round_to_bf16_matches_torch():
+    """The input generator's bf16 rounding (round to nearest, ties to even)
+    against torch's float32 -> bfloat16 conversion, bit for bit, on random
+    values, halfway cases, zeros, subnormals and values near the f32 limit."""
+    torch = pytest.importorskip("torch")
+    from serving_gdn_decode_gb300.workloads import round_to_bf16
+    x = np.random.default_rng(1).standard_normal(1 << 16).astype(np.float32) * np.float32(3)
+    x = np.concatenate([x, np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875, -1.00390625,
+                                     3.0e38, -1e-40, 1e-38], np.float32)])
+    a = round_to_bf16(x)
+    b = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

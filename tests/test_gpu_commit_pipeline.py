@@ -5,7 +5,8 @@ pipeline, through the C ABI.
   capture slice bit for bit (and that slice matches the oracle's state after
   accepted_idx + 1 tokens within the parity bar); out-of-range indices keep
   the sequence's state.
-* HostPipeline splits the batch over groups of sequences; every sequence is
+* HostPipeline splits the batch over groups of sequences, and gdn_forward_host
+  runs the kernel on pinned host buffers (zero-copy); every sequence is
   computed by the same kernel code, so results equal one device call bit for
   bit.
 """
@@ -86,3 +87,61 @@ def test_host_pipeline_rejects_device_tensors(torch):
     t = torch.zeros(4, device="cuda")
     with pytest.raises(nat.GdnError):
         pipe(t, t, t, t, t, t, t, t)
+
+
+ZC_CASES = [  # (workload, capture, act, path)
+    (Workload("zc", 128, 128, 4, 8, 1, 6), False, "f32", 0),        # decode
+    (Workload("zc", 128, 128, 2, 4, 4, 3), True, "f32", 0),         # capture window
+    (Workload("zc", 64, 96, 2, 6, 40, 2), True, "f32", 0),          # scan path
+    (Workload("zc", 128, 128, 4, 8, 3, 5), True, "bf16", 0),        # bf16 activations
+]
+
+
+@pytest.mark.parametrize("case", ZC_CASES, ids=["decode", "capture", "scan", "bf16"])
+def test_zero_copy_host_call_equals_device_call(torch, case):
+    """gdn_forward_host runs the same kernel on pinned host buffers: results
+    equal the device-buffer call bit for bit."""
+    from serving_gdn_decode_gb300 import _native as nat
+    w, capture, act, path = case
+    x = make_inputs(w, 21, act=act)
+    p = w.params(path=path)
+    adt = torch.bfloat16 if act == "bf16" else torch.float32
+
+    def on(dev):
+        t = {k: torch.from_numpy(v) for k, v in x.items()}
+        for k in ("q", "k", "v"):
+            t[k] = t[k].to(adt)
+        t = {k: (v.cuda() if dev else v.pin_memory()) for k, v in t.items()}
+        mk = (lambda n, d: torch.zeros(n, dtype=d, device="cuda")) if dev else \
+            (lambda n, d: torch.zeros(n, dtype=d).pin_memory())
+        out, st = mk(w.v_elems, adt), mk(w.state_elems, torch.float32)
+        cap = mk(w.capture_elems, torch.float32) if capture else None
+        args = (t["q"], t["k"], t["v"], t["g"], t["beta"], t["state_in"], out, st, p)
+        if dev:
+            if capture:
+                nat.gdn_forward_capture(*args, cap)
+            else:
+                nat.gdn_forward(*args)
+        else:
+            nat.gdn_forward_host(*args, state_capture=cap)
+        torch.cuda.synchronize()
+        return [None if a is None else a.cpu().view(torch.int16 if a.dtype == torch.bfloat16
+                                                   else torch.int32).numpy() for a in (out, st, cap)]
+
+    for a, b in zip(on(False), on(True)):
+        if b is not None:
+            np.testing.assert_array_equal(a, b)
+
+
+def test_zero_copy_rejects_device_and_pageable(torch):
+    from serving_gdn_decode_gb300 import _native as nat
+    w = Workload("zc", 32, 32, 1, 2, 1, 1)
+    x = {k: torch.from_numpy(v).pin_memory() for k, v in make_inputs(w, 0).items()}
+    out = torch.zeros(w.v_elems).pin_memory()
+    st = torch.zeros(w.state_elems).pin_memory()
+    with pytest.raises(nat.GdnError, match="pinned host"):
+        nat.gdn_forward_host(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state_in"],
+                             torch.zeros(w.v_elems), st, w.params())     # pageable output
+    with pytest.raises(nat.GdnError, match="pinned host"):
+        nat.gdn_forward_host(x["q"].cuda(), x["k"], x["v"], x["g"], x["beta"], x["state_in"],
+                             out, st, w.params())
