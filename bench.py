@@ -211,7 +211,10 @@ def make_sets(torch, w, n_sets, device, capture=False, act="f32"):
 
 
 def call(nat, d, params, capture):
-    if capture:
+    if "ws" in d:
+        nat.gdn_forward_ws(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], d["output"],
+                           d["state"], params, d["ws"])
+    elif capture:
         nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"], d["output"],
                                 d["state"], params, d["capture"])
     else:
@@ -375,8 +378,12 @@ def extras(torch, nat, peak_gbs, device):
     wp = WORKLOADS["long_prefill"]
     for key, params, act in (("long_prefill_scan", wp.params(path=PATH_SCAN), "f32"),
                              ("long_prefill_chunked", wp.params(path=PATH_CHUNKED), "f32"),
+                             ("long_prefill_chunked_two_pass", wp.params(path=PATH_CHUNKED), "ws"),
                              ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16")):
-        sets = make_sets(torch, wp, 1, device, act=act)
+        sets = make_sets(torch, wp, 1, device, act="f32" if act == "ws" else act)
+        if act == "ws":
+            sets[0]["ws"] = torch.empty(nat.gdn_workspace_size(params), dtype=torch.uint8,
+                                        device=device)
         steps = 5
         t, _ = time_graphed(torch, nat, sets, params, steps, 2)
         s = t / steps

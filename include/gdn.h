@@ -219,6 +219,39 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
                                     size_t n_params, float *state_capture,
                                     size_t state_capture_elems, gdn_stream_t stream);
 
+/*
+ * Two-pass chunked prefill with a caller-provided workspace.
+ *
+ * The chunked (WY / UT) form of the recurrence over 64-token chunks splits
+ * into a part that does not depend on the state -- per chunk, the Gram
+ * products, A, T = (I + A)^-1 and the masked decay-weighted Q K^T -- and the
+ * state pass.  gdn_forward_ws runs the first part for every (seq, value
+ * head, chunk) in parallel, writes it to `workspace`, then runs the state
+ * pass (one CTA per (seq, value head)).  The pages have no chunked kernel:
+ * the chunk equations are the delta rule's published chunkwise form derived
+ * from the recurrence of gated_delta_net.rs (mlx-native 0.4.0) and of the
+ * capture kernel page, with the same TF32 operands as GDN_PATH_CHUNKED.
+ *
+ * gdn_workspace_size: *bytes = the workspace gdn_forward_ws needs for
+ *   `params` -- 32 KB per (seq, value head, chunk) on the chunked path,
+ *   0 on every other path.  Same params checks and status as gdn_path_name.
+ *
+ * gdn_forward_ws: gdn_forward, plus `workspace` (DEVICE, caller-owned,
+ *   at least gdn_workspace_size bytes, 16-byte aligned, overlapping no other
+ *   buffer; may be NULL when the size is 0).  The call overwrites the
+ *   workspace; its contents afterwards are unspecified.  With the chunked
+ *   path (params[6] path bits = GDN_PATH_CHUNKED) the two-pass form runs;
+ *   the other paths run exactly as in gdn_forward and do not touch the
+ *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
+ *   short or overlapping workspace when the size is > 0.
+ */
+gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes);
+
+gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const float *g,
+                          const float *beta, const float *state_in, float *output,
+                          float *state_out, const uint32_t *params, size_t n_params,
+                          void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* gdn_layer_buffers with bf16 q, k, v and output. */
 typedef struct gdn_layer_buffers_bf16 {
   const gdn_bf16 *q, *k, *v;

@@ -11,10 +11,11 @@ from .params import (FLAG_DECAY_AFTER, FLAG_KHEAD_DIV, N_PARAMS, PATH_AUTO, PATH
 __all__ = ["FLAG_DECAY_AFTER", "FLAG_KHEAD_DIV", "N_PARAMS", "PATH_AUTO", "PATH_CHUNKED",
            "PATH_SCAN", "pack_params", "q_scale_bits", "gdn_forward", "gdn_forward_capture",
            "gdn_last_error", "gdn_path_name", "gdn_commit_capture", "gdn_forward_layers",
-           "gdn_forward_host", "HostPipeline", "GdnError"]
+           "gdn_forward_host", "gdn_forward_ws", "gdn_workspace_size", "HostPipeline", "GdnError"]
 
 _NATIVE = ("gdn_forward", "gdn_forward_capture", "gdn_last_error", "gdn_path_name",
-           "gdn_commit_capture", "gdn_forward_layers", "gdn_forward_host", "HostPipeline", "GdnError")
+           "gdn_commit_capture", "gdn_forward_layers", "gdn_forward_host", "gdn_forward_ws",
+           "gdn_workspace_size", "HostPipeline", "GdnError")
 
 
 def __getattr__(name):

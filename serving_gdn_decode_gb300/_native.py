@@ -74,6 +74,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_forward_capture_bf16.restype = ctypes.c_int
             L.gdn_forward_layers_bf16.argtypes = L.gdn_forward_layers.argtypes
             L.gdn_forward_layers_bf16.restype = ctypes.c_int
+            L.gdn_forward_ws.argtypes = [vp] * 8 + [u32p, sz, vp, sz, vp]
+            L.gdn_forward_ws.restype = ctypes.c_int
+            L.gdn_workspace_size.argtypes = [u32p, sz, ctypes.POINTER(ctypes.c_size_t)]
+            L.gdn_workspace_size.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -104,6 +108,17 @@ def gdn_path_name(params, capture: bool = False) -> str:
     return name.value.decode()
 
 
+def gdn_workspace_size(params) -> int:
+    """Bytes of device workspace gdn_forward_ws needs for ``params`` (0 off
+    the chunked path)."""
+    p, pp, n = _params_arg(params)
+    out = ctypes.c_size_t()
+    st = lib().gdn_workspace_size(pp, n, ctypes.byref(out))
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+    return out.value
+
+
 # ---------------------------------------------------------------- raw calls
 
 def forward_raw(q, k, v, g, beta, state_in, output, state_out, params, stream=0,
@@ -113,6 +128,14 @@ def forward_raw(q, k, v, g, beta, state_in, output, state_out, params, stream=0,
     p, pp, n = _params_arg(params)
     fn = lib().gdn_forward_bf16 if bf16 else lib().gdn_forward
     return fn(q, k, v, g, beta, state_in, output, state_out, pp, n, stream)
+
+
+def forward_ws_raw(q, k, v, g, beta, state_in, output, state_out, params, workspace,
+                   workspace_bytes, stream=0) -> int:
+    """Call gdn_forward_ws with integer device addresses; returns the status."""
+    p, pp, n = _params_arg(params)
+    return lib().gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, pp, n, workspace,
+                                workspace_bytes, stream)
 
 
 def forward_capture_raw(q, k, v, g, beta, state_in, output, state_out, params, state_capture,
@@ -251,6 +274,29 @@ def gdn_forward_capture(q, k, v, g, beta, state_in, output, state_out, params, s
     cap = _check("state_capture", state_capture, s["state"] * s["nt"], allow_larger=s["ns"] == 1)
     st = forward_capture_raw(*ptrs, params, cap, state_capture.numel(),
                              _stream(stream, q.device), bf16=bf16)
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+
+
+def gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, params, workspace,
+                   stream=None) -> None:
+    """gdn_forward with a device workspace (a contiguous CUDA tensor of any
+    dtype holding at least gdn_workspace_size(params) bytes, or None when that
+    is 0).  On the chunked path the two-pass form runs; elsewhere as
+    gdn_forward.  f32 activations only."""
+    import torch
+    s = _sizes(params)
+    ptrs, bf16 = _act_ptrs("", q, k, v, g, beta, state_in, output, state_out, s)
+    if bf16:
+        raise GdnError(GDN_ERR_INVALID_ARGUMENT, "gdn_forward_ws takes f32 activations")
+    if workspace is None:
+        wp, wb = None, 0
+    else:
+        if (not isinstance(workspace, torch.Tensor) or not workspace.is_cuda
+                or not workspace.is_contiguous()):
+            raise GdnError(GDN_ERR_INVALID_ARGUMENT, "workspace must be a contiguous CUDA tensor")
+        wp, wb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = forward_ws_raw(*ptrs, params, wp, wb, _stream(stream, q.device))
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 

@@ -43,18 +43,14 @@
 // the CTA writes NaN to its state_out, frees its TMEM and returns.
 #include <cuda_runtime.h>
 
+#include "chunked_common.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
 namespace {
 
-constexpr int C = 64;     // tokens per chunk
-constexpr int D = 128;    // D_k = D_v
-constexpr int NTH = 256;  // threads per CTA
-constexpr int LD = 68;    // row stride (floats) of the plain 64 x 64 work matrices
-constexpr float kMaxLogScale = 40.f;
-constexpr float kRenormLo = 9.3132257e-10f;  // 2^-30
-constexpr float kRenormHi = 1.0737418e+09f;  // 2^30
+using namespace chunked;
+
 
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_X = 128, TM_U = 192, TM_Y = 256, TM_G = 320, TM_V = 384;
@@ -104,185 +100,6 @@ struct Misc {
   int do_renorm;
   int do_fold;
 };
-
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ float tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-// canonical K-major no-swizzle byte offset of element (row, k) in a matrix
-// whose K extent is KE elements
-__device__ __forceinline__ uint32_t canon(int row, int kk, int KE) {
-  return static_cast<uint32_t>(((row >> 3) * (KE >> 2) + (kk >> 2)) * 128 + (row & 7) * 16 + (kk & 3) * 4);
-}
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(128 >> 4) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
-}
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-               "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
-               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-               "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
-               :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(mbar) : "memory");
-}
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void cta_sync() {
-  fence_before();
-  __syncthreads();
-  fence_after();
-}
-
-// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
-
-// Bounded wait on an mbarrier phase: about a second of clock at most.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
-  const long long t0 = clock64();
-  for (;;) {
-    uint32_t done;
-    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-                 "selp.u32 %0, 1, 0, p;\n}\n" : "=r"(done) : "r"(mbar), "r"(phase) : "memory");
-    if (done) return true;
-    if (clock64() - t0 > 2000000000LL) return false;
-  }
-}
-
-#define GDN_TMEM_LD32(taddr, v)                                                                \
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11," \
-               "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"   \
-               "%31}, [%32];\n"                                                                 \
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),        \
-                 "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),      \
-                 "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),  \
-                 "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),  \
-                 "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),  \
-                 "=r"(v[30]), "=r"(v[31])                                                       \
-               : "r"(taddr))
-#define GDN_TMEM_ST32(taddr, v)                                                                 \
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10," \
-               "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"  \
-               "%30,%31,%32};\n"                                                               \
-               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), \
-                  "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),          \
-                  "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),      \
-                  "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),      \
-                  "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),      \
-                  "r"(v[30]), "r"(v[31]))
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Scale the 64 TMEM columns [col, col+64) of this warp's 32 lanes by f.
-__device__ __forceinline__ void tmem_scale64(uint32_t taddr, float f) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t v[32];
-    GDN_TMEM_LD32(taddr + 32 * h, v);
-    tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-    GDN_TMEM_ST32(taddr + 32 * h, v);
-  }
-  tmem_wait_st();
-}
-
-// T = (I + A)^-1 for a strictly lower 64 x 64 A (plain, row stride LD), with
-// 16 x 16 blocks: the diagonal blocks by forward substitution (one thread per
-// column), then T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj level by level
-// (i - j = 1, 2, 3), one warp per block, each lane a 2 x 4 register tile.
-// M is 3 x 256 floats of per-warp scratch.
-__device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
-  // the six blocks above the diagonal stay zero
-  for (int e = tid; e < 6 * 256; e += NTH) {
-    const int b = e >> 8, rr = (e & 255) >> 4, cc = e & 15;
-    const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2), bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-    T[(16 * bi + rr) * LD + 16 * bj + cc] = 0.f;
-  }
-  if (tid < 64) {
-    const int base = 16 * (tid >> 4), cl = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = (r == cl) ? 1.f : 0.f;
-#pragma unroll
-      for (int i = 0; i < r; ++i) acc = fmaf(-A[(base + r) * LD + base + i], x[i], acc);
-      x[r] = acc;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) T[(base + r) * LD + base + cl] = x[r];
-  }
-  __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);  // this lane's 2 x 4 tile of a block
-  for (int d = 1; d <= 3; ++d) {
-    if (warp < 4 - d) {
-      const int j = warp, i = j + d;
-      float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kb = j; kb < i; ++kb) {
-        const float *a0 = A + (16 * i + tr) * LD + 16 * kb;
-        const float *tb = T + (16 * kb) * LD + 16 * j + tc;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float x0 = a0[q], x1 = a0[LD + q];
-          const float4 b = *reinterpret_cast<const float4 *>(tb + q * LD);
-          m0[0] = fmaf(x0, b.x, m0[0]); m0[1] = fmaf(x0, b.y, m0[1]);
-          m0[2] = fmaf(x0, b.z, m0[2]); m0[3] = fmaf(x0, b.w, m0[3]);
-          m1[0] = fmaf(x1, b.x, m1[0]); m1[1] = fmaf(x1, b.y, m1[1]);
-          m1[2] = fmaf(x1, b.z, m1[2]); m1[3] = fmaf(x1, b.w, m1[3]);
-        }
-      }
-      float *mw = M + warp * 256;
-      *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
-      *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
-      __syncwarp();
-      // T_ij = -T_ii M: T_ii is lower triangular (its upper entries are stored zeros)
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-      const float *li = T + (16 * i + tr) * LD + 16 * i;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (q <= tr + 1) {
-          const float l0 = li[q], l1 = li[LD + q];
-          const float4 mm = *reinterpret_cast<const float4 *>(mw + q * 16 + tc);
-          t0[0] = fmaf(l0, mm.x, t0[0]); t0[1] = fmaf(l0, mm.y, t0[1]);
-          t0[2] = fmaf(l0, mm.z, t0[2]); t0[3] = fmaf(l0, mm.w, t0[3]);
-          t1[0] = fmaf(l1, mm.x, t1[0]); t1[1] = fmaf(l1, mm.y, t1[1]);
-          t1[2] = fmaf(l1, mm.z, t1[2]); t1[3] = fmaf(l1, mm.w, t1[3]);
-        }
-      }
-      float *to = T + (16 * i + tr) * LD + 16 * j + tc;
-      *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
-      *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
-    }
-    __syncthreads();
-  }
-}
 
 // Asynchronous copies of one chunk's Q rows into the stack's Q half
 // (canonical layout, rows 64..127), and of its gates and betas into the

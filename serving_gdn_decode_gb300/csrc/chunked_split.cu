@@ -1,0 +1,649 @@
+// Two-pass chunked (WY / UT-transform) prefill of the Gated DeltaNet
+// recurrence on sm_103a, D_k = D_v = 128: the same chunk equations as the
+// single-pass kernel (chunked.cu), split at the state.
+//
+// Everything the chunk equations need that does not depend on the state --
+// the Gram products K K^T and Q K^T, A, T = (I + A)^-1 and
+// P' = q_scale (Q K^T o Gam)_{i<=r} -- is computed for every (seq, value
+// head, chunk) at once by pass 1, one CTA per chunk, and written to a
+// caller-provided workspace (32 KB per chunk: T as an f32 canonical image,
+// P' as a TF32 canonical image).  Pass 2 keeps one CTA per (seq, value head)
+// for the whole token range and runs only the state-dependent part per
+// chunk: operand building, U^T = V^T T''^T + X (-T')^T with X = S K^T,
+// Y^T = S Q'^T + U^T P'^T, S += U^T K'^T.  The serial chain per chunk loses
+// the Gram epilogue and the triangular inverse.
+//
+// Pass 1 is free of the lazy state scale c (S = c * TMEM S): T'' = T diag(beta)
+// and -T' = -T diag(beta gamma) are built by pass 2 from T, and c enters
+// pass 2 through the K operand of X (K_img = c K, so X = (c S~) K^T exactly as
+// in the single-pass kernel), through Q' and through K'.
+//
+// Workspace layout: float ws[head][chunk][8192], head = s * n_v + vh:
+// [0, 4096) T (64 x 64, canonical K-major image, unrounded f32),
+// [4096, 8192) P' (canonical image, rounded to TF32).
+#include <cuda_runtime.h>
+
+#include "chunked_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+using namespace chunked;
+
+constexpr uint32_t kWsFloats = 8192;  // per (head, chunk)
+
+// per-token scalar slots (64 floats each)
+enum { Q_G = 0, Q_GAM, Q_GAMP, Q_BETA, Q_GPREV, Q_EG, Q_GRAW, Q_BRAW, Q_KTS, Q_TPS, Q_QS, Q_NSC };
+
+// Per-chunk scalars of one warp (warp 0): inclusive prefix sums of g over the
+// chunk (G), exclusive ones (Gp), the decays e^-G, e^-Gp, e^G and whether any
+// |G| exceeds kMaxLogScale.  Reads raw g/beta from sc, writes the slots.
+__device__ __forceinline__ bool chunk_scalars(float *sc, int lane, float *GC_out) {
+  float g0 = sc[Q_GRAW * 64 + lane], g1 = sc[Q_GRAW * 64 + lane + 32];
+  const float b0 = sc[Q_BRAW * 64 + lane], b1 = sc[Q_BRAW * 64 + lane + 32];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u0 = __shfl_up_sync(0xffffffffu, g0, o), u1 = __shfl_up_sync(0xffffffffu, g1, o);
+    if (lane >= o) { g0 += u0; g1 += u1; }
+  }
+  g1 += __shfl_sync(0xffffffffu, g0, 31);
+  const float G0 = g0, G1 = g1;
+  const float GC = __shfl_sync(0xffffffffu, G1, 31);
+  float Gp0 = __shfl_up_sync(0xffffffffu, G0, 1);
+  if (lane == 0) Gp0 = 0.f;
+  float Gp1 = __shfl_up_sync(0xffffffffu, G1, 1);
+  const float G0_last = __shfl_sync(0xffffffffu, G0, 31);
+  if (lane == 0) Gp1 = G0_last;
+  const bool extreme = __any_sync(0xffffffffu, fabsf(G0) > kMaxLogScale || fabsf(G1) > kMaxLogScale);
+  sc[Q_G * 64 + lane] = G0; sc[Q_G * 64 + lane + 32] = G1;
+  sc[Q_GPREV * 64 + lane] = Gp0; sc[Q_GPREV * 64 + lane + 32] = Gp1;
+  sc[Q_GAM * 64 + lane] = __expf(-G0); sc[Q_GAM * 64 + lane + 32] = __expf(-G1);
+  sc[Q_GAMP * 64 + lane] = __expf(-Gp0); sc[Q_GAMP * 64 + lane + 32] = __expf(-Gp1);
+  sc[Q_EG * 64 + lane] = __expf(G0); sc[Q_EG * 64 + lane + 32] = __expf(G1);
+  sc[Q_BETA * 64 + lane] = b0; sc[Q_BETA * 64 + lane + 32] = b1;
+  *GC_out = GC;
+  return extreme;
+}
+
+// Asynchronous copies of one chunk's raw g and beta into the scalar area
+// (threads 0..127); tokens past the chunk's end read as zero.
+__device__ __forceinline__ void stage_gates_async(uint32_t sc_addr, const float *g, const float *beta,
+                                                  size_t sc0, size_t nv, int nc, int tid) {
+  if (tid < 128) {
+    const int i = tid & 63;
+    const size_t src = sc0 + static_cast<size_t>(i < nc ? i : 0) * nv;
+    cp_async4(sc_addr + ((tid < 64 ? Q_GRAW : Q_BRAW) * 64 + i) * 4, (tid < 64 ? g : beta) + src,
+              i < nc ? 4u : 0u);
+  }
+}
+
+// Asynchronous copies of 64 rows of 128 floats (row r at base + r * stride)
+// into a canonical K-major image (K extent 128) at dst; rows >= nc are zeros.
+__device__ __forceinline__ void stage_rows_canonical(uint32_t dst, const float *base, size_t stride,
+                                                     int nc, int tid) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int cc = tid + NTH * it;  // 16-byte chunk of the image
+    const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
+    cp_async16(dst + cc * 16, base + static_cast<size_t>(r < nc ? r : 0) * stride + 4 * c4,
+               r < nc ? 16u : 0u);
+  }
+}
+
+// ================================================================ pass 1
+
+// shared memory (bytes): the [K;Q] stack for the Gram, then, once the Gram
+// is in TMEM, A, T and the block products overlaid on it
+constexpr uint32_t P1_STACK = 0;
+constexpr uint32_t P1_A = 0;
+constexpr uint32_t P1_T = 64 * LD * 4;
+constexpr uint32_t P1_M = 2 * 64 * LD * 4;
+constexpr uint32_t P1_SC = 65536;
+constexpr uint32_t P1_MISC = P1_SC + Q_NSC * 64 * 4;
+constexpr uint32_t P1_SMEM = P1_MISC + 64;
+static_assert(P1_M + 3 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
+
+struct PrepArgs {
+  const float *__restrict__ q;
+  const float *__restrict__ k;
+  const float *__restrict__ g;
+  const float *__restrict__ beta;
+  float *__restrict__ ws;
+  uint32_t nk, nv, nt, group, khead_div, nchunks;
+  float q_scale;
+};
+
+struct P1Misc {
+  unsigned long long mbar;
+  uint32_t tmem_base;
+  int failed;
+  int extreme;
+};
+
+template <bool DECAY_AFTER>
+__global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *sA = reinterpret_cast<float *>(smem + P1_A);
+  float *sT = reinterpret_cast<float *>(smem + P1_T);
+  float *sM = reinterpret_cast<float *>(smem + P1_M);
+  float *sc = reinterpret_cast<float *>(smem + P1_SC);
+  P1Misc *misc = reinterpret_cast<P1Misc *>(smem + P1_MISC);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t mbar = smem_addr(&misc->mbar);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127, half = tid >> 7;
+  const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+  // block -> (seq, chunk, value head), value head fastest: the value heads
+  // that read one key head run side by side and share its K and Q in L2
+  const uint32_t vh = blockIdx.x % a.nv;
+  const uint32_t rest = blockIdx.x / a.nv;
+  const uint32_t ch = rest % a.nchunks, s = rest / a.nchunks;
+  const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
+  const uint32_t t0 = ch * C;
+  const int nc = static_cast<int>(min(static_cast<uint32_t>(C), a.nt - t0));
+  const size_t kq_tok = static_cast<size_t>(a.nk) * D;
+  const size_t kq0 = ((static_cast<size_t>(s) * a.nt + t0) * a.nk + kh) * D;
+  const size_t sc0 = (static_cast<size_t>(s) * a.nt + t0) * a.nv + vh;
+  float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
+
+  stage_rows_canonical(sbase + P1_STACK, a.k + kq0, kq_tok, nc, tid);
+  stage_rows_canonical(sbase + P1_STACK + 32768, a.q + kq0, kq_tok, nc, tid);
+  stage_gates_async(sbase + P1_SC, a.g, a.beta, sc0, a.nv, nc, tid);
+  cp_async_commit();
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    misc->failed = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(&misc->tmem_base)), "r"(64));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  cp_async_wait_all();
+  cta_sync();
+  const uint32_t tmem = misc->tmem_base;
+
+  // K and Q to TF32 (round to nearest) in place; per-token scalars (warp 0)
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
+    float4 x = *p;
+    x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
+    *p = x;
+  }
+  if (warp == 0) {
+    float GC;
+    const bool extreme = chunk_scalars(sc, lane, &GC);
+    if (lane == 0) misc->extreme = extreme;
+  }
+  fence_async_smem();
+  cta_sync();
+
+  // Gram [K;Q] K^T -> TMEM (128 lanes x 64 columns)
+  if (tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks) {
+      const uint64_t d = sdesc(sbase + P1_STACK + ks * 256, 4096);
+      mma_ss(tmem, d, d, idesc_tf32(128, 64), ks > 0);
+    }
+    mma_commit(mbar);
+  }
+  const bool ok = mbar_wait(mbar, 0);
+  if (!ok) misc->failed = 1;
+  fence_after();
+  const bool extreme = misc->extreme != 0;
+
+  // A (plain, over the dead stack) and P' (straight to the workspace)
+  {
+    uint32_t gv[32];
+    GDN_TMEM_LD32(tmem + lane_field + 32 * half, gv);
+    tmem_wait_ld();
+    __syncthreads();  // every Gram row is in registers before A overwrites the stack
+    const float *G = sc + Q_G * 64, *eG = sc + Q_EG * 64;
+    if (row < 64) {
+      const int r = row;
+      const float br = sc[Q_BETA * 64 + r];
+      const float Gr = DECAY_AFTER ? sc[Q_GPREV * 64 + r] : G[r];
+      const float bgr = br * (DECAY_AFTER ? sc[Q_GAMP * 64 + r] : sc[Q_GAM * 64 + r]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 32 * half + 4 * j + u;
+          const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
+          e[u] = i < r ? gam * __uint_as_float(gv[4 * j + u]) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
+      }
+    } else {
+      const int r = row - 64;
+      const float Gr = G[r];
+      const float qgr = a.q_scale * sc[Q_GAM * 64 + r];
+      float *wp = ws + 4096;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 32 * half + 4 * j + u;
+          const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+          e[u] = i <= r ? tf32_rna(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * j, 64) / 4) =
+            make_float4(e[0], e[1], e[2], e[3]);
+      }
+    }
+  }
+  cta_sync();
+
+  // T = (I + A)^-1, written as a canonical image (NaN if the Gram wait timed out)
+  tri_inverse(sA, sT, sM, tid);
+  {
+    const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int ci = tid + NTH * it;
+      const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
+      float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+      if (misc->failed) t = make_float4(nan, nan, nan, nan);
+      reinterpret_cast<float4 *>(ws)[ci] = t;
+    }
+  }
+  cta_sync();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(64));
+}
+
+// ================================================================ pass 2
+
+// TMEM columns
+constexpr uint32_t P2_TM_S = 0, P2_TM_X = 128, P2_TM_U = 192, P2_TM_Y = 256, P2_TM_V = 320;
+constexpr uint32_t P2_TM_COLS = 512;
+
+// shared memory (bytes)
+constexpr uint32_t P2_K = 0;                       // c K, 64 x 128 canonical (B of X = S K^T)
+constexpr uint32_t P2_Q = P2_K + 32768;            // Q rows (canonical, cp.async) -> Q' in place
+constexpr uint32_t P2_KT = P2_Q + 32768;           // K'^T, 128 x 64 canonical
+constexpr uint32_t P2_TPP = P2_KT + 32768;         // T image (cp.async) -> T'' in place
+constexpr uint32_t P2_TP = P2_TPP + 16384;         // -T'
+constexpr uint32_t P2_P = P2_TP + 16384;           // P' image (cp.async), used as is
+constexpr uint32_t P2_SC = P2_P + 16384;           // per-token scalars
+constexpr uint32_t P2_MISC = P2_SC + Q_NSC * 64 * 4;
+constexpr int LDS = 132;                           // staging row stride (floats)
+constexpr uint32_t P2_KS = P2_MISC + 64;           // next chunk's K rows (natural), 64 x LDS
+constexpr uint32_t P2_VS = P2_KS + 64 * LDS * 4;   // next chunk's V rows (natural), 64 x LDS
+constexpr uint32_t P2_SMEM = P2_VS + 64 * LDS * 4;
+static_assert(P2_SMEM <= 232448, "pass-2 shared memory");
+static_assert(P2_KS % 16 == 0, "staging alignment");
+
+struct StateArgs {
+  const float *__restrict__ q;
+  const float *__restrict__ k;
+  const float *__restrict__ v;
+  const float *__restrict__ g;
+  const float *__restrict__ beta;
+  const float *state_in;
+  const float *__restrict__ ws;
+  float *__restrict__ output;
+  float *state_out;
+  uint32_t nk, nv, nt, group, khead_div, nchunks;
+  float q_scale;
+};
+
+struct P2Misc {
+  unsigned long long mbar;
+  uint32_t tmem_base;
+  int failed;
+  float c_renorm, c_fold, c_next, c_k;
+  int do_renorm, do_fold;
+};
+
+// One chunk's K and V rows (natural layout, row stride LDS) into the staging buffers.
+__device__ __forceinline__ void p2_stage_kv(uint32_t sbase, const float *kbase, size_t kq_tok,
+                                            const float *vbase, size_t v_tok, int nc, int tid) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int ci = tid + NTH * it;
+    const int r = ci >> 5, c4 = ci & 31;
+    const uint32_t n = r < nc ? 16u : 0u;
+    const int rr = r < nc ? r : 0;
+    const uint32_t dst = static_cast<uint32_t>((r * LDS + 4 * c4) * 4);
+    cp_async16(sbase + P2_KS + dst, kbase + rr * kq_tok + 4 * c4, n);
+    cp_async16(sbase + P2_VS + dst, vbase + rr * v_tok + 4 * c4, n);
+  }
+}
+// One 16 KB workspace image into shared memory.
+__device__ __forceinline__ void p2_stage_image(uint32_t dst, const float *src, int tid) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int ci = tid + NTH * it;
+    cp_async16(dst + ci * 16, src + 4 * ci, 16u);
+  }
+}
+
+template <bool DECAY_AFTER>
+__global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *sc = reinterpret_cast<float *>(smem + P2_SC);
+  const float *sKS = reinterpret_cast<const float *>(smem + P2_KS);
+  const float *sVS = reinterpret_cast<const float *>(smem + P2_VS);
+  P2Misc *misc = reinterpret_cast<P2Misc *>(smem + P2_MISC);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t mbar = smem_addr(&misc->mbar);
+
+  const int tid = static_cast<int>(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;
+  const int half = tid >> 7;
+  const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+  const uint32_t head = blockIdx.x;  // = s * nv + vh
+  const uint32_t vh = head % a.nv, s = head / a.nv;
+  const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
+  const uint32_t nt = a.nt;
+  const size_t state_head = static_cast<size_t>(head) * D * D;
+  const size_t kq_tok = static_cast<size_t>(a.nk) * D;
+  const size_t v_tok = static_cast<size_t>(a.nv) * D;
+  const float *kseq = a.k + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
+  const float *qseq = a.q + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
+  const float *vseq = a.v + ((static_cast<size_t>(s) * nt) * a.nv + vh) * D;
+  const float *wseq = a.ws + static_cast<size_t>(head) * a.nchunks * kWsFloats;
+  const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
+  const uint32_t nchunks = a.nchunks;
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    misc->failed = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(&misc->tmem_base)), "r"(P2_TM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // chunk 0's inputs start arriving while the state is loaded
+  {
+    const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
+    p2_stage_kv(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
+    stage_rows_canonical(sbase + P2_Q, qseq, kq_tok, nc0, tid);
+    stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first, a.nv, nc0, tid);
+    p2_stage_image(sbase + P2_TPP, wseq, tid);
+    p2_stage_image(sbase + P2_P, wseq + 4096, tid);
+    cp_async_commit();
+  }
+  cta_sync();
+  const uint32_t tmem = misc->tmem_base;
+  const uint32_t tl = tmem + lane_field;
+
+  // S <- state_in (c = 1).  Thread: row d_v, columns [64*half, 64*half + 64).
+  {
+    const float4 *src = reinterpret_cast<const float4 *>(a.state_in + state_head + row * D + 64 * half);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = __ldcs(src + 8 * h + j);
+        v[4 * j] = __float_as_uint(x.x); v[4 * j + 1] = __float_as_uint(x.y);
+        v[4 * j + 2] = __float_as_uint(x.z); v[4 * j + 3] = __float_as_uint(x.w);
+      }
+      GDN_TMEM_ST32(tl + P2_TM_S + 64 * half + 32 * h, v);
+    }
+    tmem_wait_st();
+  }
+
+  float c = 1.f;
+  uint32_t phase = 0;
+  bool failed = false;
+
+  for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
+    const uint32_t t0 = ch * C;
+    const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
+    const bool more = ch + 1 < nchunks;
+    const int ncn = more ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
+
+    // ---- 0. this chunk's inputs and workspace images have landed
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- 1. per-token scalars and the lazy-scale bookkeeping (warp 0)
+    if (warp == 0) {
+      float GC;
+      const bool extreme = chunk_scalars(sc, lane, &GC);
+      float cc = c, renorm = 1.f;
+      const bool do_renorm = cc < kRenormLo || cc > kRenormHi;
+      if (do_renorm) { renorm = cc; cc = 1.f; }
+      const float gamC = __expf(-GC);
+      float cnext, fold = 1.f;
+      if (extreme) { fold = cc * gamC; cnext = 1.f; }
+      else { cnext = cc * gamC; }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        const float Gi = sc[Q_G * 64 + i];
+        const float bi = sc[Q_BETA * 64 + i];
+        sc[Q_KTS * 64 + i] = __expf(Gi - GC) / cnext;                       // K' row scale
+        sc[Q_TPS * 64 + i] = -bi * (DECAY_AFTER ? sc[Q_GAMP * 64 + i] : sc[Q_GAM * 64 + i]);  // -T' column
+        sc[Q_QS * 64 + i] = cc * a.q_scale * sc[Q_GAM * 64 + i];           // Q' row scale
+      }
+      if (lane == 0) {
+        misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext; misc->c_k = cc;
+        misc->do_renorm = do_renorm; misc->do_fold = extreme;
+      }
+    }
+    __syncthreads();
+    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold, c_k = misc->c_k;
+    const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
+
+    // ---- 2. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
+    if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
+
+    // ---- 3. operands: c K (canonical), Q' in place, K'^T, V^T (TMEM), T'' in
+    // place and -T' from the T image
+    {
+      const float *qs = sc + Q_QS * 64;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int ci = tid + NTH * it;
+        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
+        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
+        x.x = tf32_rna(x.x * c_k); x.y = tf32_rna(x.y * c_k); x.z = tf32_rna(x.z * c_k); x.w = tf32_rna(x.w * c_k);
+        *reinterpret_cast<float4 *>(smem + P2_K + ci * 16) = x;
+        float4 *pq = reinterpret_cast<float4 *>(smem + P2_Q + ci * 16);
+        float4 y = *pq;
+        const float f = qs[r];
+        y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
+        *pq = y;
+      }
+      const float *kts = sc + Q_KTS * 64;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = 32 * half + 4 * j;
+        *reinterpret_cast<float4 *>(smem + P2_KT + canon(row, i, 64)) =
+            make_float4(tf32_rna(sKS[(i + 0) * LDS + row] * kts[i + 0]),
+                        tf32_rna(sKS[(i + 1) * LDS + row] * kts[i + 1]),
+                        tf32_rna(sKS[(i + 2) * LDS + row] * kts[i + 2]),
+                        tf32_rna(sKS[(i + 3) * LDS + row] * kts[i + 3]));
+      }
+      const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int ci = tid + NTH * it;  // same chunk read and written by this thread
+        const int i0 = 4 * ((ci >> 3) & 15);
+        float4 *pt = reinterpret_cast<float4 *>(smem + P2_TPP + ci * 16);
+        const float4 t = *pt;
+        *reinterpret_cast<float4 *>(smem + P2_TP + ci * 16) =
+            make_float4(tf32_rna(t.x * tps[i0]), tf32_rna(t.y * tps[i0 + 1]),
+                        tf32_rna(t.z * tps[i0 + 2]), tf32_rna(t.w * tps[i0 + 3]));
+        *pt = make_float4(tf32_rna(t.x * bet[i0]), tf32_rna(t.y * bet[i0 + 1]),
+                          tf32_rna(t.z * bet[i0 + 2]), tf32_rna(t.w * bet[i0 + 3]));
+      }
+      uint32_t vv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * LDS + row]));
+      GDN_TMEM_ST32(tl + P2_TM_V + 32 * half, vv);
+      tmem_wait_st();
+    }
+    fence_async_smem();
+    cta_sync();
+    // the K/V staging buffers are free: start the next chunk's rows
+    if (more) {
+      p2_stage_kv(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
+      cp_async_commit();
+    }
+
+    // ---- 4. batch 1: Ut = V^T T''^T; X = S (cK)^T; Ut += X (-T')^T; Yt = S Q'^T
+    if (tid == 0) {
+      const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)
+        mma_ts(tmem + P2_TM_U, tmem + P2_TM_V + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_K + ks * 256, 4096), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)
+        mma_ts(tmem + P2_TM_U, tmem + P2_TM_X + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + P2_TM_Y, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_Q + ks * 256, 4096), i64, ks > 0);
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+    __syncthreads();
+    if (misc->failed) { failed = true; break; }
+    // Q, T'' and -T' are free: the next chunk's Q rows, gates and T image
+    if (more) {
+      stage_rows_canonical(sbase + P2_Q, qseq + (t0 + C) * kq_tok, kq_tok, ncn, tid);
+      stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv,
+                        ncn, tid);
+      p2_stage_image(sbase + P2_TPP, wseq + (ch + 1) * kWsFloats, tid);
+      cp_async_commit();
+    }
+
+    // ---- 5. U^T to TF32 (nearest) in place; extreme gates: decay S now
+    {
+      uint32_t uv[32];
+      GDN_TMEM_LD32(tl + P2_TM_U + 32 * half, uv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rna(__uint_as_float(uv[j])));
+      GDN_TMEM_ST32(tl + P2_TM_U + 32 * half, uv);
+      tmem_wait_st();
+    }
+    if (do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, c_fold);
+    cta_sync();
+
+    // ---- 6. batch 2: Yt += Ut P'^T; S += Ut K'^T
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)
+        mma_ts(tmem + P2_TM_Y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048),
+               idesc_tf32(128, 64), 1);
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)
+        mma_ts(tmem + P2_TM_S, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
+               idesc_tf32(128, 128), 1);
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+    __syncthreads();
+    if (misc->failed) { failed = true; break; }
+    // P' is free: the next chunk's P' image
+    if (more) {
+      p2_stage_image(sbase + P2_P, wseq + (ch + 1) * kWsFloats + 4096, tid);
+      cp_async_commit();
+    }
+
+    // ---- 7. outputs: thread = d_v, tokens [32*half, +32)
+    {
+      uint32_t yv[32];
+      GDN_TMEM_LD32(tl + P2_TM_Y + 32 * half, yv);
+      tmem_wait_ld();
+      float *obase = a.output + ((static_cast<size_t>(s) * nt + t0) * a.nv + vh) * D + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int i = 32 * half + j;
+        if (i < nc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      }
+    }
+    c = misc->c_next;
+    cta_sync();
+  }
+
+  cp_async_wait_all();  // no copy may still be landing in shared memory at exit
+
+  // ---- state_out = c * S (or NaN if a wait timed out)
+  {
+    float4 *dst = reinterpret_cast<float4 *>(a.state_out + state_head + row * D + 64 * half);
+    const float f = failed ? __int_as_float(0x7fc00000) : c;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+      GDN_TMEM_LD32(tl + P2_TM_S + 64 * half + 32 * h, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        __stcs(dst + 8 * h + j, make_float4(__uint_as_float(v[4 * j]) * f, __uint_as_float(v[4 * j + 1]) * f,
+                                            __uint_as_float(v[4 * j + 2]) * f, __uint_as_float(v[4 * j + 3]) * f));
+    }
+  }
+  cta_sync();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(P2_TM_COLS));
+}
+
+template <bool DA>
+cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
+  const uint32_t nchunks = (p.nt + C - 1) / C;
+  const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
+  const unsigned long long prep_blocks = heads * nchunks;
+  if (heads == 0 || prep_blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  PrepArgs pa;
+  pa.q = static_cast<const float *>(p.q); pa.k = static_cast<const float *>(p.k);
+  pa.g = p.g; pa.beta = p.beta; pa.ws = ws;
+  pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = p.nv / p.nk;
+  pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
+  auto prep = gdn_chunk_prep_kernel<DA>;
+  cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(P1_SMEM));
+  if (e != cudaSuccess) return e;
+  prep<<<static_cast<unsigned>(prep_blocks), NTH, P1_SMEM, stream>>>(pa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  StateArgs sa;
+  sa.q = pa.q; sa.k = pa.k; sa.v = static_cast<const float *>(p.v); sa.g = p.g; sa.beta = p.beta;
+  sa.state_in = p.state_in; sa.ws = ws; sa.output = static_cast<float *>(p.output);
+  sa.state_out = p.state_out;
+  sa.nk = p.nk; sa.nv = p.nv; sa.nt = p.nt; sa.group = pa.group; sa.khead_div = pa.khead_div;
+  sa.nchunks = nchunks; sa.q_scale = p.q_scale;
+  auto state = gdn_chunk_state_kernel<DA>;
+  e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
+  if (e != cudaSuccess) return e;
+  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunked_split_workspace_bytes(const Problem &p) {
+  const size_t nchunks = (static_cast<size_t>(p.nt) + C - 1) / C;
+  return static_cast<size_t>(p.nv) * p.ns * nchunks * kWsFloats * sizeof(float);
+}
+
+cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {
+  if (!chunked_supported(p)) return cudaErrorInvalidValue;
+  return p.decay_after ? launch_split<true>(p, workspace, stream) : launch_split<false>(p, workspace, stream);
+}
+
+}  // namespace gdn

@@ -235,8 +235,16 @@ void fill_problem(gdn::Problem &p, const Buffers &b, bool bf16) {
   p.io_bf16 = bf16;
 }
 
+// Workspace bytes of a decoded, path-checked problem (two-pass chunked only).
+size_t workspace_bytes_of(const Decoded &d, Path path) {
+  return path == Path::kChunked ? gdn::chunked_split_workspace_bytes(d.prob) : 0;
+}
+
+// with_ws: the caller passed a workspace argument (gdn_forward_ws); the
+// chunked path then runs in two passes.
 gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t capture_elems,
-               bool with_capture, bool bf16, gdn_stream_t stream) {
+               bool with_capture, bool bf16, gdn_stream_t stream, bool with_ws = false,
+               void *workspace = nullptr, size_t workspace_bytes = 0) {
   g_last_error[0] = '\0';
   Decoded d;
   gdn_status st = decode_params(params, n_params, &d);
@@ -246,13 +254,30 @@ gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t
   Path path;
   st = choose_path(d, with_capture, bf16, &path);
   if (st != GDN_OK) return st;
+  const size_t ws_need = with_ws ? workspace_bytes_of(d, path) : 0;
+  if (ws_need > 0) {
+    if (workspace == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace is NULL");
+    if (!aligned(workspace, 16))
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace must be 16-byte aligned");
+    if (workspace_bytes < ws_need)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace has %zu bytes, %zu needed",
+                  workspace_bytes, ws_need);
+    const Spans sp = spans_of(d, b, bf16);
+    const Span w{workspace, ws_need, "workspace"};
+    const Span all[8] = {sp.in[0], sp.in[1], sp.in[2], sp.in[3], sp.in[4], sp.in[5], sp.output,
+                         sp.state_out};
+    for (const Span &x : all)
+      if (overlap(w, x)) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace overlaps %s", x.name);
+  }
 
   gdn::Problem &p = d.prob;
   fill_problem(p, b, bf16);
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t err = path == Path::kDecode    ? gdn::launch_token_loop(p, cs)
-                          : path == Path::kChunked ? gdn::launch_chunked(p, cs)
-                                                   : gdn::launch_scan(p, cs);
+  const cudaError_t err =
+      path == Path::kDecode    ? gdn::launch_token_loop(p, cs)
+      : path == Path::kChunked ? (ws_need > 0 ? gdn::launch_chunked_split(p, static_cast<float *>(workspace), cs)
+                                              : gdn::launch_chunked(p, cs))
+                               : gdn::launch_scan(p, cs);
   if (err != cudaSuccess)
     return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
   return GDN_OK;
@@ -341,6 +366,28 @@ gdn_status gdn_forward_capture(const float *q, const float *k, const float *v, c
                                gdn_stream_t stream) {
   return run(Buffers{q, k, v, g, beta, state_in, output, state_out, state_capture}, params,
              n_params, state_capture_elems, true, false, stream);
+}
+
+gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const float *g,
+                          const float *beta, const float *state_in, float *output,
+                          float *state_out, const uint32_t *params, size_t n_params,
+                          void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, nullptr}, params, n_params, 0,
+             false, false, stream, true, workspace, workspace_bytes);
+}
+
+gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes) {
+  g_last_error[0] = '\0';
+  if (bytes == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: bytes is NULL");
+  *bytes = 0;
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  Path path;
+  st = choose_path(d, false, false, &path);
+  if (st != GDN_OK) return st;
+  *bytes = workspace_bytes_of(d, path);
+  return GDN_OK;
 }
 
 gdn_status gdn_forward_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,

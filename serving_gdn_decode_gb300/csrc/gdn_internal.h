@@ -41,6 +41,13 @@ cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 bool chunked_supported(const Problem &p);
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 
+// The same chunk equations in two passes (chunked_split.cu): a parallel pass
+// over every (seq, value head, chunk) writes the state-independent chunk
+// matrices to `workspace` (device, chunked_split_workspace_bytes(p) bytes,
+// 16-byte aligned), then one CTA per (seq, value head) runs the state pass.
+size_t chunked_split_workspace_bytes(const Problem &p);
+cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream);
+
 // Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
 // every sequence whose accepted index lies in [0, nt).
 cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,

@@ -25,8 +25,10 @@ def to_dev(x):
     return {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in x.items()}
 
 
-def run_gpu(w, x, params, capture=False, in_place=False, stream=None, dev=None):
-    """Run the CUDA path.  Returns numpy (output, state_out, capture|None)."""
+def run_gpu(w, x, params, capture=False, in_place=False, stream=None, dev=None, workspace=False):
+    """Run the CUDA path.  Returns numpy (output, state_out, capture|None).
+    ``workspace``: call gdn_forward_ws with a workspace of the size
+    gdn_workspace_size reports (the two-pass form on the chunked path)."""
     import torch
 
     from serving_gdn_decode_gb300 import _native as nat
@@ -38,7 +40,14 @@ def run_gpu(w, x, params, capture=False, in_place=False, stream=None, dev=None):
     else:
         st = torch.empty(w.state_elems, dtype=torch.float32, device="cuda")
         st_in = d["state_in"]
-    if capture:
+    if workspace:
+        assert not capture
+        cap = None
+        nb = nat.gdn_workspace_size(params)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        nat.gdn_forward_ws(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params, ws,
+                           stream=stream)
+    elif capture:
         cap = torch.empty(w.capture_elems, dtype=torch.float32, device="cuda")
         nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params,
                                 cap, stream=stream)

@@ -368,3 +368,34 @@ def test_round_to_bf16_matches_torch():
     a = round_to_bf16(x)
     b = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# ---------------------------------------------------------------- two-pass workspace
+
+def test_workspace_size_values(L):
+    w = WORKLOADS["long_prefill"].with_(n_tokens=200, n_seqs=3)
+    assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == 6 * 3 * 4 * 32768 * 8  # 48 heads
+    assert nat.gdn_workspace_size(w.params()) == 0                   # auto: scan
+    assert nat.gdn_workspace_size(SMALL.params()) == 0               # decode
+    with pytest.raises(nat.GdnError):
+        nat.gdn_workspace_size(SMALL.params()[:8])
+
+
+@no_device
+def test_workspace_checks(L):
+    w = WORKLOADS["long_prefill"].with_(n_tokens=100, n_seqs=1)
+    p = w.params(path=PATH_CHUNKED)
+    need = nat.gdn_workspace_size(p)
+    f = Fake(w)
+    args = [f.addr[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+    ws = 10 * GAP
+    assert nat.forward_ws_raw(*args, p, 0, need) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "NULL" in nat.gdn_last_error()
+    assert nat.forward_ws_raw(*args, p, ws + 8, need) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_ws_raw(*args, p, ws, need - 16) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_ws_raw(*args, p, f.addr["v"] + 64, need) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "overlaps" in nat.gdn_last_error()
+    # a good workspace passes every host check (the launch then fails here for want of a device)
+    assert nat.forward_ws_raw(*args, p, ws, need) == nat.GDN_ERR_CUDA
+    # off the chunked path the workspace is not needed
+    assert nat.forward_ws_raw(*args, w.params(), 0, 0) == nat.GDN_ERR_CUDA

@@ -1,5 +1,6 @@
 """GPU parity of the chunked tensor-core prefill path (forced with path bits
-= 2) against the oracle.
+= 2) against the oracle, in both forms: single pass (gdn_forward) and two
+passes over a workspace (gdn_forward_ws; ``split``).
 
 The chunked path rewrites the recurrence in matrix form over 64-token chunks
 and runs its products on tcgen05 with TF32 operands, so it is held to the
@@ -37,24 +38,29 @@ SHAPES = [  # (n_k, n_v, n_tokens, n_seqs)
 ]
 
 
+SPLIT = pytest.mark.parametrize("split", [False, True], ids=["one-pass", "two-pass"])
+
+
+@SPLIT
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
 @pytest.mark.parametrize("flags", [dict(), dict(decay_after=True), dict(khead_div=True),
                                    dict(decay_after=True, khead_div=True)],
                          ids=["first-mod", "after-mod", "first-div", "after-div"])
-def test_chunked_vs_oracle(torch, oracle_mod, shape, flags):
+def test_chunked_vs_oracle(torch, oracle_mod, shape, flags, split):
     nk, nv, nt, ns = shape
     w = Workload("chunked", 128, 128, nk, nv, nt, ns)
     x = make_inputs(w, 51)
     p = w.params(path=PATH_CHUNKED, **flags)
-    out, st, _ = run_gpu(w, x, p)
+    out, st, _ = run_gpu(w, x, p, workspace=split)
     ro, rs, _ = oracle_mod.forward(p, **x)
     assert_close("output", out, ro, max(nt, 9))
     assert_close("state_out", st, rs, max(nt, 9))
 
 
+@SPLIT
 @pytest.mark.parametrize("gate", ["large", "negative", "mixed", "zero"])
 @pytest.mark.parametrize("decay_after", [False, True])
-def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after):
+def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after, split):
     w = Workload("gates", 128, 128, 2, 4, 300, 2)
     x = make_inputs(w, 53)
     rng = np.random.default_rng(55)
@@ -73,7 +79,7 @@ def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after):
     else:
         x["g"] = np.zeros(w.scalar_elems, dtype=np.float32)
     p = w.params(path=PATH_CHUNKED, decay_after=decay_after)
-    out, st, _ = run_gpu(w, x, p)
+    out, st, _ = run_gpu(w, x, p, workspace=split)
     ro, rs, _ = oracle_mod.forward(p, **x)
     assert_close("output", out, ro, w.n_tokens)
     assert_close("state_out", st, rs, w.n_tokens)
@@ -100,15 +106,43 @@ def test_chunked_chaining(torch):
     assert_close("state_out", sb, st.astype(np.float64), 160)
 
 
+@SPLIT
 @pytest.mark.parametrize("flags", [dict(), dict(decay_after=True, khead_div=True)],
                          ids=["first-mod", "after-div"])
-def test_long_prefill_chunked_sampled(torch, oracle_mod, flags):
+def test_long_prefill_chunked_sampled(torch, oracle_mod, flags, split):
     w = WORKLOADS["long_prefill"]
     x = make_inputs(w, 0)
     p = w.params(path=PATH_CHUNKED, **flags)
-    out, st, _ = run_gpu(w, x, p)
+    out, st, _ = run_gpu(w, x, p, workspace=split)
     heads = sample_heads(w, 8, seed=3)
     ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
     go, gs, _ = gather_heads(w, out, st, None, heads)
     assert_close("output", go, ro, w.n_tokens)
     assert_close("state_out", gs, rs, w.n_tokens)
+
+
+def test_two_pass_chaining_and_workspace_reuse(torch):
+    """Two calls in a row through one workspace (its contents from the first
+    call must not leak into the second), and 160 tokens as 100 + 60."""
+    from serving_gdn_decode_gb300 import _native as nat
+    w = Workload("chain", 128, 128, 2, 4, 160, 2)
+    x = make_inputs(w, 59)
+    p = w.params(path=PATH_CHUNKED)
+    out, st, _ = run_gpu(w, x, p, workspace=True)
+    d = to_dev(x)
+    ws = torch.full((nat.gdn_workspace_size(p) // 4,), float("nan"), device="cuda")
+    o2 = torch.empty(w.v_elems, device="cuda")
+    s2 = torch.empty(w.state_elems, device="cuda")
+    for _ in range(2):
+        nat.gdn_forward_ws(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], o2, s2, p, ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(o2.cpu().numpy(), out)
+        np.testing.assert_array_equal(s2.cpu().numpy(), st)
+
+
+def test_two_pass_workspace_size(torch):
+    from serving_gdn_decode_gb300 import _native as nat
+    w = WORKLOADS["long_prefill"]
+    assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == \
+        w.n_v_heads * w.n_seqs * (w.n_tokens // 64) * 32768
+    assert nat.gdn_workspace_size(w.params()) == 0
