@@ -252,6 +252,41 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
                           float *state_out, const uint32_t *params, size_t n_params,
                           void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/*
+ * gdn_forward_chunked_noalloc -- the two-pass chunked prefill of
+ * gdn_forward_ws, for callers that cannot allocate device memory: its chunk
+ * scratch lives in a fixed array inside this library instead of a
+ * caller-provided workspace.  The pages have no counterpart; it exists for
+ * code that only ever receives device buffers from a host framework that
+ * owns all device memory (a plugin or an embedded runtime whose memory pool
+ * offers it no allocation hook), and for loops that must not pay for
+ * cudaMalloc, which can synchronise the device.  Nothing here allocates:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Limit: the fixed scratch is 32 MiB (32 KB per (seq, value head, 64-token
+ * chunk), so at most 1024 of them -- e.g. 16 value heads of 4096 tokens, or
+ * 256 of 256); every GPU on which the library's chunked kernels are loaded
+ * holds it until the process exits.  Larger problems return
+ * GDN_ERR_INVALID_ARGUMENT with the numbers; use gdn_forward_ws for them.
+ *
+ * Arguments, layouts and checks as gdn_forward (f32 activations), for the
+ * chunked path: the params path bits must be GDN_PATH_AUTO or
+ * GDN_PATH_CHUNKED, and the chunked path's shape rules apply (D_k = D_v =
+ * 128, else GDN_ERR_UNSUPPORTED).  Results equal gdn_forward_ws's on the
+ * chunked path.
+ *
+ * The first call on a device looks up the device address of the scratch
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call on a device shares the one scratch array:
+ * each call writes all of it that it reads, so nothing carries over between
+ * calls, but calls that overlap on the GPU (e.g. on two streams at once)
+ * race on it and must be ordered by the caller.
+ */
+gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const float *v,
+                                       const float *g, const float *beta, const float *state_in,
+                                       float *output, float *state_out, const uint32_t *params,
+                                       size_t n_params, gdn_stream_t stream);
+
 /* gdn_layer_buffers with bf16 q, k, v and output. */
 typedef struct gdn_layer_buffers_bf16 {
   const gdn_bf16 *q, *k, *v;

@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_forward_ws.restype = ctypes.c_int
             L.gdn_workspace_size.argtypes = [u32p, sz, ctypes.POINTER(ctypes.c_size_t)]
             L.gdn_workspace_size.restype = ctypes.c_int
+            L.gdn_forward_chunked_noalloc.argtypes = [vp] * 8 + [u32p, sz, vp]
+            L.gdn_forward_chunked_noalloc.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -136,6 +138,16 @@ def forward_ws_raw(q, k, v, g, beta, state_in, output, state_out, params, worksp
     p, pp, n = _params_arg(params)
     return lib().gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, pp, n, workspace,
                                 workspace_bytes, stream)
+
+
+def forward_chunked_noalloc_raw(q, k, v, g, beta, state_in, output, state_out, params,
+                                stream=0) -> int:
+    """Call gdn_forward_chunked_noalloc (two-pass chunked prefill on the
+    library's fixed scratch) with integer device addresses; returns the
+    status."""
+    p, pp, n = _params_arg(params)
+    return lib().gdn_forward_chunked_noalloc(q, k, v, g, beta, state_in, output, state_out, pp, n,
+                                             stream)
 
 
 def forward_capture_raw(q, k, v, g, beta, state_in, output, state_out, params, state_capture,

@@ -23,6 +23,8 @@
 // [4096, 8192) P' (canonical image, rounded to TF32).
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "chunked_common.cuh"
 #include "gdn_internal.h"
 
@@ -644,6 +646,45 @@ size_t chunked_split_workspace_bytes(const Problem &p) {
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {
   if (!chunked_supported(p)) return cudaErrorInvalidValue;
   return p.decay_after ? launch_split<true>(p, workspace, stream) : launch_split<false>(p, workspace, stream);
+}
+
+// ---------------------------------------------------------------- fixed scratch
+//
+// The two-pass workspace in a fixed device array, for callers that cannot
+// allocate device memory (gdn_forward_chunked_noalloc).  Every call on a
+// device uses the same array.  Pass 1 writes every workspace element pass 2
+// reads, so nothing needs clearing between calls; two calls that overlap on
+// the GPU (different streams) would race on it.
+
+static __device__ __align__(256) float g_noalloc_ws[kNoallocWorkspaceBytes / sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float *g_noalloc_addr[kMaxDevices] = {};  // device address of g_noalloc_ws, per device
+}  // namespace
+
+cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream) {
+  if (!chunked_supported(p) || chunked_split_workspace_bytes(p) > kNoallocWorkspaceBytes)
+    return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  float *ws = nullptr;
+  {
+    // Once per device, with that device current: the array's name is only a
+    // host-side stand-in, so its device address comes from the runtime.
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void *addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_noalloc_ws);
+      if (e != cudaSuccess) return e;
+      g_noalloc_addr[dev] = static_cast<float *>(addr);
+    }
+    ws = g_noalloc_addr[dev];
+  }
+  return launch_chunked_split(p, ws, stream);
 }
 
 }  // namespace gdn

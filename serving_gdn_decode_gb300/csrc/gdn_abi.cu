@@ -376,6 +376,39 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
              false, false, stream, true, workspace, workspace_bytes);
 }
 
+gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const float *v,
+                                       const float *g, const float *beta, const float *state_in,
+                                       float *output, float *state_out, const uint32_t *params,
+                                       size_t n_params, gdn_stream_t stream) {
+  g_last_error[0] = '\0';
+  Decoded d;
+  gdn_status st = decode_params(params, n_params, &d);
+  if (st != GDN_OK) return st;
+  if (d.path != GDN_PATH_AUTO && d.path != GDN_PATH_CHUNKED)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: gdn_forward_chunked_noalloc runs the chunked path only (path bits 0 or 2)");
+  d.path = GDN_PATH_CHUNKED;
+  const Buffers b{q, k, v, g, beta, state_in, output, state_out, nullptr};
+  st = check_buffers(d, b, 0, false, false);
+  if (st != GDN_OK) return st;
+  Path path;
+  st = choose_path(d, false, false, &path);
+  if (st != GDN_OK) return st;
+  const size_t need = gdn::chunked_split_workspace_bytes(d.prob);
+  if (need > gdn::kNoallocWorkspaceBytes)
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: this problem needs %zu bytes of chunk scratch; the fixed scratch of "
+                "gdn_forward_chunked_noalloc holds %zu (32 KB per (seq, value head, 64-token "
+                "chunk), at most %zu of them): use gdn_forward_ws with your own workspace",
+                need, gdn::kNoallocWorkspaceBytes, gdn::kNoallocWorkspaceBytes / 32768);
+  gdn::Problem &p = d.prob;
+  fill_problem(p, b, false);
+  const cudaError_t err = gdn::launch_chunked_split_noalloc(p, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
+  return GDN_OK;
+}
+
 gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes) {
   g_last_error[0] = '\0';
   if (bytes == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: bytes is NULL");

@@ -48,6 +48,11 @@ cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 size_t chunked_split_workspace_bytes(const Problem &p);
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream);
 
+// The two-pass form with its workspace in a fixed 32 MiB device array of
+// chunked_split.cu instead of caller memory (no allocation anywhere).
+constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(32) << 20;
+cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream);
+
 // Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
 // every sequence whose accepted index lies in [0, nt).
 cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,

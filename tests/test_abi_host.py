@@ -399,3 +399,27 @@ def test_workspace_checks(L):
     assert nat.forward_ws_raw(*args, p, ws, need) == nat.GDN_ERR_CUDA
     # off the chunked path the workspace is not needed
     assert nat.forward_ws_raw(*args, w.params(), 0, 0) == nat.GDN_ERR_CUDA
+
+
+@no_device
+def test_noalloc_host_checks(L):
+    """gdn_forward_chunked_noalloc: the fixed scratch holds 1024 chunk slots
+    (32 KB each); one more is refused before anything is enqueued, and a
+    problem that fits passes every host check (the launch then fails here for
+    want of a device).  Non-chunked path bits and shapes are refused."""
+    def call(w, params=None, **over):
+        f = Fake(w)
+        a = dict(f.addr, **over)
+        args = [a[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+        return nat.forward_chunked_noalloc_raw(*args, w.params(path=PATH_CHUNKED) if params is None
+                                               else params)
+    fits = WORKLOADS["long_prefill"].with_(n_v_heads=16, n_k_heads=16, n_seqs=1, n_tokens=4096)
+    assert call(fits) == nat.GDN_ERR_CUDA                       # 16 x 64 = 1024 slots
+    over = fits.with_(n_tokens=4097)                            # 16 x 65 slots
+    assert call(over) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "gdn_forward_ws" in nat.gdn_last_error()
+    assert call(fits, params=fits.params()) == nat.GDN_ERR_CUDA  # auto path bits: chunked
+    assert call(fits, params=fits.params(path=PATH_SCAN)) == nat.GDN_ERR_INVALID_ARGUMENT
+    small = WORKLOADS["tiny"].with_(n_tokens=64)
+    assert call(small) == nat.GDN_ERR_UNSUPPORTED               # D_k = 32
+    assert call(fits, output=Fake(fits).addr["q"]) == nat.GDN_ERR_INVALID_ARGUMENT

@@ -1,0 +1,72 @@
+"""GPU test of gdn_forward_chunked_noalloc, the entry point for callers that
+cannot allocate device memory -- code that only receives device buffers
+from a framework owning all device memory, or loops that must not call
+cudaMalloc.  It runs the two-pass chunked prefill with its chunk scratch in
+a fixed 32 MiB array inside the library instead of a caller workspace.
+
+Through the C ABI, two calls in a row (different inputs, so anything left
+in the shared scratch by the first call would show in the second) must give
+what gdn_forward_ws gives with its own workspace, within the long-window bar
+of the other GPU tests; a problem needing more than the fixed scratch is
+refused with a clear error.  The file is named to be collected last.
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_close, run_gpu, to_dev
+from serving_gdn_decode_gb300.params import PATH_CHUNKED
+from serving_gdn_decode_gb300.workloads import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    assert t.cuda.is_available(), "GPU tests need a CUDA device"
+    from serving_gdn_decode_gb300 import build
+    build.build()
+    return t
+
+
+def _noalloc(torch, w, x, params):
+    from serving_gdn_decode_gb300 import _native as nat
+    d = to_dev(x)
+    out = torch.empty(w.v_elems, dtype=torch.float32, device="cuda")
+    st = torch.empty(w.state_elems, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = nat.forward_chunked_noalloc_raw(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                         d["g"].data_ptr(), d["beta"].data_ptr(),
+                                         d["state_in"].data_ptr(), out.data_ptr(), st.data_ptr(),
+                                         params, stream)
+    assert rc == nat.GDN_OK, nat.gdn_last_error()
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), st.cpu().numpy()
+
+
+def test_noalloc_matches_workspace_entry_point_twice(torch):
+    # 4 value heads x 2 seqs x 5 chunks (300 tokens: 4 full chunks + 44)
+    w = Workload("noalloc", 128, 128, 2, 4, 300, 2)
+    for call, seed in enumerate((71, 72)):
+        x = make_inputs(w, seed)
+        p = w.params(path=PATH_CHUNKED, decay_after=call == 1)
+        out, st = _noalloc(torch, w, x, p)
+        ref_out, ref_st, _ = run_gpu(w, x, p, workspace=True)
+        assert_close("output", out, ref_out.astype(np.float64), w.n_tokens)
+        assert_close("state_out", st, ref_st.astype(np.float64), w.n_tokens)
+
+
+def test_noalloc_refuses_more_than_its_scratch(torch):
+    from serving_gdn_decode_gb300 import _native as nat
+    # 4 value heads x 16 seqs x 17 chunks = 1088 chunk slots > 1024; real
+    # buffers of that shape, so the refusal is the only thing tested
+    w = Workload("noalloc_big", 128, 128, 2, 4, 1025, 16)
+    x = to_dev(make_inputs(w, 73))
+    out = torch.empty(w.v_elems, dtype=torch.float32, device="cuda")
+    st = torch.empty(w.state_elems, dtype=torch.float32, device="cuda")
+    rc = nat.forward_chunked_noalloc_raw(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                         x["g"].data_ptr(), x["beta"].data_ptr(),
+                                         x["state_in"].data_ptr(), out.data_ptr(), st.data_ptr(),
+                                         w.params(path=PATH_CHUNKED))
+    assert rc == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "gdn_forward_ws" in nat.gdn_last_error()
