@@ -76,6 +76,11 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+// Wait until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 // Bounded wait on an mbarrier phase: about a second of clock at most.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {

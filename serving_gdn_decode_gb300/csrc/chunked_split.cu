@@ -264,7 +264,10 @@ __global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a
 // ================================================================ pass 2
 
 // TMEM columns
-constexpr uint32_t P2_TM_S = 0, P2_TM_X = 128, P2_TM_U = 192, P2_TM_Y = 256, P2_TM_V = 320;
+// (Y^T alternates between two regions so a chunk's outputs are read out while
+// the next chunk's products run)
+constexpr uint32_t P2_TM_S = 0, P2_TM_X = 128, P2_TM_U = 192, P2_TM_Y0 = 256, P2_TM_V = 320,
+                   P2_TM_Y1 = 384;
 constexpr uint32_t P2_TM_COLS = 512;
 
 // shared memory (bytes)
@@ -375,7 +378,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     stage_rows_canonical(sbase + P2_Q, qseq, kq_tok, nc0, tid);
     stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first, a.nv, nc0, tid);
     p2_stage_image(sbase + P2_TPP, wseq, tid);
-    p2_stage_image(sbase + P2_P, wseq + 4096, tid);
+    cp_async_commit();
+    p2_stage_image(sbase + P2_P, wseq + 4096, tid);  // its own group: waited for before batch 2
     cp_async_commit();
   }
   cta_sync();
@@ -409,8 +413,10 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     const bool more = ch + 1 < nchunks;
     const int ncn = more ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
 
-    // ---- 0. this chunk's inputs and workspace images have landed
-    cp_async_wait_all();
+    // ---- 0. this chunk's K, V, Q rows, gates and T image have landed.  Copy
+    // groups complete in order; the newest one is this chunk's P', which only
+    // batch 2 reads, so it may still be in flight.
+    cp_async_wait<1>();
     __syncthreads();
 
     // ---- 1. per-token scalars and the lazy-scale bookkeeping (warp 0)
@@ -445,8 +451,9 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     // ---- 2. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
     if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
 
-    // ---- 3. operands: c K (canonical), Q' in place, K'^T, V^T (TMEM), T'' in
-    // place and -T' from the T image
+    const uint32_t tm_y = (ch & 1) ? P2_TM_Y1 : P2_TM_Y0;
+
+    // ---- 3a. operands of the S products: c K (canonical) and Q' in place
     {
       const float *qs = sc + Q_QS * 64;
 #pragma unroll
@@ -462,6 +469,23 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
         y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
         *pq = y;
       }
+    }
+    fence_async_smem();
+    cta_sync();
+
+    // ---- 4a. X = S (cK)^T and Yt = S Q'^T start while the other operands are built
+    if (tid == 0) {
+      const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_K + ks * 256, 4096), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_Q + ks * 256, 4096), i64, ks > 0);
+    }
+
+    // ---- 3b. K'^T, T'' in place and -T' from the T image, V^T (TMEM)
+    {
       const float *kts = sc + Q_KTS * 64;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -499,23 +523,33 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
       cp_async_commit();
     }
 
-    // ---- 4. batch 1: Ut = V^T T''^T; X = S (cK)^T; Ut += X (-T')^T; Yt = S Q'^T
+    // ---- 4b. Ut = V^T T''^T; Ut += X (-T')^T (X was issued first, so it is done or in flight)
     if (tid == 0) {
       const uint32_t i64 = idesc_tf32(128, 64);
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
         mma_ts(tmem + P2_TM_U, tmem + P2_TM_V + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), i64, ks > 0);
 #pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_K + ks * 256, 4096), i64, ks > 0);
-#pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
         mma_ts(tmem + P2_TM_U, tmem + P2_TM_X + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + P2_TM_Y, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_Q + ks * 256, 4096), i64, ks > 0);
       mma_commit(mbar);
     }
+
+    // ---- the previous chunk's outputs, from its Y^T region, while these run
+    if (ch > 0) {
+      const uint32_t tm_yp = (ch & 1) ? P2_TM_Y0 : P2_TM_Y1;
+      const int ncp = C;  // every chunk but the last is full
+      uint32_t yv[32];
+      GDN_TMEM_LD32(tl + tm_yp + 32 * half, yv);
+      tmem_wait_ld();
+      float *obase = a.output + ((static_cast<size_t>(s) * nt + (t0 - C)) * a.nv + vh) * D + row;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int i = 32 * half + j;
+        if (i < ncp) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      }
+    }
+
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;
     fence_after();
@@ -541,13 +575,17 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
       tmem_wait_st();
     }
     if (do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, c_fold);
+    // this chunk's P' has landed (the two newer groups, the next chunk's
+    // K/V and Q/T copies, may still be in flight)
+    if (more) cp_async_wait<2>(); else cp_async_wait<0>();
+    fence_async_smem();
     cta_sync();
 
     // ---- 6. batch 2: Yt += Ut P'^T; S += Ut K'^T
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_Y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048),
+        mma_ts(tmem + tm_y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048),
                idesc_tf32(128, 64), 1);
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
@@ -566,10 +604,10 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
       cp_async_commit();
     }
 
-    // ---- 7. outputs: thread = d_v, tokens [32*half, +32)
-    {
+    // ---- 7. the last chunk's outputs now (the others are written during the next chunk)
+    if (!more) {
       uint32_t yv[32];
-      GDN_TMEM_LD32(tl + P2_TM_Y + 32 * half, yv);
+      GDN_TMEM_LD32(tl + tm_y + 32 * half, yv);
       tmem_wait_ld();
       float *obase = a.output + ((static_cast<size_t>(s) * nt + t0) * a.nv + vh) * D + row;
 #pragma unroll

@@ -4,6 +4,7 @@ For profiler captures and quick checks, e.g.::
 
     python -m serving_gdn_decode_gb300.run_case decode --calls 3
     python -m serving_gdn_decode_gb300.run_case long_prefill --tokens 512 --path scan
+    python -m serving_gdn_decode_gb300.run_case long_prefill --tokens 512 --path chunked --two-pass
 """
 from __future__ import annotations
 
@@ -25,6 +26,8 @@ def main(argv=None):
     ap.add_argument("--capture", action="store_true", help="use gdn_forward_capture")
     ap.add_argument("--decay-after", action="store_true")
     ap.add_argument("--khead-div", action="store_true")
+    ap.add_argument("--two-pass", action="store_true",
+                    help="use gdn_forward_ws with a workspace (two-pass form on the chunked path)")
     ap.add_argument("--commit", action="store_true",
                     help="after each capture call, commit a random accepted token per sequence")
     a = ap.parse_args(argv)
@@ -51,8 +54,13 @@ def main(argv=None):
         cap = torch.empty(w.capture_elems, dtype=torch.float32, device=dev)
         idx = torch.from_numpy(np.random.default_rng(0).integers(0, w.n_tokens, w.n_seqs)
                                .astype(np.int32)).to(dev)
+    ws = None
+    if a.two_pass:
+        ws = torch.empty(max(16, nat.gdn_workspace_size(p)), dtype=torch.uint8, device=dev)
     for _ in range(a.calls):
-        if capture:
+        if ws is not None:
+            nat.gdn_forward_ws(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], out, st, p, ws)
+        elif capture:
             nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state_in"], out,
                                     st, p, cap)
             if a.commit:
