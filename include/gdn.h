@@ -243,7 +243,9 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *   path (params[6] path bits = GDN_PATH_CHUNKED) the two-pass form runs;
  *   the other paths run exactly as in gdn_forward and do not touch the
  *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
- *   short or overlapping workspace when the size is > 0.
+ *   short or overlapping workspace when the size is > 0, and, on the chunked
+ *   path, for v not 16-byte aligned (the state pass reads K, Q and V rows
+ *   with the tensor memory accelerator).
  */
 gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes);
 

@@ -11,7 +11,11 @@
 // for the whole token range and runs only the state-dependent part per
 // chunk: operand building, U^T = V^T T''^T + X (-T')^T with X = S K^T,
 // Y^T = S Q'^T + U^T P'^T, S += U^T K'^T.  The serial chain per chunk loses
-// the Gram epilogue and the triangular inverse.
+// the Gram epilogue and the triangular inverse.  Pass 2 loads by TMA: K and
+// Q rows land 128-byte swizzled, which is both the MMA's K-major SWIZZLE_128B
+// operand layout and conflict-free for the transposed reads that build K'^T;
+// V rows, the T image and P' land as plain boxes and bulk copies, each group
+// on its own mbarrier, so no thread stalls issuing copies.
 //
 // Pass 1 is free of the lazy state scale c (S = c * TMEM S): T'' = T diag(beta)
 // and -T' = -T diag(beta gamma) are built by pass 2 from T, and c enters
@@ -21,6 +25,8 @@
 // Workspace layout: float ws[head][chunk][8192], head = s * n_v + vh:
 // [0, 4096) T (64 x 64, canonical K-major image, unrounded f32),
 // [4096, 8192) P' (canonical image, rounded to TF32).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -263,33 +269,31 @@ __global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a
 
 // ================================================================ pass 2
 
-// TMEM columns
-// (Y^T alternates between two regions so a chunk's outputs are read out while
-// the next chunk's products run)
+// TMEM columns (Y^T alternates between two regions so a chunk's outputs are
+// read out while the next chunk's products run)
 constexpr uint32_t P2_TM_S = 0, P2_TM_X = 128, P2_TM_U = 192, P2_TM_Y0 = 256, P2_TM_V = 320,
                    P2_TM_Y1 = 384;
 constexpr uint32_t P2_TM_COLS = 512;
 
-// shared memory (bytes)
-constexpr uint32_t P2_K = 0;                       // c K, 64 x 128 canonical (B of X = S K^T)
-constexpr uint32_t P2_Q = P2_K + 32768;            // Q rows (canonical, cp.async) -> Q' in place
-constexpr uint32_t P2_KT = P2_Q + 32768;           // K'^T, 128 x 64 canonical
-constexpr uint32_t P2_TPP = P2_KT + 32768;         // T image (cp.async) -> T'' in place
+// Shared memory (bytes from a 1024-aligned base).  K and Q arrive by TMA as
+// four 64-row x 128-byte boxes each, 128-byte swizzled: the layout the MMA
+// reads as a K-major SWIZZLE_128B operand, and one in which a warp reading
+// either a row or a column of K touches distinct banks.
+constexpr uint32_t P2_K = 0;                       // K (TMA) -> c K in TF32, in place
+constexpr uint32_t P2_Q = P2_K + 32768;            // Q (TMA) -> Q' in TF32, in place
+constexpr uint32_t P2_KT = P2_Q + 32768;           // K'^T, 128 x 64 canonical (no swizzle)
+constexpr uint32_t P2_TPP = P2_KT + 32768;         // T image (bulk copy) -> T'' in place
 constexpr uint32_t P2_TP = P2_TPP + 16384;         // -T'
-constexpr uint32_t P2_P = P2_TP + 16384;           // P' image (cp.async), used as is
-constexpr uint32_t P2_SC = P2_P + 16384;           // per-token scalars
+constexpr uint32_t P2_P = P2_TP + 16384;           // P' image (bulk copy), used as is
+constexpr uint32_t P2_VS = P2_P + 16384;           // V rows (TMA), 64 x 128 natural
+constexpr uint32_t P2_SC = P2_VS + 32768;          // per-token scalars
 constexpr uint32_t P2_MISC = P2_SC + Q_NSC * 64 * 4;
-constexpr int LDS = 132;                           // staging row stride (floats)
-constexpr uint32_t P2_KS = P2_MISC + 64;           // next chunk's K rows (natural), 64 x LDS
-constexpr uint32_t P2_VS = P2_KS + 64 * LDS * 4;   // next chunk's V rows (natural), 64 x LDS
-constexpr uint32_t P2_SMEM = P2_VS + 64 * LDS * 4;
+constexpr uint32_t P2_SMEM = P2_MISC + 128 + 1024;  // + room to align the base to 1024
 static_assert(P2_SMEM <= 232448, "pass-2 shared memory");
-static_assert(P2_KS % 16 == 0, "staging alignment");
+constexpr uint32_t kImgBytes = 16384;   // one 64 x 64 workspace image
+constexpr uint32_t kRowsBytes = 32768;  // 64 rows of 128 floats
 
 struct StateArgs {
-  const float *__restrict__ q;
-  const float *__restrict__ k;
-  const float *__restrict__ v;
   const float *__restrict__ g;
   const float *__restrict__ beta;
   const float *state_in;
@@ -301,45 +305,74 @@ struct StateArgs {
 };
 
 struct P2Misc {
-  unsigned long long mbar;
+  unsigned long long mbar1;   // batch-1 MMA commits
+  unsigned long long mbar2;   // batch-2 MMA commits
+  unsigned long long bar_in;  // TMA: K, Q rows and the T image of a chunk
+  unsigned long long bar_v;   // TMA: V rows of a chunk
+  unsigned long long bar_p;   // TMA: P' image of a chunk
   uint32_t tmem_base;
   int failed;
   float c_renorm, c_fold, c_next, c_k;
   int do_renorm, do_fold;
 };
 
-// One chunk's K and V rows (natural layout, row stride LDS) into the staging buffers.
-__device__ __forceinline__ void p2_stage_kv(uint32_t sbase, const float *kbase, size_t kq_tok,
-                                            const float *vbase, size_t v_tok, int nc, int tid) {
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int ci = tid + NTH * it;
-    const int r = ci >> 5, c4 = ci & 31;
-    const uint32_t n = r < nc ? 16u : 0u;
-    const int rr = r < nc ? r : 0;
-    const uint32_t dst = static_cast<uint32_t>((r * LDS + 4 * c4) * 4);
-    cp_async16(sbase + P2_KS + dst, kbase + rr * kq_tok + 4 * c4, n);
-    cp_async16(sbase + P2_VS + dst, vbase + rr * v_tok + 4 * c4, n);
-  }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
-// One 16 KB workspace image into shared memory.
-__device__ __forceinline__ void p2_stage_image(uint32_t dst, const float *src, int tid) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int ci = tid + NTH * it;
-    cp_async16(dst + ci * 16, src + 4 * ci, 16u);
-  }
+// One box of a 4-D tensor map (coordinates innermost first) into shared memory.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+// A contiguous global block into shared memory (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Byte offset of element (row, col) of a 64 x 128 f32 tile held as four
+// 128-byte-swizzled 64 x 32 boxes.
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return static_cast<uint32_t>((col >> 5) * 8192 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
+                               (col & 3) * 4);
 }
 
+// Thread 0: this chunk's K and Q rows (4 boxes each) and T image, on bar_in.
+__device__ __forceinline__ void p2_load_in(uint32_t sbase, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
+                                           int kh, int t0, int s, const float *timg, uint32_t bar) {
+  mbar_expect_tx(bar, 2 * kRowsBytes + kImgBytes);
+#pragma unroll
+  for (int cb = 0; cb < 4; ++cb) {
+    tma_load_4d(sbase + P2_K + cb * 8192, tm_k, 32 * cb, kh, t0, s, bar);
+    tma_load_4d(sbase + P2_Q + cb * 8192, tm_q, 32 * cb, kh, t0, s, bar);
+  }
+  bulk_load(sbase + P2_TPP, timg, kImgBytes, bar);
+}
+
+// The state pass (see the file comment); loads by TMA, waits bounded.
 template <bool DECAY_AFTER>
-__global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+__global__ void __launch_bounds__(NTH, 1)
+    gdn_chunk_state_kernel(const StateArgs a, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // operate from a 1024-byte aligned base (the swizzled boxes need it)
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
+  unsigned char *smem = smem_raw + pad;
   float *sc = reinterpret_cast<float *>(smem + P2_SC);
-  const float *sKS = reinterpret_cast<const float *>(smem + P2_KS);
   const float *sVS = reinterpret_cast<const float *>(smem + P2_VS);
   P2Misc *misc = reinterpret_cast<P2Misc *>(smem + P2_MISC);
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t mbar = smem_addr(&misc->mbar);
+  const uint32_t sbase = raw_addr + pad;
+  const uint32_t mbar1 = smem_addr(&misc->mbar1), mbar2 = smem_addr(&misc->mbar2);
+  const uint32_t bar_in = smem_addr(&misc->bar_in), bar_v = smem_addr(&misc->bar_v),
+                 bar_p = smem_addr(&misc->bar_p);
 
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -352,17 +385,17 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
   const uint32_t nt = a.nt;
   const size_t state_head = static_cast<size_t>(head) * D * D;
-  const size_t kq_tok = static_cast<size_t>(a.nk) * D;
   const size_t v_tok = static_cast<size_t>(a.nv) * D;
-  const float *kseq = a.k + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
-  const float *qseq = a.q + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
-  const float *vseq = a.v + ((static_cast<size_t>(s) * nt) * a.nv + vh) * D;
   const float *wseq = a.ws + static_cast<size_t>(head) * a.nchunks * kWsFloats;
   const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
   const uint32_t nchunks = a.nchunks;
 
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar1));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar2));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_in));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_v));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_p));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
   }
@@ -371,15 +404,18 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
                  :: "r"(smem_addr(&misc->tmem_base)), "r"(P2_TM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  __syncthreads();  // barriers initialised before anyone waits on them
   // chunk 0's inputs start arriving while the state is loaded
   {
     const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
-    p2_stage_kv(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
-    stage_rows_canonical(sbase + P2_Q, qseq, kq_tok, nc0, tid);
+    if (tid == 0) {
+      p2_load_in(sbase, &tm_k, &tm_q, static_cast<int>(kh), 0, static_cast<int>(s), wseq, bar_in);
+      mbar_expect_tx(bar_v, kRowsBytes);
+      tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), 0, static_cast<int>(s), bar_v);
+      mbar_expect_tx(bar_p, kImgBytes);
+      bulk_load(sbase + P2_P, wseq + 4096, kImgBytes, bar_p);
+    }
     stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first, a.nv, nc0, tid);
-    p2_stage_image(sbase + P2_TPP, wseq, tid);
-    cp_async_commit();
-    p2_stage_image(sbase + P2_P, wseq + 4096, tid);  // its own group: waited for before batch 2
     cp_async_commit();
   }
   cta_sync();
@@ -404,20 +440,26 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
   }
 
   float c = 1.f;
-  uint32_t phase = 0;
+  uint32_t ph1 = 0, ph2 = 0;
   bool failed = false;
+  // TMA arms and waits per barrier (uniform over the CTA): a copy is in
+  // flight while a barrier has been armed more often than waited on
+  uint32_t armed_in = 1, armed_v = 1, armed_p = 1, waited_in = 0, waited_v = 0, waited_p = 0;
 
   for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
     const uint32_t t0 = ch * C;
     const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
     const bool more = ch + 1 < nchunks;
     const int ncn = more ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
+    const uint32_t tm_y = (ch & 1) ? P2_TM_Y1 : P2_TM_Y0;
+    const uint32_t par = ch & 1;  // phase parity of this chunk's TMA barriers
 
-    // ---- 0. this chunk's K, V, Q rows, gates and T image have landed.  Copy
-    // groups complete in order; the newest one is this chunk's P', which only
-    // batch 2 reads, so it may still be in flight.
-    cp_async_wait<1>();
+    // ---- 0. this chunk's K, Q rows, T image (TMA) and gates (cp.async) have landed
+    if (!mbar_wait(bar_in, par)) misc->failed = 1;
+    ++waited_in;
+    cp_async_wait_all();
     __syncthreads();
+    if (misc->failed) { failed = true; break; }
 
     // ---- 1. per-token scalars and the lazy-scale bookkeeping (warp 0)
     if (warp == 0) {
@@ -451,50 +493,38 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     // ---- 2. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
     if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
 
-    const uint32_t tm_y = (ch & 1) ? P2_TM_Y1 : P2_TM_Y0;
+    // ---- 3a. K'^T from the raw K rows (thread: d_k = row, tokens [32*half, +32))
+    {
+      const float *kts = sc + Q_KTS * 64;
+      const unsigned char *kb = smem + P2_K;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = 32 * half + 4 * j;
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          e[u] = tf32_rna(*reinterpret_cast<const float *>(kb + sw128_off(i + u, row)) * kts[i + u]);
+        *reinterpret_cast<float4 *>(smem + P2_KT + canon(row, i, 64)) = make_float4(e[0], e[1], e[2], e[3]);
+      }
+    }
+    __syncthreads();  // every raw K value is read before K is scaled in place
 
-    // ---- 3a. operands of the S products: c K (canonical) and Q' in place
+    // ---- 3b. c K and Q' (TF32) in place; T'' in place and -T' from the T image
     {
       const float *qs = sc + Q_QS * 64;
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;
-        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
-        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
+        const int ci = tid + NTH * it;               // 16-byte chunk of the 32 KB tiles
+        const int r = (ci & 511) >> 3;               // its row: 8 chunks per 128-byte row
+        float4 *pk = reinterpret_cast<float4 *>(smem + P2_K) + ci;
+        float4 x = *pk;
         x.x = tf32_rna(x.x * c_k); x.y = tf32_rna(x.y * c_k); x.z = tf32_rna(x.z * c_k); x.w = tf32_rna(x.w * c_k);
-        *reinterpret_cast<float4 *>(smem + P2_K + ci * 16) = x;
-        float4 *pq = reinterpret_cast<float4 *>(smem + P2_Q + ci * 16);
+        *pk = x;
+        float4 *pq = reinterpret_cast<float4 *>(smem + P2_Q) + ci;
         float4 y = *pq;
         const float f = qs[r];
         y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
         *pq = y;
-      }
-    }
-    fence_async_smem();
-    cta_sync();
-
-    // ---- 4a. X = S (cK)^T and Yt = S Q'^T start while the other operands are built
-    if (tid == 0) {
-      const uint32_t i64 = idesc_tf32(128, 64);
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_K + ks * 256, 4096), i64, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks, sdesc(sbase + P2_Q + ks * 256, 4096), i64, ks > 0);
-    }
-
-    // ---- 3b. K'^T, T'' in place and -T' from the T image, V^T (TMEM)
-    {
-      const float *kts = sc + Q_KTS * 64;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = 32 * half + 4 * j;
-        *reinterpret_cast<float4 *>(smem + P2_KT + canon(row, i, 64)) =
-            make_float4(tf32_rna(sKS[(i + 0) * LDS + row] * kts[i + 0]),
-                        tf32_rna(sKS[(i + 1) * LDS + row] * kts[i + 1]),
-                        tf32_rna(sKS[(i + 2) * LDS + row] * kts[i + 2]),
-                        tf32_rna(sKS[(i + 3) * LDS + row] * kts[i + 3]));
       }
       const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
 #pragma unroll
@@ -509,21 +539,45 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
         *pt = make_float4(tf32_rna(t.x * bet[i0]), tf32_rna(t.y * bet[i0 + 1]),
                           tf32_rna(t.z * bet[i0 + 2]), tf32_rna(t.w * bet[i0 + 3]));
       }
-      uint32_t vv[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * LDS + row]));
-      GDN_TMEM_ST32(tl + P2_TM_V + 32 * half, vv);
-      tmem_wait_st();
     }
     fence_async_smem();
     cta_sync();
-    // the K/V staging buffers are free: start the next chunk's rows
-    if (more) {
-      p2_stage_kv(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
-      cp_async_commit();
+
+    // ---- 4a. X = S (cK)^T and Yt = S Q'^T (K-major, 128-byte swizzled B)
+    if (tid == 0) {
+      const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks,
+               sdesc_sw128(sbase + P2_K + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks,
+               sdesc_sw128(sbase + P2_Q + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
     }
 
-    // ---- 4b. Ut = V^T T''^T; Ut += X (-T')^T (X was issued first, so it is done or in flight)
+    // ---- 3c. V^T -> TMEM (lane d_v = row, columns = tokens [32*half, +32))
+    if (!mbar_wait(bar_v, par)) misc->failed = 1;
+    ++waited_v;
+    {
+      uint32_t vv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * D + row]));
+      GDN_TMEM_ST32(tl + P2_TM_V + 32 * half, vv);
+      tmem_wait_st();
+    }
+    cta_sync();
+    if (more) {  // the V buffer is free: the next chunk's V rows
+      if (tid == 0) {
+        fence_async_smem();
+        mbar_expect_tx(bar_v, kRowsBytes);
+        tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C),
+                    static_cast<int>(s), bar_v);
+      }
+      ++armed_v;
+    }
+
+    // ---- 4b. Ut = V^T T''^T; Ut += X (-T')^T (X was issued first)
     if (tid == 0) {
       const uint32_t i64 = idesc_tf32(128, 64);
 #pragma unroll
@@ -532,35 +586,36 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
         mma_ts(tmem + P2_TM_U, tmem + P2_TM_X + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
-      mma_commit(mbar);
+      mma_commit(mbar1);
     }
 
     // ---- the previous chunk's outputs, from its Y^T region, while these run
     if (ch > 0) {
       const uint32_t tm_yp = (ch & 1) ? P2_TM_Y0 : P2_TM_Y1;
-      const int ncp = C;  // every chunk but the last is full
       uint32_t yv[32];
       GDN_TMEM_LD32(tl + tm_yp + 32 * half, yv);
       tmem_wait_ld();
       float *obase = a.output + ((static_cast<size_t>(s) * nt + (t0 - C)) * a.nv + vh) * D + row;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int i = 32 * half + j;
-        if (i < ncp) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
-      }
+      for (int j = 0; j < 32; ++j)  // every chunk but the last is full
+        obase[static_cast<size_t>(32 * half + j) * v_tok] = __uint_as_float(yv[j]);
     }
 
-    if (!mbar_wait(mbar, phase)) misc->failed = 1;
-    phase ^= 1;
+    if (!mbar_wait(mbar1, ph1)) misc->failed = 1;
+    ph1 ^= 1;
     fence_after();
     __syncthreads();
     if (misc->failed) { failed = true; break; }
-    // Q, T'' and -T' are free: the next chunk's Q rows, gates and T image
+    // K, Q and the T image are free: the next chunk's (TMA) and its gates
     if (more) {
-      stage_rows_canonical(sbase + P2_Q, qseq + (t0 + C) * kq_tok, kq_tok, ncn, tid);
+      if (tid == 0) {
+        fence_async_smem();
+        p2_load_in(sbase, &tm_k, &tm_q, static_cast<int>(kh), static_cast<int>(t0 + C), static_cast<int>(s),
+                   wseq + (ch + 1) * kWsFloats, bar_in);
+      }
+      ++armed_in;
       stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv,
                         ncn, tid);
-      p2_stage_image(sbase + P2_TPP, wseq + (ch + 1) * kWsFloats, tid);
       cp_async_commit();
     }
 
@@ -575,10 +630,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
       tmem_wait_st();
     }
     if (do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, c_fold);
-    // this chunk's P' has landed (the two newer groups, the next chunk's
-    // K/V and Q/T copies, may still be in flight)
-    if (more) cp_async_wait<2>(); else cp_async_wait<0>();
-    fence_async_smem();
+    if (!mbar_wait(bar_p, par)) misc->failed = 1;  // this chunk's P'
+    ++waited_p;
     cta_sync();
 
     // ---- 6. batch 2: Yt += Ut P'^T; S += Ut K'^T
@@ -591,21 +644,20 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
       for (int ks = 0; ks < C / 8; ++ks)
         mma_ts(tmem + P2_TM_S, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
                idesc_tf32(128, 128), 1);
-      mma_commit(mbar);
+      mma_commit(mbar2);
     }
-    if (!mbar_wait(mbar, phase)) misc->failed = 1;
-    phase ^= 1;
+    if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
+    ph2 ^= 1;
     fence_after();
     __syncthreads();
     if (misc->failed) { failed = true; break; }
-    // P' is free: the next chunk's P' image
     if (more) {
-      p2_stage_image(sbase + P2_P, wseq + (ch + 1) * kWsFloats + 4096, tid);
-      cp_async_commit();
-    }
-
-    // ---- 7. the last chunk's outputs now (the others are written during the next chunk)
-    if (!more) {
+      if (tid == 0) {  // P' is free: the next chunk's
+        mbar_expect_tx(bar_p, kImgBytes);
+        bulk_load(sbase + P2_P, wseq + (ch + 1) * kWsFloats + 4096, kImgBytes, bar_p);
+      }
+      ++armed_p;
+    } else {  // ---- 7. the last chunk's outputs now
       uint32_t yv[32];
       GDN_TMEM_LD32(tl + tm_y + 32 * half, yv);
       tmem_wait_ld();
@@ -620,7 +672,14 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     cta_sync();
   }
 
-  cp_async_wait_all();  // no copy may still be landing in shared memory at exit
+  cp_async_wait_all();  // no cp.async may still be landing in shared memory at exit
+  // after a failure, let any TMA copy still in flight land (bounded waits)
+  // before the CTA's shared memory is released
+  if (tid == 0) {
+    if (armed_in > waited_in) (void)mbar_wait(bar_in, waited_in & 1);
+    if (armed_v > waited_v) (void)mbar_wait(bar_v, waited_v & 1);
+    if (armed_p > waited_p) (void)mbar_wait(bar_p, waited_p & 1);
+  }
 
   // ---- state_out = c * S (or NaN if a wait timed out)
   {
@@ -642,27 +701,64 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunk_state_kernel(const StateArgs
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(P2_TM_COLS));
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A [128, heads, n_tokens, n_seqs] f32 tensor (128 contiguous) as a 4-D map
+// whose box is `inner` floats x 1 head x 64 tokens x 1 seq.
+cudaError_t rows_map(CUtensorMap *tm, const void *base, uint32_t heads, uint32_t nt, uint32_t ns,
+                     uint32_t inner, CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {128, heads, nt, ns};
+  const cuuint64_t strides[3] = {512, 512ull * heads, 512ull * heads * nt};
+  const cuuint32_t box[4] = {inner, 1, 64, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <bool DA>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
   const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
   const unsigned long long prep_blocks = heads * nchunks;
   if (heads == 0 || prep_blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  if (reinterpret_cast<uintptr_t>(p.v) % 16 != 0) return cudaErrorMisalignedAddress;  // TMA source
+  CUtensorMap tm_k, tm_q, tm_v;
+  cudaError_t e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess) e = rows_map(&tm_q, p.q, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e == cudaSuccess) e = rows_map(&tm_v, p.v, p.nv, p.nt, p.ns, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+
   PrepArgs pa;
   pa.q = static_cast<const float *>(p.q); pa.k = static_cast<const float *>(p.k);
   pa.g = p.g; pa.beta = p.beta; pa.ws = ws;
   pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = p.nv / p.nk;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
   auto prep = gdn_chunk_prep_kernel<DA>;
-  cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(P1_SMEM));
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P1_SMEM));
   if (e != cudaSuccess) return e;
   prep<<<static_cast<unsigned>(prep_blocks), NTH, P1_SMEM, stream>>>(pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   StateArgs sa;
-  sa.q = pa.q; sa.k = pa.k; sa.v = static_cast<const float *>(p.v); sa.g = p.g; sa.beta = p.beta;
+  sa.g = p.g; sa.beta = p.beta;
   sa.state_in = p.state_in; sa.ws = ws; sa.output = static_cast<float *>(p.output);
   sa.state_out = p.state_out;
   sa.nk = p.nk; sa.nv = p.nv; sa.nt = p.nt; sa.group = pa.group; sa.khead_div = pa.khead_div;
@@ -670,7 +766,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   auto state = gdn_chunk_state_kernel<DA>;
   e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
   if (e != cudaSuccess) return e;
-  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa);
+  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa, tm_k, tm_q, tm_v);
   return cudaGetLastError();
 }
 

@@ -262,6 +262,9 @@ gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t
     if (workspace_bytes < ws_need)
       return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace has %zu bytes, %zu needed",
                   workspace_bytes, ws_need);
+    if (!aligned(b.v, 16))
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "gdn: the two-pass chunked path needs v 16-byte aligned (it is read by TMA)");
     const Spans sp = spans_of(d, b, bf16);
     const Span w{workspace, ws_need, "workspace"};
     const Span all[8] = {sp.in[0], sp.in[1], sp.in[2], sp.in[3], sp.in[4], sp.in[5], sp.output,
@@ -394,6 +397,9 @@ gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const flo
   Path path;
   st = choose_path(d, false, false, &path);
   if (st != GDN_OK) return st;
+  if (!aligned(v, 16))
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: the two-pass chunked path needs v 16-byte aligned (it is read by TMA)");
   const size_t need = gdn::chunked_split_workspace_bytes(d.prob);
   if (need > gdn::kNoallocWorkspaceBytes)
     return fail(GDN_ERR_INVALID_ARGUMENT,

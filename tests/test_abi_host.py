@@ -423,3 +423,17 @@ def test_noalloc_host_checks(L):
     small = WORKLOADS["tiny"].with_(n_tokens=64)
     assert call(small) == nat.GDN_ERR_UNSUPPORTED               # D_k = 32
     assert call(fits, output=Fake(fits).addr["q"]) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_two_pass_needs_aligned_v(L):
+    w = WORKLOADS["long_prefill"].with_(n_tokens=100, n_seqs=1)
+    p = w.params(path=PATH_CHUNKED)
+    f = Fake(w)
+    args = [f.addr[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+    args[2] += 4                                             # v 4-byte aligned only
+    assert nat.forward_ws_raw(*args, p, 10 * GAP, nat.gdn_workspace_size(p)) == \
+        nat.GDN_ERR_INVALID_ARGUMENT
+    assert "16-byte" in nat.gdn_last_error()
+    assert nat.forward_chunked_noalloc_raw(*args, w.with_(n_tokens=64).params(path=PATH_CHUNKED)) == \
+        nat.GDN_ERR_INVALID_ARGUMENT
