@@ -86,17 +86,34 @@ __device__ __forceinline__ void stage_gates_async(uint32_t sc_addr, const float 
   }
 }
 
-// Asynchronous copies of 64 rows of 128 floats (row r at base + r * stride)
-// into a canonical K-major image (K extent 128) at dst; rows >= nc are zeros.
-__device__ __forceinline__ void stage_rows_canonical(uint32_t dst, const float *base, size_t stride,
-                                                     int nc, int tid) {
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int cc = tid + NTH * it;  // 16-byte chunk of the image
-    const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
-    cp_async16(dst + cc * 16, base + static_cast<size_t>(r < nc ? r : 0) * stride + 4 * c4,
-               r < nc ? 16u : 0u);
-  }
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+// One box of a 4-D tensor map (coordinates innermost first) into shared memory.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+// A contiguous global block into shared memory (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Byte offset of element (row, col) of a 64 x 128 f32 tile held as four
+// 128-byte-swizzled 64 x 32 boxes.
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return static_cast<uint32_t>((col >> 5) * 8192 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
+                               (col & 3) * 4);
 }
 
 // ================================================================ pass 1
@@ -109,7 +126,7 @@ constexpr uint32_t P1_T = 64 * LD * 4;
 constexpr uint32_t P1_M = 2 * 64 * LD * 4;
 constexpr uint32_t P1_SC = 65536;
 constexpr uint32_t P1_MISC = P1_SC + Q_NSC * 64 * 4;
-constexpr uint32_t P1_SMEM = P1_MISC + 64;
+constexpr uint32_t P1_SMEM = P1_MISC + 64 + 1024;  // + room to align the base to 1024
 static_assert(P1_M + 3 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
 
 struct PrepArgs {
@@ -123,22 +140,30 @@ struct PrepArgs {
 };
 
 struct P1Misc {
-  unsigned long long mbar;
+  unsigned long long mbar;    // Gram MMA commit
+  unsigned long long bar_ld;  // TMA: the chunk's K and Q rows
   uint32_t tmem_base;
   int failed;
   int extreme;
 };
 
+// The stack [K;Q] arrives by TMA, 128-byte swizzled: column block cb (32
+// floats) holds K's 64 rows then Q's 64 rows (16 KB), so A = [K;Q] (M = 128)
+// and B = K (N = 64) of the Gram are K-major SWIZZLE_128B operands.
 template <bool DECAY_AFTER>
-__global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+__global__ void __launch_bounds__(NTH, 2)
+    gdn_chunk_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   float *sA = reinterpret_cast<float *>(smem + P1_A);
   float *sT = reinterpret_cast<float *>(smem + P1_T);
   float *sM = reinterpret_cast<float *>(smem + P1_M);
   float *sc = reinterpret_cast<float *>(smem + P1_SC);
   P1Misc *misc = reinterpret_cast<P1Misc *>(smem + P1_MISC);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t mbar = smem_addr(&misc->mbar);
+  const uint32_t mbar = smem_addr(&misc->mbar), bar_ld = smem_addr(&misc->bar_ld);
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
   const int row = tid & 127, half = tid >> 7;
@@ -152,25 +177,33 @@ __global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
   const uint32_t t0 = ch * C;
   const int nc = static_cast<int>(min(static_cast<uint32_t>(C), a.nt - t0));
-  const size_t kq_tok = static_cast<size_t>(a.nk) * D;
-  const size_t kq0 = ((static_cast<size_t>(s) * a.nt + t0) * a.nk + kh) * D;
   const size_t sc0 = (static_cast<size_t>(s) * a.nt + t0) * a.nv + vh;
   float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
 
-  stage_rows_canonical(sbase + P1_STACK, a.k + kq0, kq_tok, nc, tid);
-  stage_rows_canonical(sbase + P1_STACK + 32768, a.q + kq0, kq_tok, nc, tid);
   stage_gates_async(sbase + P1_SC, a.g, a.beta, sc0, a.nv, nc, tid);
   cp_async_commit();
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_ld));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
+    mbar_expect_tx(bar_ld, 65536);
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      tma_load_4d(sbase + P1_STACK + cb * 16384, &tm_k, 32 * cb, static_cast<int>(kh), static_cast<int>(t0),
+                  static_cast<int>(s), bar_ld);
+      tma_load_4d(sbase + P1_STACK + cb * 16384 + 8192, &tm_q, 32 * cb, static_cast<int>(kh),
+                  static_cast<int>(t0), static_cast<int>(s), bar_ld);
+    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_addr(&misc->tmem_base)), "r"(64));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  __syncthreads();  // the load barrier is initialised before anyone waits on it
+  const bool loaded = mbar_wait(bar_ld, 0);
+  if (!loaded) misc->failed = 1;
   cp_async_wait_all();
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
@@ -195,7 +228,7 @@ __global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a
   if (tid == 0) {
 #pragma unroll
     for (int ks = 0; ks < D / 8; ++ks) {
-      const uint64_t d = sdesc(sbase + P1_STACK + ks * 256, 4096);
+      const uint64_t d = sdesc_sw128(sbase + P1_STACK + (ks >> 2) * 16384 + (ks & 3) * 32);
       mma_ss(tmem, d, d, idesc_tf32(128, 64), ks > 0);
     }
     mma_commit(mbar);
@@ -262,6 +295,8 @@ __global__ void __launch_bounds__(NTH, 2) gdn_chunk_prep_kernel(const PrepArgs a
       reinterpret_cast<float4 *>(ws)[ci] = t;
     }
   }
+  // a load that timed out may still land: wait for it (bounded) before exit
+  if (tid == 0 && !loaded) (void)mbar_wait(bar_ld, 0);
   cta_sync();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(64));
@@ -315,34 +350,6 @@ struct P2Misc {
   float c_renorm, c_fold, c_next, c_k;
   int do_renorm, do_fold;
 };
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-// One box of a 4-D tensor map (coordinates innermost first) into shared memory.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
-}
-// A contiguous global block into shared memory (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-// K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Byte offset of element (row, col) of a 64 x 128 f32 tile held as four
-// 128-byte-swizzled 64 x 32 boxes.
-__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
-  return static_cast<uint32_t>((col >> 5) * 8192 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
-                               (col & 3) * 4);
-}
 
 // Thread 0: this chunk's K and Q rows (4 boxes each) and T image, on bar_in.
 __device__ __forceinline__ void p2_load_in(uint32_t sbase, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
@@ -753,7 +760,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   auto prep = gdn_chunk_prep_kernel<DA>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P1_SMEM));
   if (e != cudaSuccess) return e;
-  prep<<<static_cast<unsigned>(prep_blocks), NTH, P1_SMEM, stream>>>(pa);
+  prep<<<static_cast<unsigned>(prep_blocks), NTH, P1_SMEM, stream>>>(pa, tm_k, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
