@@ -461,14 +461,17 @@ __global__ void __launch_bounds__(NTH, 1)
     const uint32_t tm_y = (ch & 1) ? P2_TM_Y1 : P2_TM_Y0;
     const uint32_t par = ch & 1;  // phase parity of this chunk's TMA barriers
 
-    // ---- 0. this chunk's K, Q rows, T image (TMA) and gates (cp.async) have landed
-    if (!mbar_wait(bar_in, par)) misc->failed = 1;
-    ++waited_in;
+    // ---- 0. this chunk's V rows (TMA) and gates (cp.async) have landed; its
+    // K, Q rows and T image may still be on the way
+    if (!mbar_wait(bar_v, par)) misc->failed = 1;
+    ++waited_v;
     cp_async_wait_all();
     __syncthreads();
     if (misc->failed) { failed = true; break; }
 
-    // ---- 1. per-token scalars and the lazy-scale bookkeeping (warp 0)
+    // ---- 1. warp 0: per-token scalars and the lazy-scale bookkeeping.
+    // Meanwhile V^T -> TMEM (lane d_v, columns = tokens), warp 4 taking both
+    // halves of the lane quarter it shares with warp 0.
     if (warp == 0) {
       float GC;
       const bool extreme = chunk_scalars(sc, lane, &GC);
@@ -492,15 +495,41 @@ __global__ void __launch_bounds__(NTH, 1)
         misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext; misc->c_k = cc;
         misc->do_renorm = do_renorm; misc->do_fold = extreme;
       }
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = warp == 4 ? hh : half;
+        if (hh == 1 && warp != 4) break;
+        uint32_t vv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * h + j) * D + row]));
+        GDN_TMEM_ST32(tl + P2_TM_V + 32 * h, vv);
+      }
+      tmem_wait_st();
     }
-    __syncthreads();
+    cta_sync();
+    if (more) {  // the V buffer is free: the next chunk's V rows
+      if (tid == 0) {
+        fence_async_smem();
+        mbar_expect_tx(bar_v, kRowsBytes);
+        tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C),
+                    static_cast<int>(s), bar_v);
+      }
+      ++armed_v;
+    }
     const float c_renorm = misc->c_renorm, c_fold = misc->c_fold, c_k = misc->c_k;
     const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
 
     // ---- 2. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
     if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
 
-    // ---- 3a. K'^T from the raw K rows (thread: d_k = row, tokens [32*half, +32))
+    // ---- 3. K, Q rows and the T image
+    if (!mbar_wait(bar_in, par)) misc->failed = 1;
+    ++waited_in;
+    __syncthreads();
+    if (misc->failed) { failed = true; break; }
+
+    // ---- 4. K'^T from the raw K rows (thread: d_k = row, tokens [32*half, +32))
     {
       const float *kts = sc + Q_KTS * 64;
       const unsigned char *kb = smem + P2_K;
@@ -516,23 +545,48 @@ __global__ void __launch_bounds__(NTH, 1)
     }
     __syncthreads();  // every raw K value is read before K is scaled in place
 
-    // ---- 3b. c K and Q' (TF32) in place; T'' in place and -T' from the T image
+    // ---- 5. c K (TF32) in place, then X = S (cK)^T starts (K-major, 128-byte swizzled B)
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      float4 *pk = reinterpret_cast<float4 *>(smem + P2_K) + tid + NTH * it;
+      float4 x = *pk;
+      x.x = tf32_rna(x.x * c_k); x.y = tf32_rna(x.y * c_k); x.z = tf32_rna(x.z * c_k); x.w = tf32_rna(x.w * c_k);
+      *pk = x;
+    }
+    fence_async_smem();
+    cta_sync();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks,
+               sdesc_sw128(sbase + P2_K + (ks >> 2) * 8192 + (ks & 3) * 32), idesc_tf32(128, 64), ks > 0);
+    }
+
+    // ---- 6. Q' (TF32) in place, then Yt = S Q'^T starts
     {
       const float *qs = sc + Q_QS * 64;
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;               // 16-byte chunk of the 32 KB tiles
+        const int ci = tid + NTH * it;               // 16-byte chunk of the 32 KB tile
         const int r = (ci & 511) >> 3;               // its row: 8 chunks per 128-byte row
-        float4 *pk = reinterpret_cast<float4 *>(smem + P2_K) + ci;
-        float4 x = *pk;
-        x.x = tf32_rna(x.x * c_k); x.y = tf32_rna(x.y * c_k); x.z = tf32_rna(x.z * c_k); x.w = tf32_rna(x.w * c_k);
-        *pk = x;
         float4 *pq = reinterpret_cast<float4 *>(smem + P2_Q) + ci;
         float4 y = *pq;
         const float f = qs[r];
         y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
         *pq = y;
       }
+    }
+    fence_async_smem();
+    cta_sync();
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks,
+               sdesc_sw128(sbase + P2_Q + (ks >> 2) * 8192 + (ks & 3) * 32), idesc_tf32(128, 64), ks > 0);
+    }
+
+    // ---- 7. T'' in place and -T' from the T image, then Ut = V^T T''^T + X (-T')^T
+    {
       const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
@@ -549,42 +603,6 @@ __global__ void __launch_bounds__(NTH, 1)
     }
     fence_async_smem();
     cta_sync();
-
-    // ---- 4a. X = S (cK)^T and Yt = S Q'^T (K-major, 128-byte swizzled B)
-    if (tid == 0) {
-      const uint32_t i64 = idesc_tf32(128, 64);
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks,
-               sdesc_sw128(sbase + P2_K + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks,
-               sdesc_sw128(sbase + P2_Q + (ks >> 2) * 8192 + (ks & 3) * 32), i64, ks > 0);
-    }
-
-    // ---- 3c. V^T -> TMEM (lane d_v = row, columns = tokens [32*half, +32))
-    if (!mbar_wait(bar_v, par)) misc->failed = 1;
-    ++waited_v;
-    {
-      uint32_t vv[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * D + row]));
-      GDN_TMEM_ST32(tl + P2_TM_V + 32 * half, vv);
-      tmem_wait_st();
-    }
-    cta_sync();
-    if (more) {  // the V buffer is free: the next chunk's V rows
-      if (tid == 0) {
-        fence_async_smem();
-        mbar_expect_tx(bar_v, kRowsBytes);
-        tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C),
-                    static_cast<int>(s), bar_v);
-      }
-      ++armed_v;
-    }
-
-    // ---- 4b. Ut = V^T T''^T; Ut += X (-T')^T (X was issued first)
     if (tid == 0) {
       const uint32_t i64 = idesc_tf32(128, 64);
 #pragma unroll
