@@ -104,18 +104,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// Named barriers (ids 1..15): arrive without waiting, or wait for `n` threads.
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
 // K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Byte offset of element (row, col) of a 64 x 128 f32 tile held as four
-// 128-byte-swizzled 64 x 32 boxes.
-__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
-  return static_cast<uint32_t>((col >> 5) * 8192 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
-                               (col & 3) * 4);
-}
-
 // ================================================================ pass 1
 
 // shared memory (bytes): the [K;Q] stack for the Gram, then, once the Gram
@@ -306,17 +306,17 @@ __global__ void __launch_bounds__(NTH, 2)
 
 // TMEM columns (Y^T alternates between two regions so a chunk's outputs are
 // read out while the next chunk's products run)
-constexpr uint32_t P2_TM_S = 0, P2_TM_X = 128, P2_TM_U = 192, P2_TM_Y0 = 256, P2_TM_V = 320,
-                   P2_TM_Y1 = 384;
+// [X | Y^T] is one N = 128 product; its two regions alternate by chunk.
+constexpr uint32_t P2_TM_S = 0, P2_TM_XY0 = 128, P2_TM_U = 256, P2_TM_V = 320, P2_TM_XY1 = 384;
 constexpr uint32_t P2_TM_COLS = 512;
 
 // Shared memory (bytes from a 1024-aligned base).  K and Q arrive by TMA as
-// four 64-row x 128-byte boxes each, 128-byte swizzled: the layout the MMA
-// reads as a K-major SWIZZLE_128B operand, and one in which a warp reading
-// either a row or a column of K touches distinct banks.
-constexpr uint32_t P2_K = 0;                       // K (TMA) -> c K in TF32, in place
-constexpr uint32_t P2_Q = P2_K + 32768;            // Q (TMA) -> Q' in TF32, in place
-constexpr uint32_t P2_KT = P2_Q + 32768;           // K'^T, 128 x 64 canonical (no swizzle)
+// four 64-row x 128-byte boxes each, 128-byte swizzled, interleaved so that
+// column block cb (32 floats) holds K's 64 rows then Q's (16 KB): [K; Q'] is
+// then one 128-row K-major SWIZZLE_128B operand, and a warp reading either a
+// row or a column of K touches distinct banks.
+constexpr uint32_t P2_KQ = 0;                      // [K; Q] (TMA) -> [K; Q'] in TF32, in place
+constexpr uint32_t P2_KT = P2_KQ + 65536;          // K'^T, 128 x 64 canonical (no swizzle)
 constexpr uint32_t P2_TPP = P2_KT + 32768;         // T image (bulk copy) -> T'' in place
 constexpr uint32_t P2_TP = P2_TPP + 16384;         // -T'
 constexpr uint32_t P2_P = P2_TP + 16384;           // P' image (bulk copy), used as is
@@ -347,7 +347,7 @@ struct P2Misc {
   unsigned long long bar_p;   // TMA: P' image of a chunk
   uint32_t tmem_base;
   int failed;
-  float c_renorm, c_fold, c_next, c_k;
+  float c_renorm, c_fold, c_next;
   int do_renorm, do_fold;
 };
 
@@ -357,8 +357,8 @@ __device__ __forceinline__ void p2_load_in(uint32_t sbase, const CUtensorMap *tm
   mbar_expect_tx(bar, 2 * kRowsBytes + kImgBytes);
 #pragma unroll
   for (int cb = 0; cb < 4; ++cb) {
-    tma_load_4d(sbase + P2_K + cb * 8192, tm_k, 32 * cb, kh, t0, s, bar);
-    tma_load_4d(sbase + P2_Q + cb * 8192, tm_q, 32 * cb, kh, t0, s, bar);
+    tma_load_4d(sbase + P2_KQ + cb * 16384, tm_k, 32 * cb, kh, t0, s, bar);
+    tma_load_4d(sbase + P2_KQ + cb * 16384 + 8192, tm_q, 32 * cb, kh, t0, s, bar);
   }
   bulk_load(sbase + P2_TPP, timg, kImgBytes, bar);
 }
@@ -449,20 +449,25 @@ __global__ void __launch_bounds__(NTH, 1)
   float c = 1.f;
   uint32_t ph1 = 0, ph2 = 0;
   bool failed = false;
+  bool b2_pending = false;  // a batch 2 was issued and not yet waited for
   // TMA arms and waits per barrier (uniform over the CTA): a copy is in
   // flight while a barrier has been armed more often than waited on
   uint32_t armed_in = 1, armed_v = 1, armed_p = 1, waited_in = 0, waited_v = 0, waited_p = 0;
+  const int wt = tid - 32;  // worker index of warps 1..7 (steps 5-7)
+  constexpr int NW = NTH - 32;
 
   for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
     const uint32_t t0 = ch * C;
     const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
     const bool more = ch + 1 < nchunks;
     const int ncn = more ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
-    const uint32_t tm_y = (ch & 1) ? P2_TM_Y1 : P2_TM_Y0;
+    const uint32_t tm_x = (ch & 1) ? P2_TM_XY1 : P2_TM_XY0;  // X; Y^T at tm_x + 64
+    const uint32_t tm_y = tm_x + 64;
     const uint32_t par = ch & 1;  // phase parity of this chunk's TMA barriers
 
     // ---- 0. this chunk's V rows (TMA) and gates (cp.async) have landed; its
-    // K, Q rows and T image may still be on the way
+    // K, Q rows and T image may still be on the way, and the previous chunk's
+    // batch 2 may still be running
     if (!mbar_wait(bar_v, par)) misc->failed = 1;
     ++waited_v;
     cp_async_wait_all();
@@ -488,11 +493,11 @@ __global__ void __launch_bounds__(NTH, 1)
         const float Gi = sc[Q_G * 64 + i];
         const float bi = sc[Q_BETA * 64 + i];
         sc[Q_KTS * 64 + i] = __expf(Gi - GC) / cnext;                       // K' row scale
-        sc[Q_TPS * 64 + i] = -bi * (DECAY_AFTER ? sc[Q_GAMP * 64 + i] : sc[Q_GAM * 64 + i]);  // -T' column
+        sc[Q_TPS * 64 + i] = -cc * bi * (DECAY_AFTER ? sc[Q_GAMP * 64 + i] : sc[Q_GAM * 64 + i]);  // -T' column
         sc[Q_QS * 64 + i] = cc * a.q_scale * sc[Q_GAM * 64 + i];           // Q' row scale
       }
       if (lane == 0) {
-        misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext; misc->c_k = cc;
+        misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext;
         misc->do_renorm = do_renorm; misc->do_fold = extreme;
       }
     } else {
@@ -517,80 +522,84 @@ __global__ void __launch_bounds__(NTH, 1)
       }
       ++armed_v;
     }
-    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold, c_k = misc->c_k;
+    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
     const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
 
-    // ---- 2. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
+    // ---- 2. the previous chunk's batch 2 is done: S, Y, K'^T and P' are
+    // settled; this chunk's P' may load
+    if (b2_pending) {
+      if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
+      ph2 ^= 1;
+      b2_pending = false;
+      fence_after();
+      __syncthreads();
+      if (misc->failed) { failed = true; break; }
+      if (tid == 0) {
+        mbar_expect_tx(bar_p, kImgBytes);
+        bulk_load(sbase + P2_P, wseq + ch * kWsFloats + 4096, kImgBytes, bar_p);
+      }
+      ++armed_p;
+    }
+
+    // ---- 3. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
     if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
 
-    // ---- 3. K, Q rows and the T image
+    // ---- 4. K, Q rows and the T image
     if (!mbar_wait(bar_in, par)) misc->failed = 1;
     ++waited_in;
     __syncthreads();
     if (misc->failed) { failed = true; break; }
 
-    // ---- 4. K'^T from the raw K rows (thread: d_k = row, tokens [32*half, +32))
-    {
-      const float *kts = sc + Q_KTS * 64;
-      const unsigned char *kb = smem + P2_K;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = 32 * half + 4 * j;
-        float e[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          e[u] = tf32_rna(*reinterpret_cast<const float *>(kb + sw128_off(i + u, row)) * kts[i + u]);
-        *reinterpret_cast<float4 *>(smem + P2_KT + canon(row, i, 64)) = make_float4(e[0], e[1], e[2], e[3]);
-      }
-    }
-    __syncthreads();  // every raw K value is read before K is scaled in place
-
-    // ---- 5. c K (TF32) in place, then X = S (cK)^T starts (K-major, 128-byte swizzled B)
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      float4 *pk = reinterpret_cast<float4 *>(smem + P2_K) + tid + NTH * it;
-      float4 x = *pk;
-      x.x = tf32_rna(x.x * c_k); x.y = tf32_rna(x.y * c_k); x.z = tf32_rna(x.z * c_k); x.w = tf32_rna(x.w * c_k);
-      *pk = x;
-    }
-    fence_async_smem();
-    cta_sync();
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + P2_TM_X, tmem + P2_TM_S + 8 * ks,
-               sdesc_sw128(sbase + P2_K + (ks >> 2) * 8192 + (ks & 3) * 32), idesc_tf32(128, 64), ks > 0);
-    }
-
-    // ---- 6. Q' (TF32) in place, then Yt = S Q'^T starts
+    // ---- 5. all warps: K to TF32 and Q' in place (row = chunk / 8 in its box)
     {
       const float *qs = sc + Q_QS * 64;
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;               // 16-byte chunk of the 32 KB tile
-        const int r = (ci & 511) >> 3;               // its row: 8 chunks per 128-byte row
-        float4 *pq = reinterpret_cast<float4 *>(smem + P2_Q) + ci;
+        const int ci = tid + NTH * it;
+        const int off = (ci >> 9) * 16384 + (ci & 511) * 16;
+        float4 *pk = reinterpret_cast<float4 *>(smem + P2_KQ + off);
+        float4 x = *pk;
+        x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
+        *pk = x;
+        float4 *pq = reinterpret_cast<float4 *>(smem + P2_KQ + 8192 + off);
         float4 y = *pq;
-        const float f = qs[r];
+        const float f = qs[(ci & 511) >> 3];
         y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
         *pq = y;
       }
     }
     fence_async_smem();
     cta_sync();
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + tm_y, tmem + P2_TM_S + 8 * ks,
-               sdesc_sw128(sbase + P2_Q + (ks >> 2) * 8192 + (ks & 3) * 32), idesc_tf32(128, 64), ks > 0);
-    }
 
-    // ---- 7. T'' in place and -T' from the T image, then Ut = V^T T''^T + X (-T')^T
-    {
-      const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
+    // ---- 6-7. warp 0 issues [X | Y^T] = S [K; Q']^T (one N = 128 product),
+    // then, once warps 1-7 have built T'' and -T' (named barrier),
+    // Ut = V^T T''^T + X (-T')^T; warps 1-7 then build K'^T from the TF32 K
+    // while those run (only batch 2 reads it).  The scale c rides on -T' and Q'.
+    if (warp == 0) {
+      if (lane == 0) {
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int ci = tid + NTH * it;  // same chunk read and written by this thread
+        for (int ks = 0; ks < D / 8; ++ks)
+          mma_ts(tmem + tm_x, tmem + P2_TM_S + 8 * ks,
+                 sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32), idesc_tf32(128, 128),
+                 ks > 0);
+      }
+      __syncwarp();
+      named_sync(1, NTH);
+      fence_after();
+      if (lane == 0) {
+        const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
+          mma_ts(tmem + P2_TM_U, tmem + P2_TM_V + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
+          mma_ts(tmem + P2_TM_U, tmem + tm_x + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
+        mma_commit(mbar1);
+      }
+      __syncwarp();
+    } else {
+      const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
+      for (int ci = wt; ci < 1024; ci += NW) {  // T'' in place, -T' beside it
         const int i0 = 4 * ((ci >> 3) & 15);
         float4 *pt = reinterpret_cast<float4 *>(smem + P2_TPP + ci * 16);
         const float4 t = *pt;
@@ -600,23 +609,28 @@ __global__ void __launch_bounds__(NTH, 1)
         *pt = make_float4(tf32_rna(t.x * bet[i0]), tf32_rna(t.y * bet[i0 + 1]),
                           tf32_rna(t.z * bet[i0 + 2]), tf32_rna(t.w * bet[i0 + 3]));
       }
-    }
-    fence_async_smem();
-    cta_sync();
-    if (tid == 0) {
-      const uint32_t i64 = idesc_tf32(128, 64);
+      fence_async_smem();
+      fence_before();
+      named_arrive(1, NTH);
+      const float *kts = sc + Q_KTS * 64;
+      for (int oc = wt; oc < 2048; oc += NW) {  // K'^T: d_k = oc % 128, tokens 4 (oc / 128) .. +3
+        const int dk = oc & 127, i0 = (oc >> 7) * 4;
+        const unsigned char *kb = smem + P2_KQ + (dk >> 5) * 16384 + (dk & 3) * 4;
+        float e[4];
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_U, tmem + P2_TM_V + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), i64, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_U, tmem + P2_TM_X + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
-      mma_commit(mbar1);
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u;
+          e[u] = tf32_rna(*reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4)) *
+                          kts[i]);
+        }
+        *reinterpret_cast<float4 *>(smem + P2_KT + canon(dk, i0, 64)) = make_float4(e[0], e[1], e[2], e[3]);
+      }
+      fence_async_smem();
     }
 
     // ---- the previous chunk's outputs, from its Y^T region, while these run
     if (ch > 0) {
-      const uint32_t tm_yp = (ch & 1) ? P2_TM_Y0 : P2_TM_Y1;
+      const uint32_t tm_yp = ((ch & 1) ? P2_TM_XY0 : P2_TM_XY1) + 64;
       uint32_t yv[32];
       GDN_TMEM_LD32(tl + tm_yp + 32 * half, yv);
       tmem_wait_ld();
@@ -644,7 +658,7 @@ __global__ void __launch_bounds__(NTH, 1)
       cp_async_commit();
     }
 
-    // ---- 5. U^T to TF32 (nearest) in place; extreme gates: decay S now
+    // ---- 8. U^T to TF32 (nearest) in place; extreme gates: decay S now
     {
       uint32_t uv[32];
       GDN_TMEM_LD32(tl + P2_TM_U + 32 * half, uv);
@@ -659,7 +673,8 @@ __global__ void __launch_bounds__(NTH, 1)
     ++waited_p;
     cta_sync();
 
-    // ---- 6. batch 2: Yt += Ut P'^T; S += Ut K'^T
+    // ---- 9. batch 2: Yt += Ut P'^T; S += Ut K'^T.  Not waited for here unless
+    // this is the last chunk: the next chunk's first steps overlap it.
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
@@ -671,18 +686,14 @@ __global__ void __launch_bounds__(NTH, 1)
                idesc_tf32(128, 128), 1);
       mma_commit(mbar2);
     }
-    if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
-    ph2 ^= 1;
-    fence_after();
-    __syncthreads();
-    if (misc->failed) { failed = true; break; }
-    if (more) {
-      if (tid == 0) {  // P' is free: the next chunk's
-        mbar_expect_tx(bar_p, kImgBytes);
-        bulk_load(sbase + P2_P, wseq + (ch + 1) * kWsFloats + 4096, kImgBytes, bar_p);
-      }
-      ++armed_p;
-    } else {  // ---- 7. the last chunk's outputs now
+    b2_pending = true;
+    if (!more) {  // ---- 10. the last chunk: wait, then its outputs
+      if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
+      ph2 ^= 1;
+      b2_pending = false;
+      fence_after();
+      __syncthreads();
+      if (misc->failed) { failed = true; break; }
       uint32_t yv[32];
       GDN_TMEM_LD32(tl + tm_y + 32 * half, yv);
       tmem_wait_ld();
@@ -694,9 +705,13 @@ __global__ void __launch_bounds__(NTH, 1)
       }
     }
     c = misc->c_next;
-    cta_sync();
   }
 
+  // an MMA batch still in flight after a failure finishes (bounded) before
+  // TMEM is read or released
+  if (b2_pending && tid == 0) (void)mbar_wait(mbar2, ph2);
+  fence_after();
+  __syncthreads();
   cp_async_wait_all();  // no cp.async may still be landing in shared memory at exit
   // after a failure, let any TMA copy still in flight land (bounded waits)
   // before the CTA's shared memory is released
