@@ -62,8 +62,8 @@ constexpr uint32_t SM_KT = SM_STACK + 65536;         // K'^T 128 x 64 canonical,
 constexpr uint32_t SM_P = SM_KT + 32768;             // P'   64 x 64 canonical, 16 KB
 constexpr uint32_t SM_A = SM_P + 16384;              // A plain 64 x LD; then -T' (canonical)
 constexpr uint32_t SM_T = SM_A + 64 * LD * 4;        // T plain 64 x LD; then T'' (canonical)
-constexpr uint32_t SM_M = SM_T + 64 * LD * 4;        // block products, 3 x 256 f32
-constexpr uint32_t SM_SC = SM_M + 3 * 256 * 4;       // per-token scalars
+constexpr uint32_t SM_M = SM_T + 64 * LD * 4;        // block products, 4 x 256 f32
+constexpr uint32_t SM_SC = SM_M + 4 * 256 * 4;       // per-token scalars
 constexpr int NSC = 11;                              // scalar arrays of 64
 constexpr uint32_t SM_MISC = SM_SC + NSC * 64 * 4;   // mbarrier, tmem base, flags
 constexpr int LDS = 132;                             // staging row stride (floats): 528 B, so the

@@ -132,11 +132,34 @@ __device__ __forceinline__ void tmem_scale64(uint32_t taddr, float f) {
   tmem_wait_st();
 }
 
-// T = (I + A)^-1 for a strictly lower 64 x 64 A (plain, row stride LD), with
-// 16 x 16 blocks: the diagonal blocks by forward substitution (one thread per
-// column), then T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj level by level
-// (i - j = 1, 2, 3), one warp per block, each lane a 2 x 4 register tile.
-// M is 3 x 256 floats of per-warp scratch.
+// One warp accumulates C += L R for 16 x 16 blocks: L rows at stride ldl, R
+// rows at stride ldr; each lane holds a 2 x 4 tile of C (rows tr, tr+1,
+// columns tc..tc+3).  With LOWER, L is lower triangular and its upper part
+// (stored zeros) is skipped.
+template <bool LOWER>
+__device__ __forceinline__ void blk_mac(float (&c0)[4], float (&c1)[4], const float *L, int ldl,
+                                        const float *R, int ldr, int tr, int tc) {
+  const float *l0 = L + tr * ldl;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    if (!LOWER || q <= tr + 1) {
+      const float x0 = l0[q], x1 = l0[ldl + q];
+      const float4 b = *reinterpret_cast<const float4 *>(R + q * ldr + tc);
+      c0[0] = fmaf(x0, b.x, c0[0]); c0[1] = fmaf(x0, b.y, c0[1]);
+      c0[2] = fmaf(x0, b.z, c0[2]); c0[3] = fmaf(x0, b.w, c0[3]);
+      c1[0] = fmaf(x1, b.x, c1[0]); c1[1] = fmaf(x1, b.y, c1[1]);
+      c1[2] = fmaf(x1, b.z, c1[2]); c1[3] = fmaf(x1, b.w, c1[3]);
+    }
+  }
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 A (plain, row stride LD), by
+// doubling over 16 x 16 blocks: the four diagonal blocks by forward
+// substitution (one thread per column); then the two 32 x 32 diagonal blocks,
+// T_{j+1,j} = -T_{j+1,j+1} (A_{j+1,j} T_jj) for j = 0, 2; then the lower-left
+// 32 x 32 quarter, -T[hi] (A[hi,lo] T[lo]), as four 16 x 16 output blocks per
+// product, one warp each (2 x 4 register tiles).  M is 4 x 256 floats of
+// scratch for the inner products.
 __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   // the six blocks above the diagonal stay zero
   for (int e = tid; e < 6 * 256; e += NTH) {
@@ -159,48 +182,47 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
-  const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);  // this lane's 2 x 4 tile of a block
-  for (int d = 1; d <= 3; ++d) {
-    if (warp < 4 - d) {
-      const int j = warp, i = j + d;
-      float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kb = j; kb < i; ++kb) {
-        const float *a0 = A + (16 * i + tr) * LD + 16 * kb;
-        const float *tb = T + (16 * kb) * LD + 16 * j + tc;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float x0 = a0[q], x1 = a0[LD + q];
-          const float4 b = *reinterpret_cast<const float4 *>(tb + q * LD);
-          m0[0] = fmaf(x0, b.x, m0[0]); m0[1] = fmaf(x0, b.y, m0[1]);
-          m0[2] = fmaf(x0, b.z, m0[2]); m0[3] = fmaf(x0, b.w, m0[3]);
-          m1[0] = fmaf(x1, b.x, m1[0]); m1[1] = fmaf(x1, b.y, m1[1]);
-          m1[2] = fmaf(x1, b.z, m1[2]); m1[3] = fmaf(x1, b.w, m1[3]);
-        }
-      }
-      float *mw = M + warp * 256;
-      *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
-      *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
-      __syncwarp();
-      // T_ij = -T_ii M: T_ii is lower triangular (its upper entries are stored zeros)
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-      const float *li = T + (16 * i + tr) * LD + 16 * i;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (q <= tr + 1) {
-          const float l0 = li[q], l1 = li[LD + q];
-          const float4 mm = *reinterpret_cast<const float4 *>(mw + q * 16 + tc);
-          t0[0] = fmaf(l0, mm.x, t0[0]); t0[1] = fmaf(l0, mm.y, t0[1]);
-          t0[2] = fmaf(l0, mm.z, t0[2]); t0[3] = fmaf(l0, mm.w, t0[3]);
-          t1[0] = fmaf(l1, mm.x, t1[0]); t1[1] = fmaf(l1, mm.y, t1[1]);
-          t1[2] = fmaf(l1, mm.z, t1[2]); t1[3] = fmaf(l1, mm.w, t1[3]);
-        }
-      }
-      float *to = T + (16 * i + tr) * LD + 16 * j + tc;
-      *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
-      *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
-    }
-    __syncthreads();
+  const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);
+  float *mw = M + warp * 256;
+
+  // 32 x 32 diagonal blocks: warp 0 builds T_10, warp 1 builds T_32
+  if (warp < 2) {
+    const int j = 2 * warp, i = j + 1;
+    float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
+    blk_mac<false>(m0, m1, A + (16 * i) * LD + 16 * j, LD, T + (16 * j) * LD + 16 * j, LD, tr, tc);
+    *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
+    *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
+    __syncwarp();
+    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+    blk_mac<true>(t0, t1, T + (16 * i) * LD + 16 * i, LD, mw, 16, tr, tc);
+    float *to = T + (16 * i + tr) * LD + 16 * j + tc;
+    *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
+    *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
   }
+  __syncthreads();
+
+  // lower-left quarter, rows r = 2, 3 and columns c = 0, 1 (16-blocks): warp
+  // 2(r-2) + c first forms M'_rc = sum_{k=c}^{1} A_rk T_kc ...
+  const int r = 2 + (warp >> 1), cb = warp & 1;
+  if (warp < 4) {
+    float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = cb; k <= 1; ++k)
+      blk_mac<false>(m0, m1, A + (16 * r) * LD + 16 * k, LD, T + (16 * k) * LD + 16 * cb, LD, tr, tc);
+    *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
+    *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
+  }
+  __syncthreads();
+  // ... then T_rc = -sum_{k=2}^{r} T_rk M'_kc (T_rr lower triangular)
+  if (warp < 4) {
+    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r == 3)
+      blk_mac<false>(t0, t1, T + (16 * r) * LD + 32, LD, M + cb * 256, 16, tr, tc);  // T_32 M'_2c
+    blk_mac<true>(t0, t1, T + (16 * r) * LD + 16 * r, LD, M + (2 * (r - 2) + cb) * 256, 16, tr, tc);
+    float *to = T + (16 * r + tr) * LD + 16 * cb + tc;
+    *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
+    *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
+  }
+  __syncthreads();
 }
 
 }  // namespace

@@ -127,7 +127,7 @@ constexpr uint32_t P1_M = 2 * 64 * LD * 4;
 constexpr uint32_t P1_SC = 65536;
 constexpr uint32_t P1_MISC = P1_SC + Q_NSC * 64 * 4;
 constexpr uint32_t P1_SMEM = P1_MISC + 64 + 1024;  // + room to align the base to 1024
-static_assert(P1_M + 3 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
+static_assert(P1_M + 4 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
 
 struct PrepArgs {
   const float *__restrict__ q;
