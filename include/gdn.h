@@ -233,8 +233,10 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  * capture kernel page, with the same TF32 operands as GDN_PATH_CHUNKED.
  *
  * gdn_workspace_size: *bytes = the workspace gdn_forward_ws needs for
- *   `params` -- 32 KB per (seq, value head, chunk) on the chunked path,
- *   0 on every other path.  Same params checks and status as gdn_path_name.
+ *   `params` -- on the chunked path, per (seq, 64-token chunk), 32 KB per
+ *   value head plus 96 KB per key head (the rounded K and Q rows and K^T,
+ *   shared by the value heads that read the key head); 0 on every other
+ *   path.  Same params checks and status as gdn_path_name.
  *
  * gdn_forward_ws: gdn_forward, plus `workspace` (DEVICE, caller-owned,
  *   at least gdn_workspace_size bytes, 16-byte aligned, overlapping no other
@@ -244,8 +246,8 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *   the other paths run exactly as in gdn_forward and do not touch the
  *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
  *   short or overlapping workspace when the size is > 0, and, on the chunked
- *   path, for v not 16-byte aligned (the state pass reads K, Q and V rows
- *   with the tensor memory accelerator).
+ *   path, for v not 16-byte aligned (the state pass reads V rows with the
+ *   tensor memory accelerator).
  */
 gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes);
 
@@ -265,10 +267,12 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
  * cudaMalloc, which can synchronise the device.  Nothing here allocates:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *
- * Limit: the fixed scratch is 32 MiB (32 KB per (seq, value head, 64-token
- * chunk), so at most 1024 of them -- e.g. 16 value heads of 4096 tokens, or
- * 256 of 256); every GPU on which the library's chunked kernels are loaded
- * holds it until the process exits.  Larger problems return
+ * Limit: the fixed scratch is 32 MiB, and a problem needs, per (seq,
+ * 64-token chunk), 32 KB per value head plus 96 KB per key head (what
+ * gdn_workspace_size reports) -- e.g. one sequence of 1024 tokens with 16
+ * value and 16 key heads, or of 640 tokens with 48 value and 16 key heads;
+ * every GPU on which the library's chunked kernels are loaded holds it until
+ * the process exits.  Larger problems return
  * GDN_ERR_INVALID_ARGUMENT with the numbers; use gdn_forward_ws for them.
  *
  * Arguments, layouts and checks as gdn_forward (f32 activations), for the

@@ -285,11 +285,11 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         const int ci = tid + NTH * it;        // 16-byte chunk of the K half
         const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
         float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
-        x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
+        x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
         *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
         float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
         float4 y = *pq;
-        y.x = tf32_rna(y.x); y.y = tf32_rna(y.y); y.z = tf32_rna(y.z); y.w = tf32_rna(y.w);
+        y.x = tf32_rn(y.x); y.y = tf32_rn(y.y); y.z = tf32_rn(y.z); y.w = tf32_rn(y.w);
         *pq = y;
       }
       // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
@@ -298,15 +298,15 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       for (int j = 0; j < 8; ++j) {
         const int i = 32 * half + 4 * j;
         *reinterpret_cast<float4 *>(smem + SM_KT + canon(row, i, 64)) =
-            make_float4(tf32_rna(sKS[(i + 0) * LDS + row] * kts[i + 0]),
-                        tf32_rna(sKS[(i + 1) * LDS + row] * kts[i + 1]),
-                        tf32_rna(sKS[(i + 2) * LDS + row] * kts[i + 2]),
-                        tf32_rna(sKS[(i + 3) * LDS + row] * kts[i + 3]));
+            make_float4(tf32_rn(sKS[(i + 0) * LDS + row] * kts[i + 0]),
+                        tf32_rn(sKS[(i + 1) * LDS + row] * kts[i + 1]),
+                        tf32_rn(sKS[(i + 2) * LDS + row] * kts[i + 2]),
+                        tf32_rn(sKS[(i + 3) * LDS + row] * kts[i + 3]));
       }
       // V^T -> TMEM (lane d_v = row, columns = tokens [32*half, +32))
       uint32_t vv[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * half + j) * LDS + row]));
+      for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rn(sVS[(32 * half + j) * LDS + row]));
       GDN_TMEM_ST32(tl + TM_V + 32 * half, vv);
       tmem_wait_st();
     }
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           for (int u = 0; u < 4; ++u) {
             const int i = 32 * half + 4 * j + u;
             const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-            e[u] = i <= r ? tf32_rna(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
           }
           *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
               make_float4(e[0], e[1], e[2], e[3]);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         float4 *p = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + cc * 16);
         float4 x = *p;
         const float f = qs[r];
-        x.x = tf32_rna(x.x * f); x.y = tf32_rna(x.y * f); x.z = tf32_rna(x.z * f); x.w = tf32_rna(x.w * f);
+        x.x = tf32_rn(x.x * f); x.y = tf32_rn(x.y * f); x.z = tf32_rn(x.z * f); x.w = tf32_rn(x.w * f);
         *p = x;
       }
     }
@@ -404,11 +404,11 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       for (int it = 0; it < 4; ++it) {
         const int i0 = 4 * ((ci[it] >> 3) & 15);
         *reinterpret_cast<float4 *>(smem + SM_TP + ci[it] * 16) =
-            make_float4(tf32_rna(t[it].x * tps[i0]), tf32_rna(t[it].y * tps[i0 + 1]),
-                        tf32_rna(t[it].z * tps[i0 + 2]), tf32_rna(t[it].w * tps[i0 + 3]));
+            make_float4(tf32_rn(t[it].x * tps[i0]), tf32_rn(t[it].y * tps[i0 + 1]),
+                        tf32_rn(t[it].z * tps[i0 + 2]), tf32_rn(t[it].w * tps[i0 + 3]));
         *reinterpret_cast<float4 *>(smem + SM_TPP + ci[it] * 16) =
-            make_float4(tf32_rna(t[it].x * bet[i0]), tf32_rna(t[it].y * bet[i0 + 1]),
-                        tf32_rna(t[it].z * bet[i0 + 2]), tf32_rna(t[it].w * bet[i0 + 3]));
+            make_float4(tf32_rn(t[it].x * bet[i0]), tf32_rn(t[it].y * bet[i0 + 1]),
+                        tf32_rn(t[it].z * bet[i0 + 2]), tf32_rn(t[it].w * bet[i0 + 3]));
       }
     }
     fence_async_smem();
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       GDN_TMEM_LD32(tl + TM_U + 32 * half, uv);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rna(__uint_as_float(uv[j])));
+      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rn(__uint_as_float(uv[j])));
       GDN_TMEM_ST32(tl + TM_U + 32 * half, uv);
       tmem_wait_st();
     }

@@ -24,9 +24,12 @@ constexpr float kRenormHi = 1.0737418e+09f;  // 2^30
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ float tf32_rna(float x) {
+// Round to the nearest TF32 value (10 mantissa bits), ties to even; NaN
+// stays NaN, infinities stay infinite.  The rounding-to-nearest conversion
+// is one instruction here, cheaper than the ties-away form.
+__device__ __forceinline__ float tf32_rn(float x) {
   uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  asm("cvt.rn.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
 }
 // canonical K-major no-swizzle byte offset of element (row, k) in a matrix

@@ -2,29 +2,28 @@
 // recurrence on sm_103a, D_k = D_v = 128: the same chunk equations as the
 // single-pass kernel (chunked.cu), split at the state.
 //
-// Everything the chunk equations need that does not depend on the state --
-// the Gram products K K^T and Q K^T, A, T = (I + A)^-1 and
-// P' = q_scale (Q K^T o Gam)_{i<=r} -- is computed for every (seq, value
-// head, chunk) at once by pass 1, one CTA per chunk, and written to a
-// caller-provided workspace (32 KB per chunk: T as an f32 canonical image,
-// P' as a TF32 canonical image).  Pass 2 keeps one CTA per (seq, value head)
-// for the whole token range and runs only the state-dependent part per
-// chunk: operand building, U^T = V^T T''^T + X (-T')^T with X = S K^T,
-// Y^T = S Q'^T + U^T P'^T, S += U^T K'^T.  The serial chain per chunk loses
-// the Gram epilogue and the triangular inverse.  Pass 2 loads by TMA: K and
-// Q rows land 128-byte swizzled, which is both the MMA's K-major SWIZZLE_128B
-// operand layout and conflict-free for the transposed reads that build K'^T;
-// V rows, the T image and P' land as plain boxes and bulk copies, each group
-// on its own mbarrier, so no thread stalls issuing copies.
+// Pass 1, one CTA per (seq, chunk, value head), computes everything that
+// does not depend on the state and writes it to a caller-provided
+// workspace: the Gram products K K^T and Q K^T, A, T = (I + A)^-1, and from
+// them T'' = T diag(beta) and P' = q_scale (Q K^T o Gam)_{i<=r}, as TF32
+// canonical images.  The first value head of each key head also stores the
+// TF32-rounded [K; Q] rows in the 128-byte-swizzled layout the MMA reads
+// (exactly its own shared-memory stack) and K^T as a canonical image: the
+// state pass then loads every operand ready-made and rounds nothing but its
+// own TMEM products.
 //
-// Pass 1 is free of the lazy state scale c (S = c * TMEM S): T'' = T diag(beta)
-// and -T' = -T diag(beta gamma) are built by pass 2 from T, and c enters
-// pass 2 through the K operand of X (K_img = c K, so X = (c S~) K^T exactly as
-// in the single-pass kernel), through Q' and through K'.
+// Pass 2, one CTA per (seq, value head), runs the state-dependent chain per
+// chunk with the state in TMEM as S = c * S~ (c a lazy scalar): [X | Z] =
+// S~ [K; Q]^T, W = V^T - X diag(c gamma), U^T = W T''^T, Y^T = Z diag(c
+// q_scale gamma) + U^T P'^T, S~ += U~^T K^T.  Its loads are bulk copies
+// (images) and one TMA box per chunk (V rows), each on its own mbarrier.
 //
-// Workspace layout: float ws[head][chunk][8192], head = s * n_v + vh:
-// [0, 4096) T (64 x 64, canonical K-major image, unrounded f32),
-// [4096, 8192) P' (canonical image, rounded to TF32).
+// Workspace layout (floats):
+//   ws[head][chunk][8192], head = s * n_v + vh:
+//     [0, 4096) T'' and [4096, 8192) P' (canonical K-major images, TF32);
+//   then ws_k[s * n_k + kh][chunk][24576]:
+//     [0, 16384) the [K; Q] stack (column block cb = 16 KB: K's 64 rows,
+//     then Q's, 128-byte swizzled), [16384, 24576) K^T (128 x 64 canonical).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -39,10 +38,11 @@ namespace {
 
 using namespace chunked;
 
-constexpr uint32_t kWsFloats = 8192;  // per (head, chunk)
+constexpr uint32_t kWsFloats = 8192;    // per (head, chunk): T'' and P'
+constexpr uint32_t kWsKFloats = 24576;  // per (seq, key head, chunk): [K; Q] and K^T images
 
 // per-token scalar slots (64 floats each)
-enum { Q_G = 0, Q_GAM, Q_GAMP, Q_BETA, Q_GPREV, Q_EG, Q_GRAW, Q_BRAW, Q_KTS, Q_TPS, Q_QS, Q_NSC };
+enum { Q_G = 0, Q_GAM, Q_GAMP, Q_BETA, Q_GPREV, Q_EG, Q_GRAW, Q_BRAW, Q_KTS, Q_WS, Q_QS, Q_NSC };
 
 // Per-chunk scalars of one warp (warp 0): inclusive prefix sums of g over the
 // chunk (G), exclusive ones (Gp), the decays e^-G, e^-Gp, e^G and whether any
@@ -104,13 +104,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
-// Named barriers (ids 1..15): arrive without waiting, or wait for `n` threads.
-__device__ __forceinline__ void named_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
-}
 // K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
@@ -134,7 +127,8 @@ struct PrepArgs {
   const float *__restrict__ k;
   const float *__restrict__ g;
   const float *__restrict__ beta;
-  float *__restrict__ ws;
+  float *__restrict__ ws;    // per (head, chunk) images
+  float *__restrict__ ws_k;  // per (seq, key head, chunk) images
   uint32_t nk, nv, nt, group, khead_div, nchunks;
   float q_scale;
 };
@@ -179,6 +173,9 @@ __global__ void __launch_bounds__(NTH, 2)
   const int nc = static_cast<int>(min(static_cast<uint32_t>(C), a.nt - t0));
   const size_t sc0 = (static_cast<size_t>(s) * a.nt + t0) * a.nv + vh;
   float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
+  // one value head per key head stores the key-head images
+  const bool leader = a.khead_div ? vh % a.group == 0 : vh < a.nk;
+  float *wk = a.ws_k + ((static_cast<size_t>(s) * a.nk + kh) * a.nchunks + ch) * kWsKFloats;
 
   stage_gates_async(sbase + P1_SC, a.g, a.beta, sc0, a.nv, nc, tid);
   cp_async_commit();
@@ -208,13 +205,15 @@ __global__ void __launch_bounds__(NTH, 2)
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
 
-  // K and Q to TF32 (round to nearest) in place; per-token scalars (warp 0)
+  // K and Q to TF32 (round to nearest) in place -- the leader also stores
+// the swizzled stack as the [K; Q] image -- and per-token scalars (warp 0)
 #pragma unroll
   for (int it = 0; it < 16; ++it) {
     float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
     float4 x = *p;
-    x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
+    x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
     *p = x;
+    if (leader) __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
   }
   if (warp == 0) {
     float GC;
@@ -232,6 +231,21 @@ __global__ void __launch_bounds__(NTH, 2)
       mma_ss(tmem, d, d, idesc_tf32(128, 64), ks > 0);
     }
     mma_commit(mbar);
+  }
+  // while the Gram runs, the leader stores K^T (d_k rows x 64 tokens,
+  // canonical K-major image) from the TF32 stack
+  if (leader) {
+    for (int oc = tid; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
+      const int dk = oc & 127, i0 = (oc >> 7) * 4;
+      const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
+      float e[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
+      }
+      __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
+    }
   }
   const bool ok = mbar_wait(mbar, 0);
   if (!ok) misc->failed = 1;
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(NTH, 2)
         for (int u = 0; u < 4; ++u) {
           const int i = 32 * half + 4 * j + u;
           const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-          e[u] = i <= r ? tf32_rna(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+          e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
         }
         *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * j, 64) / 4) =
             make_float4(e[0], e[1], e[2], e[3]);
@@ -282,15 +296,19 @@ __global__ void __launch_bounds__(NTH, 2)
   }
   cta_sync();
 
-  // T = (I + A)^-1, written as a canonical image (NaN if the Gram wait timed out)
+  // T = (I + A)^-1; T'' = T diag(beta) written as a TF32 canonical image
+  // (NaN if the Gram wait timed out)
   tri_inverse(sA, sT, sM, tid);
   {
     const float nan = __int_as_float(0x7fc00000);
+    const float *bet = sc + Q_BETA * 64;
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int ci = tid + NTH * it;
       const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
       float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+      t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
+                      tf32_rn(t.w * bet[i0 + 3]));
       if (misc->failed) t = make_float4(nan, nan, nan, nan);
       reinterpret_cast<float4 *>(ws)[ci] = t;
     }
@@ -304,24 +322,21 @@ __global__ void __launch_bounds__(NTH, 2)
 
 // ================================================================ pass 2
 
-// TMEM columns (Y^T alternates between two regions so a chunk's outputs are
-// read out while the next chunk's products run)
-// [X | Y^T] is one N = 128 product; its two regions alternate by chunk.
-constexpr uint32_t P2_TM_S = 0, P2_TM_XY0 = 128, P2_TM_U = 256, P2_TM_V = 320, P2_TM_XY1 = 384;
+// TMEM columns: the state, U^T, W (then U~^T), and [X | Z -> Y^T] in two
+// regions that alternate by chunk, so a chunk's outputs are read out while
+// the next chunk's products run.
+constexpr uint32_t P2_TM_S = 0, P2_TM_XY0 = 128, P2_TM_U = 256, P2_TM_W = 320, P2_TM_XY1 = 384;
 constexpr uint32_t P2_TM_COLS = 512;
 
-// Shared memory (bytes from a 1024-aligned base).  K and Q arrive by TMA as
-// four 64-row x 128-byte boxes each, 128-byte swizzled, interleaved so that
-// column block cb (32 floats) holds K's 64 rows then Q's (16 KB): [K; Q'] is
-// then one 128-row K-major SWIZZLE_128B operand, and a warp reading either a
-// row or a column of K touches distinct banks.
-constexpr uint32_t P2_KQ = 0;                      // [K; Q] (TMA) -> [K; Q'] in TF32, in place
-constexpr uint32_t P2_KT = P2_KQ + 65536;          // K'^T, 128 x 64 canonical (no swizzle)
-constexpr uint32_t P2_TPP = P2_KT + 32768;         // T image (bulk copy) -> T'' in place
-constexpr uint32_t P2_TP = P2_TPP + 16384;         // -T'
-constexpr uint32_t P2_P = P2_TP + 16384;           // P' image (bulk copy), used as is
-constexpr uint32_t P2_VS = P2_P + 16384;           // V rows (TMA), 64 x 128 natural
-constexpr uint32_t P2_SC = P2_VS + 32768;          // per-token scalars
+// Shared memory (bytes from a 1024-aligned base).  The [K; Q] image is the
+// swizzled stack pass 1 stored (column block cb = 16 KB: K's 64 rows, then
+// Q's), one 128-row K-major SWIZZLE_128B operand.
+constexpr uint32_t P2_KQ = 0;                 // [K; Q] image (bulk copy)
+constexpr uint32_t P2_KT = P2_KQ + 65536;     // K^T image (bulk copy), 128 x 64 canonical
+constexpr uint32_t P2_TPP = P2_KT + 32768;    // T'' image (bulk copy)
+constexpr uint32_t P2_P = P2_TPP + 16384;     // P' image (bulk copy)
+constexpr uint32_t P2_VS = P2_P + 16384;      // V rows (TMA), 64 x 128 natural
+constexpr uint32_t P2_SC = P2_VS + 32768;     // per-token scalars
 constexpr uint32_t P2_MISC = P2_SC + Q_NSC * 64 * 4;
 constexpr uint32_t P2_SMEM = P2_MISC + 128 + 1024;  // + room to align the base to 1024
 static_assert(P2_SMEM <= 232448, "pass-2 shared memory");
@@ -332,7 +347,8 @@ struct StateArgs {
   const float *__restrict__ g;
   const float *__restrict__ beta;
   const float *state_in;
-  const float *__restrict__ ws;
+  const float *__restrict__ ws;    // per (head, chunk) images
+  const float *__restrict__ ws_k;  // per (seq, key head, chunk) images
   float *__restrict__ output;
   float *state_out;
   uint32_t nk, nv, nt, group, khead_div, nchunks;
@@ -340,36 +356,84 @@ struct StateArgs {
 };
 
 struct P2Misc {
-  unsigned long long mbar1;   // batch-1 MMA commits
-  unsigned long long mbar2;   // batch-2 MMA commits
-  unsigned long long bar_in;  // TMA: K, Q rows and the T image of a chunk
-  unsigned long long bar_v;   // TMA: V rows of a chunk
-  unsigned long long bar_p;   // TMA: P' image of a chunk
+  unsigned long long mbar_xy;  // [X | Z] MMA commit
+  unsigned long long mbar1;    // U^T MMA commit
+  unsigned long long mbar2;    // batch-2 MMA commit
+  unsigned long long bar_kq;   // bulk copy: the [K; Q] image of a chunk
+  unsigned long long bar_kt;   // bulk copy: the K^T image of a chunk
+  unsigned long long bar_t;    // bulk copy: the T'' image of a chunk
+  unsigned long long bar_v;    // TMA: V rows of a chunk
+  unsigned long long bar_p;    // bulk copy: the P' image of a chunk
   uint32_t tmem_base;
   int failed;
   float c_renorm, c_fold, c_next;
   int do_renorm, do_fold;
 };
+static_assert(sizeof(P2Misc) <= 128, "pass-2 misc area");
 
-// Thread 0: this chunk's K and Q rows (4 boxes each) and T image, on bar_in.
-__device__ __forceinline__ void p2_load_in(uint32_t sbase, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
-                                           int kh, int t0, int s, const float *timg, uint32_t bar) {
-  mbar_expect_tx(bar, 2 * kRowsBytes + kImgBytes);
+// One warp: a chunk's raw g and beta into the scalar area by 4-byte
+// asynchronous copies; tokens past the chunk's end read as zero.
+__device__ __forceinline__ void stage_gates_warp(uint32_t sc_addr, const float *g, const float *beta, size_t sc0,
+                                                 size_t nv, int nc, int lane) {
 #pragma unroll
-  for (int cb = 0; cb < 4; ++cb) {
-    tma_load_4d(sbase + P2_KQ + cb * 16384, tm_k, 32 * cb, kh, t0, s, bar);
-    tma_load_4d(sbase + P2_KQ + cb * 16384 + 8192, tm_q, 32 * cb, kh, t0, s, bar);
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    const size_t src = sc0 + static_cast<size_t>(i < nc ? i : 0) * nv;
+    const uint32_t n = i < nc ? 4u : 0u;
+    cp_async4(sc_addr + (Q_GRAW * 64 + i) * 4, g + src, n);
+    cp_async4(sc_addr + (Q_BRAW * 64 + i) * 4, beta + src, n);
   }
-  bulk_load(sbase + P2_TPP, timg, kImgBytes, bar);
 }
 
-// The state pass (see the file comment); loads by TMA, waits bounded.
+// One warp, once the chunk's raw gates have landed: the per-token scalars,
+// the lazy-scale bookkeeping of the chunk (S = c * TMEM S enters with scale
+// c) and the column scales of W, U~ and Z (below).  Returns the scale the
+// chunk hands on.
+template <bool DECAY_AFTER>
+__device__ __forceinline__ float p2_chunk_setup(float *sc, P2Misc *misc, float c, float q_scale, int lane) {
+  float GC;
+  const bool extreme = chunk_scalars(sc, lane, &GC);
+  float cc = c, renorm = 1.f;
+  const bool do_renorm = cc < kRenormLo || cc > kRenormHi;
+  if (do_renorm) { renorm = cc; cc = 1.f; }
+  const float gamC = __expf(-GC);
+  float cnext, fold = 1.f;
+  if (extreme) { fold = cc * gamC; cnext = 1.f; }
+  else { cnext = cc * gamC; }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    const float Gi = sc[Q_G * 64 + i];
+    sc[Q_KTS * 64 + i] = __expf(Gi - GC) / cnext;                                      // U~ column
+    sc[Q_WS * 64 + i] = cc * (DECAY_AFTER ? sc[Q_GAMP * 64 + i] : sc[Q_GAM * 64 + i]);  // W column
+    sc[Q_QS * 64 + i] = cc * q_scale * sc[Q_GAM * 64 + i];                             // Z column
+  }
+  if (lane == 0) {
+    misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext;
+    misc->do_renorm = do_renorm; misc->do_fold = extreme;
+  }
+  return cnext;
+}
+
+// The state pass: one CTA per (seq, value head) over all chunks, the state
+// in TMEM as S = c * S~.  Per chunk, with everything state-free read from
+// the workspace:
+//   [X | Z] = S~ [K; Q]^T                 (one N = 128 product)
+//   W  = V^T - X diag(c gamma)            (TMEM pass; gamma' with decay-after)
+//   U^T = W T''^T                         (T'' = T diag(beta), so this is
+//                                          V^T T''^T + X (-T')^T of the chunk
+//                                          equations, -T' = -c T diag(beta gamma))
+//   Y^T = Z diag(c q_scale gamma) + U^T P'^T
+//   S~ <- S~ + U~^T K^T,  U~ = U diag(e^(G_i - G_C) / c_next)
+// The serial chain is [X | Z] -> W -> U^T -> rounding -> batch 2; the
+// outputs, Z's scaling and the next chunk's V come in beside it.  Thread 32
+// issues the MMAs, thread 0 the copies, warp 2 sets up the next chunk's
+// scalars while batch 2 runs.  Waits are bounded.
 template <bool DECAY_AFTER>
 __global__ void __launch_bounds__(NTH, 1)
-    gdn_chunk_state_kernel(const StateArgs a, const __grid_constant__ CUtensorMap tm_k,
-                           const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v) {
+    gdn_chunk_state_kernel(const StateArgs a, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // operate from a 1024-byte aligned base (the swizzled boxes need it)
+  // operate from a 1024-byte aligned base (the swizzled image needs it)
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t pad = ((raw_addr + 1023u) & ~1023u) - raw_addr;
   unsigned char *smem = smem_raw + pad;
@@ -377,32 +441,33 @@ __global__ void __launch_bounds__(NTH, 1)
   const float *sVS = reinterpret_cast<const float *>(smem + P2_VS);
   P2Misc *misc = reinterpret_cast<P2Misc *>(smem + P2_MISC);
   const uint32_t sbase = raw_addr + pad;
-  const uint32_t mbar1 = smem_addr(&misc->mbar1), mbar2 = smem_addr(&misc->mbar2);
-  const uint32_t bar_in = smem_addr(&misc->bar_in), bar_v = smem_addr(&misc->bar_v),
-                 bar_p = smem_addr(&misc->bar_p);
+  const uint32_t mbar_xy = smem_addr(&misc->mbar_xy), mbar1 = smem_addr(&misc->mbar1),
+                 mbar2 = smem_addr(&misc->mbar2);
+  const uint32_t bar_kq = smem_addr(&misc->bar_kq), bar_kt = smem_addr(&misc->bar_kt),
+                 bar_t = smem_addr(&misc->bar_t), bar_v = smem_addr(&misc->bar_v), bar_p = smem_addr(&misc->bar_p);
 
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
   const int row = tid & 127;
   const int half = tid >> 7;
   const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  constexpr int ISSUER = 32;  // thread that issues (and commits) every MMA
 
   const uint32_t head = blockIdx.x;  // = s * nv + vh
   const uint32_t vh = head % a.nv, s = head / a.nv;
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
   const uint32_t nt = a.nt;
+  const uint32_t nchunks = a.nchunks;
   const size_t state_head = static_cast<size_t>(head) * D * D;
   const size_t v_tok = static_cast<size_t>(a.nv) * D;
-  const float *wseq = a.ws + static_cast<size_t>(head) * a.nchunks * kWsFloats;
+  const float *wseq = a.ws + static_cast<size_t>(head) * nchunks * kWsFloats;
+  const float *wkseq = a.ws_k + (static_cast<size_t>(s) * a.nk + kh) * nchunks * kWsKFloats;
   const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
-  const uint32_t nchunks = a.nchunks;
 
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar1));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar2));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_in));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_v));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_p));
+    const uint32_t bars[8] = {mbar_xy, mbar1, mbar2, bar_kq, bar_kt, bar_t, bar_v, bar_p};
+#pragma unroll
+    for (int b = 0; b < 8; ++b) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bars[b]));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
   }
@@ -413,17 +478,35 @@ __global__ void __launch_bounds__(NTH, 1)
   }
   __syncthreads();  // barriers initialised before anyone waits on them
   // chunk 0's inputs start arriving while the state is loaded
-  {
-    const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
-    if (tid == 0) {
-      p2_load_in(sbase, &tm_k, &tm_q, static_cast<int>(kh), 0, static_cast<int>(s), wseq, bar_in);
-      mbar_expect_tx(bar_v, kRowsBytes);
-      tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), 0, static_cast<int>(s), bar_v);
-      mbar_expect_tx(bar_p, kImgBytes);
-      bulk_load(sbase + P2_P, wseq + 4096, kImgBytes, bar_p);
-    }
-    stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first, a.nv, nc0, tid);
+  if (tid == 0) {
+    mbar_expect_tx(bar_kq, 65536);
+    bulk_load(sbase + P2_KQ, wkseq, 65536, bar_kq);
+    mbar_expect_tx(bar_kt, kRowsBytes);
+    bulk_load(sbase + P2_KT, wkseq + 16384, kRowsBytes, bar_kt);
+    mbar_expect_tx(bar_t, kImgBytes);
+    bulk_load(sbase + P2_TPP, wseq, kImgBytes, bar_t);
+    mbar_expect_tx(bar_p, kImgBytes);
+    bulk_load(sbase + P2_P, wseq + 4096, kImgBytes, bar_p);
+    mbar_expect_tx(bar_v, kRowsBytes);
+    tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), 0, static_cast<int>(s), bar_v);
+  }
+  // copies armed and MMA batches committed per barrier (uniform over the
+  // CTA), for the bounded waits at exit
+  uint32_t n_ld = 1, n_v = 1, n_mma = 0;
+  float c_carry = 1.f;  // warp 2: the scale the next chunk starts with
+  if (warp == 2) {
+    stage_gates_warp(sbase + P2_SC, a.g, a.beta, sc_first, a.nv, static_cast<int>(min(nt, static_cast<uint32_t>(C))),
+                     lane);
     cp_async_commit();
+    cp_async_wait_all();
+    __syncwarp();
+    c_carry = p2_chunk_setup<DECAY_AFTER>(sc, misc, 1.f, a.q_scale, lane);
+    __syncwarp();  // every lane is done with the raw gates
+    if (nchunks > 1) {
+      stage_gates_warp(sbase + P2_SC, a.g, a.beta, sc_first + static_cast<size_t>(C) * a.nv, a.nv,
+                       static_cast<int>(min(nt - C, static_cast<uint32_t>(C))), lane);
+      cp_async_commit();
+    }
   }
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
@@ -445,286 +528,226 @@ __global__ void __launch_bounds__(NTH, 1)
     }
     tmem_wait_st();
   }
+  // This thread's V^T values of a chunk: row d_v, tokens 32*half .. +31.
+  float vr[32];
+  if (!mbar_wait(bar_v, 0)) misc->failed = 1;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) vr[j] = sVS[(32 * half + j) * D + row];
 
-  float c = 1.f;
-  uint32_t ph1 = 0, ph2 = 0;
   bool failed = false;
-  bool b2_pending = false;  // a batch 2 was issued and not yet waited for
-  // TMA arms and waits per barrier (uniform over the CTA): a copy is in
-  // flight while a barrier has been armed more often than waited on
-  uint32_t armed_in = 1, armed_v = 1, armed_p = 1, waited_in = 0, waited_v = 0, waited_p = 0;
-  const int wt = tid - 32;  // worker index of warps 1..7 (steps 5-7)
-  constexpr int NW = NTH - 32;
-
-  for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
+  for (uint32_t ch = 0; ch < nchunks; ++ch) {
     const uint32_t t0 = ch * C;
-    const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
     const bool more = ch + 1 < nchunks;
-    const int ncn = more ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
-    const uint32_t tm_x = (ch & 1) ? P2_TM_XY1 : P2_TM_XY0;  // X; Y^T at tm_x + 64
+    const uint32_t par = ch & 1;                         // phase parity of this chunk's barriers
+    const uint32_t tm_x = par ? P2_TM_XY1 : P2_TM_XY0;  // X; Z -> Y^T at tm_x + 64
     const uint32_t tm_y = tm_x + 64;
-    const uint32_t par = ch & 1;  // phase parity of this chunk's TMA barriers
 
-    // ---- 0. this chunk's V rows (TMA) and gates (cp.async) have landed; its
-    // K, Q rows and T image may still be on the way, and the previous chunk's
-    // batch 2 may still be running
-    if (!mbar_wait(bar_v, par)) misc->failed = 1;
-    ++waited_v;
-    cp_async_wait_all();
-    __syncthreads();
+    // ---- 0. the previous chunk's batch 2 is done (thread 0 waited), this
+    // chunk's scalars are set and its V is in registers
+    cta_sync();
     if (misc->failed) { failed = true; break; }
+    if (misc->do_renorm) {  // c left [2^-30, 2^30]: fold it into S (rare)
+      if (ch > 0 && !mbar_wait(mbar2, par ^ 1)) misc->failed = 1;
+      __syncwarp();
+      fence_after();
+      tmem_scale64(tl + P2_TM_S + 64 * half, misc->c_renorm);
+      cta_sync();
+    }
+    if (tid == 0 && more) {  // V rows are free: the next chunk's
+      fence_async_smem();
+      mbar_expect_tx(bar_v, kRowsBytes);
+      tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C), static_cast<int>(s),
+                  bar_v);
+    }
 
-    // ---- 1. warp 0: per-token scalars and the lazy-scale bookkeeping.
-    // Meanwhile V^T -> TMEM (lane d_v, columns = tokens), warp 4 taking both
-    // halves of the lane quarter it shares with warp 0.
-    if (warp == 0) {
-      float GC;
-      const bool extreme = chunk_scalars(sc, lane, &GC);
-      float cc = c, renorm = 1.f;
-      const bool do_renorm = cc < kRenormLo || cc > kRenormHi;
-      if (do_renorm) { renorm = cc; cc = 1.f; }
-      const float gamC = __expf(-GC);
-      float cnext, fold = 1.f;
-      if (extreme) { fold = cc * gamC; cnext = 1.f; }
-      else { cnext = cc * gamC; }
+    // ---- 1. [X | Z] = S~ [K; Q]^T
+    if (tid == ISSUER) {
+      if (!mbar_wait(bar_kq, par)) misc->failed = 1;
+#pragma unroll
+      for (int ks = 0; ks < D / 8; ++ks)
+        mma_ts(tmem + tm_x, tmem + P2_TM_S + 8 * ks,
+               sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32), idesc_tf32(128, 128), ks > 0);
+      mma_commit(mbar_xy);
+    }
+    // meanwhile warps 4-7: the previous chunk's outputs (every chunk but the
+    // last is full)
+    if (warp >= 4 && ch > 0) {
+      if (!mbar_wait(mbar2, par ^ 1)) misc->failed = 1;
+      __syncwarp();
+      fence_after();
+      const uint32_t tm_yp = (par ? P2_TM_XY0 : P2_TM_XY1) + 64;
+      float *obase = a.output + ((static_cast<size_t>(s) * nt + (t0 - C)) * a.nv + vh) * D + row;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int i = lane + 32 * h;
-        const float Gi = sc[Q_G * 64 + i];
-        const float bi = sc[Q_BETA * 64 + i];
-        sc[Q_KTS * 64 + i] = __expf(Gi - GC) / cnext;                       // K' row scale
-        sc[Q_TPS * 64 + i] = -cc * bi * (DECAY_AFTER ? sc[Q_GAMP * 64 + i] : sc[Q_GAM * 64 + i]);  // -T' column
-        sc[Q_QS * 64 + i] = cc * a.q_scale * sc[Q_GAM * 64 + i];           // Q' row scale
-      }
-      if (lane == 0) {
-        misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext;
-        misc->do_renorm = do_renorm; misc->do_fold = extreme;
-      }
-    } else {
+        uint32_t yv[32];
+        GDN_TMEM_LD32(tl + tm_yp + 32 * h, yv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int h = warp == 4 ? hh : half;
-        if (hh == 1 && warp != 4) break;
-        uint32_t vv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rna(sVS[(32 * h + j) * D + row]));
-        GDN_TMEM_ST32(tl + P2_TM_V + 32 * h, vv);
+        for (int j = 0; j < 32; ++j) obase[static_cast<size_t>(32 * h + j) * v_tok] = __uint_as_float(yv[j]);
       }
+    }
+
+    // ---- 2. W = V^T - X diag(c gamma), rounded to TF32, into TMEM
+    if (!mbar_wait(mbar_xy, par)) misc->failed = 1;
+    __syncwarp();
+    fence_after();
+    {
+      const float *wsc = sc + Q_WS * 64 + 32 * half;
+      uint32_t xv[32];
+      GDN_TMEM_LD32(tl + tm_x + 32 * half, xv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xv[j] = __float_as_uint(tf32_rn(fmaf(-wsc[j], __uint_as_float(xv[j]), vr[j])));
+      GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, xv);
       tmem_wait_st();
     }
     cta_sync();
-    if (more) {  // the V buffer is free: the next chunk's V rows
-      if (tid == 0) {
-        fence_async_smem();
-        mbar_expect_tx(bar_v, kRowsBytes);
-        tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C),
-                    static_cast<int>(s), bar_v);
-      }
-      ++armed_v;
+
+    // ---- 3. U^T = W T''^T; [K; Q] is free for the next chunk's
+    if (tid == 0 && more) {
+      mbar_expect_tx(bar_kq, 65536);
+      bulk_load(sbase + P2_KQ, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats, 65536, bar_kq);
     }
-    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
-    const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
-
-    // ---- 2. the previous chunk's batch 2 is done: S, Y, K'^T and P' are
-    // settled; this chunk's P' may load
-    if (b2_pending) {
-      if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
-      ph2 ^= 1;
-      b2_pending = false;
-      fence_after();
-      __syncthreads();
-      if (misc->failed) { failed = true; break; }
-      if (tid == 0) {
-        mbar_expect_tx(bar_p, kImgBytes);
-        bulk_load(sbase + P2_P, wseq + ch * kWsFloats + 4096, kImgBytes, bar_p);
-      }
-      ++armed_p;
+    if (tid == ISSUER) {
+      if (!mbar_wait(bar_t, par)) misc->failed = 1;
+#pragma unroll
+      for (int ks = 0; ks < C / 8; ++ks)
+        mma_ts(tmem + P2_TM_U, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), idesc_tf32(128, 64),
+               ks > 0);
+      mma_commit(mbar1);
     }
-
-    // ---- 3. fold c into S if it left [2^-30, 2^30] (no MMA in flight here)
-    if (do_renorm) tmem_scale64(tl + P2_TM_S + 64 * half, c_renorm);
-
-    // ---- 4. K, Q rows and the T image
-    if (!mbar_wait(bar_in, par)) misc->failed = 1;
-    ++waited_in;
-    __syncthreads();
-    if (misc->failed) { failed = true; break; }
-
-    // ---- 5. all warps: K to TF32 and Q' in place (row = chunk / 8 in its box)
-    {
+    // meanwhile warps 4-7: Y^T = Z diag(c q_scale gamma)
+    __syncwarp();
+    if (warp >= 4) {
       const float *qs = sc + Q_QS * 64;
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;
-        const int off = (ci >> 9) * 16384 + (ci & 511) * 16;
-        float4 *pk = reinterpret_cast<float4 *>(smem + P2_KQ + off);
-        float4 x = *pk;
-        x.x = tf32_rna(x.x); x.y = tf32_rna(x.y); x.z = tf32_rna(x.z); x.w = tf32_rna(x.w);
-        *pk = x;
-        float4 *pq = reinterpret_cast<float4 *>(smem + P2_KQ + 8192 + off);
-        float4 y = *pq;
-        const float f = qs[(ci & 511) >> 3];
-        y.x = tf32_rna(y.x * f); y.y = tf32_rna(y.y * f); y.z = tf32_rna(y.z * f); y.w = tf32_rna(y.w * f);
-        *pq = y;
-      }
-    }
-    fence_async_smem();
-    cta_sync();
-
-    // ---- 6-7. warp 0 issues [X | Y^T] = S [K; Q']^T (one N = 128 product),
-    // then, once warps 1-7 have built T'' and -T' (named barrier),
-    // Ut = V^T T''^T + X (-T')^T; warps 1-7 then build K'^T from the TF32 K
-    // while those run (only batch 2 reads it).  The scale c rides on -T' and Q'.
-    if (warp == 0) {
-      if (lane == 0) {
+      for (int h = 0; h < 2; ++h) {
+        uint32_t zv[32];
+        GDN_TMEM_LD32(tl + tm_y + 32 * h, zv);
+        tmem_wait_ld();
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)
-          mma_ts(tmem + tm_x, tmem + P2_TM_S + 8 * ks,
-                 sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32), idesc_tf32(128, 128),
-                 ks > 0);
+        for (int j = 0; j < 32; ++j) zv[j] = __float_as_uint(__uint_as_float(zv[j]) * qs[32 * h + j]);
+        GDN_TMEM_ST32(tl + tm_y + 32 * h, zv);
       }
-      __syncwarp();
-      named_sync(1, NTH);
-      fence_after();
-      if (lane == 0) {
-        const uint32_t i64 = idesc_tf32(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
-          mma_ts(tmem + P2_TM_U, tmem + P2_TM_V + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), i64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
-          mma_ts(tmem + P2_TM_U, tmem + tm_x + 8 * ks, sdesc(sbase + P2_TP + ks * 256, 2048), i64, 1);
-        mma_commit(mbar1);
-      }
-      __syncwarp();
-    } else {
-      const float *tps = sc + Q_TPS * 64, *bet = sc + Q_BETA * 64;
-      for (int ci = wt; ci < 1024; ci += NW) {  // T'' in place, -T' beside it
-        const int i0 = 4 * ((ci >> 3) & 15);
-        float4 *pt = reinterpret_cast<float4 *>(smem + P2_TPP + ci * 16);
-        const float4 t = *pt;
-        *reinterpret_cast<float4 *>(smem + P2_TP + ci * 16) =
-            make_float4(tf32_rna(t.x * tps[i0]), tf32_rna(t.y * tps[i0 + 1]),
-                        tf32_rna(t.z * tps[i0 + 2]), tf32_rna(t.w * tps[i0 + 3]));
-        *pt = make_float4(tf32_rna(t.x * bet[i0]), tf32_rna(t.y * bet[i0 + 1]),
-                          tf32_rna(t.z * bet[i0 + 2]), tf32_rna(t.w * bet[i0 + 3]));
-      }
-      fence_async_smem();
-      fence_before();
-      named_arrive(1, NTH);
-      const float *kts = sc + Q_KTS * 64;
-      for (int oc = wt; oc < 2048; oc += NW) {  // K'^T: d_k = oc % 128, tokens 4 (oc / 128) .. +3
-        const int dk = oc & 127, i0 = (oc >> 7) * 4;
-        const unsigned char *kb = smem + P2_KQ + (dk >> 5) * 16384 + (dk & 3) * 4;
-        float e[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u;
-          e[u] = tf32_rna(*reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4)) *
-                          kts[i]);
-        }
-        *reinterpret_cast<float4 *>(smem + P2_KT + canon(dk, i0, 64)) = make_float4(e[0], e[1], e[2], e[3]);
-      }
-      fence_async_smem();
+      tmem_wait_st();
     }
 
-    // ---- the previous chunk's outputs, from its Y^T region, while these run
-    if (ch > 0) {
-      const uint32_t tm_yp = ((ch & 1) ? P2_TM_XY0 : P2_TM_XY1) + 64;
-      uint32_t yv[32];
-      GDN_TMEM_LD32(tl + tm_yp + 32 * half, yv);
-      tmem_wait_ld();
-      float *obase = a.output + ((static_cast<size_t>(s) * nt + (t0 - C)) * a.nv + vh) * D + row;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)  // every chunk but the last is full
-        obase[static_cast<size_t>(32 * half + j) * v_tok] = __uint_as_float(yv[j]);
-    }
-
-    if (!mbar_wait(mbar1, ph1)) misc->failed = 1;
-    ph1 ^= 1;
+    // ---- 4. U^T to TF32 (nearest) in place and U~^T over W; extreme gates:
+    // decay S now
+    if (!mbar_wait(mbar1, par)) misc->failed = 1;
+    __syncwarp();
     fence_after();
-    __syncthreads();
-    if (misc->failed) { failed = true; break; }
-    // K, Q and the T image are free: the next chunk's (TMA) and its gates
-    if (more) {
-      if (tid == 0) {
-        fence_async_smem();
-        p2_load_in(sbase, &tm_k, &tm_q, static_cast<int>(kh), static_cast<int>(t0 + C), static_cast<int>(s),
-                   wseq + (ch + 1) * kWsFloats, bar_in);
-      }
-      ++armed_in;
-      stage_gates_async(sbase + P2_SC, a.g, a.beta, sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv,
-                        ncn, tid);
-      cp_async_commit();
-    }
-
-    // ---- 8. U^T to TF32 (nearest) in place; extreme gates: decay S now
     {
-      uint32_t uv[32];
+      const float *kts = sc + Q_KTS * 64 + 32 * half;
+      uint32_t uv[32], us[32];
       GDN_TMEM_LD32(tl + P2_TM_U + 32 * half, uv);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rna(__uint_as_float(uv[j])));
+      for (int j = 0; j < 32; ++j) {
+        const float u = __uint_as_float(uv[j]);
+        uv[j] = __float_as_uint(tf32_rn(u));
+        us[j] = __float_as_uint(tf32_rn(u * kts[j]));
+      }
       GDN_TMEM_ST32(tl + P2_TM_U + 32 * half, uv);
+      GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, us);
       tmem_wait_st();
     }
-    if (do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, c_fold);
-    if (!mbar_wait(bar_p, par)) misc->failed = 1;  // this chunk's P'
-    ++waited_p;
+    if (misc->do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, misc->c_fold);
     cta_sync();
 
-    // ---- 9. batch 2: Yt += Ut P'^T; S += Ut K'^T.  Not waited for here unless
-    // this is the last chunk: the next chunk's first steps overlap it.
-    if (tid == 0) {
+    // ---- 5. batch 2: Yt += Ut P'^T; S~ += U~t K^T.  Meanwhile warp 2 sets up
+    // the next chunk's scalars and every thread takes the next chunk's V.
+    if (tid == 0 && more) {  // U^T is done: T'' is free
+      mbar_expect_tx(bar_t, kImgBytes);
+      bulk_load(sbase + P2_TPP, wseq + static_cast<size_t>(ch + 1) * kWsFloats, kImgBytes, bar_t);
+    }
+    if (tid == ISSUER) {
+      if (!mbar_wait(bar_p, par)) misc->failed = 1;
+      if (!mbar_wait(bar_kt, par)) misc->failed = 1;
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + tm_y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048),
-               idesc_tf32(128, 64), 1);
+        mma_ts(tmem + tm_y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048), idesc_tf32(128, 64), 1);
 #pragma unroll
       for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_S, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
+        mma_ts(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
                idesc_tf32(128, 128), 1);
       mma_commit(mbar2);
     }
-    b2_pending = true;
-    if (!more) {  // ---- 10. the last chunk: wait, then its outputs
-      if (!mbar_wait(mbar2, ph2)) misc->failed = 1;
-      ph2 ^= 1;
-      b2_pending = false;
-      fence_after();
-      __syncthreads();
-      if (misc->failed) { failed = true; break; }
-      uint32_t yv[32];
-      GDN_TMEM_LD32(tl + tm_y + 32 * half, yv);
-      tmem_wait_ld();
-      float *obase = a.output + ((static_cast<size_t>(s) * nt + t0) * a.nv + vh) * D + row;
+    ++n_mma;
+    if (more) {
+      if (warp == 2) {
+        cp_async_wait_all();
+        __syncwarp();
+        c_carry = p2_chunk_setup<DECAY_AFTER>(sc, misc, c_carry, a.q_scale, lane);
+        __syncwarp();
+        if (ch + 2 < nchunks) {
+          stage_gates_warp(sbase + P2_SC, a.g, a.beta, sc_first + static_cast<size_t>(t0 + 2 * C) * a.nv, a.nv,
+                           static_cast<int>(min(nt - t0 - 2 * C, static_cast<uint32_t>(C))), lane);
+          cp_async_commit();
+        }
+      }
+      if (!mbar_wait(bar_v, par ^ 1)) misc->failed = 1;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int i = 32 * half + j;
-        if (i < nc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      for (int j = 0; j < 32; ++j) vr[j] = sVS[(32 * half + j) * D + row];
+    }
+    if (tid == 0) {  // batch 2 done: P' and K^T are free for the next chunk's
+      if (!mbar_wait(mbar2, par)) misc->failed = 1;
+      if (more) {
+        mbar_expect_tx(bar_p, kImgBytes);
+        bulk_load(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, kImgBytes, bar_p);
+        mbar_expect_tx(bar_kt, kRowsBytes);
+        bulk_load(sbase + P2_KT, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats + 16384, kRowsBytes, bar_kt);
       }
     }
-    c = misc->c_next;
+    if (more) { ++n_ld; ++n_v; }
   }
 
-  // an MMA batch still in flight after a failure finishes (bounded) before
-  // TMEM is read or released
-  if (b2_pending && tid == 0) (void)mbar_wait(mbar2, ph2);
-  fence_after();
-  __syncthreads();
-  cp_async_wait_all();  // no cp.async may still be landing in shared memory at exit
-  // after a failure, let any TMA copy still in flight land (bounded waits)
-  // before the CTA's shared memory is released
+  // ---- the last chunk's outputs
+  cta_sync();
+  if (!failed && !misc->failed) {
+    const uint32_t cl = nchunks - 1;
+    if (!mbar_wait(mbar2, cl & 1)) misc->failed = 1;
+    __syncwarp();
+    fence_after();
+    const uint32_t tm_yl = ((cl & 1) ? P2_TM_XY1 : P2_TM_XY0) + 64;
+    const int ncl = static_cast<int>(nt - cl * C);
+    uint32_t yv[32];
+    GDN_TMEM_LD32(tl + tm_yl + 32 * half, yv);
+    tmem_wait_ld();
+    float *obase = a.output + ((static_cast<size_t>(s) * nt + cl * C) * a.nv + vh) * D + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int i = 32 * half + j;
+      if (i < ncl) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+    }
+  }
+
+  // Nothing may still be in flight when TMEM is read or released or the
+  // CTA's shared memory is freed: after a failure, wait (bounded) for the
+  // last MMA batch and the last copy on every barrier.
+  cp_async_wait_all();
   if (tid == 0) {
-    if (armed_in > waited_in) (void)mbar_wait(bar_in, waited_in & 1);
-    if (armed_v > waited_v) (void)mbar_wait(bar_v, waited_v & 1);
-    if (armed_p > waited_p) (void)mbar_wait(bar_p, waited_p & 1);
+    if (n_mma > 0) {  // every chunk commits once on each MMA barrier
+      (void)mbar_wait(mbar_xy, (n_mma - 1) & 1);
+      (void)mbar_wait(mbar1, (n_mma - 1) & 1);
+      (void)mbar_wait(mbar2, (n_mma - 1) & 1);
+    }
+    const uint32_t pl = (n_ld - 1) & 1;  // every image barrier is armed once per chunk
+    (void)mbar_wait(bar_kq, pl);
+    (void)mbar_wait(bar_kt, pl);
+    (void)mbar_wait(bar_t, pl);
+    (void)mbar_wait(bar_p, pl);
+    (void)mbar_wait(bar_v, (n_v - 1) & 1);
   }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  failed = failed || misc->failed != 0;
 
-  // ---- state_out = c * S (or NaN if a wait timed out)
+  // ---- state_out = c * S~ (or NaN if a wait timed out)
   {
+    const float f = failed ? __int_as_float(0x7fc00000) : misc->c_next;
     float4 *dst = reinterpret_cast<float4 *>(a.state_out + state_head + row * D + 64 * half);
-    const float f = failed ? __int_as_float(0x7fc00000) : c;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
@@ -785,9 +808,10 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   if (e == cudaSuccess) e = rows_map(&tm_v, p.v, p.nv, p.nt, p.ns, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
 
+  float *ws_k = ws + static_cast<size_t>(p.nv) * p.ns * nchunks * kWsFloats;
   PrepArgs pa;
   pa.q = static_cast<const float *>(p.q); pa.k = static_cast<const float *>(p.k);
-  pa.g = p.g; pa.beta = p.beta; pa.ws = ws;
+  pa.g = p.g; pa.beta = p.beta; pa.ws = ws; pa.ws_k = ws_k;
   pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = p.nv / p.nk;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
   auto prep = gdn_chunk_prep_kernel<DA>;
@@ -799,14 +823,14 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 
   StateArgs sa;
   sa.g = p.g; sa.beta = p.beta;
-  sa.state_in = p.state_in; sa.ws = ws; sa.output = static_cast<float *>(p.output);
+  sa.state_in = p.state_in; sa.ws = ws; sa.ws_k = ws_k; sa.output = static_cast<float *>(p.output);
   sa.state_out = p.state_out;
   sa.nk = p.nk; sa.nv = p.nv; sa.nt = p.nt; sa.group = pa.group; sa.khead_div = pa.khead_div;
   sa.nchunks = nchunks; sa.q_scale = p.q_scale;
   auto state = gdn_chunk_state_kernel<DA>;
   e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
   if (e != cudaSuccess) return e;
-  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa, tm_k, tm_q, tm_v);
+  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa, tm_v);
   return cudaGetLastError();
 }
 
@@ -814,7 +838,8 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 
 size_t chunked_split_workspace_bytes(const Problem &p) {
   const size_t nchunks = (static_cast<size_t>(p.nt) + C - 1) / C;
-  return static_cast<size_t>(p.nv) * p.ns * nchunks * kWsFloats * sizeof(float);
+  return (static_cast<size_t>(p.nv) * kWsFloats + static_cast<size_t>(p.nk) * kWsKFloats) * p.ns * nchunks *
+         sizeof(float);
 }
 
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {

@@ -404,9 +404,10 @@ gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const flo
   if (need > gdn::kNoallocWorkspaceBytes)
     return fail(GDN_ERR_INVALID_ARGUMENT,
                 "gdn: this problem needs %zu bytes of chunk scratch; the fixed scratch of "
-                "gdn_forward_chunked_noalloc holds %zu (32 KB per (seq, value head, 64-token "
-                "chunk), at most %zu of them): use gdn_forward_ws with your own workspace",
-                need, gdn::kNoallocWorkspaceBytes, gdn::kNoallocWorkspaceBytes / 32768);
+                "gdn_forward_chunked_noalloc holds %zu (per seq and 64-token chunk the problem "
+                "takes 32 KB per value head and 96 KB per key head): use gdn_forward_ws with "
+                "your own workspace",
+                need, gdn::kNoallocWorkspaceBytes);
   gdn::Problem &p = d.prob;
   fill_problem(p, b, false);
   const cudaError_t err = gdn::launch_chunked_split_noalloc(p, reinterpret_cast<cudaStream_t>(stream));

@@ -374,7 +374,8 @@ def test_round_to_bf16_matches_torch():
 
 def test_workspace_size_values(L):
     w = WORKLOADS["long_prefill"].with_(n_tokens=200, n_seqs=3)
-    assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == 6 * 3 * 4 * 32768 * 8  # 48 heads
+    # per (seq, chunk): 32 KB per value head (48) + 96 KB per key head (16); 3 seqs x 4 chunks
+    assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == 3 * 4 * (48 * 32768 + 16 * 98304)
     assert nat.gdn_workspace_size(w.params()) == 0                   # auto: scan
     assert nat.gdn_workspace_size(SMALL.params()) == 0               # decode
     with pytest.raises(nat.GdnError):
@@ -403,8 +404,9 @@ def test_workspace_checks(L):
 
 @no_device
 def test_noalloc_host_checks(L):
-    """gdn_forward_chunked_noalloc: the fixed scratch holds 1024 chunk slots
-    (32 KB each); one more is refused before anything is enqueued, and a
+    """gdn_forward_chunked_noalloc: the fixed 32 MiB scratch holds 16 chunks
+    of 16 value and 16 key heads (2 MiB each); one more chunk is refused
+    before anything is enqueued, and a
     problem that fits passes every host check (the launch then fails here for
     want of a device).  Non-chunked path bits and shapes are refused."""
     def call(w, params=None, **over):
@@ -413,9 +415,9 @@ def test_noalloc_host_checks(L):
         args = [a[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
         return nat.forward_chunked_noalloc_raw(*args, w.params(path=PATH_CHUNKED) if params is None
                                                else params)
-    fits = WORKLOADS["long_prefill"].with_(n_v_heads=16, n_k_heads=16, n_seqs=1, n_tokens=4096)
-    assert call(fits) == nat.GDN_ERR_CUDA                       # 16 x 64 = 1024 slots
-    over = fits.with_(n_tokens=4097)                            # 16 x 65 slots
+    fits = WORKLOADS["long_prefill"].with_(n_v_heads=16, n_k_heads=16, n_seqs=1, n_tokens=1024)
+    assert call(fits) == nat.GDN_ERR_CUDA                       # 16 chunks x 2 MiB = 32 MiB
+    over = fits.with_(n_tokens=1025)                            # 17 chunks
     assert call(over) == nat.GDN_ERR_INVALID_ARGUMENT
     assert "gdn_forward_ws" in nat.gdn_last_error()
     assert call(fits, params=fits.params()) == nat.GDN_ERR_CUDA  # auto path bits: chunked

@@ -144,5 +144,5 @@ def test_two_pass_workspace_size(torch):
     from serving_gdn_decode_gb300 import _native as nat
     w = WORKLOADS["long_prefill"]
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == \
-        w.n_v_heads * w.n_seqs * (w.n_tokens // 64) * 32768
+        w.n_seqs * (w.n_tokens // 64) * (w.n_v_heads * 32768 + w.n_k_heads * 98304)
     assert nat.gdn_workspace_size(w.params()) == 0

@@ -58,7 +58,7 @@ def test_noalloc_matches_workspace_entry_point_twice(torch):
 
 def test_noalloc_refuses_more_than_its_scratch(torch):
     from serving_gdn_decode_gb300 import _native as nat
-    # 4 value heads x 16 seqs x 17 chunks = 1088 chunk slots > 1024; real
+    # 16 seqs x 17 chunks x (4 x 32 KB + 2 x 96 KB) = 85 MiB > 32 MiB; real
     # buffers of that shape, so the refusal is the only thing tested
     w = Workload("noalloc_big", 128, 128, 2, 4, 1025, 16)
     x = to_dev(make_inputs(w, 73))
