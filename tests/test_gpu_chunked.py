@@ -35,6 +35,9 @@ SHAPES = [  # (n_k, n_v, n_tokens, n_seqs)
     (2, 6, 65, 2),     # one chunk + 1 token
     (4, 8, 200, 2),    # ragged tail
     (16, 48, 256, 1),  # wide GQA, 4 chunks
+    (4, 4, 70, 1),     # one value head per key head: every head stores its key head's images
+    (1, 8, 130, 1),    # eight value heads on one key head
+    (2, 2, 1, 3),      # a single token
 ]
 
 
