@@ -74,18 +74,6 @@ __device__ __forceinline__ bool chunk_scalars(float *sc, int lane, float *GC_out
   return extreme;
 }
 
-// Asynchronous copies of one chunk's raw g and beta into the scalar area
-// (threads 0..127); tokens past the chunk's end read as zero.
-__device__ __forceinline__ void stage_gates_async(uint32_t sc_addr, const float *g, const float *beta,
-                                                  size_t sc0, size_t nv, int nc, int tid) {
-  if (tid < 128) {
-    const int i = tid & 63;
-    const size_t src = sc0 + static_cast<size_t>(i < nc ? i : 0) * nv;
-    cp_async4(sc_addr + ((tid < 64 ? Q_GRAW : Q_BRAW) * 64 + i) * 4, (tid < 64 ? g : beta) + src,
-              i < nc ? 4u : 0u);
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -112,15 +100,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 // ================================================================ pass 1
 
 // shared memory (bytes): the [K;Q] stack for the Gram, then, once the Gram
-// is in TMEM, A, T and the block products overlaid on it
+// is in TMEM, A, T and the block products overlaid on it; the per-token
+// scalars of the value head in hand; the raw g and beta of every value head
+// of the key head (group x 128 floats); the barriers.
 constexpr uint32_t P1_STACK = 0;
 constexpr uint32_t P1_A = 0;
 constexpr uint32_t P1_T = 64 * LD * 4;
 constexpr uint32_t P1_M = 2 * 64 * LD * 4;
 constexpr uint32_t P1_SC = 65536;
-constexpr uint32_t P1_MISC = P1_SC + Q_NSC * 64 * 4;
-constexpr uint32_t P1_SMEM = P1_MISC + 64 + 1024;  // + room to align the base to 1024
+constexpr uint32_t P1_RG = P1_SC + Q_NSC * 64 * 4;
 static_assert(P1_M + 4 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
+__host__ __device__ constexpr uint32_t p1_misc(uint32_t group) { return P1_RG + group * 512u; }
+__host__ __device__ constexpr uint32_t p1_smem(uint32_t group) {  // + room to align the base to 1024
+  return p1_misc(group) + 64u + 1024u;
+}
 
 struct PrepArgs {
   const float *__restrict__ q;
@@ -141,11 +134,15 @@ struct P1Misc {
   int extreme;
 };
 
-// The stack [K;Q] arrives by TMA, 128-byte swizzled: column block cb (32
-// floats) holds K's 64 rows then Q's 64 rows (16 KB), so A = [K;Q] (M = 128)
-// and B = K (N = 64) of the Gram are K-major SWIZZLE_128B operands.
+// One CTA per (seq, chunk, key head).  The stack [K;Q] arrives by TMA,
+// 128-byte swizzled: column block cb (32 floats) holds K's 64 rows then Q's
+// 64 rows (16 KB), so A = [K;Q] (M = 128) and B = K (N = 64) of the Gram are
+// K-major SWIZZLE_128B operands.  K and Q are rounded and the Gram formed
+// once for the key head; the key-head images ([K; Q] stack and K^T) are
+// stored; then, for each value head that reads this key head in turn, its
+// gates turn the Gram into A and P', and T'' follows from T = (I + A)^-1.
 template <bool DECAY_AFTER>
-__global__ void __launch_bounds__(NTH, 2)
+__global__ void __launch_bounds__(NTH, 3)
     gdn_chunk_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -155,7 +152,8 @@ __global__ void __launch_bounds__(NTH, 2)
   float *sT = reinterpret_cast<float *>(smem + P1_T);
   float *sM = reinterpret_cast<float *>(smem + P1_M);
   float *sc = reinterpret_cast<float *>(smem + P1_SC);
-  P1Misc *misc = reinterpret_cast<P1Misc *>(smem + P1_MISC);
+  const float *rg = reinterpret_cast<const float *>(smem + P1_RG);
+  P1Misc *misc = reinterpret_cast<P1Misc *>(smem + p1_misc(a.group));
   const uint32_t sbase = smem_addr(smem);
   const uint32_t mbar = smem_addr(&misc->mbar), bar_ld = smem_addr(&misc->bar_ld);
   const int tid = static_cast<int>(threadIdx.x);
@@ -163,21 +161,23 @@ __global__ void __launch_bounds__(NTH, 2)
   const int row = tid & 127, half = tid >> 7;
   const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-  // block -> (seq, chunk, value head), value head fastest: the value heads
-  // that read one key head run side by side and share its K and Q in L2
-  const uint32_t vh = blockIdx.x % a.nv;
-  const uint32_t rest = blockIdx.x / a.nv;
+  // block -> (seq, chunk, key head), key head fastest
+  const uint32_t kh = blockIdx.x % a.nk;
+  const uint32_t rest = blockIdx.x / a.nk;
   const uint32_t ch = rest % a.nchunks, s = rest / a.nchunks;
-  const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
   const uint32_t t0 = ch * C;
   const int nc = static_cast<int>(min(static_cast<uint32_t>(C), a.nt - t0));
-  const size_t sc0 = (static_cast<size_t>(s) * a.nt + t0) * a.nv + vh;
-  float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
-  // one value head per key head stores the key-head images
-  const bool leader = a.khead_div ? vh % a.group == 0 : vh < a.nk;
   float *wk = a.ws_k + ((static_cast<size_t>(s) * a.nk + kh) * a.nchunks + ch) * kWsKFloats;
+  // value head j of this key head
+  auto vhead = [&](uint32_t j) { return a.khead_div ? kh * a.group + j : kh + j * a.nk; };
 
-  stage_gates_async(sbase + P1_SC, a.g, a.beta, sc0, a.nv, nc, tid);
+  // raw g and beta of every value head of the key head (tokens past the
+  // chunk's end read as zero)
+  for (uint32_t e = static_cast<uint32_t>(tid); e < a.group * 128u; e += NTH) {
+    const uint32_t j = e >> 7, w = e & 127, i = w & 63;
+    const size_t src = (static_cast<size_t>(s) * a.nt + t0 + (static_cast<int>(i) < nc ? i : 0)) * a.nv + vhead(j);
+    cp_async4(sbase + P1_RG + e * 4, (w < 64 ? a.g : a.beta) + src, static_cast<int>(i) < nc ? 4u : 0u);
+  }
   cp_async_commit();
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
@@ -205,20 +205,14 @@ __global__ void __launch_bounds__(NTH, 2)
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
 
-  // K and Q to TF32 (round to nearest) in place -- the leader also stores
-// the swizzled stack as the [K; Q] image -- and per-token scalars (warp 0)
+  // K and Q to TF32 (round to nearest) in place, stored as the [K; Q] image
 #pragma unroll
   for (int it = 0; it < 16; ++it) {
     float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
     float4 x = *p;
     x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
     *p = x;
-    if (leader) __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
-  }
-  if (warp == 0) {
-    float GC;
-    const bool extreme = chunk_scalars(sc, lane, &GC);
-    if (lane == 0) misc->extreme = extreme;
+    __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
   }
   fence_async_smem();
   cta_sync();
@@ -232,86 +226,104 @@ __global__ void __launch_bounds__(NTH, 2)
     }
     mma_commit(mbar);
   }
-  // while the Gram runs, the leader stores K^T (d_k rows x 64 tokens,
-  // canonical K-major image) from the TF32 stack
-  if (leader) {
-    for (int oc = tid; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
-      const int dk = oc & 127, i0 = (oc >> 7) * 4;
-      const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
-      float e[4];
+  // while the Gram runs, K^T (d_k rows x 64 tokens, canonical K-major image)
+  // from the TF32 stack
+  for (int oc = tid; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
+    const int dk = oc & 127, i0 = (oc >> 7) * 4;
+    const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
+    float e[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u;
-        e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
-      }
-      __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
+      e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
     }
+    __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
   }
-  const bool ok = mbar_wait(mbar, 0);
-  if (!ok) misc->failed = 1;
+  if (!mbar_wait(mbar, 0)) misc->failed = 1;
   fence_after();
-  const bool extreme = misc->extreme != 0;
+  cta_sync();  // the stack is dead: A, T and M may overlay it
 
-  // A (plain, over the dead stack) and P' (straight to the workspace)
-  {
-    uint32_t gv[32];
-    GDN_TMEM_LD32(tmem + lane_field + 32 * half, gv);
-    tmem_wait_ld();
-    __syncthreads();  // every Gram row is in registers before A overwrites the stack
-    const float *G = sc + Q_G * 64, *eG = sc + Q_EG * 64;
-    if (row < 64) {
-      const int r = row;
-      const float br = sc[Q_BETA * 64 + r];
-      const float Gr = DECAY_AFTER ? sc[Q_GPREV * 64 + r] : G[r];
-      const float bgr = br * (DECAY_AFTER ? sc[Q_GAMP * 64 + r] : sc[Q_GAM * 64 + r]);
+  for (uint32_t j = 0; j < a.group; ++j) {
+    const uint32_t vh = vhead(j);
+    float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
+    // this value head's per-token scalars (warp 0)
+    if (warp == 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float e[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 32 * half + 4 * j + u;
-          const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
-          e[u] = i < r ? gam * __uint_as_float(gv[4 * j + u]) : 0.f;
-        }
-        *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
+      for (int h = 0; h < 2; ++h) {
+        sc[Q_GRAW * 64 + lane + 32 * h] = rg[j * 128 + lane + 32 * h];
+        sc[Q_BRAW * 64 + lane + 32 * h] = rg[j * 128 + 64 + lane + 32 * h];
       }
-    } else {
-      const int r = row - 64;
-      const float Gr = G[r];
-      const float qgr = a.q_scale * sc[Q_GAM * 64 + r];
-      float *wp = ws + 4096;
+      __syncwarp();
+      float GC;
+      const bool extreme = chunk_scalars(sc, lane, &GC);
+      if (lane == 0) misc->extreme = extreme;
+    }
+    cta_sync();
+    const bool extreme = misc->extreme != 0;
+
+    // A (plain, over the dead stack) and P' (straight to the workspace), from
+    // the Gram in TMEM
+    {
+      uint32_t gv[32];
+      GDN_TMEM_LD32(tmem + lane_field + 32 * half, gv);
+      tmem_wait_ld();
+      const float *G = sc + Q_G * 64, *eG = sc + Q_EG * 64;
+      if (row < 64) {
+        const int r = row;
+        const float br = sc[Q_BETA * 64 + r];
+        const float Gr = DECAY_AFTER ? sc[Q_GPREV * 64 + r] : G[r];
+        const float bgr = br * (DECAY_AFTER ? sc[Q_GAMP * 64 + r] : sc[Q_GAM * 64 + r]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float e[4];
+        for (int jj = 0; jj < 8; ++jj) {
+          float e[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 32 * half + 4 * j + u;
-          const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-          e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+          for (int u = 0; u < 4; ++u) {
+            const int i = 32 * half + 4 * jj + u;
+            const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
+            e[u] = i < r ? gam * __uint_as_float(gv[4 * jj + u]) : 0.f;
+          }
+          *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * jj) = make_float4(e[0], e[1], e[2], e[3]);
         }
-        *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * j, 64) / 4) =
-            make_float4(e[0], e[1], e[2], e[3]);
+      } else {
+        const int r = row - 64;
+        const float Gr = G[r];
+        const float qgr = a.q_scale * sc[Q_GAM * 64 + r];
+        float *wp = ws + 4096;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 32 * half + 4 * jj + u;
+            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
+          }
+          *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) =
+              make_float4(e[0], e[1], e[2], e[3]);
+        }
       }
     }
-  }
-  cta_sync();
+    cta_sync();
 
-  // T = (I + A)^-1; T'' = T diag(beta) written as a TF32 canonical image
-  // (NaN if the Gram wait timed out)
-  tri_inverse(sA, sT, sM, tid);
-  {
-    const float nan = __int_as_float(0x7fc00000);
-    const float *bet = sc + Q_BETA * 64;
+    // T = (I + A)^-1; T'' = T diag(beta) written as a TF32 canonical image
+    // (NaN if a wait timed out)
+    tri_inverse(sA, sT, sM, tid);
+    {
+      const float nan = __int_as_float(0x7fc00000);
+      const float *bet = sc + Q_BETA * 64;
+      const bool failed = misc->failed != 0;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int ci = tid + NTH * it;
-      const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
-      float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
-      t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
-                      tf32_rn(t.w * bet[i0 + 3]));
-      if (misc->failed) t = make_float4(nan, nan, nan, nan);
-      reinterpret_cast<float4 *>(ws)[ci] = t;
+      for (int it = 0; it < 4; ++it) {
+        const int ci = tid + NTH * it;
+        const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
+        float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+        t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
+                        tf32_rn(t.w * bet[i0 + 3]));
+        if (failed) t = make_float4(nan, nan, nan, nan);
+        reinterpret_cast<float4 *>(ws)[ci] = t;
+      }
     }
+    cta_sync();  // A, T and the scalars are free for the next value head
   }
   // a load that timed out may still land: wait for it (bounded) before exit
   if (tid == 0 && !loaded) (void)mbar_wait(bar_ld, 0);
@@ -799,8 +811,10 @@ template <bool DA>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
   const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
-  const unsigned long long prep_blocks = heads * nchunks;
-  if (heads == 0 || prep_blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  const unsigned long long prep_blocks = static_cast<unsigned long long>(p.nk) * p.ns * nchunks;
+  if (heads == 0 || heads * nchunks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  const uint32_t group = p.nv / p.nk;
+  if (p1_smem(group) > 232448u) return cudaErrorInvalidConfiguration;  // raw gates of the group
   if (reinterpret_cast<uintptr_t>(p.v) % 16 != 0) return cudaErrorMisalignedAddress;  // TMA source
   CUtensorMap tm_k, tm_q, tm_v;
   cudaError_t e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -815,9 +829,9 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = p.nv / p.nk;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
   auto prep = gdn_chunk_prep_kernel<DA>;
-  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P1_SMEM));
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p1_smem(group)));
   if (e != cudaSuccess) return e;
-  prep<<<static_cast<unsigned>(prep_blocks), NTH, P1_SMEM, stream>>>(pa, tm_k, tm_q);
+  prep<<<static_cast<unsigned>(prep_blocks), NTH, p1_smem(group), stream>>>(pa, tm_k, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
