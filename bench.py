@@ -336,6 +336,11 @@ def extras(torch, nat, peak_gbs, device):
     wd = WORKLOADS["decode"]
     hbm_case("decode_bf16", wd, wd.params(), False, 4, 400, act="bf16")
     hbm_case("spec_capture_s32_bf16", wc, wc.params(), True, 4, 200, act="bf16")
+    # other head sizes, each with the decode workload's 134 MB of state per call
+    for key, dk, dv, ns in (("decode_dk64", 64, 64, 256), ("decode_dk32", 32, 32, 1024),
+                            ("decode_dk128_dv64", 128, 64, 128)):
+        wx = wd.with_(d_k=dk, d_v=dv, n_seqs=ns)
+        hbm_case(key, wx, wx.params(), False, 4, 400)
 
     # speculative-decode rollback commit: gathers one captured state per sequence
     import numpy as np

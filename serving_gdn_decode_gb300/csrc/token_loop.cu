@@ -294,19 +294,24 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
 }
 
 // ---- launch shape: several rows per warp (R = 16/NSG, 64 B of state per
-// lane) and 4 warps per CTA (8 KB of state per CTA at D_k = 128), so each SM
-// keeps tens of KB of state loads in flight across many small CTAs and the
-// fixed cost of a CTA is shared by few rows; tokens are staged 8 at a time.
-// (Measured at D_k = 128: 4 warps beat 8 by 8 % on 32 one-sequence layers per
-// launch and by 1 % on 64-sequence decode; 2 and 16 warps were slower.)
+// lane) and small CTAs (8 KB of state per CTA), so each SM keeps tens of KB
+// of state loads in flight across many CTAs and the fixed cost of a CTA is
+// shared by few rows; tokens are staged 8 at a time.  4 warps for
+// D_k >= 64; at D_k = 32 a warp already holds 16 rows, so 2 warps (32 rows:
+// one value head of D_v = 32 per CTA).  (Measured: at D_k = 128, 4 warps beat
+// 8 by 8 % on 32 one-sequence layers per launch and by 1 % on 64-sequence
+// decode; at D_k = 32, 2 warps reach 0.88 of the HBM roofline where 4 reach
+// 0.55, half their rows lying past D_v.)
 
-constexpr int kWarps = 4;
+template <int NSG>
+constexpr int kWarpsFor = NSG == 1 ? 2 : 4;
 constexpr int kTcMax = 8;
 
 template <typename IO, int NSG, bool CAPTURE, bool DA, int MAXL>
 cudaError_t launch_layers(const Problem &p, const Problem *layers, uint32_t n_layers,
                           cudaStream_t stream) {
   constexpr int R = 16 / NSG;
+  constexpr int kWarps = kWarpsFor<NSG>;
   constexpr int ROWS = kWarps * R;
   constexpr int DK = 32 * NSG;
   LoopArgs a;
