@@ -277,9 +277,10 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
  *
  * Arguments, layouts and checks as gdn_forward (f32 activations), for the
  * chunked path: the params path bits must be GDN_PATH_AUTO or
- * GDN_PATH_CHUNKED, and the chunked path's shape rules apply (D_k = D_v =
- * 128, else GDN_ERR_UNSUPPORTED).  Results equal gdn_forward_ws's on the
- * chunked path.
+ * GDN_PATH_CHUNKED, the chunked path's shape rules apply (D_k = D_v = 128,
+ * else GDN_ERR_UNSUPPORTED), and v must be 16-byte aligned as for
+ * gdn_forward_ws (INVALID_ARGUMENT otherwise).  Results equal
+ * gdn_forward_ws's on the chunked path.
  *
  * The first call on a device looks up the device address of the scratch
  * (once per device, with that device current); make that first call before
