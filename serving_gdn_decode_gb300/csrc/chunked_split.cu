@@ -100,19 +100,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 // ================================================================ pass 1
 
 // shared memory (bytes): the [K;Q] stack for the Gram, then, once the Gram
-// is in TMEM, A, T and the block products overlaid on it; the per-token
-// scalars of the value head in hand; the raw g and beta of every value head
-// of the key head (group x 128 floats); the barriers.
+// is in TMEM, A, T and the block products overlaid on it; one set of
+// per-token scalars per value head of the key head (group x Q_NSC slots);
+// the raw g and beta of those heads (group x 128 floats); the barriers and
+// one "extreme gates" flag per head.
 constexpr uint32_t P1_STACK = 0;
 constexpr uint32_t P1_A = 0;
 constexpr uint32_t P1_T = 64 * LD * 4;
 constexpr uint32_t P1_M = 2 * 64 * LD * 4;
 constexpr uint32_t P1_SC = 65536;
-constexpr uint32_t P1_RG = P1_SC + Q_NSC * 64 * 4;
+constexpr uint32_t kScSet = Q_NSC * 64;  // floats of one head's scalar set
 static_assert(P1_M + 4 * 256 * 4 <= P1_SC, "pass-1 overlay must fit in the stack");
-__host__ __device__ constexpr uint32_t p1_misc(uint32_t group) { return P1_RG + group * 512u; }
+__host__ __device__ constexpr uint32_t p1_rg(uint32_t group) { return P1_SC + group * kScSet * 4u; }
+__host__ __device__ constexpr uint32_t p1_misc(uint32_t group) { return p1_rg(group) + group * 512u; }
 __host__ __device__ constexpr uint32_t p1_smem(uint32_t group) {  // + room to align the base to 1024
-  return p1_misc(group) + 64u + 1024u;
+  return p1_misc(group) + 32u + 4u * group + 1024u;
 }
 
 struct PrepArgs {
@@ -131,8 +133,8 @@ struct P1Misc {
   unsigned long long bar_ld;  // TMA: the chunk's K and Q rows
   uint32_t tmem_base;
   int failed;
-  int extreme;
 };
+static_assert(sizeof(P1Misc) <= 32, "pass-1 misc area");  // then one int per value head: extreme gates
 
 // One CTA per (seq, chunk, key head).  The stack [K;Q] arrives by TMA,
 // 128-byte swizzled: column block cb (32 floats) holds K's 64 rows then Q's
@@ -152,8 +154,9 @@ __global__ void __launch_bounds__(NTH, 3)
   float *sT = reinterpret_cast<float *>(smem + P1_T);
   float *sM = reinterpret_cast<float *>(smem + P1_M);
   float *sc = reinterpret_cast<float *>(smem + P1_SC);
-  const float *rg = reinterpret_cast<const float *>(smem + P1_RG);
+  const float *rg = reinterpret_cast<const float *>(smem + p1_rg(a.group));
   P1Misc *misc = reinterpret_cast<P1Misc *>(smem + p1_misc(a.group));
+  int *extreme_of = reinterpret_cast<int *>(smem + p1_misc(a.group) + 32);  // [group]
   const uint32_t sbase = smem_addr(smem);
   const uint32_t mbar = smem_addr(&misc->mbar), bar_ld = smem_addr(&misc->bar_ld);
   const int tid = static_cast<int>(threadIdx.x);
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(NTH, 3)
   for (uint32_t e = static_cast<uint32_t>(tid); e < a.group * 128u; e += NTH) {
     const uint32_t j = e >> 7, w = e & 127, i = w & 63;
     const size_t src = (static_cast<size_t>(s) * a.nt + t0 + (static_cast<int>(i) < nc ? i : 0)) * a.nv + vhead(j);
-    cp_async4(sbase + P1_RG + e * 4, (w < 64 ? a.g : a.beta) + src, static_cast<int>(i) < nc ? 4u : 0u);
+    cp_async4(sbase + p1_rg(a.group) + e * 4, (w < 64 ? a.g : a.beta) + src, static_cast<int>(i) < nc ? 4u : 0u);
   }
   cp_async_commit();
   if (tid == 0) {
@@ -239,91 +242,95 @@ __global__ void __launch_bounds__(NTH, 3)
     }
     __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
   }
+  // and every value head's per-token scalars, one warp per head
+  for (uint32_t j = static_cast<uint32_t>(warp); j < a.group; j += NTH / 32) {
+    float *scj = sc + j * kScSet;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      scj[Q_GRAW * 64 + lane + 32 * h] = rg[j * 128 + lane + 32 * h];
+      scj[Q_BRAW * 64 + lane + 32 * h] = rg[j * 128 + 64 + lane + 32 * h];
+    }
+    __syncwarp();
+    float GC;
+    const bool ex = chunk_scalars(scj, lane, &GC);
+    if (lane == 0) extreme_of[j] = ex;
+  }
   if (!mbar_wait(mbar, 0)) misc->failed = 1;
   fence_after();
   cta_sync();  // the stack is dead: A, T and M may overlay it
 
+  // A (plain, over the dead stack) and P' (straight to the workspace) of
+  // value head j, from the Gram in TMEM and that head's gates
+  auto epilogue = [&](uint32_t j) {
+    const float *scj = sc + j * kScSet;
+    const bool extreme = extreme_of[j] != 0;
+    float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vhead(j)) * a.nchunks + ch) * kWsFloats;
+    uint32_t gv[32];
+    GDN_TMEM_LD32(tmem + lane_field + 32 * half, gv);
+    tmem_wait_ld();
+    const float *G = scj + Q_G * 64, *eG = scj + Q_EG * 64;
+    if (row < 64) {
+      const int r = row;
+      const float br = scj[Q_BETA * 64 + r];
+      const float Gr = DECAY_AFTER ? scj[Q_GPREV * 64 + r] : G[r];
+      const float bgr = br * (DECAY_AFTER ? scj[Q_GAMP * 64 + r] : scj[Q_GAM * 64 + r]);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 32 * half + 4 * jj + u;
+          const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
+          e[u] = i < r ? gam * __uint_as_float(gv[4 * jj + u]) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * jj) = make_float4(e[0], e[1], e[2], e[3]);
+      }
+    } else {
+      const int r = row - 64;
+      const float Gr = G[r];
+      const float qgr = a.q_scale * scj[Q_GAM * 64 + r];
+      float *wp = ws + 4096;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = 32 * half + 4 * jj + u;
+          const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+          e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) = make_float4(e[0], e[1], e[2], e[3]);
+      }
+    }
+  };
+  // T'' = T diag(beta) of value head j as a TF32 canonical image (NaN if a
+  // wait timed out)
+  auto store_tpp = [&](uint32_t j) {
+    const float nan = __int_as_float(0x7fc00000);
+    const float *bet = sc + j * kScSet + Q_BETA * 64;
+    const bool failed = misc->failed != 0;
+    float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vhead(j)) * a.nchunks + ch) * kWsFloats;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int ci = tid + NTH * it;
+      const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
+      float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+      t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
+                      tf32_rn(t.w * bet[i0 + 3]));
+      if (failed) t = make_float4(nan, nan, nan, nan);
+      reinterpret_cast<float4 *>(ws)[ci] = t;
+    }
+  };
+
+  // per value head: T = (I + A)^-1, then its T'' is stored while the next
+  // head's A and P' are formed (different buffers)
+  epilogue(0);
+  cta_sync();
   for (uint32_t j = 0; j < a.group; ++j) {
-    const uint32_t vh = vhead(j);
-    float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vh) * a.nchunks + ch) * kWsFloats;
-    // this value head's per-token scalars (warp 0)
-    if (warp == 0) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        sc[Q_GRAW * 64 + lane + 32 * h] = rg[j * 128 + lane + 32 * h];
-        sc[Q_BRAW * 64 + lane + 32 * h] = rg[j * 128 + 64 + lane + 32 * h];
-      }
-      __syncwarp();
-      float GC;
-      const bool extreme = chunk_scalars(sc, lane, &GC);
-      if (lane == 0) misc->extreme = extreme;
-    }
+    tri_inverse(sA, sT, sM, tid);  // ends with a barrier: A is consumed
+    store_tpp(j);
+    if (j + 1 < a.group) epilogue(j + 1);
     cta_sync();
-    const bool extreme = misc->extreme != 0;
-
-    // A (plain, over the dead stack) and P' (straight to the workspace), from
-    // the Gram in TMEM
-    {
-      uint32_t gv[32];
-      GDN_TMEM_LD32(tmem + lane_field + 32 * half, gv);
-      tmem_wait_ld();
-      const float *G = sc + Q_G * 64, *eG = sc + Q_EG * 64;
-      if (row < 64) {
-        const int r = row;
-        const float br = sc[Q_BETA * 64 + r];
-        const float Gr = DECAY_AFTER ? sc[Q_GPREV * 64 + r] : G[r];
-        const float bgr = br * (DECAY_AFTER ? sc[Q_GAMP * 64 + r] : sc[Q_GAM * 64 + r]);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          float e[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = 32 * half + 4 * jj + u;
-            const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
-            e[u] = i < r ? gam * __uint_as_float(gv[4 * jj + u]) : 0.f;
-          }
-          *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * jj) = make_float4(e[0], e[1], e[2], e[3]);
-        }
-      } else {
-        const int r = row - 64;
-        const float Gr = G[r];
-        const float qgr = a.q_scale * sc[Q_GAM * 64 + r];
-        float *wp = ws + 4096;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          float e[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = 32 * half + 4 * jj + u;
-            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
-          }
-          *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) =
-              make_float4(e[0], e[1], e[2], e[3]);
-        }
-      }
-    }
-    cta_sync();
-
-    // T = (I + A)^-1; T'' = T diag(beta) written as a TF32 canonical image
-    // (NaN if a wait timed out)
-    tri_inverse(sA, sT, sM, tid);
-    {
-      const float nan = __int_as_float(0x7fc00000);
-      const float *bet = sc + Q_BETA * 64;
-      const bool failed = misc->failed != 0;
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int ci = tid + NTH * it;
-        const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
-        float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
-        t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
-                        tf32_rn(t.w * bet[i0 + 3]));
-        if (failed) t = make_float4(nan, nan, nan, nan);
-        reinterpret_cast<float4 *>(ws)[ci] = t;
-      }
-    }
-    cta_sync();  // A, T and the scalars are free for the next value head
   }
   // a load that timed out may still land: wait for it (bounded) before exit
   if (tid == 0 && !loaded) (void)mbar_wait(bar_ld, 0);
