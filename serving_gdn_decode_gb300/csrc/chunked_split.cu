@@ -2,15 +2,16 @@
 // recurrence on sm_103a, D_k = D_v = 128: the same chunk equations as the
 // single-pass kernel (chunked.cu), split at the state.
 //
-// Pass 1, one CTA per (seq, chunk, value head), computes everything that
-// does not depend on the state and writes it to a caller-provided
-// workspace: the Gram products K K^T and Q K^T, A, T = (I + A)^-1, and from
-// them T'' = T diag(beta) and P' = q_scale (Q K^T o Gam)_{i<=r}, as TF32
-// canonical images.  The first value head of each key head also stores the
-// TF32-rounded [K; Q] rows in the 128-byte-swizzled layout the MMA reads
-// (exactly its own shared-memory stack) and K^T as a canonical image: the
-// state pass then loads every operand ready-made and rounds nothing but its
-// own TMEM products.
+// Pass 1, one CTA per (seq, chunk, key head), computes everything that does
+// not depend on the state and writes it to a caller-provided workspace.  It
+// rounds the key head's K and Q to TF32 once and stores them in the
+// 128-byte-swizzled layout the MMA reads (exactly its shared-memory stack),
+// stores K^T as a canonical image, and forms the Gram products K K^T and
+// Q K^T once; then, for each value head that reads the key head, that head's
+// gates give A, T = (I + A)^-1, T'' = T diag(beta) and
+// P' = q_scale (Q K^T o Gam)_{i<=r}, stored as TF32 canonical images.  The
+// state pass loads every operand ready-made and rounds nothing but its own
+// TMEM products.
 //
 // Pass 2, one CTA per (seq, value head), runs the state-dependent chain per
 // chunk with the state in TMEM as S = c * S~ (c a lazy scalar): [X | Z] =
