@@ -225,9 +225,10 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  * The chunked (WY / UT) form of the recurrence over 64-token chunks splits
  * into a part that does not depend on the state -- per chunk, the Gram
  * products, A, T = (I + A)^-1 and the masked decay-weighted Q K^T -- and the
- * state pass.  gdn_forward_ws runs the first part for every (seq, value
- * head, chunk) in parallel, writes it to `workspace`, then runs the state
- * pass (one CTA per (seq, value head)).  The pages have no chunked kernel:
+ * state pass.  gdn_forward_ws runs the first part for every (seq, chunk) in
+ * parallel -- the products of K and Q once per key head, the gated parts per
+ * value head -- writes it to `workspace`, then runs the state pass (one CTA
+ * per (seq, value head)).  The pages have no chunked kernel:
  * the chunk equations are the delta rule's published chunkwise form derived
  * from the recurrence of gated_delta_net.rs (mlx-native 0.4.0) and of the
  * capture kernel page, with the same TF32 operands as GDN_PATH_CHUNKED.
