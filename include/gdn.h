@@ -103,7 +103,8 @@ typedef enum gdn_status {
  *     not 16-byte aligned, or v, g, beta, output not 4-byte aligned;
  *     state_in and state_out overlapping without being the same pointer
  *     (state_in == state_out, an in-place update, is allowed); output
- *     overlapping any other buffer.
+ *     overlapping any other buffer; on the chunked path, v not 16-byte
+ *     aligned (its rows are copied 16 bytes at a time).
  *   UNSUPPORTED: D_k = 96 (D_k/32 = 3 has no kernel, as on the pages);
  *     the chunked path forced for a shape it does not cover.
  * Buffer sizes cannot be checked through raw pointers: each buffer must hold
@@ -237,7 +238,9 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *   `params` -- on the chunked path, per (seq, 64-token chunk), 32 KB per
  *   value head plus 96 KB per key head (the rounded K and Q rows and K^T,
  *   shared by the value heads that read the key head); 0 on every other
- *   path.  Same params checks and status as gdn_path_name.
+ *   path, and 0 when a key head has more than 32 value heads (the two-pass
+ *   form takes at most 32; gdn_forward_ws then runs the one-pass chunked
+ *   form of gdn_forward).  Same params checks and status as gdn_path_name.
  *
  * gdn_forward_ws: gdn_forward, plus `workspace` (DEVICE, caller-owned,
  *   at least gdn_workspace_size bytes, 16-byte aligned, overlapping no other
@@ -246,9 +249,7 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *   path (params[6] path bits = GDN_PATH_CHUNKED) the two-pass form runs;
  *   the other paths run exactly as in gdn_forward and do not touch the
  *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
- *   short or overlapping workspace when the size is > 0, and, on the chunked
- *   path, for v not 16-byte aligned (the state pass reads V rows with the
- *   tensor memory accelerator).
+ *   short or overlapping workspace when the size is > 0.
  */
 gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes);
 
@@ -281,7 +282,9 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
  * GDN_PATH_CHUNKED, the chunked path's shape rules apply (D_k = D_v = 128,
  * else GDN_ERR_UNSUPPORTED), and v must be 16-byte aligned as for
  * gdn_forward_ws (INVALID_ARGUMENT otherwise).  Results equal
- * gdn_forward_ws's on the chunked path.
+ * gdn_forward_ws's on the chunked path.  With more than 32 value heads per
+ * key head it runs the one-pass chunked form of gdn_forward, which needs no
+ * scratch (as gdn_forward_ws does).
  *
  * The first call on a device looks up the device address of the scratch
  * (once per device, with that device current); make that first call before

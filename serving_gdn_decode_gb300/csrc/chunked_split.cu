@@ -858,6 +858,10 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 
 }  // namespace
 
+bool chunked_split_supported(const Problem &p) {
+  return chunked_supported(p) && p.nk > 0 && p.nv / p.nk <= kMaxSplitGroup;
+}
+
 size_t chunked_split_workspace_bytes(const Problem &p) {
   const size_t nchunks = (static_cast<size_t>(p.nt) + C - 1) / C;
   return (static_cast<size_t>(p.nv) * kWsFloats + static_cast<size_t>(p.nk) * kWsKFloats) * p.ns * nchunks *
@@ -865,7 +869,7 @@ size_t chunked_split_workspace_bytes(const Problem &p) {
 }
 
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {
-  if (!chunked_supported(p)) return cudaErrorInvalidValue;
+  if (!chunked_split_supported(p)) return cudaErrorInvalidValue;
   return p.decay_after ? launch_split<true>(p, workspace, stream) : launch_split<false>(p, workspace, stream);
 }
 
@@ -886,7 +890,7 @@ float *g_noalloc_addr[kMaxDevices] = {};  // device address of g_noalloc_ws, per
 }  // namespace
 
 cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream) {
-  if (!chunked_supported(p) || chunked_split_workspace_bytes(p) > kNoallocWorkspaceBytes)
+  if (!chunked_split_supported(p) || chunked_split_workspace_bytes(p) > kNoallocWorkspaceBytes)
     return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -236,8 +236,11 @@ void fill_problem(gdn::Problem &p, const Buffers &b, bool bf16) {
 }
 
 // Workspace bytes of a decoded, path-checked problem (two-pass chunked only).
+// The two-pass form's workspace; 0 (the one-pass form runs) off the chunked
+// path and for more than kMaxSplitGroup value heads per key head.
 size_t workspace_bytes_of(const Decoded &d, Path path) {
-  return path == Path::kChunked ? gdn::chunked_split_workspace_bytes(d.prob) : 0;
+  return path == Path::kChunked && gdn::chunked_split_supported(d.prob) ? gdn::chunked_split_workspace_bytes(d.prob)
+                                                                         : 0;
 }
 
 // with_ws: the caller passed a workspace argument (gdn_forward_ws); the
@@ -254,6 +257,9 @@ gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t
   Path path;
   st = choose_path(d, with_capture, bf16, &path);
   if (st != GDN_OK) return st;
+  if (path == Path::kChunked && !aligned(b.v, 16))
+    return fail(GDN_ERR_INVALID_ARGUMENT,
+                "gdn: the chunked path needs v 16-byte aligned (its rows are copied 16 bytes at a time)");
   const size_t ws_need = with_ws ? workspace_bytes_of(d, path) : 0;
   if (ws_need > 0) {
     if (workspace == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace is NULL");
@@ -262,9 +268,6 @@ gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t
     if (workspace_bytes < ws_need)
       return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: workspace has %zu bytes, %zu needed",
                   workspace_bytes, ws_need);
-    if (!aligned(b.v, 16))
-      return fail(GDN_ERR_INVALID_ARGUMENT,
-                  "gdn: the two-pass chunked path needs v 16-byte aligned (it is read by TMA)");
     const Spans sp = spans_of(d, b, bf16);
     const Span w{workspace, ws_need, "workspace"};
     const Span all[8] = {sp.in[0], sp.in[1], sp.in[2], sp.in[3], sp.in[4], sp.in[5], sp.output,
@@ -311,6 +314,10 @@ gdn_status run_layers(const L *layers, size_t n_layers, const uint32_t *params, 
       std::snprintf(msg, sizeof msg, "%s", g_last_error);
       return fail(st, "%s (layer %zu)", msg, i);
     }
+    if (path == Path::kChunked && !aligned(layers[i].v, 16))
+      return fail(GDN_ERR_INVALID_ARGUMENT,
+                  "gdn: the chunked path needs v 16-byte aligned (its rows are copied 16 bytes at a time) "
+                  "(layer %zu)", i);
   }
   // No layer may write where another layer reads or writes.
   for (size_t i = 0; i < n_layers; ++i) {
@@ -399,7 +406,15 @@ gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const flo
   if (st != GDN_OK) return st;
   if (!aligned(v, 16))
     return fail(GDN_ERR_INVALID_ARGUMENT,
-                "gdn: the two-pass chunked path needs v 16-byte aligned (it is read by TMA)");
+                "gdn: the chunked path needs v 16-byte aligned (its rows are copied 16 bytes at a time)");
+  gdn::Problem &p = d.prob;
+  if (!gdn::chunked_split_supported(p)) {  // more value heads per key head than the two-pass form takes
+    fill_problem(p, b, false);
+    const cudaError_t err = gdn::launch_chunked(p, reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess)
+      return fail(GDN_ERR_CUDA, "gdn: kernel launch failed: %s", cudaGetErrorString(err));
+    return GDN_OK;
+  }
   const size_t need = gdn::chunked_split_workspace_bytes(d.prob);
   if (need > gdn::kNoallocWorkspaceBytes)
     return fail(GDN_ERR_INVALID_ARGUMENT,
@@ -408,7 +423,6 @@ gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const flo
                 "takes 32 KB per value head and 96 KB per key head): use gdn_forward_ws with "
                 "your own workspace",
                 need, gdn::kNoallocWorkspaceBytes);
-  gdn::Problem &p = d.prob;
   fill_problem(p, b, false);
   const cudaError_t err = gdn::launch_chunked_split_noalloc(p, reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess)

@@ -42,9 +42,13 @@ bool chunked_supported(const Problem &p);
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 
 // The same chunk equations in two passes (chunked_split.cu): a parallel pass
-// over every (seq, value head, chunk) writes the state-independent chunk
+// over every (seq, chunk, key head) writes the state-independent chunk
 // matrices to `workspace` (device, chunked_split_workspace_bytes(p) bytes,
 // 16-byte aligned), then one CTA per (seq, value head) runs the state pass.
+// The chunk pass holds the gate scalars of all value heads of a key head in
+// shared memory, so the form takes at most kMaxSplitGroup of them.
+constexpr uint32_t kMaxSplitGroup = 32;
+bool chunked_split_supported(const Problem &p);  // chunked_supported and n_v / n_k <= kMaxSplitGroup
 size_t chunked_split_workspace_bytes(const Problem &p);
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream);
 

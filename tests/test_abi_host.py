@@ -15,7 +15,7 @@ import pytest
 
 from serving_gdn_decode_gb300 import _native as nat
 from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN, pack_params
-from serving_gdn_decode_gb300.workloads import WORKLOADS
+from serving_gdn_decode_gb300.workloads import WORKLOADS, Workload
 
 
 @pytest.fixture(scope="module")
@@ -439,3 +439,32 @@ def test_two_pass_needs_aligned_v(L):
     assert "16-byte" in nat.gdn_last_error()
     assert nat.forward_chunked_noalloc_raw(*args, w.with_(n_tokens=64).params(path=PATH_CHUNKED)) == \
         nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
+def test_chunked_path_needs_aligned_v(L):
+    # the chunked path copies v rows 16 bytes at a time (one-pass form, two-pass
+    # form and layer table alike); the other paths take a 4-byte-aligned v
+    w = Workload("cv", 128, 128, 2, 4, 100, 1)
+    f = Fake(w)
+    v4 = f.addr["v"] + 4
+    assert f.call(params=w.params(path=PATH_CHUNKED), v=v4) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "16-byte" in nat.gdn_last_error()
+    assert f.call(params=w.params(path=PATH_SCAN), v=v4) == nat.GDN_ERR_CUDA  # host checks pass
+    rows = _layer_rows(2)
+    rows[1][2] += 4
+    assert nat.forward_layers_raw(rows, w.params(path=PATH_CHUNKED)) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "layer 1" in nat.gdn_last_error() and "16-byte" in nat.gdn_last_error()
+
+
+@no_device
+def test_two_pass_group_limit(L):
+    # more than 32 value heads per key head: no workspace, the one-pass form runs
+    w40 = Workload("g40", 128, 128, 1, 40, 100, 1)
+    assert nat.gdn_workspace_size(w40.params(path=PATH_CHUNKED)) == 0
+    w32 = Workload("g32", 128, 128, 1, 32, 100, 1)
+    assert nat.gdn_workspace_size(w32.params(path=PATH_CHUNKED)) == 2 * (32 * 32768 + 98304)
+    f = Fake(w40)
+    args = [f.addr[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+    # a NULL workspace is then fine (host checks pass; the launch fails here for want of a device)
+    assert nat.forward_ws_raw(*args, w40.params(path=PATH_CHUNKED), 0, 0) == nat.GDN_ERR_CUDA

@@ -143,6 +143,23 @@ def test_two_pass_chaining_and_workspace_reuse(torch):
         np.testing.assert_array_equal(s2.cpu().numpy(), st)
 
 
+def test_two_pass_group_limit_runs_one_pass(torch, oracle_mod):
+    """More than 32 value heads per key head: gdn_forward_ws needs no
+    workspace and gives the one-pass form's results exactly."""
+    from serving_gdn_decode_gb300 import _native as nat
+    w = Workload("g40", 128, 128, 1, 40, 70, 1)
+    x = make_inputs(w, 63)
+    p = w.params(path=PATH_CHUNKED)
+    assert nat.gdn_workspace_size(p) == 0
+    out1, st1, _ = run_gpu(w, x, p)
+    out2, st2, _ = run_gpu(w, x, p, workspace=True)
+    np.testing.assert_array_equal(out2, out1)
+    np.testing.assert_array_equal(st2, st1)
+    ro, rs, _ = oracle_mod.forward(p, **x)
+    assert_close("output", out2, ro, w.n_tokens)
+    assert_close("state_out", st2, rs, w.n_tokens)
+
+
 def test_two_pass_workspace_size(torch):
     from serving_gdn_decode_gb300 import _native as nat
     w = WORKLOADS["long_prefill"]

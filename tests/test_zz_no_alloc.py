@@ -70,3 +70,15 @@ def test_noalloc_refuses_more_than_its_scratch(torch):
                                          w.params(path=PATH_CHUNKED))
     assert rc == nat.GDN_ERR_INVALID_ARGUMENT
     assert "gdn_forward_ws" in nat.gdn_last_error()
+
+
+def test_noalloc_beyond_the_two_pass_group_limit(torch):
+    # 40 value heads on one key head: the entry point runs the one-pass form,
+    # which needs no scratch, and matches gdn_forward exactly
+    w = Workload("noalloc_g40", 128, 128, 1, 40, 70, 1)
+    x = make_inputs(w, 74)
+    p = w.params(path=PATH_CHUNKED)
+    out, st = _noalloc(torch, w, x, p)
+    ref_out, ref_st, _ = run_gpu(w, x, p)
+    np.testing.assert_array_equal(out, ref_out)
+    np.testing.assert_array_equal(st, ref_st)
