@@ -126,6 +126,7 @@ struct PrepArgs {
   float *__restrict__ ws;    // per (head, chunk) images
   float *__restrict__ ws_k;  // per (seq, key head, chunk) images
   uint32_t nk, nv, nt, group, khead_div, nchunks;
+  uint32_t hpc, parts;       // value heads per CTA; CTAs per (seq, chunk, key head)
   float q_scale;
 };
 
@@ -137,7 +138,8 @@ struct P1Misc {
 };
 static_assert(sizeof(P1Misc) <= 32, "pass-1 misc area");  // then one int per value head: extreme gates
 
-// One CTA per (seq, chunk, key head).  The stack [K;Q] arrives by TMA,
+// One CTA per (seq, chunk, key head) -- or per part of its value heads when
+// there are fewer of those than SMs.  The stack [K;Q] arrives by TMA,
 // 128-byte swizzled: column block cb (32 floats) holds K's 64 rows then Q's
 // 64 rows (16 KB), so A = [K;Q] (M = 128) and B = K (N = 64) of the Gram are
 // K-major SWIZZLE_128B operands.  K and Q are rounded and the Gram formed
@@ -155,9 +157,9 @@ __global__ void __launch_bounds__(NTH, 3)
   float *sT = reinterpret_cast<float *>(smem + P1_T);
   float *sM = reinterpret_cast<float *>(smem + P1_M);
   float *sc = reinterpret_cast<float *>(smem + P1_SC);
-  const float *rg = reinterpret_cast<const float *>(smem + p1_rg(a.group));
-  P1Misc *misc = reinterpret_cast<P1Misc *>(smem + p1_misc(a.group));
-  int *extreme_of = reinterpret_cast<int *>(smem + p1_misc(a.group) + 32);  // [group]
+  const float *rg = reinterpret_cast<const float *>(smem + p1_rg(a.hpc));
+  P1Misc *misc = reinterpret_cast<P1Misc *>(smem + p1_misc(a.hpc));
+  int *extreme_of = reinterpret_cast<int *>(smem + p1_misc(a.hpc) + 32);  // [hpc]
   const uint32_t sbase = smem_addr(smem);
   const uint32_t mbar = smem_addr(&misc->mbar), bar_ld = smem_addr(&misc->bar_ld);
   const int tid = static_cast<int>(threadIdx.x);
@@ -165,22 +167,29 @@ __global__ void __launch_bounds__(NTH, 3)
   const int row = tid & 127, half = tid >> 7;
   const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-  // block -> (seq, chunk, key head), key head fastest
-  const uint32_t kh = blockIdx.x % a.nk;
-  const uint32_t rest = blockIdx.x / a.nk;
+  // block -> (seq, chunk, key head, part), part fastest; this CTA takes the
+  // key head's value heads j0 .. j0 + nh - 1
+  const uint32_t part = blockIdx.x % a.parts;
+  const uint32_t kh = (blockIdx.x / a.parts) % a.nk;
+  const uint32_t rest = blockIdx.x / a.parts / a.nk;
   const uint32_t ch = rest % a.nchunks, s = rest / a.nchunks;
+  const uint32_t j0 = part * a.hpc, nh = min(a.hpc, a.group - j0);
+  const bool store_k = part == 0;  // the first part stores the key-head images
   const uint32_t t0 = ch * C;
   const int nc = static_cast<int>(min(static_cast<uint32_t>(C), a.nt - t0));
   float *wk = a.ws_k + ((static_cast<size_t>(s) * a.nk + kh) * a.nchunks + ch) * kWsKFloats;
-  // value head j of this key head
-  auto vhead = [&](uint32_t j) { return a.khead_div ? kh * a.group + j : kh + j * a.nk; };
+  // value head jl of this CTA (j0 + jl of the key head)
+  auto vhead = [&](uint32_t jl) {
+    const uint32_t j = j0 + jl;
+    return a.khead_div ? kh * a.group + j : kh + j * a.nk;
+  };
 
-  // raw g and beta of every value head of the key head (tokens past the
-  // chunk's end read as zero)
-  for (uint32_t e = static_cast<uint32_t>(tid); e < a.group * 128u; e += NTH) {
-    const uint32_t j = e >> 7, w = e & 127, i = w & 63;
-    const size_t src = (static_cast<size_t>(s) * a.nt + t0 + (static_cast<int>(i) < nc ? i : 0)) * a.nv + vhead(j);
-    cp_async4(sbase + p1_rg(a.group) + e * 4, (w < 64 ? a.g : a.beta) + src, static_cast<int>(i) < nc ? 4u : 0u);
+  // raw g and beta of this CTA's value heads (tokens past the chunk's end
+  // read as zero)
+  for (uint32_t e = static_cast<uint32_t>(tid); e < nh * 128u; e += NTH) {
+    const uint32_t jl = e >> 7, w = e & 127, i = w & 63;
+    const size_t src = (static_cast<size_t>(s) * a.nt + t0 + (static_cast<int>(i) < nc ? i : 0)) * a.nv + vhead(jl);
+    cp_async4(sbase + p1_rg(a.hpc) + e * 4, (w < 64 ? a.g : a.beta) + src, static_cast<int>(i) < nc ? 4u : 0u);
   }
   cp_async_commit();
   if (tid == 0) {
@@ -210,13 +219,14 @@ __global__ void __launch_bounds__(NTH, 3)
   const uint32_t tmem = misc->tmem_base;
 
   // K and Q to TF32 (round to nearest) in place, stored as the [K; Q] image
+  // (by the first part)
 #pragma unroll
   for (int it = 0; it < 16; ++it) {
     float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
     float4 x = *p;
     x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
     *p = x;
-    __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
+    if (store_k) __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
   }
   fence_async_smem();
   cta_sync();
@@ -231,8 +241,8 @@ __global__ void __launch_bounds__(NTH, 3)
     mma_commit(mbar);
   }
   // while the Gram runs, K^T (d_k rows x 64 tokens, canonical K-major image)
-  // from the TF32 stack
-  for (int oc = tid; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
+  // from the TF32 stack (by the first part)
+  for (int oc = store_k ? tid : 2048; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
     const int dk = oc & 127, i0 = (oc >> 7) * 4;
     const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
     float e[4];
@@ -244,17 +254,17 @@ __global__ void __launch_bounds__(NTH, 3)
     __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
   }
   // and every value head's per-token scalars, one warp per head
-  for (uint32_t j = static_cast<uint32_t>(warp); j < a.group; j += NTH / 32) {
-    float *scj = sc + j * kScSet;
+  for (uint32_t jl = static_cast<uint32_t>(warp); jl < nh; jl += NTH / 32) {
+    float *scj = sc + jl * kScSet;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      scj[Q_GRAW * 64 + lane + 32 * h] = rg[j * 128 + lane + 32 * h];
-      scj[Q_BRAW * 64 + lane + 32 * h] = rg[j * 128 + 64 + lane + 32 * h];
+      scj[Q_GRAW * 64 + lane + 32 * h] = rg[jl * 128 + lane + 32 * h];
+      scj[Q_BRAW * 64 + lane + 32 * h] = rg[jl * 128 + 64 + lane + 32 * h];
     }
     __syncwarp();
     float GC;
     const bool ex = chunk_scalars(scj, lane, &GC);
-    if (lane == 0) extreme_of[j] = ex;
+    if (lane == 0) extreme_of[jl] = ex;
   }
   if (!mbar_wait(mbar, 0)) misc->failed = 1;
   fence_after();
@@ -327,10 +337,10 @@ __global__ void __launch_bounds__(NTH, 3)
   // head's A and P' are formed (different buffers)
   epilogue(0);
   cta_sync();
-  for (uint32_t j = 0; j < a.group; ++j) {
+  for (uint32_t jl = 0; jl < nh; ++jl) {
     tri_inverse(sA, sT, sM, tid);  // ends with a barrier: A is consumed
-    store_tpp(j);
-    if (j + 1 < a.group) epilogue(j + 1);
+    store_tpp(jl);
+    if (jl + 1 < nh) epilogue(jl + 1);
     cta_sync();
   }
   // a load that timed out may still land: wait for it (bounded) before exit
@@ -819,13 +829,28 @@ template <bool DA>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
   const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
-  const unsigned long long prep_blocks = static_cast<unsigned long long>(p.nk) * p.ns * nchunks;
   if (heads == 0 || heads * nchunks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   const uint32_t group = p.nv / p.nk;
-  if (p1_smem(group) > 232448u) return cudaErrorInvalidConfiguration;  // raw gates of the group
+  // one CTA per (seq, chunk, key head) takes all its value heads, unless
+  // there are fewer of those than SMs: then the value heads are split into
+  // parts, one CTA each (measured: one sequence of 256 tokens 43.3 -> 38.8
+  // us; splitting already at 1024 tokens cost more in repeated K, Q and Gram
+  // work than it gained)
+  const unsigned long long tasks = static_cast<unsigned long long>(p.nk) * p.ns * nchunks;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long want = static_cast<unsigned long long>(sms > 0 ? sms : 1);
+  uint32_t parts = tasks >= want ? 1u : static_cast<uint32_t>(min(static_cast<unsigned long long>(group),
+                                                                   (want + tasks - 1) / tasks));
+  const uint32_t hpc = (group + parts - 1) / parts;
+  parts = (group + hpc - 1) / hpc;
+  const unsigned long long prep_blocks = tasks * parts;
+  if (p1_smem(hpc) > 232448u) return cudaErrorInvalidConfiguration;  // raw gates of the heads in a CTA
   if (reinterpret_cast<uintptr_t>(p.v) % 16 != 0) return cudaErrorMisalignedAddress;  // TMA source
   CUtensorMap tm_k, tm_q, tm_v;
-  cudaError_t e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess) e = rows_map(&tm_q, p.q, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e == cudaSuccess) e = rows_map(&tm_v, p.v, p.nv, p.nt, p.ns, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
@@ -834,12 +859,12 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   PrepArgs pa;
   pa.q = static_cast<const float *>(p.q); pa.k = static_cast<const float *>(p.k);
   pa.g = p.g; pa.beta = p.beta; pa.ws = ws; pa.ws_k = ws_k;
-  pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = p.nv / p.nk;
+  pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = group; pa.hpc = hpc; pa.parts = parts;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
   auto prep = gdn_chunk_prep_kernel<DA>;
-  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p1_smem(group)));
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p1_smem(hpc)));
   if (e != cudaSuccess) return e;
-  prep<<<static_cast<unsigned>(prep_blocks), NTH, p1_smem(group), stream>>>(pa, tm_k, tm_q);
+  prep<<<static_cast<unsigned>(prep_blocks), NTH, p1_smem(hpc), stream>>>(pa, tm_k, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
