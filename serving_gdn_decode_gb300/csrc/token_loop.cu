@@ -5,22 +5,26 @@
 // Work decomposition.  The D_v rows of a (seq, value head) state are
 // independent (each row i only meets v_t[i] and the shared k_t, q_t), so a
 // warp owns R consecutive rows and a CTA owns WARPS*R rows of one pair.
-// Lane l keeps the D_k/32 contiguous f32 cells [l*NSG, l*NSG+NSG) of each of
-// its R rows in registers for the whole token range (NSG = D_k/32), as the
-// capture kernel of "gated_delta_net_decode_capture.metal" (mlx-native 0.9.2)
-// keeps NSG cells per lane; state therefore crosses HBM once in and once out
-// per call whatever n_tokens is ("Threading" section of gated_delta_net.rs,
-// mlx-native 0.4.0).  Loads and stores of state are coalesced 128-bit
-// (D_k = 128) streaming accesses.
+// A row is spread over LR = D_k/CW lanes, each keeping CW contiguous f32
+// cells of it in registers for the whole token range; one warp-wide access
+// thus covers RPI = 32/LR consecutive rows, and a lane holds J = R/RPI rows
+// (slots), row j*RPI + lane/LR of the warp's R in slot j.  With CW = D_k/32
+// (one row per access, the D_k = 128 and 64 shapes) this is the layout of the
+// capture kernel of "gated_delta_net_decode_capture.metal" (mlx-native
+// 0.9.2), NSG cells per lane; at D_k = 32, CW = 4 puts a row on 8 lanes so
+// that state moves in 128-bit accesses there too.  State crosses HBM once in
+// and once out per call whatever n_tokens is ("Threading" section of
+// gated_delta_net.rs, mlx-native 0.4.0).
 //
 // Per token (decay-first; the kernel body's steps "decay + partial s_k" and
 // "state update + output partial"):
 //     S *= alpha;  sk = S@k;  delta = (v - sk)*beta;  S += delta k^T;  y = S@q
-// The two row reductions (S@k, S@q) are warp reductions over the 32 lanes.
-// Reducing R rows at once uses a transpose-reduce: at each of log2(R)
-// butterfly stages a lane keeps half of its remaining row partials and
-// trades the other half with its partner, so R rows cost R-1+5-log2(R)
-// shuffles instead of 5R; lane l ends with the total of row l/(32/R).
+// The two row reductions (S@k, S@q) are reductions over a row's LR lanes.
+// Reducing J slots at once uses a transpose-reduce: at each of log2(J)
+// butterfly stages a lane keeps half of its remaining slot partials and
+// trades the other half with its partner, so J slots cost
+// J-1+log2(LR)-log2(J) shuffles instead of J*log2(LR); lane l ends with the
+// total of slot (l % LR)/(LR/J) of its row group l/LR.
 //
 // k_t, q_t (shared by every row of the CTA), v_t for the CTA's rows, g_t and
 // beta_t are staged into shared memory with cp.async, in chunks of `tc`
@@ -83,12 +87,12 @@ struct Cells<1> {
   static __device__ __forceinline__ void store_cs(float *p, const float (&c)[1]) { __stcs(p, c[0]); }
 };
 
-// Transpose-reduce R per-lane partials over the warp.  Returns, in every
-// lane l, the warp-wide total of row l / (32/R).
-template <int R>
-__device__ __forceinline__ float reduce_rows(float (&a)[R], int lane) {
+// Transpose-reduce J per-lane partials over groups of LR lanes.  Returns, in
+// every lane l, the total over its group of slot (l % LR) / (LR/J).
+template <int J, int LR>
+__device__ __forceinline__ float reduce_slots(float (&a)[J], int lane) {
 #pragma unroll
-  for (int m = R, o = 16; m > 1; m >>= 1, o >>= 1) {
+  for (int m = J, o = LR / 2; m > 1; m >>= 1, o >>= 1) {
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < m / 2; ++i) {
@@ -99,7 +103,7 @@ __device__ __forceinline__ float reduce_rows(float (&a)[R], int lane) {
   }
   float x = a[0];
 #pragma unroll
-  for (int o = 16 / R; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  for (int o = LR / (2 * J); o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
   return x;
 }
 
@@ -120,16 +124,21 @@ __host__ __device__ constexpr int staging_bytes(int tc) {
 
 // Single-layer launches leave the register count to the compiler (48 at
 // D_k = 128: five 8-warp CTAs per SM); multi-layer launches are held to 64.
-template <typename IO, int NSG, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER, int MAXL>
+template <typename IO, int NSG, int CW, int R, int WARPS, bool CAPTURE, bool DECAY_AFTER, int MAXL>
 __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
     gdn_token_loop_kernel(const LoopArgs a, const LayerPtrs one,
                           const __grid_constant__ LayerTable<MAXL> tab) {
   constexpr int DK = 32 * NSG;
   constexpr int ROWS = WARPS * R;  // rows per CTA
-  constexpr int LPR = 32 / R;      // lanes that end up holding one row's total
+  constexpr int LR = DK / CW;      // lanes per row
+  constexpr int RPI = 32 / LR;     // rows per warp-wide access
+  constexpr int J = R / RPI;       // rows (slots) per lane
+  constexpr int LPS = LR / J;      // lanes that end up holding one slot's total
   constexpr int E16 = 16 / static_cast<int>(sizeof(IO));  // elements per 16-byte copy
   constexpr int E4 = Act<IO>::kPer4B;                      // elements per 4-byte copy
   static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+  static_assert(CW * LR == DK && LR <= 32 && (LR & (LR - 1)) == 0, "a row spans a power of two of lanes");
+  static_assert(J >= 1 && J * RPI == R && J <= LR, "whole slots, at most one per lane of a row");
   static_assert(DK % E16 == 0 && ROWS % E4 == 0, "staging granularity");
 
   extern __shared__ __align__(16) unsigned char smem[];
@@ -151,18 +160,22 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
   const uint32_t row_cta0 = rb * ROWS;
   const uint32_t row0 = row_cta0 + static_cast<uint32_t>(warp * R);
   const uint32_t nt = a.nt;
+  const int rg = lane / LR;  // this lane's row within each access: slot j holds row row0 + j*RPI + rg
+  const int cell0 = (lane % LR) * CW;
 
   // 1. Issue the state loads first: they are the bulk of the HBM traffic.
+  //    Slot j of lane l is at (row0 + j*RPI)*DK + l*CW: the warp's lanes
+  //    read RPI whole rows, contiguous.
   const size_t state_head = static_cast<size_t>(head) * a.dv * DK;
-  float st[R][NSG];
+  float st[J][CW];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (row0 + r < a.dv) {
-      Cells<NSG>::load_cs(GDN_LAYER(state_in) + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
-                          st[r]);
+  for (int j = 0; j < J; ++j) {
+    if (row0 + j * RPI + rg < a.dv) {
+      Cells<CW>::load_cs(
+          GDN_LAYER(state_in) + state_head + static_cast<size_t>(row0 + j * RPI) * DK + lane * CW, st[j]);
     } else {
 #pragma unroll
-      for (int j = 0; j < NSG; ++j) st[r][j] = 0.f;
+      for (int c = 0; c < CW; ++c) st[j][c] = 0.f;
     }
   }
 
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
   };
 
   const uint32_t nchunks = (nt + tc - 1) / tc;
-  const int my_r = lane / LPR;  // the row whose totals this lane ends up holding
+  const int my_r = ((lane % LR) / LPS) * RPI + rg;  // the row (within the warp's R) whose totals this lane holds
   const uint32_t my_row = row0 + my_r;
 
   stage(0, 0);
@@ -234,51 +247,51 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
 
     for (int tt = 0; tt < n; ++tt) {
       const uint32_t t = c * tc + tt;
-      float kk[NSG], qq[NSG];
-      Act<IO>::template get_n<NSG>(ks + tt * DK + lane * NSG, kk);
-      Act<IO>::template get_n<NSG>(qs + tt * DK + lane * NSG, qq);
+      float kk[CW], qq[CW];
+      Act<IO>::template get_n<CW>(ks + tt * DK + cell0, kk);
+      Act<IO>::template get_n<CW>(qs + tt * DK + cell0, qq);
       const float alpha = expf(-gs[tt]);
       const float b = bs[tt];
 
       // S@k (on the decayed state for decay-first, the old one for decay-after)
-      float part[R];
+      float part[J];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        part[r] = 0.f;
+      for (int j = 0; j < J; ++j) {
+        part[j] = 0.f;
 #pragma unroll
-        for (int j = 0; j < NSG; ++j) {
-          if (!DECAY_AFTER) st[r][j] *= alpha;
-          part[r] = fmaf(st[r][j], kk[j], part[r]);
+        for (int c = 0; c < CW; ++c) {
+          if (!DECAY_AFTER) st[j][c] *= alpha;
+          part[j] = fmaf(st[j][c], kk[c], part[j]);
         }
       }
-      const float sk = reduce_rows<R>(part, lane);
+      const float sk = reduce_slots<J, LR>(part, lane);
       const float d = (Act<IO>::get(vs + tt * ROWS + warp * R + my_r) - sk) * b;
 
       // rank-1 update and S@q
-      float py[R];
+      float py[J];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float dr = __shfl_sync(kFull, d, r * LPR);
-        py[r] = 0.f;
+      for (int j = 0; j < J; ++j) {
+        const float dr = __shfl_sync(kFull, d, rg * LR + j * LPS);
+        py[j] = 0.f;
 #pragma unroll
-        for (int j = 0; j < NSG; ++j) {
+        for (int c = 0; c < CW; ++c) {
           if (DECAY_AFTER)
-            st[r][j] = fmaf(alpha, st[r][j], dr * kk[j]);
+            st[j][c] = fmaf(alpha, st[j][c], dr * kk[c]);
           else
-            st[r][j] = fmaf(dr, kk[j], st[r][j]);
-          py[r] = fmaf(st[r][j], qq[j], py[r]);
+            st[j][c] = fmaf(dr, kk[c], st[j][c]);
+          py[j] = fmaf(st[j][c], qq[c], py[j]);
         }
       }
-      const float y = reduce_rows<R>(py, lane);
+      const float y = reduce_slots<J, LR>(py, lane);
       const size_t tok_head = (static_cast<size_t>(s) * nt + t) * a.nv + vh;
-      if ((lane % LPR) == 0 && my_row < a.dv) Act<IO>::put(gout + tok_head * a.dv + my_row, y * a.q_scale);
+      if ((lane % LPS) == 0 && my_row < a.dv) Act<IO>::put(gout + tok_head * a.dv + my_row, y * a.q_scale);
 
       if (CAPTURE) {
         float *cap = GDN_LAYER(capture) + tok_head * a.dv * DK;
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (row0 + r < a.dv)
-            Cells<NSG>::store_cs(cap + static_cast<size_t>(row0 + r) * DK + lane * NSG, st[r]);
+        for (int j = 0; j < J; ++j)
+          if (row0 + j * RPI + rg < a.dv)
+            Cells<CW>::store_cs(cap + static_cast<size_t>(row0 + j * RPI) * DK + lane * CW, st[j]);
       }
     }
     __syncthreads();  // this buffer is refilled by the stage() of chunk c+2
@@ -286,10 +299,10 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
 
   // 3. Final state, from the same registers as the last capture slice.
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (row0 + r < a.dv)
-      Cells<NSG>::store_cs(GDN_LAYER(state_out) + state_head + static_cast<size_t>(row0 + r) * DK + lane * NSG,
-                           st[r]);
+  for (int j = 0; j < J; ++j)
+    if (row0 + j * RPI + rg < a.dv)
+      Cells<CW>::store_cs(GDN_LAYER(state_out) + state_head + static_cast<size_t>(row0 + j * RPI) * DK + lane * CW,
+                          st[j]);
 #undef GDN_LAYER
 }
 
@@ -298,13 +311,19 @@ __global__ void __launch_bounds__(WARPS * 32, MAXL == 1 ? 0 : 32 / WARPS)
 // of state loads in flight across many CTAs and the fixed cost of a CTA is
 // shared by few rows; tokens are staged 8 at a time.  4 warps for
 // D_k >= 64; at D_k = 32 a warp already holds 16 rows, so 2 warps (32 rows:
-// one value head of D_v = 32 per CTA).  (Measured: at D_k = 128, 4 warps beat
-// 8 by 8 % on 32 one-sequence layers per launch and by 1 % on 64-sequence
-// decode; at D_k = 32, 2 warps reach 0.88 of the HBM roofline where 4 reach
-// 0.55, half their rows lying past D_v.)
+// one value head of D_v = 32 per CTA), each row on 8 lanes of 4 cells.
+// (Measured on decode with 134 MB of state: at D_k = 128, 4 warps beat 8 by
+// 8 % on 32 one-sequence layers per launch and by 1 % on 64-sequence decode.
+// At D_k = 32, rows on 8 lanes (128-bit accesses, 4-shuffle reductions, 48
+// registers) move 6738 GB/s where one cell of every row per lane (16 scalar
+// accesses and 16-shuffle reductions a lane, 96 registers) moved 5989; 8 rows
+// per warp and 4 warps 5688; two 2-warp value heads per CTA 4586.  4 cells
+// per lane at D_k = 64 measured the same as 2.)
 
 template <int NSG>
 constexpr int kWarpsFor = NSG == 1 ? 2 : 4;
+template <int NSG>
+constexpr int kCellsFor = NSG == 1 ? 4 : NSG;  // cells of a row per lane
 constexpr int kTcMax = 8;
 
 template <typename IO, int NSG, bool CAPTURE, bool DA, int MAXL>
@@ -333,7 +352,7 @@ cudaError_t launch_layers(const Problem &p, const Problem *layers, uint32_t n_la
   }
   const LayerPtrs one = t.l[0];
   const size_t smem = 2u * static_cast<size_t>(staging_bytes<IO, DK, ROWS>(static_cast<int>(a.tc)));
-  gdn_token_loop_kernel<IO, NSG, R, kWarps, CAPTURE, DA, MAXL>
+  gdn_token_loop_kernel<IO, NSG, kCellsFor<NSG>, R, kWarps, CAPTURE, DA, MAXL>
       <<<static_cast<unsigned>(per_layer * n_layers), kWarps * 32, smem, stream>>>(a, one, t);
   return cudaGetLastError();
 }

@@ -145,6 +145,7 @@ RAGGED = [
     (64, 2, 2, 2, 2, 1, 0),
     (32, 33, 3, 3, 2, 3, 0),        # D_k = 32, odd D_v
     (32, 1, 1, 1, 9, 1, 0),         # one row
+    (32, 32, 1, 3, 4, 1, 0),        # D_k = 32, three value heads, four tokens
     (32, 32, 1, 2, 8, 1, PATH_SCAN),
     (128, 128, 16, 32, 37, 2, PATH_SCAN),   # 3 token chunks, partial last one
     (64, 70, 2, 4, 100, 1, PATH_SCAN),

@@ -42,6 +42,7 @@ CASES = [  # (d_k, d_v, n_k, n_v, n_tokens, n_seqs, n_layers, capture, path)
     (128, 128, 2, 4, 4, 2, 70, True, 0),     # two launches (64 + 6 layers), capture
     (64, 96, 2, 6, 3, 2, 9, False, 0),
     (32, 33, 1, 3, 2, 1, 4, True, 0),
+    (32, 32, 1, 3, 1, 1, 3, False, 0),        # D_k = 32 decode, three layers
     (128, 64, 2, 4, 20, 2, 3, False, 0),      # past the decode window: one launch per layer
     (128, 128, 2, 4, 5, 1, 3, True, PATH_SCAN),
 ]
