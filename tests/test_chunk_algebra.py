@@ -21,6 +21,13 @@ chunk, gamma = e^-G, the state kept as S = c * St:
 
 with c folded into St when it leaves [2^-30, 2^30], and, for a chunk whose
 |G| exceeds 40 somewhere, St decayed by c e^-G_C before the update and c' = 1.
+
+The one-pass kernel groups the same products differently (form "one_pass"):
+
+  U^T  = V^T T''^T + X (-T')^T,   T' = c T diag(beta gamma)   (gamma' with
+                                                               decay-after)
+  Y^T  = St Q'^T + U^T P'^T,      Q' = c q_scale diag(gamma) Q
+  St  += U^T K'^T,                K' = diag(e^(G_i - G_C) / c') K
 """
 import numpy as np
 import pytest
@@ -38,7 +45,7 @@ def _q_scale(params):
     return 1.0 if bits == 0 else float(np.array([bits], dtype=np.uint32).view(np.float32)[0])
 
 
-def chunk_forward(params, q, k, v, g, beta, state_in, stats=None, mutate=None):
+def chunk_forward(params, q, k, v, g, beta, state_in, stats=None, mutate=None, form="two_pass"):
     """The chunk equations above for a whole problem; flat arrays in and out
     in the library's innermost-first layouts.  `stats` (a dict) counts the
     renorm and extreme-chunk branches taken; `mutate` plants one mistake, to
@@ -91,16 +98,26 @@ def chunk_forward(params, q, k, v, g, beta, state_in, stats=None, mutate=None):
                 T = np.linalg.inv(np.eye(n) + A)
                 Tpp = T * (b[None, :] if mutate != "beta_rows" else b[:, None])
                 P = np.where(i_idx <= r_idx, qs * np.exp(G[None, :] - G[:, None]) * (Q @ K.T), 0.0)
-                # state pass
-                X, Z = St @ K.T, St @ Q.T
-                W = V.T - X * (c * (gamp if decay_after else gam))[None, :]
-                U = W @ Tpp.T
-                Y = U @ P.T
-                if mutate != "no_Z":
-                    Y = Y + Z * (c * qs * gam)[None, :]
-                out[s, sl, vh] = Y.T
                 kts = np.exp(G - GC) if mutate != "kts_sign" else np.exp(GC - G)
-                St = St * fold + (U * (kts / c_next)[None, :]) @ K
+                if form == "two_pass":
+                    X, Z = St @ K.T, St @ Q.T
+                    W = V.T - X * (c * (gamp if decay_after else gam))[None, :]
+                    U = W @ Tpp.T
+                    Y = U @ P.T
+                    if mutate != "no_Z":
+                        Y = Y + Z * (c * qs * gam)[None, :]
+                    St = St * fold + (U * (kts / c_next)[None, :]) @ K
+                else:
+                    X = St @ K.T
+                    Tp = c * T * (b * (gamp if decay_after else gam))[None, :]
+                    U = V.T @ Tpp.T + X @ (-Tp).T
+                    Qp = (c * qs * gam)[:, None] * Q
+                    Y = U @ P.T
+                    if mutate != "no_Z":
+                        Y = Y + St @ Qp.T
+                    Kp = (kts / c_next)[:, None] * K
+                    St = St * fold + U @ Kp
+                out[s, sl, vh] = Y.T
                 c = c_next
             st_out[s, vh] = c * St
     return out.reshape(-1), st_out.reshape(-1)
@@ -113,7 +130,8 @@ def _max_rel(a, b):
 @pytest.mark.parametrize("decay_after", [False, True], ids=["decay-first", "decay-after"])
 @pytest.mark.parametrize("khead_div", [False, True], ids=["mod", "div"])
 @pytest.mark.parametrize("gates", ["plain", "long", "extreme"])
-def test_chunk_equations_are_the_recurrence(oracle_mod, decay_after, khead_div, gates):
+@pytest.mark.parametrize("form", ["two_pass", "one_pass"])
+def test_chunk_equations_are_the_recurrence(oracle_mod, decay_after, khead_div, gates, form):
     # 150 tokens: two full chunks and a ragged one; D = 16 keeps the oracle quick
     # (the equations do not depend on D)
     w = Workload("algebra", 16, 16, 2, 4, 150, 2)
@@ -132,7 +150,7 @@ def test_chunk_equations_are_the_recurrence(oracle_mod, decay_after, khead_div, 
     p = w.params(path=PATH_CHUNKED, decay_after=decay_after, khead_div=khead_div)
     ro, rs, _ = oracle_mod.forward(p, **x)
     stats = {}
-    co, cs = chunk_forward(p, **x, stats=stats)
+    co, cs = chunk_forward(p, **x, stats=stats, form=form)
     assert _max_rel(co, ro) < 1e-10
     assert _max_rel(cs, rs) < 1e-10
     assert (stats["renorm"] > 0) == (gates == "long")
@@ -140,7 +158,8 @@ def test_chunk_equations_are_the_recurrence(oracle_mod, decay_after, khead_div, 
 
 
 @pytest.mark.parametrize("mutate", ["diag_in_A", "beta_rows", "no_Z", "kts_sign", "flags"])
-def test_a_planted_mistake_is_caught(oracle_mod, mutate):
+@pytest.mark.parametrize("form", ["two_pass", "one_pass"])
+def test_a_planted_mistake_is_caught(oracle_mod, mutate, form):
     # each plausible slip in the equations (the diagonal inside A, beta scaling
     # rows instead of columns, the inter-chunk output term dropped, the key
     # decay of the state update inverted, decay-first read as decay-after)
@@ -150,7 +169,7 @@ def test_a_planted_mistake_is_caught(oracle_mod, mutate):
     p = w.params(path=PATH_CHUNKED)
     ro, rs, _ = oracle_mod.forward(p, **x)
     if mutate == "flags":
-        co, cs = chunk_forward(w.params(path=PATH_CHUNKED, decay_after=True), **x)
+        co, cs = chunk_forward(w.params(path=PATH_CHUNKED, decay_after=True), **x, form=form)
     else:
-        co, cs = chunk_forward(p, **x, mutate=mutate)
+        co, cs = chunk_forward(p, **x, mutate=mutate, form=form)
     assert max(_max_rel(co, ro), _max_rel(cs, rs)) > 1e-4
