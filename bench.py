@@ -71,9 +71,12 @@ def load_peaks():
                 "sm_max_mhz": 2070.0}, "fallback"
 
 
-def kernel_traffic(kernel: str):
+def kernel_traffic(kernel: str, n_tokens: int | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source; else None.  A record taken on a shorter
+    prefill (its "n_tokens") is scaled to ``n_tokens`` by the tokens
+    processed (the kernels' traffic grows in proportion); a record with
+    several kernels (one call launching both passes) is summed."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -86,7 +89,81 @@ def kernel_traffic(kernel: str):
             h = hashlib.sha256(f.read()).hexdigest()
     except OSError:
         return None
-    return t["dram_bytes_per_launch"] if h == t["source_sha256"] else None
+    if h != t["source_sha256"]:
+        return None
+    b = t["dram_bytes_per_launch"]
+    if isinstance(b, dict):
+        b = sum(b.values())
+    if n_tokens is not None and t.get("n_tokens"):
+        b = int(round(b * n_tokens / t["n_tokens"]))
+    return b
+
+
+# ---------------------------------------------------------------- prefill rooflines
+
+def chunked_mma_flops(w, two_pass: bool) -> int:
+    """Tensor-core flops the chunked prefill issues per call (2 per MAC of
+    every tcgen05 product, full 64-token chunks even for a ragged last one).
+    Per (seq, value head, chunk) the one-pass form runs the Gram [K;Q]K^T
+    (M 128, N 64, K 128), V^T T''^T, X = S K^T, X(-T')^T, S Q'^T, U^T P'^T
+    (each M 128, N 64; K 64, 128, 64, 128, 64) and S += U^T K'^T (M 128,
+    N 128, K 64).  The two-pass form runs the Gram once per (seq, key head,
+    chunk) in its chunk pass, and per (seq, value head, chunk) [X | Z] =
+    S [K; Q]^T (M 128, N 128, K 128), U^T = W T''^T and U^T P'^T (M 128, N 64,
+    K 64) and S += U~^T K^T (M 128, N 128, K 64)."""
+    nch = -(-w.n_tokens // 64)
+    mm = lambda m, n, k: 2 * m * n * k  # noqa: E731
+    gram = mm(128, 64, 128)
+    if two_pass:
+        per_head = mm(128, 128, 128) + 2 * mm(128, 64, 64) + mm(128, 128, 64)
+        return nch * w.n_seqs * (w.n_v_heads * per_head + w.n_k_heads * gram)
+    per_head = gram + mm(128, 64, 64) + mm(128, 64, 128) + mm(128, 64, 64) + mm(128, 64, 128) \
+        + mm(128, 64, 64) + mm(128, 128, 64)
+    return nch * w.n_seqs * w.n_v_heads * per_head
+
+
+def scan_executed_flops(w) -> int:
+    """Flops the FP32 scan executes per call: with the state kept as c * S~
+    (lazy decay) every state cell takes 3 FMAs per token (S~ k, the rank-1
+    update, S~ q) = 6 flops; the decay multiply of the method's 7 is folded
+    into per-token scalars."""
+    return 6 * w.d_k * w.d_v * w.n_v_heads * w.n_seqs * w.n_tokens
+
+
+def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, clk: dict | None,
+                     act: str = "f32") -> dict:
+    """Compute roofline of one prefill call.  ``kind``: "scan" (FP32 CUDA
+    cores), "chunked" (one-pass) or "chunked_two_pass" (tensor cores, TF32)."""
+    mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    mhz_src = "median SM clock sampled in the timed region" if (clk or {}).get("sm_mhz") \
+        else "maximum SM clock (no clock samples)"
+    hbm = float(peaks["hbm_gbs"])
+    bytes_ = w.algorithmic_bytes(act)
+    out = {"unit": "TFLOP/s"}
+    if kind == "scan":
+        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        ex = scan_executed_flops(w)
+        out.update(bound="alu", achieved=round(ex / seconds / 1e12, 2), peak=round(peak, 1),
+                   peak_kind=f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop "
+                             f"(FMA) x {mhz:.0f} MHz ({mhz_src})",
+                   flops_per_call=ex, flops_counted="executed: 3 FMAs per state cell per token")
+        traffic_key = "scan"
+    else:
+        tf32_peak = float(peaks["bf16_tflops"]) * 0.5
+        ex = chunked_mma_flops(w, kind == "chunked_two_pass")
+        out.update(bound="tensor", achieved=round(ex / seconds / 1e12, 2), peak=round(tf32_peak, 1),
+                   peak_kind=f"of {peak_kind}: bf16 dense tensor peak "
+                             f"({'bf16_tflops, MEASURED_PEAKS.json' if peak_kind == 'measured' else 'recipe fallback'})"
+                             f" x 1/2, the nominal tf32:bf16 rate ratio",
+                   flops_per_call=ex, flops_counted="tcgen05 kind::tf32 MMA flops issued per call")
+        traffic_key = "chunked_split" if kind == "chunked_two_pass" else "chunked"
+    out["frac"] = round(out["achieved"] / out["peak"], 3)
+    out["hbm_achieved_GB_s"] = round(bytes_ / seconds / 1e9, 1)
+    out["hbm_frac"] = round(bytes_ / seconds / 1e9 / hbm, 3)
+    out["algorithmic_bytes"] = bytes_
+    out["traffic"] = kernel_traffic(traffic_key, w.n_tokens)
+    out["scope"] = "one C-ABI call (both passes for the two-pass form)"
+    return out
 
 
 class ClockSampler:
@@ -96,8 +173,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, local: int):
+    def __init__(self, local: int, interval_ms: int = 100):
         self.index = self.smi_id(local)
+        self.interval_ms = int(interval_ms)
         self.proc = None
         self.file = None
 
@@ -116,7 +194,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=self.file, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -310,7 +388,8 @@ def time_e2e(torch, nat, w, params, steps, device):
     return res, pipe.h2d_bytes(), pipe.d2h_bytes()
 
 
-def extras(torch, nat, peak_gbs, device):
+def extras(torch, nat, peaks, peak_kind, device):
+    peak_gbs = float(peaks["hbm_gbs"])
     from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN
     from serving_gdn_decode_gb300.workloads import WORKLOADS
     res = {}
@@ -380,22 +459,36 @@ def extras(torch, nat, peak_gbs, device):
         res[f"decode_32_layers_s{S}"] = layers_case(torch, nat, WORKLOADS["decode"].with_(n_seqs=S),
                                                     32, peak_gbs, device)
 
+    # long prefill: each form timed over about 0.3 s so the clock sampler sees
+    # the load; inputs (1.1 GB) are larger than L2
     wp = WORKLOADS["long_prefill"]
-    for key, params, act in (("long_prefill_scan", wp.params(path=PATH_SCAN), "f32"),
-                             ("long_prefill_chunked", wp.params(path=PATH_CHUNKED), "f32"),
-                             ("long_prefill_chunked_two_pass", wp.params(path=PATH_CHUNKED), "ws"),
-                             ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16")):
+    for key, params, act, kind, steps in (
+            ("long_prefill_auto", wp.params(), "f32", None, 100),
+            ("long_prefill_scan", wp.params(path=PATH_SCAN), "f32", "scan", 100),
+            ("long_prefill_chunked", wp.params(path=PATH_CHUNKED), "f32", "chunked", 200),
+            ("long_prefill_chunked_two_pass", wp.params(path=PATH_CHUNKED), "ws", "chunked_two_pass",
+             400),
+            ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16", "scan", 100)):
         sets = make_sets(torch, wp, 1, device, act="f32" if act == "ws" else act)
         if act == "ws":
             sets[0]["ws"] = torch.empty(nat.gdn_workspace_size(params), dtype=torch.uint8,
                                         device=device)
-        steps = 5
-        t, _ = time_graphed(torch, nat, sets, params, steps, 2)
+        path = nat.gdn_path_name(params)
+        if kind is None:
+            kind = "scan" if path.startswith("scan") else "chunked"
+        clocks = ClockSampler(device.index or 0, interval_ms=50)
+        t, clk = time_graphed(torch, nat, sets, params, steps, 3, clocks=clocks)
         s = t / steps
-        res[key] = {"path": nat.gdn_path_name(params), "ms_per_call": round(s * 1e3, 3),
+        res[key] = {"path": path + (" (two-pass, gdn_forward_ws)" if act == "ws" else ""),
+                    "ms_per_call": round(s * 1e3, 3),
                     "tokens_per_s": round(wp.n_tokens * wp.n_seqs / s, 1),
                     "head_tokens_per_s": round(wp.n_tokens * wp.n_seqs * wp.n_v_heads / s, 1),
-                    "fp32_tflops": round(wp.flops() / s / 1e12, 2)}
+                    "method_tflops_equiv": round(wp.flops() / s / 1e12, 2),
+                    "method_tflops_note": "7 flops per state cell per token of the sequential "
+                                          "recurrence / time: an equivalent rate, not work done",
+                    "roofline": prefill_roofline(kind, wp, s, peaks, peak_kind, clk,
+                                                 act="bf16" if act == "bf16" else "f32"),
+                    "clocks": clk}
         del sets
         torch.cuda.empty_cache()
     return res
@@ -555,7 +648,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if not args.no_extras and rank == 0:
-        line["other_workloads"] = extras(torch, nat, peak_gbs, device)
+        line["other_workloads"] = extras(torch, nat, peaks, peak_kind, device)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -44,7 +44,8 @@
  *
  * Ownership and lifetime.  Every buffer pointer is a DEVICE pointer owned by
  * the caller; the library allocates no memory, keeps no state between calls
- * and never synchronises.  All work is enqueued on `stream` (NULL = the
+ * (apart from the device status word of gdn_device_status) and never
+ * synchronises (apart from gdn_device_status).  All work is enqueued on `stream` (NULL = the
  * legacy default stream) and is asynchronous: buffers must stay valid until
  * the stream reaches the call.  Calls on different streams with disjoint
  * buffers may run concurrently.
@@ -54,6 +55,18 @@
  * enqueues nothing.  A failed launch returns GDN_ERR_CUDA.  Faults during
  * kernel execution surface through the stream like any CUDA error.  After a
  * non-OK status, gdn_last_error() gives a message (per calling thread).
+ *
+ * Device-side failures.  The chunked prefill kernels (GDN_PATH_CHUNKED in
+ * gdn_forward, gdn_forward_ws, gdn_forward_chunked_noalloc) wait on
+ * asynchronous copies and tensor-core work through barriers, and every such
+ * wait is bounded (about a second of GPU clock).  A wait that runs out does
+ * not hang or fault the GPU: the kernel writes NaN into the affected
+ * (seq, value head) state_out (the two-pass form also into its chunk
+ * matrices, so the outputs that depend on them become NaN), releases its
+ * tensor memory, returns, and sets GDN_DEVICE_WAIT_TIMEOUT in the library's
+ * device status word.  The call itself has already returned GDN_OK by then;
+ * gdn_device_status() reads the word, which tells a timed-out wait from NaN
+ * inputs.  The other kernels have no waits of this kind.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
@@ -287,8 +300,10 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
  * scratch (as gdn_forward_ws does).
  *
  * The first call on a device looks up the device address of the scratch
- * (once per device, with that device current); make that first call before
- * any stream capture.  Every call on a device shares the one scratch array:
+ * (once per device and context, with that device current; if the context is
+ * destroyed and created again, e.g. by cudaDeviceReset, the next call looks
+ * it up again); make that first call before any stream capture.  Every call
+ * on a device shares the one scratch array:
  * each call writes all of it that it reads, so nothing carries over between
  * calls, but calls that overlap on the GPU (e.g. on two streams at once)
  * race on it and must be ordered by the caller.
@@ -315,6 +330,28 @@ gdn_status gdn_forward_layers_bf16(const gdn_layer_buffers_bf16 *layers, size_t 
 /* Message for the last non-OK status returned on the calling thread ("" if
  * none).  The pointer stays valid until the thread's next call. */
 const char *gdn_last_error(void);
+
+/* Bits of the device status word. */
+#define GDN_DEVICE_WAIT_TIMEOUT 0x1u /* a chunked kernel's bounded wait ran out */
+
+/*
+ * gdn_device_status -- the library's device-side failure channel (see
+ * "Device-side failures" above).  The pages report errors as a Result from
+ * validation on the host ("validate", gated_delta_net_decode.rs); a failure
+ * that can only happen while a kernel runs needs a channel of its own, and
+ * this is it.
+ *
+ * Waits for all work enqueued on `stream` so far (it synchronises the
+ * stream), then stores in *status (HOST pointer) the OR of the GDN_DEVICE_*
+ * bits set by any kernel of this library on the CURRENT device since the
+ * word was last cleared (0 = no failure); with reset != 0 the word is
+ * cleared afterwards.  One word per device, shared by every stream and
+ * thread: read it after the calls of interest have been enqueued on
+ * `stream`, and order work on other streams yourself.  Allocates nothing.
+ * Returns INVALID_ARGUMENT for status == NULL, GDN_ERR_CUDA if the read
+ * fails (e.g. an earlier fault left the context unusable).
+ */
+gdn_status gdn_device_status(uint32_t *status, int reset, gdn_stream_t stream);
 
 /* The kernel path the library would run for `params` (with or without
  * capture): on GDN_OK, *name points to a static string such as

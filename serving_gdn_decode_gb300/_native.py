@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_workspace_size.restype = ctypes.c_int
             L.gdn_forward_chunked_noalloc.argtypes = [vp] * 8 + [u32p, sz, vp]
             L.gdn_forward_chunked_noalloc.restype = ctypes.c_int
+            L.gdn_device_status.argtypes = [u32p, ctypes.c_int, vp]
+            L.gdn_device_status.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -108,6 +110,27 @@ def gdn_path_name(params, capture: bool = False) -> str:
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
     return name.value.decode()
+
+
+GDN_DEVICE_WAIT_TIMEOUT = 0x1
+
+
+def gdn_device_status(reset: bool = False, stream=0) -> int:
+    """The library's device status word on the current device (0 = no
+    failure; GDN_DEVICE_WAIT_TIMEOUT when a chunked kernel's bounded wait ran
+    out), after all work enqueued on ``stream`` so far (the call synchronises
+    that stream); cleared afterwards when ``reset``."""
+    out = ctypes.c_uint32()
+    st = lib().gdn_device_status(ctypes.byref(out), 1 if reset else 0, _stream_ptr(stream))
+    if st != GDN_OK:
+        raise GdnError(st, gdn_last_error())
+    return int(out.value)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None or isinstance(stream, int):
+        return int(stream or 0)
+    return int(getattr(stream, "cuda_stream", stream))
 
 
 def gdn_workspace_size(params) -> int:

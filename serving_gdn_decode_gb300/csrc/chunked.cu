@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   }
 
   cp_async_wait_all();  // no copy may still be landing in shared memory at exit
+  if (failed && tid == 0) report_wait_timeout();
 
   // ---- state_out = c * S (or NaN if a wait timed out)
   {
@@ -542,6 +543,10 @@ bool chunked_supported(const Problem &p) {
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream) {
   if (!chunked_supported(p)) return cudaErrorInvalidValue;
   return p.decay_after ? launch<true>(p, stream) : launch<false>(p, stream);
+}
+
+cudaError_t chunked_wait_status(unsigned int *bits, bool reset, cudaStream_t stream) {
+  return chunked::read_wait_status(bits, reset, stream);
 }
 
 }  // namespace gdn

@@ -85,6 +85,29 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Failure bits of the kernels of one translation unit, one word per device
+// (a module global), read and cleared by read_wait_status.  A kernel whose
+// bounded wait ran out ORs in kWaitTimeoutBit (the value of
+// GDN_DEVICE_WAIT_TIMEOUT in gdn.h) besides writing NaN into its outputs.
+constexpr unsigned int kWaitTimeoutBit = 0x1u;
+__device__ unsigned int g_wait_status = 0u;
+__device__ __forceinline__ void report_wait_timeout() { atomicOr(&g_wait_status, kWaitTimeoutBit); }
+
+// Host: after all work on `stream` so far, *bits = this translation unit's
+// word on the current device; cleared afterwards when `reset`.  Symbol
+// copies only (no allocation); synchronises `stream`.
+inline cudaError_t read_wait_status(unsigned int *bits, bool reset, cudaStream_t stream) {
+  unsigned int h = 0u;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_wait_status, sizeof h, 0, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess && reset) {
+    static const unsigned int zero = 0u;
+    e = cudaMemcpyToSymbolAsync(g_wait_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  *bits = e == cudaSuccess ? h : 0u;
+  return e;
+}
+
 // Bounded wait on an mbarrier phase: about a second of clock at most.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
   const long long t0 = clock64();

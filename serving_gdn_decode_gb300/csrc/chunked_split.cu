@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(NTH, 3)
   }
   // a load that timed out may still land: wait for it (bounded) before exit
   if (tid == 0 && !loaded) (void)mbar_wait(bar_ld, 0);
+  if (tid == 0 && misc->failed) report_wait_timeout();
   cta_sync();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(64));
@@ -773,6 +774,7 @@ __global__ void __launch_bounds__(NTH, 1)
   __syncthreads();
   fence_after();
   failed = failed || misc->failed != 0;
+  if (failed && tid == 0) report_wait_timeout();
 
   // ---- state_out = c * S~ (or NaN if a wait timed out)
   {
@@ -911,7 +913,42 @@ static __device__ __align__(256) float g_noalloc_ws[kNoallocWorkspaceBytes / siz
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-float *g_noalloc_addr[kMaxDevices] = {};  // device address of g_noalloc_ws, per device
+// Device address of g_noalloc_ws per device, with the id of the context it
+// was looked up in (0: none yet).  A context torn down and created again
+// (cudaDeviceReset) gets a new id, so the address is looked up again.
+struct NoallocAddr {
+  unsigned long long ctx_id;
+  float *addr;
+};
+NoallocAddr g_noalloc_addr[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Unique id of the calling thread's current context (never reused within a
+// process), or 0 when there is none or the driver cannot say.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 }  // namespace
 
 cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream) {
@@ -923,18 +960,26 @@ cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream) 
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   float *ws = nullptr;
   {
-    // Once per device, with that device current: the array's name is only a
-    // host-side stand-in, so its device address comes from the runtime.
+    // Once per device and context, with that device current: the array's
+    // name is only a host-side stand-in, so its device address comes from
+    // the runtime.
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
+    NoallocAddr &c = g_noalloc_addr[dev];
+    const unsigned long long id = current_context_id();
+    if (c.addr == nullptr || id == 0 || c.ctx_id != id) {
       void *addr = nullptr;
       e = cudaGetSymbolAddress(&addr, g_noalloc_ws);
       if (e != cudaSuccess) return e;
-      g_noalloc_addr[dev] = static_cast<float *>(addr);
+      c.addr = static_cast<float *>(addr);
+      c.ctx_id = current_context_id();  // the lookup made the context current if there was none
     }
-    ws = g_noalloc_addr[dev];
+    ws = c.addr;
   }
   return launch_chunked_split(p, ws, stream);
+}
+
+cudaError_t chunked_split_wait_status(unsigned int *bits, bool reset, cudaStream_t stream) {
+  return chunked::read_wait_status(bits, reset, stream);
 }
 
 }  // namespace gdn

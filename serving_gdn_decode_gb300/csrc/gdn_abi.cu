@@ -509,6 +509,20 @@ gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_e
 
 const char *gdn_last_error(void) { return g_last_error; }
 
+gdn_status gdn_device_status(uint32_t *status, int reset, gdn_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (status == nullptr) return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: status is NULL");
+  *status = 0;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int one = 0, two = 0;
+  cudaError_t err = gdn::chunked_wait_status(&one, reset != 0, cs);
+  if (err == cudaSuccess) err = gdn::chunked_split_wait_status(&two, reset != 0, cs);
+  if (err != cudaSuccess)
+    return fail(GDN_ERR_CUDA, "gdn: reading the device status failed: %s", cudaGetErrorString(err));
+  *status = one | two;
+  return GDN_OK;
+}
+
 gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
                          const char **name) {
   g_last_error[0] = '\0';

@@ -57,6 +57,12 @@ cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_
 constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(32) << 20;
 cudaError_t launch_chunked_split_noalloc(const Problem &p, cudaStream_t stream);
 
+// Failure bits of the chunked kernels (chunked.cu, chunked_split.cu): each
+// file's word on the current device after all work on `stream` so far
+// (synchronises the stream); cleared afterwards when `reset`.
+cudaError_t chunked_wait_status(unsigned int *bits, bool reset, cudaStream_t stream);
+cudaError_t chunked_split_wait_status(unsigned int *bits, bool reset, cudaStream_t stream);
+
 // Rollback commit (commit.cu): state[.., s] = capture[.., accepted[s], s] for
 // every sequence whose accepted index lies in [0, nt).
 cudaError_t launch_commit(const float *capture, const int32_t *accepted, float *state,

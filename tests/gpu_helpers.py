@@ -11,6 +11,8 @@ Tolerances (the parity bar):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 MAXABS_TOL = 1e-4
@@ -71,15 +73,28 @@ def rel_l2(gpu, ref) -> float:
     return float(np.sqrt(np.sum(d * d)) / max(np.sqrt(np.sum(ref * ref)), 1e-300))
 
 
+# Every comparison made through assert_close: (test id, buffer, measure,
+# error, bar).  conftest.py prints the long-window ones at the end of the run,
+# so the margin to the bar is visible in the log of a passing run.
+MEASURED: list[tuple[str, str, str, float, float]] = []
+
+
+def _record(name, measure, err, bar):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MEASURED.append((test, name, measure, float(err), float(bar)))
+
+
 def assert_close(name, gpu, ref, n_tokens):
     assert np.all(np.isfinite(gpu)), f"{name}: non-finite GPU values"
     if n_tokens > 8:
         e = rel_l2(gpu, ref)
+        _record(name, "rel-L2", e, RELL2_TOL)
         assert e <= RELL2_TOL, f"{name}: rel-L2 {e:.3e} > {RELL2_TOL}"
         m = max_abs_rel(gpu, ref)
         assert m <= LONG_MAXABS_GUARD, f"{name}: max-abs/max|ref| {m:.3e} > {LONG_MAXABS_GUARD}"
     else:
         e = max_abs_rel(gpu, ref)
+        _record(name, "max-abs", e, MAXABS_TOL)
         assert e <= MAXABS_TOL, f"{name}: max-abs/max|ref| {e:.3e} > {MAXABS_TOL}"
     return e
 

@@ -52,6 +52,15 @@ def test_header_constants_match_binding():
     assert "#define GDN_FLAG_DECAY_AFTER 0x1u" in text and "#define GDN_FLAG_KHEAD_DIV 0x2u" in text
 
 
+def test_device_status_constants_and_null(L):
+    text = open(nat.HEADER_PATH).read()
+    assert "#define GDN_DEVICE_WAIT_TIMEOUT 0x1u" in text
+    assert nat.GDN_DEVICE_WAIT_TIMEOUT == 0x1
+    # a NULL result pointer is refused before any CUDA call
+    assert L.gdn_device_status(None, 0, None) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert "status is NULL" in nat.gdn_last_error()
+
+
 # ---------------------------------------------------------------- params-only checks
 
 def _path(p, capture=False):

@@ -84,3 +84,45 @@ def test_committed_traffic_records_name_existing_sources():
         assert os.path.exists(os.path.join(ROOT, r["source"])), name
         assert len(r["source_sha256"]) == 64, name
         assert os.path.exists(os.path.join(ROOT, r["profile"])), name
+
+
+def test_traffic_record_scaled_and_summed(tmp_path, monkeypatch):
+    src = tmp_path / "kern.cu"
+    src.write_text("// two kernels\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"k": {"source": "kern.cu", "source_sha256": h, "n_tokens": 512,
+               "dram_bytes_per_launch": {"a": 100, "b": 300}}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("k") == 400
+    assert bench.kernel_traffic("k", 4096) == 3200
+
+
+def test_prefill_flop_counts():
+    from serving_gdn_decode_gb300.workloads import WORKLOADS
+    w = WORKLOADS["long_prefill"]
+    # two-pass: 64 chunks x 4 seqs x (48 value heads x 8 x 2^20 + 16 key heads x 2 x 2^20)
+    mib = 1 << 20
+    assert bench.chunked_mma_flops(w, True) == 64 * 4 * (48 * 8 * mib + 16 * 2 * mib)
+    # one-pass: per (value head, chunk) 2 + 1 + 2 + 1 + 2 + 1 + 2 = 11 x 2^20
+    assert bench.chunked_mma_flops(w, False) == 64 * 4 * 48 * 11 * mib
+    # a ragged last chunk still runs whole products
+    assert bench.chunked_mma_flops(w.with_(n_tokens=4095), True) == bench.chunked_mma_flops(w, True)
+    assert bench.scan_executed_flops(w) == 6 * 128 * 128 * 48 * 4 * 4096
+
+
+def test_prefill_roofline_fields():
+    from serving_gdn_decode_gb300.workloads import WORKLOADS
+    w = WORKLOADS["long_prefill"]
+    peaks = {"hbm_gbs": 6700.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
+    r = bench.prefill_roofline("chunked_two_pass", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
+    assert r["bound"] == "tensor" and r["peak"] == 950.0
+    assert abs(r["frac"] - r["achieved"] / 950.0) < 2e-3
+    assert r["hbm_frac"] == round(w.algorithmic_bytes() / 1e-3 / 1e9 / 6700.0, 3)
+    s = bench.prefill_roofline("scan", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
+    assert s["bound"] == "alu"
+    assert abs(s["peak"] - 152 * 128 * 2 * 2000e6 / 1e12) < 0.1
+    # no clock samples: the maximum clock, and the record says so
+    s2 = bench.prefill_roofline("scan", w, 1e-3, peaks, "measured", None)
+    assert abs(s2["peak"] - 152 * 128 * 2 * 2070e6 / 1e12) < 0.1 and "maximum" in s2["peak_kind"]

@@ -56,6 +56,11 @@ def test_chunked_vs_oracle(torch, oracle_mod, shape, flags, split):
     p = w.params(path=PATH_CHUNKED, **flags)
     out, st, _ = run_gpu(w, x, p, workspace=split)
     ro, rs, _ = oracle_mod.forward(p, **x)
+    # Windows of 8 tokens or fewer take the long-window bar (rel-L2 1e-3, not
+    # max-abs 1e-4) here: the chunked path computes its products with TF32
+    # operands, so it is held to the bar of the long prefills it exists for.
+    # The automatic path never sends such windows to it (they run the FP32
+    # token-loop kernel, which the short-window bar is checked on).
     assert_close("output", out, ro, max(nt, 9))
     assert_close("state_out", st, rs, max(nt, 9))
 

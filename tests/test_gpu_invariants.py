@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 from gpu_helpers import assert_close, run_gpu, to_dev
-from serving_gdn_decode_gb300.params import PATH_SCAN, pack_params
+from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN, pack_params
 from serving_gdn_decode_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -89,6 +89,39 @@ def test_in_place_equals_out_of_place(torch, capture):
     for u, v in zip(a, b):
         if u is not None:
             np.testing.assert_array_equal(u, v)
+
+
+@pytest.mark.parametrize("path,capture,workspace", [
+    (PATH_SCAN, False, False), (PATH_SCAN, True, False),
+    (PATH_CHUNKED, False, False), (PATH_CHUNKED, False, True)],
+    ids=["scan", "scan-capture", "chunked-one-pass", "chunked-two-pass"])
+def test_in_place_equals_out_of_place_long(torch, path, capture, workspace):
+    """state_in == state_out on the prefill kernels: 100 tokens (one full
+    64-token chunk and a partial one; six full 16-token scan chunks and a
+    partial one), bit for bit equal to the out-of-place call.  Each of these
+    kernels reads and writes the state through its own code."""
+    w = Workload("inplace_long", 128, 128, 2, 4, 100, 2)
+    x = make_inputs(w, 12)
+    p = w.params(path=path)
+    a = run_gpu(w, x, p, capture=capture, workspace=workspace)
+    b = run_gpu(w, x, p, capture=capture, workspace=workspace, in_place=True)
+    for u, v in zip(a, b):
+        if u is not None:
+            np.testing.assert_array_equal(u, v)
+
+
+def test_device_status_clean_after_normal_runs(torch):
+    """The device status word stays 0 through normal calls on every chunked
+    form (no bounded wait runs out), and reading it with reset leaves 0."""
+    from serving_gdn_decode_gb300 import _native as nat
+    w = Workload("status", 128, 128, 2, 4, 130, 2)
+    x = make_inputs(w, 14)
+    nat.gdn_device_status(reset=True)
+    for ws in (False, True):
+        run_gpu(w, x, w.params(path=PATH_CHUNKED), workspace=ws)
+    assert nat.gdn_device_status() == 0
+    assert nat.gdn_device_status(reset=True) == 0
+    assert nat.gdn_device_status(stream=torch.cuda.current_stream()) == 0
 
 
 def test_guard_bands_untouched(torch):

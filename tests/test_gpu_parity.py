@@ -101,7 +101,7 @@ def test_spec_capture_full(cuda, oracle_mod, flags):
                                   st.reshape(w.n_seqs, -1).reshape(-1))
 
 
-@pytest.mark.parametrize("flags", [FLAGS[0], FLAGS[3]], ids=[FLAG_IDS[0], FLAG_IDS[3]])
+@pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
 def test_long_prefill_sampled(cuda, oracle_mod, flags):
     w, x, d = _inputs("long_prefill")
     p = w.params(**flags)

@@ -6,9 +6,11 @@ a fixed 32 MiB array inside the library instead of a caller workspace.
 
 Through the C ABI, two calls in a row (different inputs, so anything left
 in the shared scratch by the first call would show in the second) must give
-what gdn_forward_ws gives with its own workspace, within the long-window bar
-of the other GPU tests; a problem needing more than the fixed scratch is
-refused with a clear error.  The file is named to be collected last.
+what gdn_forward_ws gives with its own workspace, and what the oracle gives,
+within the long-window bar of the other GPU tests; an in-place call
+(state_in == state_out) must equal the out-of-place one bit for bit; a
+problem needing more than the fixed scratch is refused with a clear error.
+The file is named to be collected last.
 """
 import numpy as np
 import pytest
@@ -29,22 +31,24 @@ def torch():
     return t
 
 
-def _noalloc(torch, w, x, params):
+def _noalloc(torch, w, x, params, in_place=False):
     from serving_gdn_decode_gb300 import _native as nat
     d = to_dev(x)
     out = torch.empty(w.v_elems, dtype=torch.float32, device="cuda")
-    st = torch.empty(w.state_elems, dtype=torch.float32, device="cuda")
+    st = d["state_in"].clone() if in_place else torch.empty(w.state_elems, dtype=torch.float32,
+                                                            device="cuda")
+    st_in = st if in_place else d["state_in"]
     stream = torch.cuda.current_stream().cuda_stream
     rc = nat.forward_chunked_noalloc_raw(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
                                          d["g"].data_ptr(), d["beta"].data_ptr(),
-                                         d["state_in"].data_ptr(), out.data_ptr(), st.data_ptr(),
+                                         st_in.data_ptr(), out.data_ptr(), st.data_ptr(),
                                          params, stream)
     assert rc == nat.GDN_OK, nat.gdn_last_error()
     torch.cuda.synchronize()
     return out.cpu().numpy(), st.cpu().numpy()
 
 
-def test_noalloc_matches_workspace_entry_point_twice(torch):
+def test_noalloc_matches_workspace_entry_point_twice(torch, oracle_mod):
     # 4 value heads x 2 seqs x 5 chunks (300 tokens: 4 full chunks + 44)
     w = Workload("noalloc", 128, 128, 2, 4, 300, 2)
     for call, seed in enumerate((71, 72)):
@@ -54,6 +58,22 @@ def test_noalloc_matches_workspace_entry_point_twice(torch):
         ref_out, ref_st, _ = run_gpu(w, x, p, workspace=True)
         assert_close("output", out, ref_out.astype(np.float64), w.n_tokens)
         assert_close("state_out", st, ref_st.astype(np.float64), w.n_tokens)
+        # and against the oracle directly, for both this call and the
+        # workspace call it was compared with
+        ro, rs, _ = oracle_mod.forward(p, **x)
+        for o, s_ in ((out, st), (ref_out, ref_st)):
+            assert_close("output", o, ro, w.n_tokens)
+            assert_close("state_out", s_, rs, w.n_tokens)
+
+
+def test_noalloc_in_place(torch):
+    w = Workload("noalloc_inplace", 128, 128, 2, 4, 100, 2)
+    x = make_inputs(w, 75)
+    p = w.params(path=PATH_CHUNKED)
+    out, st = _noalloc(torch, w, x, p)
+    out2, st2 = _noalloc(torch, w, x, p, in_place=True)
+    np.testing.assert_array_equal(out2, out)
+    np.testing.assert_array_equal(st2, st)
 
 
 def test_noalloc_refuses_more_than_its_scratch(torch):
