@@ -105,8 +105,7 @@ static int decode_params(const uint32_t *params, size_t n_params, problem_t *p) 
   if (p->dk == 0 || p->dv == 0 || p->nk == 0 || p->nv == 0 || p->nt == 0 || p->ns == 0)
     return ORACLE_BAD_ARGUMENT;
   if (p->nv % p->nk != 0) return ORACLE_BAD_ARGUMENT;
-  if ((p->flags & ~FLAG_KNOWN) != 0 || ((p->flags & FLAG_PATH_MASK) >> 2) > 2)
-    return ORACLE_BAD_ARGUMENT;
+  if ((p->flags & ~FLAG_KNOWN) != 0) return ORACLE_BAD_ARGUMENT;
   if (params[7] != 0) return ORACLE_BAD_ARGUMENT;
   if (params[8] == 0) {
     p->q_scale = 1.0;

@@ -280,7 +280,7 @@ def test_heads_subset_matches_full(oracle_mod):
     dict(slot=3, value=3),          # n_v % n_k != 0 (n_k = 2)
     dict(slot=7, value=1),          # reserved slot
     dict(slot=6, value=0x10),       # unknown flag bit
-    dict(slot=6, value=0xC),        # path 3 does not exist
+    dict(slot=6, value=0x80000000),  # unknown flag bit
 ])
 def test_oracle_rejects_what_the_pages_reject(oracle_mod, bad):
     _, x = _small(dk=8, dv=6, nk=2, nv=4, nt=2, ns=1)
@@ -291,6 +291,16 @@ def test_oracle_rejects_what_the_pages_reject(oracle_mod, bad):
         p[bad["slot"]] = bad["value"]
     with pytest.raises(oracle_mod.OracleError):
         oracle_mod.forward(p, **x)
+
+
+@pytest.mark.parametrize("path", [0, 1, 2, 3])
+def test_oracle_ignores_the_path_bits(oracle_mod, path):
+    # params[6] bits 2-3 choose a GPU kernel; the recurrence is the same
+    _, x = _small(dk=8, dv=6, nk=2, nv=4, nt=3, ns=2)
+    ref = oracle_mod.forward(pack_params(8, 6, 2, 4, 3, 2), **x)
+    got = oracle_mod.forward(pack_params(8, 6, 2, 4, 3, 2, path=path), **x)
+    for a, b in zip(got[:2], ref[:2]):
+        np.testing.assert_array_equal(a, b)
 
 
 def test_tiny_workload_runs_and_is_finite(oracle_mod):
