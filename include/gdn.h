@@ -120,6 +120,15 @@ typedef enum gdn_status {
  *     aligned (its rows are copied 16 bytes at a time).
  *   UNSUPPORTED: D_k = 96 (D_k/32 = 3 has no kernel, as on the pages);
  *     the chunked path forced for a shape it does not cover.
+ *
+ * Path choice (params[6] bits 2-3).  GDN_PATH_AUTO runs the token-loop
+ * kernel for n_tokens <= 16 and the token-by-token FP32 scan for longer
+ * windows; both compute every product in f32 (relative errors of about 1e-7
+ * against a double-precision evaluation).  GDN_PATH_SCAN forces the scan.
+ * GDN_PATH_CHUNKED forces the tensor-core chunked form (D_k = D_v = 128, f32
+ * activations, no capture, v 16-byte aligned), whose products take TF32
+ * operands: relative errors of a few 1e-4, growing with the state's growth
+ * for negative gates, so the automatic choice never makes it.
  * Buffer sizes cannot be checked through raw pointers: each buffer must hold
  * the element count its layout above gives.
  */
