@@ -384,6 +384,10 @@ struct StateArgs {
   float *state_out;
   uint32_t nk, nv, nt, group, khead_div, nchunks;
   float q_scale;
+  // the chain of each (seq, value head) runs as segments of seg_len chunks,
+  // one launch per group of segments: CTA b of the launch takes segment
+  // (seg_base + b) / heads of head (seg_base + b) % heads
+  uint32_t heads, seg_len, seg_base;
 };
 
 struct P2Misc {
@@ -484,16 +488,26 @@ __global__ void __launch_bounds__(NTH, 1)
   const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   constexpr int ISSUER = 32;  // thread that issues (and commits) every MMA
 
-  const uint32_t head = blockIdx.x;  // = s * nv + vh
+  const uint32_t task = a.seg_base + blockIdx.x;
+  const uint32_t seg = task / a.heads;
+  const uint32_t head = task % a.heads;  // = s * nv + vh
   const uint32_t vh = head % a.nv, s = head / a.nv;
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
-  const uint32_t nt = a.nt;
-  const uint32_t nchunks = a.nchunks;
+  // this segment: chunks [cb, cb + nchunks) of the window, tokens from tb on;
+  // below, chunk and token indices count from the segment's start, and nt is
+  // the number of tokens from there to the window's end
+  const uint32_t cb = seg * a.seg_len;
+  const uint32_t nchunks = min(a.seg_len, a.nchunks - cb);
+  const uint32_t tb = cb * C;
+  const uint32_t nt = a.nt - tb;
   const size_t state_head = static_cast<size_t>(head) * D * D;
   const size_t v_tok = static_cast<size_t>(a.nv) * D;
-  const float *wseq = a.ws + static_cast<size_t>(head) * nchunks * kWsFloats;
-  const float *wkseq = a.ws_k + (static_cast<size_t>(s) * a.nk + kh) * nchunks * kWsKFloats;
-  const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
+  const float *wseq = a.ws + (static_cast<size_t>(head) * a.nchunks + cb) * kWsFloats;
+  const float *wkseq = a.ws_k + ((static_cast<size_t>(s) * a.nk + kh) * a.nchunks + cb) * kWsKFloats;
+  const size_t sc_first = (static_cast<size_t>(s) * a.nt + tb) * a.nv + vh;
+  // the state enters from state_in, or, after an earlier segment, from
+  // state_out, where that segment left it (an earlier launch)
+  const float *state_src = seg == 0 ? a.state_in : a.state_out;
 
   if (tid == 0) {
     const uint32_t bars[8] = {mbar_xy, mbar1, mbar2, bar_kq, bar_kt, bar_t, bar_v, bar_p};
@@ -519,7 +533,7 @@ __global__ void __launch_bounds__(NTH, 1)
     mbar_expect_tx(bar_p, kImgBytes);
     bulk_load(sbase + P2_P, wseq + 4096, kImgBytes, bar_p);
     mbar_expect_tx(bar_v, kRowsBytes);
-    tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), 0, static_cast<int>(s), bar_v);
+    tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb), static_cast<int>(s), bar_v);
   }
   // copies armed and MMA batches committed per barrier (uniform over the
   // CTA), for the bounded waits at exit
@@ -545,7 +559,7 @@ __global__ void __launch_bounds__(NTH, 1)
 
   // S <- state_in (c = 1).  Thread: row d_v, columns [64*half, 64*half + 64).
   {
-    const float4 *src = reinterpret_cast<const float4 *>(a.state_in + state_head + row * D + 64 * half);
+    const float4 *src = reinterpret_cast<const float4 *>(state_src + state_head + row * D + 64 * half);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
@@ -587,7 +601,7 @@ __global__ void __launch_bounds__(NTH, 1)
     if (tid == 0 && more) {  // V rows are free: the next chunk's
       fence_async_smem();
       mbar_expect_tx(bar_v, kRowsBytes);
-      tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(t0 + C), static_cast<int>(s),
+      tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb + t0 + C), static_cast<int>(s),
                   bar_v);
     }
 
@@ -607,7 +621,7 @@ __global__ void __launch_bounds__(NTH, 1)
       __syncwarp();
       fence_after();
       const uint32_t tm_yp = (par ? P2_TM_XY0 : P2_TM_XY1) + 64;
-      float *obase = a.output + ((static_cast<size_t>(s) * nt + (t0 - C)) * a.nv + vh) * D + row;
+      float *obase = a.output + ((static_cast<size_t>(s) * a.nt + tb + (t0 - C)) * a.nv + vh) * D + row;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t yv[32];
@@ -745,7 +759,7 @@ __global__ void __launch_bounds__(NTH, 1)
     uint32_t yv[32];
     GDN_TMEM_LD32(tl + tm_yl + 32 * half, yv);
     tmem_wait_ld();
-    float *obase = a.output + ((static_cast<size_t>(s) * nt + cl * C) * a.nv + vh) * D + row;
+    float *obase = a.output + ((static_cast<size_t>(s) * a.nt + tb + cl * C) * a.nv + vh) * D + row;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int i = 32 * half + j;
@@ -827,6 +841,27 @@ cudaError_t rows_map(CUtensorMap *tm, const void *base, uint32_t heads, uint32_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// How many segments each (seq, value head) chain of the state pass is cut
+// into.  The state pass runs one CTA per SM (its shared memory and tensor
+// memory fill one), so `heads` chains of `nchunks` chunks on `sms` SMs take
+// ceil(heads / sms) rounds of the whole chain.  Cut into m segments, run in
+// ceil(m heads / sms) launches of ceil(nchunks / m) chunks each, with about
+// kRestartChunks chunks' worth of extra time per launch (the launch, the
+// state load and the first chunk's copies).  A segment must land in a later
+// launch than the one before it, which holds when heads >= sms.
+constexpr double kRestartChunks = 1.5;
+uint32_t state_segments(unsigned long long heads, uint32_t nchunks, unsigned long long sms) {
+  auto cost = [&](uint32_t m) {
+    const unsigned long long len = (nchunks + m - 1) / m, segs = (nchunks + len - 1) / len;
+    return static_cast<double>((segs * heads + sms - 1) / sms) * (static_cast<double>(len) + kRestartChunks);
+  };
+  uint32_t best = 1;
+  if (heads < sms) return best;
+  for (uint32_t m = 2; m <= 8 && m <= nchunks; ++m)
+    if (cost(m) < cost(best)) best = m;
+  return best;
+}
+
 template <bool DA>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
@@ -876,11 +911,25 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   sa.state_out = p.state_out;
   sa.nk = p.nk; sa.nv = p.nv; sa.nt = p.nt; sa.group = pa.group; sa.khead_div = pa.khead_div;
   sa.nchunks = nchunks; sa.q_scale = p.q_scale;
+  sa.heads = static_cast<uint32_t>(heads);
+  const uint32_t segs = state_segments(heads, nchunks, want);
+  sa.seg_len = (nchunks + segs - 1) / segs;
+  const unsigned long long tasks2 = heads * ((nchunks + sa.seg_len - 1) / sa.seg_len);
   auto state = gdn_chunk_state_kernel<DA>;
   e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
   if (e != cudaSuccess) return e;
-  state<<<static_cast<unsigned>(heads), NTH, P2_SMEM, stream>>>(sa, tm_v);
-  return cudaGetLastError();
+  // one launch per group of up to `want` (one CTA per SM) segments, in the
+  // order segment-major: a head's segment j + 1 lies at least `heads` >=
+  // `want` tasks after its segment j, so in a later launch
+  const unsigned long long per_launch = segs > 1 ? want : tasks2;
+  for (unsigned long long base = 0; base < tasks2; base += per_launch) {
+    sa.seg_base = static_cast<uint32_t>(base);
+    const unsigned long long n = min(per_launch, tasks2 - base);
+    state<<<static_cast<unsigned>(n), NTH, P2_SMEM, stream>>>(sa, tm_v);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

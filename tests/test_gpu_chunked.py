@@ -171,3 +171,24 @@ def test_two_pass_workspace_size(torch):
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == \
         w.n_seqs * (w.n_tokens // 64) * (w.n_v_heads * 32768 + w.n_k_heads * 98304)
     assert nat.gdn_workspace_size(w.params()) == 0
+
+
+def test_two_pass_state_segments(torch, oracle_mod):
+    """More (seq, value head) chains than SMs: the state pass cuts each chain
+    into segments run by consecutive launches, the state handed on through
+    state_out.  160 chains of 16 chunks (1000 tokens, a ragged last chunk)
+    take four segments on a 152-SM GPU; sampled heads against the oracle,
+    both decay orders, and in place (state_in == state_out) bit for bit."""
+    w = Workload("segments", 128, 128, 2, 40, 1000, 4)
+    x = make_inputs(w, 65)
+    heads = sample_heads(w, 8, seed=5)
+    for flags in (dict(), dict(decay_after=True, khead_div=True)):
+        p = w.params(path=PATH_CHUNKED, **flags)
+        out, st, _ = run_gpu(w, x, p, workspace=True)
+        ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
+        go, gs, _ = gather_heads(w, out, st, None, heads)
+        assert_close("output", go, ro, w.n_tokens)
+        assert_close("state_out", gs, rs, w.n_tokens)
+        out2, st2, _ = run_gpu(w, x, p, workspace=True, in_place=True)
+        np.testing.assert_array_equal(out2, out)
+        np.testing.assert_array_equal(st2, st)
