@@ -160,21 +160,24 @@ __device__ __forceinline__ void tmem_scale64(uint32_t taddr, float f) {
 
 // One warp accumulates C += L R for 16 x 16 blocks: L rows at stride ldl, R
 // rows at stride ldr; each lane holds a 2 x 4 tile of C (rows tr, tr+1,
-// columns tc..tc+3).  With LOWER, L is lower triangular and its upper part
-// (stored zeros) is skipped.
-template <bool LOWER>
+// columns tc..tc+3).  Where L is triangular its other half is stored zeros
+// and is multiplied like the rest: skipping it per lane would save nothing
+// (the lanes of a warp need different lengths) and would keep the loads
+// from being issued ahead of the multiply-adds.
 __device__ __forceinline__ void blk_mac(float (&c0)[4], float (&c1)[4], const float *L, int ldl,
                                         const float *R, int ldr, int tr, int tc) {
   const float *l0 = L + tr * ldl;
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    if (!LOWER || q <= tr + 1) {
-      const float x0 = l0[q], x1 = l0[ldl + q];
-      const float4 b = *reinterpret_cast<const float4 *>(R + q * ldr + tc);
-      c0[0] = fmaf(x0, b.x, c0[0]); c0[1] = fmaf(x0, b.y, c0[1]);
-      c0[2] = fmaf(x0, b.z, c0[2]); c0[3] = fmaf(x0, b.w, c0[3]);
-      c1[0] = fmaf(x1, b.x, c1[0]); c1[1] = fmaf(x1, b.y, c1[1]);
-      c1[2] = fmaf(x1, b.z, c1[2]); c1[3] = fmaf(x1, b.w, c1[3]);
+  for (int q = 0; q < 16; q += 4) {
+    const float4 x0 = *reinterpret_cast<const float4 *>(l0 + q), x1 = *reinterpret_cast<const float4 *>(l0 + ldl + q);
+    const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 b = *reinterpret_cast<const float4 *>(R + (q + u) * ldr + tc);
+      c0[0] = fmaf(a0[u], b.x, c0[0]); c0[1] = fmaf(a0[u], b.y, c0[1]);
+      c0[2] = fmaf(a0[u], b.z, c0[2]); c0[3] = fmaf(a0[u], b.w, c0[3]);
+      c1[0] = fmaf(a1[u], b.x, c1[0]); c1[1] = fmaf(a1[u], b.y, c1[1]);
+      c1[2] = fmaf(a1[u], b.z, c1[2]); c1[3] = fmaf(a1[u], b.w, c1[3]);
     }
   }
 }
@@ -215,12 +218,12 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   if (warp < 2) {
     const int j = 2 * warp, i = j + 1;
     float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
-    blk_mac<false>(m0, m1, A + (16 * i) * LD + 16 * j, LD, T + (16 * j) * LD + 16 * j, LD, tr, tc);
+    blk_mac(m0, m1, A + (16 * i) * LD + 16 * j, LD, T + (16 * j) * LD + 16 * j, LD, tr, tc);
     *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
     *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
     __syncwarp();
     float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-    blk_mac<true>(t0, t1, T + (16 * i) * LD + 16 * i, LD, mw, 16, tr, tc);
+    blk_mac(t0, t1, T + (16 * i) * LD + 16 * i, LD, mw, 16, tr, tc);
     float *to = T + (16 * i + tr) * LD + 16 * j + tc;
     *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
     *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
@@ -233,7 +236,7 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   if (warp < 4) {
     float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = cb; k <= 1; ++k)
-      blk_mac<false>(m0, m1, A + (16 * r) * LD + 16 * k, LD, T + (16 * k) * LD + 16 * cb, LD, tr, tc);
+      blk_mac(m0, m1, A + (16 * r) * LD + 16 * k, LD, T + (16 * k) * LD + 16 * cb, LD, tr, tc);
     *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
     *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
   }
@@ -242,8 +245,8 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   if (warp < 4) {
     float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
     if (r == 3)
-      blk_mac<false>(t0, t1, T + (16 * r) * LD + 32, LD, M + cb * 256, 16, tr, tc);  // T_32 M'_2c
-    blk_mac<true>(t0, t1, T + (16 * r) * LD + 16 * r, LD, M + (2 * (r - 2) + cb) * 256, 16, tr, tc);
+      blk_mac(t0, t1, T + (16 * r) * LD + 32, LD, M + cb * 256, 16, tr, tc);  // T_32 M'_2c
+    blk_mac(t0, t1, T + (16 * r) * LD + 16 * r, LD, M + (2 * (r - 2) + cb) * 256, 16, tr, tc);
     float *to = T + (16 * r + tr) * LD + 16 * cb + tc;
     *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
     *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
