@@ -73,7 +73,8 @@ def load_peaks():
 
 def kernel_traffic(kernel: str, n_tokens: int | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None.  A record taken on a shorter
+    on the current kernel source (the record's "source" and every file in its
+    "deps", each matching its sha256); else None.  A record taken on a shorter
     prefill (its "n_tokens") is scaled to ``n_tokens`` by the tokens
     processed (the kernels' traffic grows in proportion); a record with
     several kernels (one call launching both passes) is summed."""
@@ -83,14 +84,15 @@ def kernel_traffic(kernel: str, n_tokens: int | None = None):
             t = json.load(f)[kernel]
     except Exception:
         return None
-    src = os.path.join(ROOT, t["source"])
-    try:
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()
-    except OSError:
-        return None
-    if h != t["source_sha256"]:
-        return None
+    # every file the kernel is built from, each with the hash it was profiled at
+    pairs = [(t["source"], t["source_sha256"])] + list(t.get("deps", {}).items())
+    for rel, want in pairs:
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != want:
+                    return None
+        except OSError:
+            return None
     b = t["dram_bytes_per_launch"]
     if isinstance(b, dict):
         b = sum(b.values())

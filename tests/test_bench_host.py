@@ -82,6 +82,8 @@ def test_committed_traffic_records_name_existing_sources():
         records = json.load(f)
     for name, r in records.items():
         assert os.path.exists(os.path.join(ROOT, r["source"])), name
+        for dep in r.get("deps", {}):
+            assert os.path.exists(os.path.join(ROOT, dep)), (name, dep)
         assert len(r["source_sha256"]) == 64, name
         assert os.path.exists(os.path.join(ROOT, r["profile"])), name
 
@@ -126,3 +128,18 @@ def test_prefill_roofline_fields():
     # no clock samples: the maximum clock, and the record says so
     s2 = bench.prefill_roofline("scan", w, 1e-3, peaks, "measured", None)
     assert abs(s2["peak"] - 152 * 128 * 2 * 2070e6 / 1e12) < 0.1 and "maximum" in s2["peak_kind"]
+
+
+def test_traffic_record_follows_its_headers(tmp_path, monkeypatch):
+    src, dep = tmp_path / "kern.cu", tmp_path / "common.cuh"
+    src.write_text("// kernel\n")
+    dep.write_text("// shared helpers v1\n")
+    h = lambda p: hashlib.sha256(p.read_bytes()).hexdigest()  # noqa: E731
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"k": {"source": "kern.cu", "source_sha256": h(src), "deps": {"common.cuh": h(dep)},
+               "dram_bytes_per_launch": 77}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic("k") == 77
+    dep.write_text("// shared helpers v2\n")
+    assert bench.kernel_traffic("k") is None
