@@ -98,6 +98,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
+// T'' and P' are lower triangular (diagonal included).  In the canonical
+// K-major image of a 64 x 64 matrix the 8 x 4 core block (R, Kc) -- rows
+// 8R .. 8R+7, columns 4Kc .. 4Kc+3 -- holds a nonzero only if Kc <= 2R + 1,
+// so the used cores of each 8-row group (2 KB) are a prefix of 2R + 2 cores
+// (128 bytes each): 72 of 128.  Pass 1 writes only those, pass 2 copies only
+// those into image buffers whose other cores it zeroed once.
+__host__ __device__ constexpr bool tri_core_used(int R, int Kc) { return Kc <= 2 * R + 1; }
+constexpr uint32_t kTriBytes = 72 * 128;  // the used cores of one image
+// The used cores of the image at src (global) into the image at dst (shared).
+__device__ __forceinline__ void load_tri(uint32_t dst, const float *src, uint32_t bar) {
+  mbar_expect_tx(bar, kTriBytes);
+#pragma unroll
+  for (int R = 0; R < 8; ++R) bulk_load(dst + R * 2048, src + R * 512, (2 * R + 2) * 128, bar);
+}
+
 // ================================================================ pass 1
 
 // shared memory (bytes): the [K;Q] stack for the Gram, then, once the Gram
@@ -310,7 +325,8 @@ __global__ void __launch_bounds__(NTH, 3)
           const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
           e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
         }
-        *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) = make_float4(e[0], e[1], e[2], e[3]);
+        if (tri_core_used(r >> 3, 8 * half + jj))  // the rest of the image stays unwritten (zeros)
+          *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) = make_float4(e[0], e[1], e[2], e[3]);
       }
     }
   };
@@ -329,7 +345,7 @@ __global__ void __launch_bounds__(NTH, 3)
       t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
                       tf32_rn(t.w * bet[i0 + 3]));
       if (failed) t = make_float4(nan, nan, nan, nan);
-      reinterpret_cast<float4 *>(ws)[ci] = t;
+      if (tri_core_used(core >> 4, core & 15)) reinterpret_cast<float4 *>(ws)[ci] = t;
     }
   };
 
@@ -521,17 +537,19 @@ __global__ void __launch_bounds__(NTH, 1)
                  :: "r"(smem_addr(&misc->tmem_base)), "r"(P2_TM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  __syncthreads();  // barriers initialised before anyone waits on them
+  // the T'' and P' buffers (adjacent): zeros where the copies write nothing
+  for (int i = tid; i < 2 * static_cast<int>(kImgBytes) / 16; i += NTH)
+    reinterpret_cast<float4 *>(smem + P2_TPP)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  fence_async_smem();
+  __syncthreads();  // barriers initialised and buffers zeroed before anyone uses them
   // chunk 0's inputs start arriving while the state is loaded
   if (tid == 0) {
     mbar_expect_tx(bar_kq, 65536);
     bulk_load(sbase + P2_KQ, wkseq, 65536, bar_kq);
     mbar_expect_tx(bar_kt, kRowsBytes);
     bulk_load(sbase + P2_KT, wkseq + 16384, kRowsBytes, bar_kt);
-    mbar_expect_tx(bar_t, kImgBytes);
-    bulk_load(sbase + P2_TPP, wseq, kImgBytes, bar_t);
-    mbar_expect_tx(bar_p, kImgBytes);
-    bulk_load(sbase + P2_P, wseq + 4096, kImgBytes, bar_p);
+    load_tri(sbase + P2_TPP, wseq, bar_t);
+    load_tri(sbase + P2_P, wseq + 4096, bar_p);
     mbar_expect_tx(bar_v, kRowsBytes);
     tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb), static_cast<int>(s), bar_v);
   }
@@ -703,8 +721,7 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- 5. batch 2: Yt += Ut P'^T; S~ += U~t K^T.  Meanwhile warp 2 sets up
     // the next chunk's scalars and every thread takes the next chunk's V.
     if (tid == 0 && more) {  // U^T is done: T'' is free
-      mbar_expect_tx(bar_t, kImgBytes);
-      bulk_load(sbase + P2_TPP, wseq + static_cast<size_t>(ch + 1) * kWsFloats, kImgBytes, bar_t);
+      load_tri(sbase + P2_TPP, wseq + static_cast<size_t>(ch + 1) * kWsFloats, bar_t);
     }
     if (tid == ISSUER) {
       if (!mbar_wait(bar_p, par)) misc->failed = 1;
@@ -738,8 +755,7 @@ __global__ void __launch_bounds__(NTH, 1)
     if (tid == 0) {  // batch 2 done: P' and K^T are free for the next chunk's
       if (!mbar_wait(mbar2, par)) misc->failed = 1;
       if (more) {
-        mbar_expect_tx(bar_p, kImgBytes);
-        bulk_load(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, kImgBytes, bar_p);
+        load_tri(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, bar_p);
         mbar_expect_tx(bar_kt, kRowsBytes);
         bulk_load(sbase + P2_KT, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats + 16384, kRowsBytes, bar_kt);
       }
