@@ -56,7 +56,7 @@
  * kernel execution surface through the stream like any CUDA error.  After a
  * non-OK status, gdn_last_error() gives a message (per calling thread).
  *
- * Device-side failures.  The chunked prefill kernels (GDN_PATH_CHUNKED in
+ * Device-side failures.  The chunked prefill kernels (the chunked path of
  * gdn_forward, gdn_forward_ws, gdn_forward_chunked_noalloc) wait on
  * asynchronous copies and tensor-core work through barriers, and every such
  * wait is bounded (about a second of GPU clock).  A wait that runs out does
@@ -97,7 +97,10 @@ typedef enum gdn_status {
 #define GDN_PATH_MASK 0xCu
 #define GDN_PATH_AUTO 0u          /* the library picks by shape            */
 #define GDN_PATH_SCAN 1u          /* token-by-token scan kernel            */
-#define GDN_PATH_CHUNKED 2u       /* chunked tensor-core prefill           */
+#define GDN_PATH_CHUNKED 2u       /* chunked tensor-core prefill, split-bf16
+                                     operands                              */
+#define GDN_PATH_CHUNKED_TF32 3u  /* the same with TF32 operands (faster,
+                                     about 1e-3 less accurate)             */
 
 /*
  * gdn_forward -- run the recurrence over n_tokens tokens for every
@@ -112,23 +115,31 @@ typedef enum gdn_status {
  *   INVALID_ARGUMENT: params == NULL or n_params < 9; any of D_k, D_v,
  *     n_k_heads, n_v_heads, n_tokens, n_seqs == 0; n_v_heads % n_k_heads != 0;
  *     D_k % 32 != 0 or D_k > 128; D_v % (D_k/32) != 0; params[7] != 0;
- *     unknown flag bits or path 3; a NULL buffer; q, k, state_in or state_out
+ *     unknown flag bits; a NULL buffer; q, k, state_in or state_out
  *     not 16-byte aligned, or v, g, beta, output not 4-byte aligned;
  *     state_in and state_out overlapping without being the same pointer
  *     (state_in == state_out, an in-place update, is allowed); output
- *     overlapping any other buffer; on the chunked path, v not 16-byte
+ *     overlapping any other buffer; on a forced chunked path, v not 16-byte
  *     aligned (its rows are copied 16 bytes at a time).
  *   UNSUPPORTED: D_k = 96 (D_k/32 = 3 has no kernel, as on the pages);
  *     the chunked path forced for a shape it does not cover.
  *
  * Path choice (params[6] bits 2-3).  GDN_PATH_AUTO runs the token-loop
- * kernel for n_tokens <= 16 and the token-by-token FP32 scan for longer
- * windows; both compute every product in f32 (relative errors of about 1e-7
- * against a double-precision evaluation).  GDN_PATH_SCAN forces the scan.
- * GDN_PATH_CHUNKED forces the tensor-core chunked form (D_k = D_v = 128, f32
- * activations, no capture, v 16-byte aligned), whose products take TF32
- * operands: relative errors of a few 1e-4, growing with the state's growth
- * for negative gates, so the automatic choice never makes it.
+ * kernel for n_tokens <= 16; for longer windows it runs the tensor-core
+ * chunked form when that form covers the call (D_k = D_v = 128, f32
+ * activations, no capture, v 16-byte aligned) and n_tokens >= 64, and the
+ * token-by-token FP32 scan otherwise.  GDN_PATH_SCAN forces the scan;
+ * GDN_PATH_CHUNKED and GDN_PATH_CHUNKED_TF32 force the chunked form
+ * (UNSUPPORTED for a shape it does not cover).
+ * Accuracy against a double-precision evaluation of the recurrence (rel-L2,
+ * 4 x 4096-token windows): the token-loop kernel and the scan compute every
+ * product in f32, about 1e-7; the chunked form takes each tensor-core
+ * product as three bf16 products of split operands (x = hi + lo), about
+ * 1e-5 (3e-5 for negative gates, whose states grow by e^20 over the
+ * window); GDN_PATH_CHUNKED_TF32 rounds the operands to TF32 instead, one
+ * product each, about 5e-4 (3e-3 for those negative gates).
+ * gdn_forward runs the chunked form in one pass; gdn_forward_ws, given a
+ * workspace, in two (faster).
  * Buffer sizes cannot be checked through raw pointers: each buffer must hold
  * the element count its layout above gives.
  */
@@ -254,11 +265,13 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  * per (seq, value head)).  The pages have no chunked kernel:
  * the chunk equations are the delta rule's published chunkwise form derived
  * from the recurrence of gated_delta_net.rs (mlx-native 0.4.0) and of the
- * capture kernel page, with the same TF32 operands as GDN_PATH_CHUNKED.
+ * capture kernel page, with the operands of the path bits (split bf16 for
+ * GDN_PATH_AUTO and GDN_PATH_CHUNKED, TF32 for GDN_PATH_CHUNKED_TF32).
  *
  * gdn_workspace_size: *bytes = the workspace gdn_forward_ws needs for
- *   `params` -- on the chunked path, per (seq, 64-token chunk), 32 KB per
- *   value head plus 96 KB per key head (the rounded K and Q rows and K^T,
+ *   `params` -- on the chunked path (forced, or chosen by GDN_PATH_AUTO for
+ *   the shape, assuming a 16-byte-aligned v), per (seq, 64-token chunk),
+ *   32 KB per value head plus 96 KB per key head (the K and Q operands and K^T,
  *   shared by the value heads that read the key head); 0 on every other
  *   path, and 0 when a key head has more than 32 value heads (the two-pass
  *   form takes at most 32; gdn_forward_ws then runs the one-pass chunked
@@ -267,9 +280,9 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  * gdn_forward_ws: gdn_forward, plus `workspace` (DEVICE, caller-owned,
  *   at least gdn_workspace_size bytes, 16-byte aligned, overlapping no other
  *   buffer; may be NULL when the size is 0).  The call overwrites the
- *   workspace; its contents afterwards are unspecified.  With the chunked
- *   path (params[6] path bits = GDN_PATH_CHUNKED) the two-pass form runs;
- *   the other paths run exactly as in gdn_forward and do not touch the
+ *   workspace; its contents afterwards are unspecified.  On the chunked
+ *   path (forced, or chosen by GDN_PATH_AUTO) the two-pass form runs; the
+ *   other paths run exactly as in gdn_forward and do not touch the
  *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
  *   short or overlapping workspace when the size is > 0.
  */
@@ -300,8 +313,8 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
  * GDN_ERR_INVALID_ARGUMENT with the numbers; use gdn_forward_ws for them.
  *
  * Arguments, layouts and checks as gdn_forward (f32 activations), for the
- * chunked path: the params path bits must be GDN_PATH_AUTO or
- * GDN_PATH_CHUNKED, the chunked path's shape rules apply (D_k = D_v = 128,
+ * chunked path: the params path bits must not be GDN_PATH_SCAN
+ * (GDN_PATH_AUTO means GDN_PATH_CHUNKED here), the chunked path's shape rules apply (D_k = D_v = 128,
  * else GDN_ERR_UNSUPPORTED), and v must be 16-byte aligned as for
  * gdn_forward_ws (INVALID_ARGUMENT otherwise).  Results equal
  * gdn_forward_ws's on the chunked path.  With more than 32 value heads per

@@ -6,10 +6,10 @@ The compute lives in ``libgdn_gb300.so`` (CUDA kernels behind the C ABI of
 parameter packer and the seeded synthetic-input generator.
 """
 from .params import (FLAG_DECAY_AFTER, FLAG_KHEAD_DIV, N_PARAMS, PATH_AUTO, PATH_CHUNKED,
-                     PATH_SCAN, pack_params, q_scale_bits)
+                     PATH_CHUNKED_TF32, PATH_SCAN, pack_params, q_scale_bits)
 
 __all__ = ["FLAG_DECAY_AFTER", "FLAG_KHEAD_DIV", "N_PARAMS", "PATH_AUTO", "PATH_CHUNKED",
-           "PATH_SCAN", "pack_params", "q_scale_bits", "gdn_forward", "gdn_forward_capture",
+           "PATH_CHUNKED_TF32", "PATH_SCAN", "pack_params", "q_scale_bits", "gdn_forward", "gdn_forward_capture",
            "gdn_last_error", "gdn_path_name", "gdn_commit_capture", "gdn_forward_layers",
            "gdn_forward_host", "gdn_forward_ws", "gdn_workspace_size", "HostPipeline", "GdnError"]
 

@@ -31,16 +31,23 @@
 // c * S (c = product of the chunk decays since the last fold), so the decay
 // never needs a read-modify-write of TMEM; c is folded into S when it leaves
 // [2^-30, 2^30], and a chunk whose |G| exceeds 40 (extreme gates) folds its
-// decay into S before the update instead.  Operands are rounded to TF32
-// (round-to-nearest) when staged in shared memory; accumulation is f32.
+// decay into S before the update instead.  Accumulation is f32.  Operands are
+// either rounded to TF32 (round-to-nearest) when staged, or split into bf16
+// hi and lo halves with every product taken as three bf16 MMAs
+// (chunked_common.cuh); the split form computes Yt = S Q^T and scales its
+// columns by c q_scale gamma_r in TMEM instead of scaling Q, and runs
+// Ut += X (-T')^T as a batch of its own once X is split.
 // The triangular inverse (64 x 64) runs on the CUDA cores, blocked 16 x 16.
 //
-// One CTA (8 warps) owns one (seq, value head) for the whole token range;
-// TMEM: S 128 cols, X 64, Ut 64, Yt 64, G 64, V^T 64 (512 allocated).
-// Shared-memory operands use the canonical K-major no-swizzle layout:
-// 8-row x 16-byte core matrices, cores adjacent along K (LBO = 128 B), core
-// rows SBO = (K/4)*128 B apart.  Every mbarrier wait is bounded; on a timeout
-// the CTA writes NaN to its state_out, frees its TMEM and returns.
+// One CTA (8 warps) owns one (seq, value head) for the whole token range,
+// with 512 TMEM columns: TF32: S 128 cols, X 64, Ut 64, Yt 64, G 64, V^T 64;
+// split: S 128, S hi 64 (then X hi | lo), S lo 64 (then Ut hi | lo), V^T
+// hi | lo 64, Ut 64, Yt 64, G 64 (then X).  Shared-memory operands use the
+// canonical K-major no-swizzle layout: 8-row x 16-byte core matrices, cores
+// adjacent along K (LBO = 128 B), core rows SBO = (K bytes / 16) * 128 B
+// apart; a split operand is its hi image followed by its lo image.  Every
+// mbarrier wait is bounded; on a timeout the CTA writes NaN to its
+// state_out, frees its TMEM and returns.
 #include <cuda_runtime.h>
 
 #include "chunked_common.cuh"
@@ -53,11 +60,18 @@ using namespace chunked;
 
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_X = 128, TM_U = 192, TM_Y = 256, TM_G = 320, TM_V = 384;
+template <bool SPLIT> struct Tm;
+template <> struct Tm<false> {
+  static constexpr uint32_t S = 0, X = 128, U = 192, Y = 256, G = 320, V = 384;
+};
+template <> struct Tm<true> {  // SH / SL: S~ hi and lo, then X hi | lo and Ut hi | lo
+  static constexpr uint32_t S = 0, SH = 128, SL = 192, V = 256, U = 320, Y = 384, G = 448, X = 448;
+};
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (bytes)
-constexpr uint32_t SM_STACK = 0;                     // [K;Q] 128 x 128 canonical, 64 KB
+constexpr uint32_t SM_STACK = 0;                     // [K;Q] 128 x 128 canonical, 64 KB (split:
+                                                     // hi 32 KB, then lo; Q rows from 16 KB on)
 constexpr uint32_t SM_KT = SM_STACK + 65536;         // K'^T 128 x 64 canonical, 32 KB
 constexpr uint32_t SM_P = SM_KT + 32768;             // P'   64 x 64 canonical, 16 KB
 constexpr uint32_t SM_A = SM_P + 16384;              // A plain 64 x LD; then -T' (canonical)
@@ -86,8 +100,12 @@ struct ChunkArgs {
   const float *state_in;
   float *__restrict__ output;
   float *state_out;
-  uint32_t nk, nv, nt, group, khead_div;
+  uint32_t nk, nv, nt, group, khead_div, nchunks;
   float q_scale;
+  // the chain of each (seq, value head) runs as segments of seg_len chunks,
+  // one launch per group of segments: CTA b of the launch takes segment
+  // (seg_base + b) / heads of head (seg_base + b) % heads
+  uint32_t heads, seg_len, seg_base;
 };
 
 struct Misc {
@@ -140,8 +158,9 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const float *kbas
   cp_async_commit();
 }
 
-template <bool DECAY_AFTER>
+template <bool DECAY_AFTER, bool SPLIT>
 __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) {
+  using TM = Tm<SPLIT>;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *sA = reinterpret_cast<float *>(smem + SM_A);
   float *sT = reinterpret_cast<float *>(smem + SM_T);
@@ -159,18 +178,29 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   const int half = tid >> 7;          // which half of a 64-column group this thread handles
   const uint32_t lane_field = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-  const uint32_t head = blockIdx.x;   // = s * nv + vh
+  const uint32_t task = a.seg_base + blockIdx.x;
+  const uint32_t seg = task / a.heads;
+  const uint32_t head = task % a.heads;  // = s * nv + vh
   const uint32_t vh = head % a.nv, s = head / a.nv;
   const uint32_t kh = a.khead_div ? vh / a.group : vh % a.nk;
-  const uint32_t nt = a.nt;
+  // this segment: chunks [cb, cb + nchunks) of the window, tokens from tb on;
+  // below, chunk and token indices count from the segment's start, and nt is
+  // the number of tokens from there to the window's end
+  const uint32_t cb = seg * a.seg_len;
+  const uint32_t nchunks = min(a.seg_len, a.nchunks - cb);
+  const uint32_t tb = cb * C;
+  const uint32_t nt = a.nt - tb;
   const size_t state_head = static_cast<size_t>(head) * D * D;
   const size_t kq_tok = static_cast<size_t>(a.nk) * D;
   const size_t v_tok = static_cast<size_t>(a.nv) * D;
-  const float *kseq = a.k + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;  // token 0 of this seq
-  const float *qseq = a.q + ((static_cast<size_t>(s) * nt) * a.nk + kh) * D;
-  const float *vseq = a.v + ((static_cast<size_t>(s) * nt) * a.nv + vh) * D;
-  const size_t sc_first = static_cast<size_t>(s) * nt * a.nv + vh;
-  const uint32_t nchunks = (nt + C - 1) / C;
+  const size_t tok0 = static_cast<size_t>(s) * a.nt + tb;  // the segment's first token of this seq
+  const float *kseq = a.k + (tok0 * a.nk + kh) * D;
+  const float *qseq = a.q + (tok0 * a.nk + kh) * D;
+  const float *vseq = a.v + (tok0 * a.nv + vh) * D;
+  const size_t sc_first = tok0 * a.nv + vh;
+  // the state enters from state_in, or, after an earlier segment, from
+  // state_out, where that segment left it (an earlier launch)
+  const float *state_src = seg == 0 ? a.state_in : a.state_out;
 
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
@@ -194,7 +224,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 
   // S <- state_in (c = 1).  Thread: row d_v, columns [64*half, 64*half + 64).
   {
-    const float4 *src = reinterpret_cast<const float4 *>(a.state_in + state_head + row * D + 64 * half);
+    const float4 *src = reinterpret_cast<const float4 *>(state_src + state_head + row * D + 64 * half);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
@@ -204,7 +234,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         v[4 * j] = __float_as_uint(x.x); v[4 * j + 1] = __float_as_uint(x.y);
         v[4 * j + 2] = __float_as_uint(x.z); v[4 * j + 3] = __float_as_uint(x.w);
       }
-      GDN_TMEM_ST32(tl + TM_S + 64 * half + 32 * h, v);
+      GDN_TMEM_ST32(tl + TM::S + 64 * half + 32 * h, v);
     }
     tmem_wait_st();
   }
@@ -275,11 +305,68 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
 
     // ---- 2. fold c into S if needed (no MMA in flight here)
-    if (do_renorm) tmem_scale64(tl + TM_S + 64 * half, c_renorm);
+    if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);
 
-    // ---- 3. operands from the staged rows: the stack's K half (canonical,
-    // TF32), the Q half rounded in place, K'^T (smem), V^T (TMEM)
-    {
+    // ---- 3. operands from the staged rows: the stack's K half (canonical),
+    // its Q half from the staged Q rows, K'^T (smem), V^T (TMEM); split: S~
+    // as hi and lo (TMEM)
+    if constexpr (SPLIT) {
+      // the staged Q rows (f32, in the TF32 canonical order of the Q half),
+      // read before the bf16 images overwrite them
+      float4 qv[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it)
+        qv[it] = *reinterpret_cast<const float4 *>(smem + SM_STACK + 32768 + (tid + NTH * it) * 16);
+      __syncthreads();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int cc = tid + NTH * it;        // element group: row r, d_k 4 c4 .. +3
+        const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), d0 = 4 * (core & 31);
+        const float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + d0);
+        uint2 h, l;
+        split2(x.x, x.y, h.x, l.x); split2(x.z, x.w, h.y, l.y);
+        *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(r, d0, 128)) = h;
+        *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(r, d0, 128)) = l;
+        split2(qv[it].x, qv[it].y, h.x, l.x); split2(qv[it].z, qv[it].w, h.y, l.y);
+        *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(64 + r, d0, 128)) = h;
+        *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(64 + r, d0, 128)) = l;
+      }
+      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
+      const float *kts = sc + SC_KTS * 64;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 32 * half + 8 * j;
+        float e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) e[u] = sKS[(i + u) * LDS + row] * kts[i + u];
+        uint4 h, l;
+        split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+        split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+        *reinterpret_cast<uint4 *>(smem + SM_KT + canon16(row, i, 64)) = h;
+        *reinterpret_cast<uint4 *>(smem + SM_KT + 16384 + canon16(row, i, 64)) = l;
+      }
+      // V^T -> TMEM as hi | lo (lane d_v = row, token pairs of [32*half, +32))
+      {
+        uint32_t vh[16], vl[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          split2(sVS[(32 * half + 2 * j) * LDS + row], sVS[(32 * half + 2 * j + 1) * LDS + row], vh[j], vl[j]);
+        GDN_TMEM_ST16(tl + TM::V + 16 * half, vh);
+        GDN_TMEM_ST16(tl + TM::V + 32 + 16 * half, vl);
+      }
+      // S~ -> hi and lo (the previous chunk's products are done)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32], sh[16], sl[16];
+        GDN_TMEM_LD32(tl + TM::S + 64 * half + 32 * h, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sh[j], sl[j]);
+        GDN_TMEM_ST16(tl + TM::SH + 32 * half + 16 * h, sh);
+        GDN_TMEM_ST16(tl + TM::SL + 32 * half + 16 * h, sl);
+      }
+      tmem_wait_st();
+    } else {
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
         const int ci = tid + NTH * it;        // 16-byte chunk of the K half
@@ -307,7 +394,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       uint32_t vv[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rn(sVS[(32 * half + j) * LDS + row]));
-      GDN_TMEM_ST32(tl + TM_V + 32 * half, vv);
+      GDN_TMEM_ST32(tl + TM::V + 32 * half, vv);
       tmem_wait_st();
     }
     fence_async_smem();
@@ -320,10 +407,20 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 
     // ---- 4. Gram [K;Q] K^T -> TMEM G
     if (tid == 0) {
+      if constexpr (SPLIT) {
 #pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks) {
-        const uint64_t d = sdesc(sbase + SM_STACK + ks * 256, 4096);
-        mma_ss(tmem + TM_G, d, d, idesc_tf32(128, 64), ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t dh = sdesc(sbase + SM_STACK + ks * 256, 2048), dl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
+          mma_ss<true>(tmem + TM::G, dh, dh, idesc_bf16(128, 64), ks > 0);
+          mma_ss<true>(tmem + TM::G, dh, dl, idesc_bf16(128, 64), 1);
+          mma_ss<true>(tmem + TM::G, dl, dh, idesc_bf16(128, 64), 1);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks) {
+          const uint64_t d = sdesc(sbase + SM_STACK + ks * 256, 4096);
+          mma_ss(tmem + TM::G, d, d, idesc_tf32(128, 64), ks > 0);
+        }
       }
       mma_commit(mbar);
     }
@@ -334,7 +431,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // ---- 5. A (plain), P' (canonical), Q' (in place)
     {
       uint32_t gv[32];
-      GDN_TMEM_LD32(tl + TM_G + 32 * half, gv);
+      GDN_TMEM_LD32(tl + TM::G + 32 * half, gv);
       tmem_wait_ld();
       const float *G = sc + SC_G * 64, *eG = sc + SC_EG * 64;
       if (row < 64) {
@@ -359,37 +456,83 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         const int r = row - 64;
         const float Gr = G[r];
         const float qgr = a.q_scale * sc[SC_GAM * 64 + r];
+        if constexpr (SPLIT) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float e[4];
+          for (int j = 0; j < 4; ++j) {
+            float e[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = 32 * half + 4 * j + u;
-            const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+            for (int u = 0; u < 8; ++u) {
+              const int i = 32 * half + 8 * j + u;
+              const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+              e[u] = i <= r ? gam * __uint_as_float(gv[8 * j + u]) : 0.f;
+            }
+            uint4 h, l;
+            split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+            split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+            *reinterpret_cast<uint4 *>(smem + SM_P + canon16(r, 32 * half + 8 * j, 64)) = h;
+            *reinterpret_cast<uint4 *>(smem + SM_P + 8192 + canon16(r, 32 * half + 8 * j, 64)) = l;
           }
-          *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
-              make_float4(e[0], e[1], e[2], e[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float e[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = 32 * half + 4 * j + u;
+              const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+              e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+            }
+            *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
+                make_float4(e[0], e[1], e[2], e[3]);
+          }
         }
       }
-      // Q' = c q_scale gamma_r Q, in place in the stack's Q half (rows 64..127)
-      const float *qs = sc + SC_QS * 64;
+      if constexpr (!SPLIT) {
+        // Q' = c q_scale gamma_r Q, in place in the stack's Q half (rows 64..127)
+        const float *qs = sc + SC_QS * 64;
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int cc = tid + NTH * it;        // chunk within the Q half
-        const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7);
-        float4 *p = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + cc * 16);
-        float4 x = *p;
-        const float f = qs[r];
-        x.x = tf32_rn(x.x * f); x.y = tf32_rn(x.y * f); x.z = tf32_rn(x.z * f); x.w = tf32_rn(x.w * f);
-        *p = x;
+        for (int it = 0; it < 8; ++it) {
+          const int cc = tid + NTH * it;        // chunk within the Q half
+          const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7);
+          float4 *p = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + cc * 16);
+          float4 x = *p;
+          const float f = qs[r];
+          x.x = tf32_rn(x.x * f); x.y = tf32_rn(x.y * f); x.z = tf32_rn(x.z * f); x.w = tf32_rn(x.w * f);
+          *p = x;
+        }
       }
     }
     cta_sync();
 
     // ---- 6. T = (I + A)^-1, then -T' (over A) and T'' (over T), canonical
     tri_inverse(sA, sT, sM, tid);
-    {
+    if constexpr (SPLIT) {
+      const float *tps = sc + SC_TPS * 64, *bet = sc + SC_BETA * 64;
+      float4 t0[2], t1[2];
+      int ci[2];
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        ci[it] = tid + NTH * it;              // 16-byte row ci & 7 of bf16 core ci >> 3 = (R, Kc)
+        const int core = ci[it] >> 3, r = (core >> 3) * 8 + (ci[it] & 7), i0 = 8 * (core & 7);
+        t0[it] = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+        t1[it] = *reinterpret_cast<const float4 *>(sT + r * LD + i0 + 4);
+      }
+      __syncthreads();                        // every thread has read T before it is overwritten
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int i0 = 8 * ((ci[it] >> 3) & 7);
+        const float t[8] = {t0[it].x, t0[it].y, t0[it].z, t0[it].w, t1[it].x, t1[it].y, t1[it].z, t1[it].w};
+        uint4 h, l;
+        split2(t[0] * tps[i0], t[1] * tps[i0 + 1], h.x, l.x); split2(t[2] * tps[i0 + 2], t[3] * tps[i0 + 3], h.y, l.y);
+        split2(t[4] * tps[i0 + 4], t[5] * tps[i0 + 5], h.z, l.z); split2(t[6] * tps[i0 + 6], t[7] * tps[i0 + 7], h.w, l.w);
+        *reinterpret_cast<uint4 *>(smem + SM_TP + ci[it] * 16) = h;
+        *reinterpret_cast<uint4 *>(smem + SM_TP + 8192 + ci[it] * 16) = l;
+        split2(t[0] * bet[i0], t[1] * bet[i0 + 1], h.x, l.x); split2(t[2] * bet[i0 + 2], t[3] * bet[i0 + 3], h.y, l.y);
+        split2(t[4] * bet[i0 + 4], t[5] * bet[i0 + 5], h.z, l.z); split2(t[6] * bet[i0 + 6], t[7] * bet[i0 + 7], h.w, l.w);
+        *reinterpret_cast<uint4 *>(smem + SM_TPP + ci[it] * 16) = h;
+        *reinterpret_cast<uint4 *>(smem + SM_TPP + 8192 + ci[it] * 16) = l;
+      }
+    } else {
       const float *tps = sc + SC_TPS * 64, *bet = sc + SC_BETA * 64;
       float4 t[4];
       int ci[4];
@@ -416,59 +559,161 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     if (misc->failed) { failed = true; break; }
 
     // ---- 7. the state-dependent products.  Batch 1 builds U^T and the
-    // inter-chunk output; then U^T is rounded to TF32 (nearest) in place -- the
-    // tensor core would otherwise truncate it as an A operand -- and, for an
-    // extreme-gate chunk, the chunk's decay is folded into S; batch 2 adds the
-    // intra-chunk output and updates S.
-    if (tid == 0) {
-      const uint32_t i64 = idesc_tf32(128, 64);
+    // inter-chunk output; then U^T is made an A operand (rounded to TF32 in
+    // place -- the tensor core would otherwise truncate it -- or split) and,
+    // for an extreme-gate chunk, the chunk's decay is folded into S; batch 2
+    // adds the intra-chunk output and updates S.  Split: batch 1 is X = S~ K^T,
+    // Yt = S~ Q^T and Ut = V^T T''^T; X is split and Yt's columns scaled; then
+    // Ut += X (-T')^T runs on its own.
+    if constexpr (SPLIT) {
+      if (tid == 0) {
+        const uint32_t i64 = idesc_bf16(128, 64);
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
-        mma_ts(tmem + TM_U, tmem + TM_V + 8 * ks, sdesc(sbase + SM_TPP + ks * 256, 2048), i64, ks > 0);
+        for (int ks = 0; ks < C / 16; ++ks) {  // Ut = V^T T''^T
+          const uint64_t bh = sdesc(sbase + SM_TPP + ks * 256, 1024), bl = sdesc(sbase + SM_TPP + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + TM::U, tmem + TM::V + 8 * ks, bh, i64, ks > 0);
+          mma_ts<true>(tmem + TM::U, tmem + TM::V + 8 * ks, bl, i64, 1);
+          mma_ts<true>(tmem + TM::U, tmem + TM::V + 32 + 8 * ks, bh, i64, 1);
+        }
 #pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
-        mma_ts(tmem + TM_X, tmem + TM_S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) {  // X = S~ K^T
+          const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i64, 1);
+        }
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
-        mma_ts(tmem + TM_U, tmem + TM_X + 8 * ks, sdesc(sbase + SM_TP + ks * 256, 2048), i64, 1);
+        for (int ks = 0; ks < D / 16; ++ks) {  // Yt = S~ Q^T
+          const uint64_t bh = sdesc(sbase + SM_STACK + 16384 + ks * 256, 2048),
+                         bl = sdesc(sbase + SM_STACK + 49152 + ks * 256, 2048);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i64, 1);
+        }
+        mma_commit(mbar);
+      }
+      if (!mbar_wait(mbar, phase)) misc->failed = 1;
+      phase ^= 1;
+      fence_after();
+      __syncthreads();
+      if (misc->failed) { failed = true; break; }
+      // the stack is free now: start the next chunk's Q rows and gates
+      if (ch + 1 < nchunks) {
+        const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+        stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+      }
+      {
+        // X -> hi | lo over S~ hi; Yt's columns times c q_scale gamma_r
+        const float *qs = sc + SC_QS * 64;
+        uint32_t xv[32], xh[16], xl[16];
+        GDN_TMEM_LD32(tl + TM::X + 32 * half, xv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
-        mma_ts(tmem + TM_Y, tmem + TM_S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
-               ks > 0);
-      mma_commit(mbar);
-    }
-    if (!mbar_wait(mbar, phase)) misc->failed = 1;
-    phase ^= 1;
-    fence_after();
-    __syncthreads();
-    if (misc->failed) { failed = true; break; }
-    // the stack's Q half is free now: start the next chunk's Q rows and gates
-    if (ch + 1 < nchunks) {
-      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-      stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                              sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
-    }
-    {
-      uint32_t uv[32];
-      GDN_TMEM_LD32(tl + TM_U + 32 * half, uv);
-      tmem_wait_ld();
+        for (int j = 0; j < 16; ++j) split2(__uint_as_float(xv[2 * j]), __uint_as_float(xv[2 * j + 1]), xh[j], xl[j]);
+        GDN_TMEM_ST16(tl + TM::SH + 16 * half, xh);
+        GDN_TMEM_ST16(tl + TM::SH + 32 + 16 * half, xl);
+        GDN_TMEM_LD32(tl + TM::Y + 32 * half, xv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rn(__uint_as_float(uv[j])));
-      GDN_TMEM_ST32(tl + TM_U + 32 * half, uv);
-      tmem_wait_st();
-    }
-    if (do_fold) tmem_scale64(tl + TM_S + 64 * half, c_fold);  // extreme gates: decay S now
-    cta_sync();
-    if (tid == 0) {
+        for (int j = 0; j < 32; ++j) xv[j] = __float_as_uint(__uint_as_float(xv[j]) * qs[32 * half + j]);
+        GDN_TMEM_ST32(tl + TM::Y + 32 * half, xv);
+        tmem_wait_st();
+      }
+      cta_sync();
+      if (tid == 0) {
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)   // Yt += Ut P'^T
-        mma_ts(tmem + TM_Y, tmem + TM_U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048),
-               idesc_tf32(128, 64), 1);
+        for (int ks = 0; ks < C / 16; ++ks) {  // Ut += X (-T')^T
+          const uint64_t bh = sdesc(sbase + SM_TP + ks * 256, 1024), bl = sdesc(sbase + SM_TP + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + TM::U, tmem + TM::SH + 8 * ks, bh, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + TM::U, tmem + TM::SH + 8 * ks, bl, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + TM::U, tmem + TM::SH + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
+        }
+        mma_commit(mbar);
+      }
+      if (!mbar_wait(mbar, phase)) misc->failed = 1;
+      phase ^= 1;
+      fence_after();
+      {  // Ut -> hi | lo over S~ lo
+        uint32_t uv[32], uh[16], ul[16];
+        GDN_TMEM_LD32(tl + TM::U + 32 * half, uv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)   // S += Ut K'^T
-        mma_ts(tmem + TM_S, tmem + TM_U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
-               idesc_tf32(128, 128), 1);
-      mma_commit(mbar);
+        for (int j = 0; j < 16; ++j) split2(__uint_as_float(uv[2 * j]), __uint_as_float(uv[2 * j + 1]), uh[j], ul[j]);
+        GDN_TMEM_ST16(tl + TM::SL + 16 * half, uh);
+        GDN_TMEM_ST16(tl + TM::SL + 32 + 16 * half, ul);
+        tmem_wait_st();
+      }
+      if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
+      cta_sync();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {  // Yt += Ut P'^T
+          const uint64_t bh = sdesc(sbase + SM_P + ks * 256, 1024), bl = sdesc(sbase + SM_P + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bl, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
+        }
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {  // S += Ut K'^T
+          const uint64_t bh = sdesc(sbase + SM_KT + ks * 256, 1024), bl = sdesc(sbase + SM_KT + 16384 + ks * 256, 1024);
+          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 8 * ks, bh, idesc_bf16(128, 128), 1);
+          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 8 * ks, bl, idesc_bf16(128, 128), 1);
+          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        }
+        mma_commit(mbar);
+      }
+    } else {
+      if (tid == 0) {
+        const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
+          mma_ts(tmem + TM::U, tmem + TM::V + 8 * ks, sdesc(sbase + SM_TPP + ks * 256, 2048), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
+          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
+          mma_ts(tmem + TM::U, tmem + TM::X + 8 * ks, sdesc(sbase + SM_TP + ks * 256, 2048), i64, 1);
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
+          mma_ts(tmem + TM::Y, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
+                 ks > 0);
+        mma_commit(mbar);
+      }
+      if (!mbar_wait(mbar, phase)) misc->failed = 1;
+      phase ^= 1;
+      fence_after();
+      __syncthreads();
+      if (misc->failed) { failed = true; break; }
+      // the stack's Q half is free now: start the next chunk's Q rows and gates
+      if (ch + 1 < nchunks) {
+        const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+        stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+      }
+      {
+        uint32_t uv[32];
+        GDN_TMEM_LD32(tl + TM::U + 32 * half, uv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rn(__uint_as_float(uv[j])));
+        GDN_TMEM_ST32(tl + TM::U + 32 * half, uv);
+        tmem_wait_st();
+      }
+      if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
+      cta_sync();
+      if (tid == 0) {
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Yt += Ut P'^T
+          mma_ts(tmem + TM::Y, tmem + TM::U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048),
+                 idesc_tf32(128, 64), 1);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // S += Ut K'^T
+          mma_ts(tmem + TM::S, tmem + TM::U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
+                 idesc_tf32(128, 128), 1);
+        mma_commit(mbar);
+      }
     }
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;
@@ -477,9 +722,9 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // ---- 8. outputs: thread = d_v, tokens [32*half, +32)
     {
       uint32_t yv[32];
-      GDN_TMEM_LD32(tl + TM_Y + 32 * half, yv);
+      GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
       tmem_wait_ld();
-      float *obase = a.output + ((static_cast<size_t>(s) * nt + t0) * a.nv + vh) * D + row;
+      float *obase = a.output + ((tok0 + t0) * a.nv + vh) * D + row;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int i = 32 * half + j;
@@ -501,7 +746,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
-      GDN_TMEM_LD32(tl + TM_S + 64 * half + 32 * h, v);
+      GDN_TMEM_LD32(tl + TM::S + 64 * half + 32 * h, v);
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -514,7 +759,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TM_COLS));
 }
 
-template <bool DA>
+template <bool DA, bool SPLIT>
 cudaError_t launch(const Problem &p, cudaStream_t stream) {
   ChunkArgs a;
   a.q = static_cast<const float *>(p.q); a.k = static_cast<const float *>(p.k);
@@ -524,14 +769,34 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
   a.group = p.nv / p.nk;
   a.khead_div = p.khead_div ? 1u : 0u;
   a.q_scale = p.q_scale;
-  const unsigned long long blocks = static_cast<unsigned long long>(p.nv) * p.ns;
-  if (blocks == 0 || blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  auto kern = gdn_chunked_kernel<DA>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+  const uint32_t nchunks = (p.nt + C - 1) / C;
+  const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
+  if (heads == 0 || heads * nchunks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(blocks), NTH, SMEM_BYTES, stream>>>(a);
-  return cudaGetLastError();
+  const unsigned long long want = static_cast<unsigned long long>(sms > 0 ? sms : 1);
+  a.nchunks = nchunks;
+  a.heads = static_cast<uint32_t>(heads);
+  const uint32_t segs = state_segments(heads, nchunks, want);
+  a.seg_len = (nchunks + segs - 1) / segs;
+  const unsigned long long tasks = heads * ((nchunks + a.seg_len - 1) / a.seg_len);
+  auto kern = gdn_chunked_kernel<DA, SPLIT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  // one launch per group of up to `want` (one CTA per SM) segments, in the
+  // order segment-major: a head's segment j + 1 lies at least `heads` >=
+  // `want` tasks after its segment j, so in a later launch
+  const unsigned long long per_launch = segs > 1 ? want : tasks;
+  for (unsigned long long base = 0; base < tasks; base += per_launch) {
+    a.seg_base = static_cast<uint32_t>(base);
+    const unsigned long long n = min(per_launch, tasks - base);
+    kern<<<static_cast<unsigned>(n), NTH, SMEM_BYTES, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -542,7 +807,8 @@ bool chunked_supported(const Problem &p) {
 
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream) {
   if (!chunked_supported(p)) return cudaErrorInvalidValue;
-  return p.decay_after ? launch<true>(p, stream) : launch<false>(p, stream);
+  if (p.tf32) return p.decay_after ? launch<true, false>(p, stream) : launch<false, false>(p, stream);
+  return p.decay_after ? launch<true, true>(p, stream) : launch<false, true>(p, stream);
 }
 
 cudaError_t chunked_wait_status(unsigned int *bits, bool reset, cudaStream_t stream) {

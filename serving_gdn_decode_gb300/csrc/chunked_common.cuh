@@ -45,15 +45,62 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-               "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
-               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+// bf16 A and B, f32 accumulator (kind::f16): 16 K elements per instruction,
+// the same 32 bytes of a K-major row as the 8 of a TF32 instruction.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
+// D (+)= A B with both operands in shared memory; BF16 selects kind::f16
+// (bf16 operands) over kind::tf32.
+template <bool BF16 = false>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (BF16)
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+  else
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// The same with A in tensor memory (lane = row; a bf16 A packs two K
+// elements per 32-bit column, the lower K index in the low half).
+template <bool BF16 = false>
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-               "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
-               :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+  if constexpr (BF16)
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+  else
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// Split-bf16 operands.  x = hi + lo with hi = bf16(x) and lo = bf16(x - hi),
+// both rounded to nearest (x - hi is exact in f32), so |x - hi - lo| <=
+// 2^-18 |x|; a product is taken as A_hi B_hi + A_hi B_lo + A_lo B_hi with
+// f32 accumulation -- the three-term bf16 scheme of Henry, Tang and Heinecke
+// ("Leveraging the bfloat16 artificial intelligence datatype for
+// higher-precision computations", 2019).  The dropped A_lo B_lo and the
+// remainders are about 2^-16 of each term, against 2^-11 for TF32 operands.
+// NaN stays NaN in both halves.
+//
+// pack_bf16x2(a, b): a in the low 16 bits, b in the high, each rounded to nearest.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+}
+// canonical K-major no-swizzle byte offset of bf16 element (row, k) in a
+// matrix whose K extent is KE elements (8 x 8-element cores of 128 bytes)
+__host__ __device__ constexpr uint32_t canon16(int row, int kk, int KE) {
+  return static_cast<uint32_t>(((row >> 3) * (KE >> 3) + (kk >> 3)) * 128 + (row & 7) * 16 + (kk & 7) * 2);
 }
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -108,6 +155,28 @@ inline cudaError_t read_wait_status(unsigned int *bits, bool reset, cudaStream_t
   return e;
 }
 
+// How many segments each (seq, value head) chain of a state-carrying kernel
+// (the one-pass kernel, the two-pass state pass) is cut into.  Both run one
+// CTA per SM (their shared memory and tensor memory fill one), so `heads`
+// chains of `nchunks` chunks on `sms` SMs take
+// ceil(heads / sms) rounds of the whole chain.  Cut into m segments, run in
+// ceil(m heads / sms) launches of ceil(nchunks / m) chunks each, with about
+// kRestartChunks chunks' worth of extra time per launch (the launch, the
+// state load and the first chunk's copies).  A segment must land in a later
+// launch than the one before it, which holds when heads >= sms.
+constexpr double kRestartChunks = 1.5;
+uint32_t state_segments(unsigned long long heads, uint32_t nchunks, unsigned long long sms) {
+  auto cost = [&](uint32_t m) {
+    const unsigned long long len = (nchunks + m - 1) / m, segs = (nchunks + len - 1) / len;
+    return static_cast<double>((segs * heads + sms - 1) / sms) * (static_cast<double>(len) + kRestartChunks);
+  };
+  uint32_t best = 1;
+  if (heads < sms) return best;
+  for (uint32_t m = 2; m <= 8 && m <= nchunks; ++m)
+    if (cost(m) < cost(best)) best = m;
+  return best;
+}
+
 // Bounded wait on an mbarrier phase: about a second of clock at most.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
   const long long t0 = clock64();
@@ -141,6 +210,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
                   "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),      \
                   "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),      \
                   "r"(v[30]), "r"(v[31]))
+#define GDN_TMEM_ST16(taddr, v)                                                                 \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10," \
+               "%11,%12,%13,%14,%15,%16};\n"                                                   \
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), \
+                  "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]),          \
+                  "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]))
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -4,14 +4,14 @@
 //
 // Pass 1, one CTA per (seq, chunk, key head), computes everything that does
 // not depend on the state and writes it to a caller-provided workspace.  It
-// rounds the key head's K and Q to TF32 once and stores them in the
-// 128-byte-swizzled layout the MMA reads (exactly its shared-memory stack),
-// stores K^T as a canonical image, and forms the Gram products K K^T and
-// Q K^T once; then, for each value head that reads the key head, that head's
-// gates give A, T = (I + A)^-1, T'' = T diag(beta) and
-// P' = q_scale (Q K^T o Gam)_{i<=r}, stored as TF32 canonical images.  The
-// state pass loads every operand ready-made and rounds nothing but its own
-// TMEM products.
+// turns the key head's K and Q into tensor-core operands once and stores them
+// in the 128-byte-swizzled layout the MMA reads (exactly its shared-memory
+// stack), stores K^T as a canonical image, and forms the Gram products K K^T
+// and Q K^T once; then, for each value head that reads the key head, that
+// head's gates give A, T = (I + A)^-1, T'' = T diag(beta) and
+// P' = q_scale (Q K^T o Gam)_{i<=r}, stored as canonical images.  The state
+// pass loads every operand ready-made and converts nothing but its own TMEM
+// products.
 //
 // Pass 2, one CTA per (seq, value head), runs the state-dependent chain per
 // chunk with the state in TMEM as S = c * S~ (c a lazy scalar): [X | Z] =
@@ -19,12 +19,23 @@
 // q_scale gamma) + U^T P'^T, S~ += U~^T K^T.  Its loads are bulk copies
 // (images) and one TMA box per chunk (V rows), each on its own mbarrier.
 //
+// Operands are either split bf16 (every product as three bf16 MMAs of the
+// halves, chunked_common.cuh) or TF32 (one MMA, rounded to nearest); both
+// take four bytes per element, so the layouts below have the same sizes.
+//
 // Workspace layout (floats):
 //   ws[head][chunk][8192], head = s * n_v + vh:
-//     [0, 4096) T'' and [4096, 8192) P' (canonical K-major images, TF32);
+//     TF32:  [0, 4096) T'' and [4096, 8192) P' (64 x 64 canonical images);
+//     split: T'' hi, T'' lo, P' hi, P' lo (2048 floats each, 64 x 64 bf16
+//            canonical images);
 //   then ws_k[s * n_k + kh][chunk][24576]:
-//     [0, 16384) the [K; Q] stack (column block cb = 16 KB: K's 64 rows,
-//     then Q's, 128-byte swizzled), [16384, 24576) K^T (128 x 64 canonical).
+//     TF32:  [0, 16384) the [K; Q] stack (column block cb = 16 KB: K's 64
+//            rows, then Q's, 128-byte swizzled, 32 d_k each),
+//            [16384, 24576) K^T (128 x 64 canonical);
+//     split: [0, 16384) the stack as blocks hi(d_k 0-63), lo(0-63),
+//            hi(64-127), lo(64-127) of 16 KB (128 rows x 64 bf16, swizzled),
+//            [16384, 20480) K^T hi, [20480, 24576) K^T lo (128 x 64 bf16
+//            canonical).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -112,6 +123,23 @@ __device__ __forceinline__ void load_tri(uint32_t dst, const float *src, uint32_
 #pragma unroll
   for (int R = 0; R < 8; ++R) bulk_load(dst + R * 2048, src + R * 512, (2 * R + 2) * 128, bar);
 }
+// The same for a bf16 image (8 x 8-element cores, 1 KB per 8-row group):
+// core (R, Kc) is used if Kc <= R, 36 of 64.  The hi and lo images of a
+// matrix (8 KB apart, both sides) come on one barrier.
+__host__ __device__ constexpr bool tri16_used(int R, int Kc) { return Kc <= R; }
+constexpr uint32_t kTri16Bytes = 36 * 128;
+__device__ __forceinline__ void load_tri16_pair(uint32_t dst, const float *src, uint32_t bar) {
+  mbar_expect_tx(bar, 2 * kTri16Bytes);
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int R = 0; R < 8; ++R) bulk_load(dst + h * 8192 + R * 1024, src + h * 2048 + R * 256, (R + 1) * 128, bar);
+}
+template <bool SPLIT>
+__device__ __forceinline__ void load_image(uint32_t dst, const float *src, uint32_t bar) {
+  if constexpr (SPLIT) load_tri16_pair(dst, src, bar);
+  else load_tri(dst, src, bar);
+}
 
 // ================================================================ pass 1
 
@@ -161,7 +189,8 @@ static_assert(sizeof(P1Misc) <= 32, "pass-1 misc area");  // then one int per va
 // once for the key head; the key-head images ([K; Q] stack and K^T) are
 // stored; then, for each value head that reads this key head in turn, its
 // gates turn the Gram into A and P', and T'' follows from T = (I + A)^-1.
-template <bool DECAY_AFTER>
+// SPLIT: split-bf16 operands, else TF32.
+template <bool DECAY_AFTER, bool SPLIT>
 __global__ void __launch_bounds__(NTH, 3)
     gdn_chunk_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_q) {
@@ -233,40 +262,106 @@ __global__ void __launch_bounds__(NTH, 3)
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
 
-  // K and Q to TF32 (round to nearest) in place, stored as the [K; Q] image
-  // (by the first part)
+  if constexpr (SPLIT) {
+    // K^T (d_k rows x 64 tokens) as bf16 hi and lo canonical images, from
+    // the f32 stack (by the first part)
+    unsigned char *wkb = reinterpret_cast<unsigned char *>(wk);
+    for (int oc = store_k ? tid : 1024; oc < 1024; oc += NTH) {  // d_k = oc % 128, tokens 8 (oc / 128) .. +7
+      const int dk = oc & 127, i0 = (oc >> 7) * 8;
+      const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
+      float e[8];
 #pragma unroll
-  for (int it = 0; it < 16; ++it) {
-    float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
-    float4 x = *p;
-    x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
-    *p = x;
-    if (store_k) __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
-  }
-  fence_async_smem();
-  cta_sync();
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u;
+        e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
+      }
+      uint4 h, l;
+      split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+      split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+      __stcg(reinterpret_cast<uint4 *>(wkb + 65536 + canon16(dk, i0, 64)), h);
+      __stcg(reinterpret_cast<uint4 *>(wkb + 81920 + canon16(dk, i0, 64)), l);
+    }
+    // The stack to bf16 hi and lo in place, 32 KB at a time: f32 column
+    // blocks 2p and 2p+1 (d_k 64p .. 64p+63) become the hi block (128 rows x
+    // 128 bytes, swizzled like the f32 ones) and the lo block after it.
+    // Every thread reads its elements before any writes (the barrier), and
+    // the first part stores the same bytes as the workspace image.
+#pragma unroll 1
+    for (int p = 0; p < 2; ++p) {
+      unsigned char *reg = smem + P1_STACK + 32768 * p;
+      uint2 hv[8], lv[8];
+      uint32_t dst[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int f = tid + NTH * it;  // float4 of the region: block f >> 10, row (f >> 3) & 127, chunk f & 7
+        const int rr = (f >> 3) & 127;
+        const int dkb = 32 * (f >> 10) + 4 * ((f & 7) ^ (rr & 7));  // d_k - 64p of its first element
+        const float4 x = reinterpret_cast<const float4 *>(reg)[f];
+        split2(x.x, x.y, hv[it].x, lv[it].x);
+        split2(x.z, x.w, hv[it].y, lv[it].y);
+        dst[it] = static_cast<uint32_t>(rr * 128 + (((dkb >> 3) ^ (rr & 7)) << 4) + (dkb & 7) * 2);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        *reinterpret_cast<uint2 *>(reg + dst[it]) = hv[it];
+        *reinterpret_cast<uint2 *>(reg + 16384 + dst[it]) = lv[it];
+        if (store_k) {
+          __stcg(reinterpret_cast<uint2 *>(wkb + 32768 * p + dst[it]), hv[it]);
+          __stcg(reinterpret_cast<uint2 *>(wkb + 32768 * p + 16384 + dst[it]), lv[it]);
+        }
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+    // Gram [K;Q] K^T -> TMEM (128 lanes x 64 columns), three bf16 terms per K step
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ah = sbase + P1_STACK + (ks >> 2) * 32768 + (ks & 3) * 32;
+        const uint64_t dh = sdesc_sw128(ah), dl = sdesc_sw128(ah + 16384);
+        mma_ss<true>(tmem, dh, dh, idesc_bf16(128, 64), ks > 0);
+        mma_ss<true>(tmem, dh, dl, idesc_bf16(128, 64), 1);
+        mma_ss<true>(tmem, dl, dh, idesc_bf16(128, 64), 1);
+      }
+      mma_commit(mbar);
+    }
+  } else {
+    // K and Q to TF32 (round to nearest) in place, stored as the [K; Q] image
+    // (by the first part)
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      float4 *p = reinterpret_cast<float4 *>(smem + P1_STACK) + tid + NTH * it;
+      float4 x = *p;
+      x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
+      *p = x;
+      if (store_k) __stcg(reinterpret_cast<float4 *>(wk) + tid + NTH * it, x);
+    }
+    fence_async_smem();
+    cta_sync();
 
-  // Gram [K;Q] K^T -> TMEM (128 lanes x 64 columns)
-  if (tid == 0) {
+    // Gram [K;Q] K^T -> TMEM (128 lanes x 64 columns)
+    if (tid == 0) {
 #pragma unroll
-    for (int ks = 0; ks < D / 8; ++ks) {
-      const uint64_t d = sdesc_sw128(sbase + P1_STACK + (ks >> 2) * 16384 + (ks & 3) * 32);
-      mma_ss(tmem, d, d, idesc_tf32(128, 64), ks > 0);
+      for (int ks = 0; ks < D / 8; ++ks) {
+        const uint64_t d = sdesc_sw128(sbase + P1_STACK + (ks >> 2) * 16384 + (ks & 3) * 32);
+        mma_ss(tmem, d, d, idesc_tf32(128, 64), ks > 0);
+      }
+      mma_commit(mbar);
     }
-    mma_commit(mbar);
-  }
-  // while the Gram runs, K^T (d_k rows x 64 tokens, canonical K-major image)
-  // from the TF32 stack (by the first part)
-  for (int oc = store_k ? tid : 2048; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
-    const int dk = oc & 127, i0 = (oc >> 7) * 4;
-    const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
-    float e[4];
+    // while the Gram runs, K^T (d_k rows x 64 tokens, canonical K-major image)
+    // from the TF32 stack (by the first part)
+    for (int oc = store_k ? tid : 2048; oc < 2048; oc += NTH) {  // d_k = oc % 128, tokens 4 (oc / 128) .. +3
+      const int dk = oc & 127, i0 = (oc >> 7) * 4;
+      const unsigned char *kb = smem + P1_STACK + (dk >> 5) * 16384 + (dk & 3) * 4;
+      float e[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u;
-      e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        e[u] = *reinterpret_cast<const float *>(kb + i * 128 + ((((dk & 31) >> 2) ^ (i & 7)) << 4));
+      }
+      __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
     }
-    __stcg(reinterpret_cast<float4 *>(wk + 16384 + canon(dk, i0, 64) / 4), make_float4(e[0], e[1], e[2], e[3]));
   }
   // and every value head's per-token scalars, one warp per head
   for (uint32_t jl = static_cast<uint32_t>(warp); jl < nh; jl += NTH / 32) {
@@ -316,36 +411,76 @@ __global__ void __launch_bounds__(NTH, 3)
       const float Gr = G[r];
       const float qgr = a.q_scale * scj[Q_GAM * 64 + r];
       float *wp = ws + 4096;
+      if constexpr (SPLIT) {
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float e[4];
+        for (int jj = 0; jj < 4; ++jj) {
+          if (!tri16_used(r >> 3, 4 * half + jj)) continue;  // the rest of the image stays unwritten (zeros)
+          float e[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 32 * half + 4 * jj + u;
-          const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-          e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
+          for (int u = 0; u < 8; ++u) {
+            const int i = 32 * half + 8 * jj + u;
+            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+            e[u] = i <= r ? gam * __uint_as_float(gv[8 * jj + u]) : 0.f;
+          }
+          uint4 h, l;
+          split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+          split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+          unsigned char *wb = reinterpret_cast<unsigned char *>(wp) + canon16(r, 32 * half + 8 * jj, 64);
+          *reinterpret_cast<uint4 *>(wb) = h;
+          *reinterpret_cast<uint4 *>(wb + 8192) = l;
         }
-        if (tri_core_used(r >> 3, 8 * half + jj))  // the rest of the image stays unwritten (zeros)
-          *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) = make_float4(e[0], e[1], e[2], e[3]);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          float e[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 32 * half + 4 * jj + u;
+            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
+            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
+          }
+          if (tri_core_used(r >> 3, 8 * half + jj))  // the rest of the image stays unwritten (zeros)
+            *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) =
+                make_float4(e[0], e[1], e[2], e[3]);
+        }
       }
     }
   };
-  // T'' = T diag(beta) of value head j as a TF32 canonical image (NaN if a
-  // wait timed out)
+  // T'' = T diag(beta) of value head j as canonical images (NaN if a wait
+  // timed out)
   auto store_tpp = [&](uint32_t j) {
     const float nan = __int_as_float(0x7fc00000);
     const float *bet = sc + j * kScSet + Q_BETA * 64;
     const bool failed = misc->failed != 0;
     float *ws = a.ws + ((static_cast<size_t>(s) * a.nv + vhead(j)) * a.nchunks + ch) * kWsFloats;
+    if constexpr (SPLIT) {
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int ci = tid + NTH * it;
-      const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
-      float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
-      t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
-                      tf32_rn(t.w * bet[i0 + 3]));
-      if (failed) t = make_float4(nan, nan, nan, nan);
-      if (tri_core_used(core >> 4, core & 15)) reinterpret_cast<float4 *>(ws)[ci] = t;
+      for (int it = 0; it < 2; ++it) {
+        const int ci = tid + NTH * it;  // 16-byte row ci & 7 of core ci >> 3 = (R, Kc)
+        const int core = ci >> 3, r = (core >> 3) * 8 + (ci & 7), i0 = 8 * (core & 7);
+        if (!tri16_used(core >> 3, core & 7)) continue;
+        const float4 t0 = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+        const float4 t1 = *reinterpret_cast<const float4 *>(sT + r * LD + i0 + 4);
+        uint4 h, l;
+        split2(t0.x * bet[i0], t0.y * bet[i0 + 1], h.x, l.x);
+        split2(t0.z * bet[i0 + 2], t0.w * bet[i0 + 3], h.y, l.y);
+        split2(t1.x * bet[i0 + 4], t1.y * bet[i0 + 5], h.z, l.z);
+        split2(t1.z * bet[i0 + 6], t1.w * bet[i0 + 7], h.w, l.w);
+        if (failed) { h = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u); l = h; }
+        reinterpret_cast<uint4 *>(ws)[ci] = h;
+        reinterpret_cast<uint4 *>(ws + 2048)[ci] = l;
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int ci = tid + NTH * it;
+        const int core = ci >> 3, r = (core >> 4) * 8 + (ci & 7), i0 = 4 * (core & 15);
+        float4 t = *reinterpret_cast<const float4 *>(sT + r * LD + i0);
+        t = make_float4(tf32_rn(t.x * bet[i0]), tf32_rn(t.y * bet[i0 + 1]), tf32_rn(t.z * bet[i0 + 2]),
+                        tf32_rn(t.w * bet[i0 + 3]));
+        if (failed) t = make_float4(nan, nan, nan, nan);
+        if (tri_core_used(core >> 4, core & 15)) reinterpret_cast<float4 *>(ws)[ci] = t;
+      }
     }
   };
 
@@ -371,7 +506,10 @@ __global__ void __launch_bounds__(NTH, 3)
 
 // TMEM columns: the state, U^T, W (then U~^T), and [X | Z -> Y^T] in two
 // regions that alternate by chunk, so a chunk's outputs are read out while
-// the next chunk's products run.
+// the next chunk's products run.  With split-bf16 operands every A operand
+// is a hi and a lo half of packed bf16 pairs: S~ as hi over W's columns and
+// lo over U's at the chunk start, W as hi | lo (32 columns each) in W's,
+// U^T as hi | lo over X (dead once W is formed) and U~^T as hi | lo in W's.
 constexpr uint32_t P2_TM_S = 0, P2_TM_XY0 = 128, P2_TM_U = 256, P2_TM_W = 320, P2_TM_XY1 = 384;
 constexpr uint32_t P2_TM_COLS = 512;
 
@@ -480,7 +618,7 @@ __device__ __forceinline__ float p2_chunk_setup(float *sc, P2Misc *misc, float c
 // outputs, Z's scaling and the next chunk's V come in beside it.  Thread 32
 // issues the MMAs, thread 0 the copies, warp 2 sets up the next chunk's
 // scalars while batch 2 runs.  Waits are bounded.
-template <bool DECAY_AFTER>
+template <bool DECAY_AFTER, bool SPLIT>
 __global__ void __launch_bounds__(NTH, 1)
     gdn_chunk_state_kernel(const StateArgs a, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -548,8 +686,8 @@ __global__ void __launch_bounds__(NTH, 1)
     bulk_load(sbase + P2_KQ, wkseq, 65536, bar_kq);
     mbar_expect_tx(bar_kt, kRowsBytes);
     bulk_load(sbase + P2_KT, wkseq + 16384, kRowsBytes, bar_kt);
-    load_tri(sbase + P2_TPP, wseq, bar_t);
-    load_tri(sbase + P2_P, wseq + 4096, bar_p);
+    load_image<SPLIT>(sbase + P2_TPP, wseq, bar_t);
+    load_image<SPLIT>(sbase + P2_P, wseq + 4096, bar_p);
     mbar_expect_tx(bar_v, kRowsBytes);
     tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb), static_cast<int>(s), bar_v);
   }
@@ -588,6 +726,13 @@ __global__ void __launch_bounds__(NTH, 1)
         v[4 * j + 2] = __float_as_uint(x.z); v[4 * j + 3] = __float_as_uint(x.w);
       }
       GDN_TMEM_ST32(tl + P2_TM_S + 64 * half + 32 * h, v);
+      if constexpr (SPLIT) {  // chunk 0's A operand S~ = S
+        uint32_t sh[16], sl[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sh[j], sl[j]);
+        GDN_TMEM_ST16(tl + P2_TM_W + 32 * half + 16 * h, sh);
+        GDN_TMEM_ST16(tl + P2_TM_U + 32 * half + 16 * h, sl);
+      }
     }
     tmem_wait_st();
   }
@@ -616,6 +761,25 @@ __global__ void __launch_bounds__(NTH, 1)
       tmem_scale64(tl + P2_TM_S + 64 * half, misc->c_renorm);
       cta_sync();
     }
+    if constexpr (SPLIT) {
+      if (ch > 0) {  // the A operand S~ = hi + lo (batch 2 is done: S~ is final)
+        if (!mbar_wait(mbar2, par ^ 1)) misc->failed = 1;
+        __syncwarp();
+        fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32], sh[16], sl[16];
+          GDN_TMEM_LD32(tl + P2_TM_S + 64 * half + 32 * h, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sh[j], sl[j]);
+          GDN_TMEM_ST16(tl + P2_TM_W + 32 * half + 16 * h, sh);
+          GDN_TMEM_ST16(tl + P2_TM_U + 32 * half + 16 * h, sl);
+        }
+        tmem_wait_st();
+        cta_sync();
+      }
+    }
     if (tid == 0 && more) {  // V rows are free: the next chunk's
       fence_async_smem();
       mbar_expect_tx(bar_v, kRowsBytes);
@@ -626,10 +790,21 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- 1. [X | Z] = S~ [K; Q]^T
     if (tid == ISSUER) {
       if (!mbar_wait(bar_kq, par)) misc->failed = 1;
+      if constexpr (SPLIT) {
 #pragma unroll
-      for (int ks = 0; ks < D / 8; ++ks)
-        mma_ts(tmem + tm_x, tmem + P2_TM_S + 8 * ks,
-               sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32), idesc_tf32(128, 128), ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t b = sbase + P2_KQ + (ks >> 2) * 32768 + (ks & 3) * 32;
+          const uint64_t bh = sdesc_sw128(b), bl = sdesc_sw128(b + 16384);
+          mma_ts<true>(tmem + tm_x, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 128), ks > 0);
+          mma_ts<true>(tmem + tm_x, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 128), 1);
+          mma_ts<true>(tmem + tm_x, tmem + P2_TM_U + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)
+          mma_ts(tmem + tm_x, tmem + P2_TM_S + 8 * ks,
+                 sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32), idesc_tf32(128, 128), ks > 0);
+      }
       mma_commit(mbar_xy);
     }
     // meanwhile warps 4-7: the previous chunk's outputs (every chunk but the
@@ -650,7 +825,7 @@ __global__ void __launch_bounds__(NTH, 1)
       }
     }
 
-    // ---- 2. W = V^T - X diag(c gamma), rounded to TF32, into TMEM
+    // ---- 2. W = V^T - X diag(c gamma), as an A operand, into TMEM
     if (!mbar_wait(mbar_xy, par)) misc->failed = 1;
     __syncwarp();
     fence_after();
@@ -659,9 +834,20 @@ __global__ void __launch_bounds__(NTH, 1)
       uint32_t xv[32];
       GDN_TMEM_LD32(tl + tm_x + 32 * half, xv);
       tmem_wait_ld();
+      if constexpr (SPLIT) {
+        uint32_t wh[16], wl[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) xv[j] = __float_as_uint(tf32_rn(fmaf(-wsc[j], __uint_as_float(xv[j]), vr[j])));
-      GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, xv);
+        for (int j = 0; j < 16; ++j)
+          split2(fmaf(-wsc[2 * j], __uint_as_float(xv[2 * j]), vr[2 * j]),
+                 fmaf(-wsc[2 * j + 1], __uint_as_float(xv[2 * j + 1]), vr[2 * j + 1]), wh[j], wl[j]);
+        GDN_TMEM_ST16(tl + P2_TM_W + 16 * half, wh);
+        GDN_TMEM_ST16(tl + P2_TM_W + 32 + 16 * half, wl);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          xv[j] = __float_as_uint(tf32_rn(fmaf(-wsc[j], __uint_as_float(xv[j]), vr[j])));
+        GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, xv);
+      }
       tmem_wait_st();
     }
     cta_sync();
@@ -673,10 +859,20 @@ __global__ void __launch_bounds__(NTH, 1)
     }
     if (tid == ISSUER) {
       if (!mbar_wait(bar_t, par)) misc->failed = 1;
+      if constexpr (SPLIT) {
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_U, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048), idesc_tf32(128, 64),
-               ks > 0);
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t bh = sdesc(sbase + P2_TPP + ks * 256, 1024), bl = sdesc(sbase + P2_TPP + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + P2_TM_U, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 64), ks > 0);
+          mma_ts<true>(tmem + P2_TM_U, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + P2_TM_U, tmem + P2_TM_W + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)
+          mma_ts(tmem + P2_TM_U, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_TPP + ks * 256, 2048),
+                 idesc_tf32(128, 64), ks > 0);
+      }
       mma_commit(mbar1);
     }
     // meanwhile warps 4-7: Y^T = Z diag(c q_scale gamma)
@@ -695,24 +891,39 @@ __global__ void __launch_bounds__(NTH, 1)
       tmem_wait_st();
     }
 
-    // ---- 4. U^T to TF32 (nearest) in place and U~^T over W; extreme gates:
-    // decay S now
+    // ---- 4. U^T and U~^T as A operands: TF32 (nearest) in place and over W,
+    // or split over X and W; extreme gates: decay S now
     if (!mbar_wait(mbar1, par)) misc->failed = 1;
     __syncwarp();
     fence_after();
     {
       const float *kts = sc + Q_KTS * 64 + 32 * half;
-      uint32_t uv[32], us[32];
+      uint32_t uv[32];
       GDN_TMEM_LD32(tl + P2_TM_U + 32 * half, uv);
       tmem_wait_ld();
+      if constexpr (SPLIT) {
+        uint32_t uh[16], ul[16], th[16], tlo[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float u = __uint_as_float(uv[j]);
-        uv[j] = __float_as_uint(tf32_rn(u));
-        us[j] = __float_as_uint(tf32_rn(u * kts[j]));
+        for (int j = 0; j < 16; ++j) {
+          const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+          split2(u0, u1, uh[j], ul[j]);
+          split2(u0 * kts[2 * j], u1 * kts[2 * j + 1], th[j], tlo[j]);
+        }
+        GDN_TMEM_ST16(tl + tm_x + 16 * half, uh);
+        GDN_TMEM_ST16(tl + tm_x + 32 + 16 * half, ul);
+        GDN_TMEM_ST16(tl + P2_TM_W + 16 * half, th);
+        GDN_TMEM_ST16(tl + P2_TM_W + 32 + 16 * half, tlo);
+      } else {
+        uint32_t us[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float u = __uint_as_float(uv[j]);
+          uv[j] = __float_as_uint(tf32_rn(u));
+          us[j] = __float_as_uint(tf32_rn(u * kts[j]));
+        }
+        GDN_TMEM_ST32(tl + P2_TM_U + 32 * half, uv);
+        GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, us);
       }
-      GDN_TMEM_ST32(tl + P2_TM_U + 32 * half, uv);
-      GDN_TMEM_ST32(tl + P2_TM_W + 32 * half, us);
       tmem_wait_st();
     }
     if (misc->do_fold) tmem_scale64(tl + P2_TM_S + 64 * half, misc->c_fold);
@@ -721,18 +932,36 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- 5. batch 2: Yt += Ut P'^T; S~ += U~t K^T.  Meanwhile warp 2 sets up
     // the next chunk's scalars and every thread takes the next chunk's V.
     if (tid == 0 && more) {  // U^T is done: T'' is free
-      load_tri(sbase + P2_TPP, wseq + static_cast<size_t>(ch + 1) * kWsFloats, bar_t);
+      load_image<SPLIT>(sbase + P2_TPP, wseq + static_cast<size_t>(ch + 1) * kWsFloats, bar_t);
     }
     if (tid == ISSUER) {
       if (!mbar_wait(bar_p, par)) misc->failed = 1;
       if (!mbar_wait(bar_kt, par)) misc->failed = 1;
+      if constexpr (SPLIT) {
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + tm_y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048), idesc_tf32(128, 64), 1);
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t bh = sdesc(sbase + P2_P + ks * 256, 1024), bl = sdesc(sbase + P2_P + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bh, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bl, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
+        }
 #pragma unroll
-      for (int ks = 0; ks < C / 8; ++ks)
-        mma_ts(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
-               idesc_tf32(128, 128), 1);
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t bh = sdesc(sbase + P2_KT + ks * 256, 1024), bl = sdesc(sbase + P2_KT + 16384 + ks * 256, 1024);
+          mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 128), 1);
+          mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 128), 1);
+          mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)
+          mma_ts(tmem + tm_y, tmem + P2_TM_U + 8 * ks, sdesc(sbase + P2_P + ks * 256, 2048), idesc_tf32(128, 64),
+                 1);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)
+          mma_ts(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, sdesc(sbase + P2_KT + ks * 256, 2048),
+                 idesc_tf32(128, 128), 1);
+      }
       mma_commit(mbar2);
     }
     ++n_mma;
@@ -755,7 +984,7 @@ __global__ void __launch_bounds__(NTH, 1)
     if (tid == 0) {  // batch 2 done: P' and K^T are free for the next chunk's
       if (!mbar_wait(mbar2, par)) misc->failed = 1;
       if (more) {
-        load_tri(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, bar_p);
+        load_image<SPLIT>(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, bar_p);
         mbar_expect_tx(bar_kt, kRowsBytes);
         bulk_load(sbase + P2_KT, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats + 16384, kRowsBytes, bar_kt);
       }
@@ -857,28 +1086,7 @@ cudaError_t rows_map(CUtensorMap *tm, const void *base, uint32_t heads, uint32_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// How many segments each (seq, value head) chain of the state pass is cut
-// into.  The state pass runs one CTA per SM (its shared memory and tensor
-// memory fill one), so `heads` chains of `nchunks` chunks on `sms` SMs take
-// ceil(heads / sms) rounds of the whole chain.  Cut into m segments, run in
-// ceil(m heads / sms) launches of ceil(nchunks / m) chunks each, with about
-// kRestartChunks chunks' worth of extra time per launch (the launch, the
-// state load and the first chunk's copies).  A segment must land in a later
-// launch than the one before it, which holds when heads >= sms.
-constexpr double kRestartChunks = 1.5;
-uint32_t state_segments(unsigned long long heads, uint32_t nchunks, unsigned long long sms) {
-  auto cost = [&](uint32_t m) {
-    const unsigned long long len = (nchunks + m - 1) / m, segs = (nchunks + len - 1) / len;
-    return static_cast<double>((segs * heads + sms - 1) / sms) * (static_cast<double>(len) + kRestartChunks);
-  };
-  uint32_t best = 1;
-  if (heads < sms) return best;
-  for (uint32_t m = 2; m <= 8 && m <= nchunks; ++m)
-    if (cost(m) < cost(best)) best = m;
-  return best;
-}
-
-template <bool DA>
+template <bool DA, bool SPLIT>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
   const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
@@ -914,7 +1122,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   pa.g = p.g; pa.beta = p.beta; pa.ws = ws; pa.ws_k = ws_k;
   pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = group; pa.hpc = hpc; pa.parts = parts;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
-  auto prep = gdn_chunk_prep_kernel<DA>;
+  auto prep = gdn_chunk_prep_kernel<DA, SPLIT>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p1_smem(hpc)));
   if (e != cudaSuccess) return e;
   prep<<<static_cast<unsigned>(prep_blocks), NTH, p1_smem(hpc), stream>>>(pa, tm_k, tm_q);
@@ -931,7 +1139,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t segs = state_segments(heads, nchunks, want);
   sa.seg_len = (nchunks + segs - 1) / segs;
   const unsigned long long tasks2 = heads * ((nchunks + sa.seg_len - 1) / sa.seg_len);
-  auto state = gdn_chunk_state_kernel<DA>;
+  auto state = gdn_chunk_state_kernel<DA, SPLIT>;
   e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
   if (e != cudaSuccess) return e;
   // one launch per group of up to `want` (one CTA per SM) segments, in the
@@ -962,7 +1170,11 @@ size_t chunked_split_workspace_bytes(const Problem &p) {
 
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {
   if (!chunked_split_supported(p)) return cudaErrorInvalidValue;
-  return p.decay_after ? launch_split<true>(p, workspace, stream) : launch_split<false>(p, workspace, stream);
+  if (p.tf32)
+    return p.decay_after ? launch_split<true, false>(p, workspace, stream)
+                         : launch_split<false, false>(p, workspace, stream);
+  return p.decay_after ? launch_split<true, true>(p, workspace, stream)
+                       : launch_split<false, true>(p, workspace, stream);
 }
 
 // ---------------------------------------------------------------- fixed scratch

@@ -25,6 +25,11 @@ gdn_status fail(gdn_status st, const char *fmt, ...) {
 
 // Largest n_tokens that runs on the decode launch shape under GDN_PATH_AUTO.
 constexpr uint32_t kDecodeMaxTokens = 16;
+// Shortest window GDN_PATH_AUTO runs on the chunked form where it covers
+// the call.  Measured on GB300 for 16 to 256 (seq, value head) chains: the
+// one-pass and two-pass forms overtake the scan between 32 and 64 tokens
+// (at 64 tokens, 4 x 48 chains: 41.7 / 42.6 against 51.9 us).
+constexpr uint32_t kChunkedMinTokens = 64;
 // Upper bound on any buffer's element count (keeps byte counts far from
 // 64-bit overflow).
 constexpr unsigned long long kMaxElems = 1ull << 60;
@@ -93,8 +98,7 @@ gdn_status decode_params(const uint32_t *params, size_t n_params, Decoded *d) {
   if (flags & ~(GDN_FLAG_DECAY_AFTER | GDN_FLAG_KHEAD_DIV | GDN_PATH_MASK))
     return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: unknown flag bits 0x%x in params[6]", flags);
   d->path = (flags & GDN_PATH_MASK) >> GDN_PATH_SHIFT;
-  if (d->path > GDN_PATH_CHUNKED)
-    return fail(GDN_ERR_INVALID_ARGUMENT, "gdn: path %u in params[6] does not exist", d->path);
+  p.tf32 = d->path == GDN_PATH_CHUNKED_TF32;
   p.decay_after = (flags & GDN_FLAG_DECAY_AFTER) != 0;
   p.khead_div = (flags & GDN_FLAG_KHEAD_DIV) != 0;
   if (params[8] == 0) {
@@ -114,10 +118,10 @@ gdn_status decode_params(const uint32_t *params, size_t n_params, Decoded *d) {
 
 enum class Path { kDecode, kScan, kChunked };
 
-const char *path_name(Path path, bool capture) {
+const char *path_name(Path path, bool capture, bool tf32) {
   switch (path) {
     case Path::kDecode: return capture ? "token_loop_decode_capture" : "token_loop_decode";
-    case Path::kChunked: return "chunked";
+    case Path::kChunked: return tf32 ? "chunked_tf32" : "chunked";
     default: return capture ? "scan_capture" : "scan";
   }
 }
@@ -130,6 +134,7 @@ gdn_status choose_path(const Decoded &d, bool capture, bool bf16, Path *out) {
       *out = Path::kScan;
       return GDN_OK;
     case GDN_PATH_CHUNKED:
+    case GDN_PATH_CHUNKED_TF32:
       if (capture)
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path keeps no per-token state (capture)");
       if (d.prob.dk != 128 || d.prob.dv != 128)
@@ -139,9 +144,21 @@ gdn_status choose_path(const Decoded &d, bool capture, bool bf16, Path *out) {
       *out = Path::kChunked;
       return GDN_OK;
     default:
-      *out = d.prob.nt <= kDecodeMaxTokens ? Path::kDecode : Path::kScan;
+      if (d.prob.nt <= kDecodeMaxTokens)
+        *out = Path::kDecode;
+      else if (!capture && !bf16 && d.prob.dk == 128 && d.prob.dv == 128 && d.prob.nt >= kChunkedMinTokens)
+        *out = Path::kChunked;
+      else
+        *out = Path::kScan;
       return GDN_OK;
   }
+}
+
+// The automatic choice falls back to the scan where the chunked form cannot
+// take v (rows copied 16 bytes at a time); a forced chunked path is refused
+// instead (below).
+Path fit_auto(const Decoded &d, Path path, const void *v) {
+  return d.path == GDN_PATH_AUTO && path == Path::kChunked && !aligned(v, 16) ? Path::kScan : path;
 }
 
 // The buffers of one call, in slot order; q, k, v and output hold f32 or bf16.
@@ -257,6 +274,7 @@ gdn_status run(const Buffers &b, const uint32_t *params, size_t n_params, size_t
   Path path;
   st = choose_path(d, with_capture, bf16, &path);
   if (st != GDN_OK) return st;
+  path = fit_auto(d, path, b.v);
   if (path == Path::kChunked && !aligned(b.v, 16))
     return fail(GDN_ERR_INVALID_ARGUMENT,
                 "gdn: the chunked path needs v 16-byte aligned (its rows are copied 16 bytes at a time)");
@@ -307,6 +325,8 @@ gdn_status run_layers(const L *layers, size_t n_layers, const uint32_t *params, 
   Path path;
   st = choose_path(d, cap, bf16, &path);
   if (st != GDN_OK) return st;
+  for (size_t i = 0; i < n_layers; ++i)
+    path = fit_auto(d, path, layers[i].v);
   for (size_t i = 0; i < n_layers; ++i) {
     st = check_buffers(d, buffers_of(layers[i], cap), state_capture_elems, cap, bf16);
     if (st != GDN_OK) {
@@ -394,10 +414,10 @@ gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const flo
   Decoded d;
   gdn_status st = decode_params(params, n_params, &d);
   if (st != GDN_OK) return st;
-  if (d.path != GDN_PATH_AUTO && d.path != GDN_PATH_CHUNKED)
+  if (d.path == GDN_PATH_SCAN)
     return fail(GDN_ERR_INVALID_ARGUMENT,
-                "gdn: gdn_forward_chunked_noalloc runs the chunked path only (path bits 0 or 2)");
-  d.path = GDN_PATH_CHUNKED;
+                "gdn: gdn_forward_chunked_noalloc runs the chunked path only (path bits 0, 2 or 3)");
+  if (d.path == GDN_PATH_AUTO) d.path = GDN_PATH_CHUNKED;
   const Buffers b{q, k, v, g, beta, state_in, output, state_out, nullptr};
   st = check_buffers(d, b, 0, false, false);
   if (st != GDN_OK) return st;
@@ -534,7 +554,7 @@ gdn_status gdn_path_name(const uint32_t *params, size_t n_params, int capture,
   Path path;
   st = choose_path(d, capture != 0, false, &path);
   if (st != GDN_OK) return st;
-  *name = path_name(path, capture != 0);
+  *name = path_name(path, capture != 0, d.prob.tf32);
   return GDN_OK;
 }
 

@@ -20,6 +20,7 @@ struct Problem {
   bool decay_after;
   bool khead_div;
   bool io_bf16;
+  bool tf32;  // chunked forms: TF32 operands instead of split bf16
   float q_scale;
 };
 

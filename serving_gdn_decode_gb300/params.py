@@ -17,7 +17,8 @@ bits, with 0 selecting the pages' kernel behaviour, and keeps slot 7 reserved
 * bit 1 -- ``k_head = v_head / (n_v_heads / n_k_heads)`` (the "GQA broadcast"
   section of ``gated_delta_net.rs``) instead of ``v_head % n_k_heads`` (the
   capture kernel);
-* bits 2-3 -- path choice: 0 automatic, 1 token-loop scan, 2 chunked prefill.
+* bits 2-3 -- path choice: 0 automatic, 1 token-loop scan, 2 chunked prefill
+  (split-bf16 tensor-core operands), 3 chunked prefill with TF32 operands.
 
 This module only packs numbers; it holds none of the recurrence.
 """
@@ -32,6 +33,7 @@ FLAG_KHEAD_DIV = 0x2
 PATH_AUTO = 0
 PATH_SCAN = 1
 PATH_CHUNKED = 2
+PATH_CHUNKED_TF32 = 3
 PATH_SHIFT = 2
 
 

@@ -8,6 +8,16 @@ Tolerances (the parity bar):
   the ragged-chunk tests): ||gpu - ref||_2 / ||ref||_2 <= 1e-3 for output,
   state_out and state_capture, and, as a guard against a few wild elements
   hiding in the L2 norm, max|gpu - ref| <= 1e-2 * max|ref|.
+
+The split-bf16 chunked form (path bits 2, and the automatic choice for long
+D = 128 windows) is held, beyond that bar, to rel-L2 <= SPLIT_RELL2_TOL: each
+of its tensor-core products is three bf16 products of split operands
+(x = hi + lo, |x - hi - lo| <= 2^-18 |x|, the dropped lo*lo term <= 2^-18
+of the product), about 2^-16 of each term, and a chunk chains four such
+products (X, U, Y, S), so about 5e-5 at worst; it measures 7.6e-6 on the
+long-prefill workload.  States that grow (negative gates; e^20 over 4096
+tokens) amplify the state's error, hence SPLIT_RELL2_TOL_GROWING (measured
+3.5e-5).
 """
 from __future__ import annotations
 
@@ -20,6 +30,8 @@ RELL2_TOL = 1e-3
 
 
 LONG_MAXABS_GUARD = 1e-2
+SPLIT_RELL2_TOL = 5e-5
+SPLIT_RELL2_TOL_GROWING = 2e-4
 
 
 def to_dev(x):
@@ -96,6 +108,14 @@ def assert_close(name, gpu, ref, n_tokens):
         e = max_abs_rel(gpu, ref)
         _record(name, "max-abs", e, MAXABS_TOL)
         assert e <= MAXABS_TOL, f"{name}: max-abs/max|ref| {e:.3e} > {MAXABS_TOL}"
+    return e
+
+
+def assert_rel_l2(name, gpu, ref, tol):
+    """rel-L2 <= tol (a tighter bar on top of assert_close)."""
+    e = rel_l2(gpu, ref)
+    _record(name, "rel-L2", e, tol)
+    assert e <= tol, f"{name}: rel-L2 {e:.3e} > {tol}"
     return e
 
 

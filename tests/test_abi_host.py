@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 from serving_gdn_decode_gb300 import _native as nat
-from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN, pack_params
+from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_CHUNKED_TF32, PATH_SCAN, pack_params
 from serving_gdn_decode_gb300.workloads import WORKLOADS, Workload
 
 
@@ -71,11 +71,18 @@ def test_path_choice(L):
     assert _path(WORKLOADS["decode"].params()) == "token_loop_decode"
     assert _path(WORKLOADS["decode_wide_gqa"].params(khead_div=True)) == "token_loop_decode"
     assert _path(WORKLOADS["spec_capture"].params(), True) == "token_loop_decode_capture"
-    assert _path(WORKLOADS["long_prefill"].params()) == "scan"
+    assert _path(WORKLOADS["long_prefill"].params()) == "chunked"
     assert _path(WORKLOADS["long_prefill"].params(path=PATH_SCAN)) == "scan"
+    assert _path(WORKLOADS["long_prefill"].params(path=PATH_CHUNKED_TF32)) == "chunked_tf32"
     assert _path(WORKLOADS["tiny"].params(path=PATH_SCAN), True) == "scan_capture"
     assert _path(WORKLOADS["decode"].with_(n_tokens=16).params()) == "token_loop_decode"
     assert _path(WORKLOADS["decode"].with_(n_tokens=17).params()) == "scan"
+    # the automatic choice takes the chunked form from 64 tokens on, where it covers the shape
+    assert _path(WORKLOADS["decode"].with_(n_tokens=63).params()) == "scan"
+    assert _path(WORKLOADS["decode"].with_(n_tokens=64).params()) == "chunked"
+    assert _path(WORKLOADS["long_prefill"].params(), True) == "scan_capture"
+    assert _path(pack_params(64, 64, 2, 4, 4096, 1)) == "scan"
+    assert _path(pack_params(128, 64, 2, 4, 4096, 1)) == "scan"
 
 
 @pytest.mark.parametrize("mutate,status", [
@@ -93,7 +100,6 @@ def test_path_choice(L):
     (lambda p: _set(p, 1, 126), nat.GDN_ERR_INVALID_ARGUMENT),       # D_v % (D_k/32) != 0
     (lambda p: _set(p, 7, 1), nat.GDN_ERR_INVALID_ARGUMENT),         # reserved slot
     (lambda p: _set(p, 6, 0x10), nat.GDN_ERR_INVALID_ARGUMENT),      # unknown flag bit
-    (lambda p: _set(p, 6, 0xC), nat.GDN_ERR_INVALID_ARGUMENT),       # path 3
 ])
 def test_params_rejected(L, mutate, status):
     p = mutate(WORKLOADS["decode"].params())
@@ -385,7 +391,12 @@ def test_workspace_size_values(L):
     w = WORKLOADS["long_prefill"].with_(n_tokens=200, n_seqs=3)
     # per (seq, chunk): 32 KB per value head (48) + 96 KB per key head (16); 3 seqs x 4 chunks
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == 3 * 4 * (48 * 32768 + 16 * 98304)
-    assert nat.gdn_workspace_size(w.params()) == 0                   # auto: scan
+    # auto: the chunked form from 64 tokens on (two passes given a workspace), else the scan
+    assert nat.gdn_workspace_size(w.params()) == nat.gdn_workspace_size(w.params(path=PATH_CHUNKED))
+    assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED_TF32)) == \
+        nat.gdn_workspace_size(w.params(path=PATH_CHUNKED))       # same layout sizes
+    assert nat.gdn_workspace_size(w.with_(n_tokens=63).params()) == 0
+    assert nat.gdn_workspace_size(w.params(path=PATH_SCAN)) == 0
     assert nat.gdn_workspace_size(SMALL.params()) == 0               # decode
     with pytest.raises(nat.GdnError):
         nat.gdn_workspace_size(SMALL.params()[:8])
@@ -408,7 +419,9 @@ def test_workspace_checks(L):
     # a good workspace passes every host check (the launch then fails here for want of a device)
     assert nat.forward_ws_raw(*args, p, ws, need) == nat.GDN_ERR_CUDA
     # off the chunked path the workspace is not needed
-    assert nat.forward_ws_raw(*args, w.params(), 0, 0) == nat.GDN_ERR_CUDA
+    assert nat.forward_ws_raw(*args, w.params(path=PATH_SCAN), 0, 0) == nat.GDN_ERR_CUDA
+    # the automatic choice at 100 tokens is the chunked form, which needs it
+    assert nat.forward_ws_raw(*args, w.params(), 0, need) == nat.GDN_ERR_INVALID_ARGUMENT
 
 
 @no_device
@@ -460,10 +473,13 @@ def test_chunked_path_needs_aligned_v(L):
     assert f.call(params=w.params(path=PATH_CHUNKED), v=v4) == nat.GDN_ERR_INVALID_ARGUMENT
     assert "16-byte" in nat.gdn_last_error()
     assert f.call(params=w.params(path=PATH_SCAN), v=v4) == nat.GDN_ERR_CUDA  # host checks pass
+    # the automatic choice falls back to the scan for such a v (host checks pass)
+    assert f.call(params=w.params(), v=v4) == nat.GDN_ERR_CUDA
     rows = _layer_rows(2)
     rows[1][2] += 4
     assert nat.forward_layers_raw(rows, w.params(path=PATH_CHUNKED)) == nat.GDN_ERR_INVALID_ARGUMENT
     assert "layer 1" in nat.gdn_last_error() and "16-byte" in nat.gdn_last_error()
+    assert nat.forward_layers_raw(rows, w.params()) == nat.GDN_ERR_CUDA  # auto: the scan for every layer
 
 
 @no_device

@@ -1,20 +1,25 @@
-"""GPU parity of the chunked tensor-core prefill path (forced with path bits
-= 2) against the oracle, in both forms: single pass (gdn_forward) and two
-passes over a workspace (gdn_forward_ws; ``split``).
+"""GPU parity of the chunked tensor-core prefill path against the oracle, in
+both forms -- single pass (gdn_forward) and two passes over a workspace
+(gdn_forward_ws; ``split``) -- and both operand precisions: split bf16 (path
+bits 2, also the automatic choice for long D = 128 windows) and TF32 (path
+bits 3).
 
 The chunked path rewrites the recurrence in matrix form over 64-token chunks
-and runs its products on tcgen05 with TF32 operands, so it is held to the
-long-window bar (rel-L2 <= 1e-3, plus the max-abs guard) and is used for
-windows of more than 8 tokens only.  Cases: single partial chunk, exact
-chunks, ragged tails, both decay orders and k_head mappings, gates that make
-the kernel fold its lazy scale (large, negative, underflowing), chaining
-calls, and the long-prefill workload at full size on sampled heads.
+and runs its products on tcgen05.  Split-bf16 operands take the standard
+bars plus rel-L2 <= SPLIT_RELL2_TOL (gpu_helpers); TF32 operands take the
+long-window bar (rel-L2 <= 1e-3, plus the max-abs guard) at every window
+length.  Cases: single partial chunk, exact chunks, ragged tails, both decay
+orders and k_head mappings, gates that make the kernel fold its lazy scale
+(large, negative, underflowing), chaining calls, the long-prefill workload at
+full size on sampled heads, and strongly growing states over the full 4096
+tokens (split operands).
 """
 import numpy as np
 import pytest
 
-from gpu_helpers import assert_close, gather_heads, run_gpu, sample_heads, to_dev
-from serving_gdn_decode_gb300.params import PATH_CHUNKED
+from gpu_helpers import (SPLIT_RELL2_TOL, SPLIT_RELL2_TOL_GROWING, assert_close, assert_rel_l2, gather_heads,
+                         run_gpu, sample_heads, to_dev)
+from serving_gdn_decode_gb300.params import PATH_AUTO, PATH_CHUNKED, PATH_CHUNKED_TF32
 from serving_gdn_decode_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -42,33 +47,46 @@ SHAPES = [  # (n_k, n_v, n_tokens, n_seqs)
 
 
 SPLIT = pytest.mark.parametrize("split", [False, True], ids=["one-pass", "two-pass"])
+PREC = pytest.mark.parametrize("path", [PATH_CHUNKED, PATH_CHUNKED_TF32], ids=["bf16x3", "tf32"])
+
+
+def check(name, gpu, ref, n_tokens, path, tol=SPLIT_RELL2_TOL):
+    """The bar of the operand precision: TF32 takes the long-window bar at
+    every window length (a few 1e-4 from its rounding); split bf16 takes the
+    standard bar for the window and rel-L2 <= tol."""
+    if path == PATH_CHUNKED_TF32:
+        assert_close(name, gpu, ref, max(n_tokens, 9))
+    else:
+        assert_close(name, gpu, ref, n_tokens)
+        assert_rel_l2(name, gpu, ref, tol)
 
 
 @SPLIT
+@PREC
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
 @pytest.mark.parametrize("flags", [dict(), dict(decay_after=True), dict(khead_div=True),
                                    dict(decay_after=True, khead_div=True)],
                          ids=["first-mod", "after-mod", "first-div", "after-div"])
-def test_chunked_vs_oracle(torch, oracle_mod, shape, flags, split):
+def test_chunked_vs_oracle(torch, oracle_mod, shape, flags, split, path):
     nk, nv, nt, ns = shape
     w = Workload("chunked", 128, 128, nk, nv, nt, ns)
     x = make_inputs(w, 51)
-    p = w.params(path=PATH_CHUNKED, **flags)
+    p = w.params(path=path, **flags)
     out, st, _ = run_gpu(w, x, p, workspace=split)
     ro, rs, _ = oracle_mod.forward(p, **x)
-    # Windows of 8 tokens or fewer take the long-window bar (rel-L2 1e-3, not
-    # max-abs 1e-4) here: the chunked path computes its products with TF32
-    # operands, so it is held to the bar of the long prefills it exists for.
-    # The automatic path never sends such windows to it (they run the FP32
-    # token-loop kernel, which the short-window bar is checked on).
-    assert_close("output", out, ro, max(nt, 9))
-    assert_close("state_out", st, rs, max(nt, 9))
+    # With TF32 operands windows of 8 tokens or fewer take the long-window
+    # bar (rel-L2 1e-3, not max-abs 1e-4): that path is held to the bar of
+    # the long prefills it exists for.  The automatic path never sends such
+    # windows to the chunked form (they run the FP32 token-loop kernel).
+    check("output", out, ro, nt, path)
+    check("state_out", st, rs, nt, path)
 
 
 @SPLIT
+@PREC
 @pytest.mark.parametrize("gate", ["large", "negative", "mixed", "zero"])
 @pytest.mark.parametrize("decay_after", [False, True])
-def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after, split):
+def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after, split, path):
     w = Workload("gates", 128, 128, 2, 4, 300, 2)
     x = make_inputs(w, 53)
     rng = np.random.default_rng(55)
@@ -76,8 +94,8 @@ def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after, split):
         x["g"] = rng.uniform(0.0, 4.0, w.scalar_elems).astype(np.float32)
     elif gate == "negative":
         # alpha > 1: the state grows (about e^1.5 over the window); TF32
-        # rounding errors grow with it, so the growth is kept mild here (the
-        # FP32 scan path is the one for strongly growing states)
+        # rounding errors grow with it, so the growth is kept mild here
+        # (test_long_prefill_growing_state takes split operands to e^20)
         x["g"] = rng.uniform(-0.01, 0.0, w.scalar_elems).astype(np.float32)
     elif gate == "mixed":
         g = rng.uniform(0.0, 0.5, w.scalar_elems).astype(np.float32)
@@ -86,11 +104,11 @@ def test_chunked_gates_vs_oracle(torch, oracle_mod, gate, decay_after, split):
         x["g"] = g
     else:
         x["g"] = np.zeros(w.scalar_elems, dtype=np.float32)
-    p = w.params(path=PATH_CHUNKED, decay_after=decay_after)
+    p = w.params(path=path, decay_after=decay_after)
     out, st, _ = run_gpu(w, x, p, workspace=split)
     ro, rs, _ = oracle_mod.forward(p, **x)
-    assert_close("output", out, ro, w.n_tokens)
-    assert_close("state_out", st, rs, w.n_tokens)
+    check("output", out, ro, w.n_tokens, path)
+    check("state_out", st, rs, w.n_tokens, path)
 
 
 def test_chunked_chaining(torch):
@@ -115,18 +133,56 @@ def test_chunked_chaining(torch):
 
 
 @SPLIT
+@PREC
 @pytest.mark.parametrize("flags", [dict(), dict(decay_after=True, khead_div=True)],
                          ids=["first-mod", "after-div"])
-def test_long_prefill_chunked_sampled(torch, oracle_mod, flags, split):
+def test_long_prefill_chunked_sampled(torch, oracle_mod, flags, split, path):
     w = WORKLOADS["long_prefill"]
     x = make_inputs(w, 0)
-    p = w.params(path=PATH_CHUNKED, **flags)
+    p = w.params(path=path, **flags)
     out, st, _ = run_gpu(w, x, p, workspace=split)
     heads = sample_heads(w, 8, seed=3)
     ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
     go, gs, _ = gather_heads(w, out, st, None, heads)
-    assert_close("output", go, ro, w.n_tokens)
-    assert_close("state_out", gs, rs, w.n_tokens)
+    check("output", go, ro, w.n_tokens, path)
+    check("state_out", gs, rs, w.n_tokens, path)
+
+
+@SPLIT
+@pytest.mark.parametrize("gate", ["negative", "zero"])
+def test_long_prefill_growing_state(torch, oracle_mod, split, gate):
+    """The long-prefill workload over its full 4096 tokens with gates that
+    never decay the state (g = 0) or make it grow (g in [-0.01, 0]: about
+    e^20 over the window), split-bf16 operands, sampled heads.  (TF32
+    operands reach about 3e-3 here, over the 1e-3 bar.)"""
+    w = WORKLOADS["long_prefill"]
+    x = make_inputs(w, 0)
+    rng = np.random.default_rng(67)
+    x["g"] = (rng.uniform(-0.01, 0.0, w.scalar_elems).astype(np.float32) if gate == "negative"
+              else np.zeros(w.scalar_elems, dtype=np.float32))
+    p = w.params(path=PATH_CHUNKED)
+    out, st, _ = run_gpu(w, x, p, workspace=split)
+    heads = sample_heads(w, 6, seed=7)
+    ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
+    go, gs, _ = gather_heads(w, out, st, None, heads)
+    tol = SPLIT_RELL2_TOL_GROWING if gate == "negative" else SPLIT_RELL2_TOL
+    check("output", go, ro, w.n_tokens, PATH_CHUNKED, tol)
+    check("state_out", gs, rs, w.n_tokens, PATH_CHUNKED, tol)
+
+
+def test_auto_is_the_split_chunked_form(torch):
+    """A long D = 128 window under the automatic choice runs the split-bf16
+    chunked form: one pass through gdn_forward, two through gdn_forward_ws,
+    bit for bit the results of forcing path bits 2."""
+    from serving_gdn_decode_gb300 import _native as nat
+    w = Workload("auto", 128, 128, 2, 6, 200, 2)
+    x = make_inputs(w, 69)
+    assert nat.gdn_path_name(w.params()) == "chunked"
+    for ws in (False, True):
+        a = run_gpu(w, x, w.params(), workspace=ws)
+        b = run_gpu(w, x, w.params(path=PATH_CHUNKED), workspace=ws)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
 
 
 def test_two_pass_chaining_and_workspace_reuse(torch):
@@ -170,25 +226,27 @@ def test_two_pass_workspace_size(torch):
     w = WORKLOADS["long_prefill"]
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == \
         w.n_seqs * (w.n_tokens // 64) * (w.n_v_heads * 32768 + w.n_k_heads * 98304)
-    assert nat.gdn_workspace_size(w.params()) == 0
+    assert nat.gdn_workspace_size(w.params()) == nat.gdn_workspace_size(w.params(path=PATH_CHUNKED))
 
 
-def test_two_pass_state_segments(torch, oracle_mod):
-    """More (seq, value head) chains than SMs: the state pass cuts each chain
-    into segments run by consecutive launches, the state handed on through
-    state_out.  160 chains of 16 chunks (1000 tokens, a ragged last chunk)
-    take four segments on a 152-SM GPU; sampled heads against the oracle,
-    both decay orders, and in place (state_in == state_out) bit for bit."""
+@SPLIT
+def test_state_segments(torch, oracle_mod, split):
+    """More (seq, value head) chains than SMs: the one-pass kernel and the
+    two-pass state pass cut each chain into segments run by consecutive
+    launches, the state handed on through state_out.  160 chains of 16
+    chunks (1000 tokens, a ragged last chunk) take several segments on a
+    152-SM GPU; sampled heads against the oracle, both decay orders, and in
+    place (state_in == state_out) bit for bit."""
     w = Workload("segments", 128, 128, 2, 40, 1000, 4)
     x = make_inputs(w, 65)
     heads = sample_heads(w, 8, seed=5)
     for flags in (dict(), dict(decay_after=True, khead_div=True)):
         p = w.params(path=PATH_CHUNKED, **flags)
-        out, st, _ = run_gpu(w, x, p, workspace=True)
+        out, st, _ = run_gpu(w, x, p, workspace=split)
         ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
         go, gs, _ = gather_heads(w, out, st, None, heads)
-        assert_close("output", go, ro, w.n_tokens)
-        assert_close("state_out", gs, rs, w.n_tokens)
-        out2, st2, _ = run_gpu(w, x, p, workspace=True, in_place=True)
+        check("output", go, ro, w.n_tokens, PATH_CHUNKED)
+        check("state_out", gs, rs, w.n_tokens, PATH_CHUNKED)
+        out2, st2, _ = run_gpu(w, x, p, workspace=split, in_place=True)
         np.testing.assert_array_equal(out2, out)
         np.testing.assert_array_equal(st2, st)

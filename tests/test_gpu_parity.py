@@ -9,7 +9,9 @@ element by element.
 import numpy as np
 import pytest
 
-from gpu_helpers import assert_close, gather_heads, run_gpu, sample_heads, to_dev
+from gpu_helpers import (SPLIT_RELL2_TOL, assert_close, assert_rel_l2, gather_heads, run_gpu, sample_heads,
+                         to_dev)
+from serving_gdn_decode_gb300.params import PATH_AUTO, PATH_SCAN
 from serving_gdn_decode_gb300.workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -102,12 +104,18 @@ def test_spec_capture_full(cuda, oracle_mod, flags):
 
 
 @pytest.mark.parametrize("flags", FLAGS, ids=FLAG_IDS)
-def test_long_prefill_sampled(cuda, oracle_mod, flags):
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_SCAN], ids=["auto", "scan"])
+def test_long_prefill_sampled(cuda, oracle_mod, flags, path):
+    """The automatic choice (the split-bf16 chunked form, one pass) and the
+    FP32 scan forced, on sampled heads at full size."""
     w, x, d = _inputs("long_prefill")
-    p = w.params(**flags)
+    p = w.params(path=path, **flags)
     out, st, _ = run_gpu(w, x, p, dev=d)
     heads = sample_heads(w, 8, seed=3)
     ro, rs, _ = oracle_mod.forward_heads(p, **x, heads=heads)
     go, gs, _ = gather_heads(w, out, st, None, heads)
     assert_close("output", go, ro, w.n_tokens)
     assert_close("state_out", gs, rs, w.n_tokens)
+    if path == PATH_AUTO:
+        assert_rel_l2("output", go, ro, SPLIT_RELL2_TOL)
+        assert_rel_l2("state_out", gs, rs, SPLIT_RELL2_TOL)
