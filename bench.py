@@ -103,9 +103,11 @@ def kernel_traffic(kernel: str, n_tokens: int | None = None):
 
 # ---------------------------------------------------------------- prefill rooflines
 
-def chunked_mma_flops(w, two_pass: bool) -> int:
+def chunked_mma_flops(w, two_pass: bool, split: bool = False) -> int:
     """Tensor-core flops the chunked prefill issues per call (2 per MAC of
-    every tcgen05 product, full 64-token chunks even for a ragged last one).
+    every tcgen05 product, full 64-token chunks even for a ragged last one;
+    with split-bf16 operands every product runs as three bf16 MMAs, so three
+    times the TF32 form's count).
     Per (seq, value head, chunk) the one-pass form runs the Gram [K;Q]K^T
     (M 128, N 64, K 128), V^T T''^T, X = S K^T, X(-T')^T, S Q'^T, U^T P'^T
     (each M 128, N 64; K 64, 128, 64, 128, 64) and S += U^T K'^T (M 128,
@@ -113,15 +115,16 @@ def chunked_mma_flops(w, two_pass: bool) -> int:
     chunk) in its chunk pass, and per (seq, value head, chunk) [X | Z] =
     S [K; Q]^T (M 128, N 128, K 128), U^T = W T''^T and U^T P'^T (M 128, N 64,
     K 64) and S += U~^T K^T (M 128, N 128, K 64)."""
+    terms = 3 if split else 1
     nch = -(-w.n_tokens // 64)
     mm = lambda m, n, k: 2 * m * n * k  # noqa: E731
     gram = mm(128, 64, 128)
     if two_pass:
         per_head = mm(128, 128, 128) + 2 * mm(128, 64, 64) + mm(128, 128, 64)
-        return nch * w.n_seqs * (w.n_v_heads * per_head + w.n_k_heads * gram)
+        return terms * nch * w.n_seqs * (w.n_v_heads * per_head + w.n_k_heads * gram)
     per_head = gram + mm(128, 64, 64) + mm(128, 64, 128) + mm(128, 64, 64) + mm(128, 64, 128) \
         + mm(128, 64, 64) + mm(128, 128, 64)
-    return nch * w.n_seqs * w.n_v_heads * per_head
+    return terms * nch * w.n_seqs * w.n_v_heads * per_head
 
 
 def scan_executed_flops(w) -> int:
@@ -135,7 +138,8 @@ def scan_executed_flops(w) -> int:
 def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, clk: dict | None,
                      act: str = "f32") -> dict:
     """Compute roofline of one prefill call.  ``kind``: "scan" (FP32 CUDA
-    cores), "chunked" (one-pass) or "chunked_two_pass" (tensor cores, TF32)."""
+    cores), "chunked" (one-pass) or "chunked_two_pass" (tensor cores,
+    split-bf16 operands), each chunked kind with "_tf32" for TF32 operands."""
     mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
     mhz_src = "median SM clock sampled in the timed region" if (clk or {}).get("sm_mhz") \
         else "maximum SM clock (no clock samples)"
@@ -151,14 +155,23 @@ def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, 
                    flops_per_call=ex, flops_counted="executed: 3 FMAs per state cell per token")
         traffic_key = "scan"
     else:
-        tf32_peak = float(peaks["bf16_tflops"]) * 0.5
-        ex = chunked_mma_flops(w, kind == "chunked_two_pass")
-        out.update(bound="tensor", achieved=round(ex / seconds / 1e12, 2), peak=round(tf32_peak, 1),
-                   peak_kind=f"of {peak_kind}: bf16 dense tensor peak "
-                             f"({'bf16_tflops, MEASURED_PEAKS.json' if peak_kind == 'measured' else 'recipe fallback'})"
-                             f" x 1/2, the nominal tf32:bf16 rate ratio",
-                   flops_per_call=ex, flops_counted="tcgen05 kind::tf32 MMA flops issued per call")
-        traffic_key = "chunked_split" if kind == "chunked_two_pass" else "chunked"
+        tf32 = kind.endswith("_tf32")
+        two = kind.startswith("chunked_two_pass")
+        src = "bf16_tflops, MEASURED_PEAKS.json" if peak_kind == "measured" else "recipe fallback"
+        ex = chunked_mma_flops(w, two, split=not tf32)
+        if tf32:
+            peak = float(peaks["bf16_tflops"]) * 0.5
+            out.update(peak_kind=f"of {peak_kind}: bf16 dense tensor peak ({src}) x 1/2, the nominal "
+                                 "tf32:bf16 rate ratio",
+                       flops_counted="tcgen05 kind::tf32 MMA flops issued per call")
+        else:
+            peak = float(peaks["bf16_tflops"])
+            out.update(peak_kind=f"of {peak_kind}: bf16 dense tensor peak ({src})",
+                       flops_counted="tcgen05 kind::f16 (bf16) MMA flops issued per call: three per "
+                                     "product of split operands")
+        out.update(bound="tensor", achieved=round(ex / seconds / 1e12, 2), peak=round(peak, 1),
+                   flops_per_call=ex)
+        traffic_key = ("chunked_split" if two else "chunked") + ("_tf32" if tf32 else "")
     out["frac"] = round(out["achieved"] / out["peak"], 3)
     out["hbm_achieved_GB_s"] = round(bytes_ / seconds / 1e9, 1)
     out["hbm_frac"] = round(bytes_ / seconds / 1e9 / hbm, 3)
@@ -392,7 +405,7 @@ def time_e2e(torch, nat, w, params, steps, device):
 
 def extras(torch, nat, peaks, peak_kind, device):
     peak_gbs = float(peaks["hbm_gbs"])
-    from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN
+    from serving_gdn_decode_gb300.params import PATH_CHUNKED_TF32, PATH_SCAN
     from serving_gdn_decode_gb300.workloads import WORKLOADS
     res = {}
 
@@ -465,11 +478,12 @@ def extras(torch, nat, peaks, peak_kind, device):
     # the load; inputs (1.1 GB) are larger than L2
     wp = WORKLOADS["long_prefill"]
     for key, params, act, kind, steps in (
-            ("long_prefill_auto", wp.params(), "f32", None, 100),
+            ("long_prefill_auto", wp.params(), "f32", None, 300),
+            ("long_prefill_auto_ws", wp.params(), "ws", None, 400),
             ("long_prefill_scan", wp.params(path=PATH_SCAN), "f32", "scan", 100),
-            ("long_prefill_chunked", wp.params(path=PATH_CHUNKED), "f32", "chunked", 200),
-            ("long_prefill_chunked_two_pass", wp.params(path=PATH_CHUNKED), "ws", "chunked_two_pass",
-             400),
+            ("long_prefill_chunked_tf32", wp.params(path=PATH_CHUNKED_TF32), "f32", "chunked_tf32", 300),
+            ("long_prefill_chunked_two_pass_tf32", wp.params(path=PATH_CHUNKED_TF32), "ws",
+             "chunked_two_pass_tf32", 500),
             ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16", "scan", 100)):
         sets = make_sets(torch, wp, 1, device, act="f32" if act == "ws" else act)
         if act == "ws":
@@ -477,7 +491,7 @@ def extras(torch, nat, peaks, peak_kind, device):
                                         device=device)
         path = nat.gdn_path_name(params)
         if kind is None:
-            kind = "scan" if path.startswith("scan") else "chunked"
+            kind = "scan" if path.startswith("scan") else "chunked" if act != "ws" else "chunked_two_pass"
         clocks = ClockSampler(device.index or 0, interval_ms=50)
         t, clk = time_graphed(torch, nat, sets, params, steps, 3, clocks=clocks)
         s = t / steps

@@ -5,15 +5,16 @@ For profiler captures and quick checks, e.g.::
     python -m serving_gdn_decode_gb300.run_case decode --calls 3
     python -m serving_gdn_decode_gb300.run_case long_prefill --tokens 512 --path scan
     python -m serving_gdn_decode_gb300.run_case long_prefill --tokens 512 --path chunked --two-pass
+    python -m serving_gdn_decode_gb300.run_case long_prefill --tokens 512 --path chunked_tf32
 """
 from __future__ import annotations
 
 import argparse
 
-from .params import PATH_AUTO, PATH_CHUNKED, PATH_SCAN
+from .params import PATH_AUTO, PATH_CHUNKED, PATH_CHUNKED_TF32, PATH_SCAN
 from .workloads import WORKLOADS, make_inputs
 
-PATHS = {"auto": PATH_AUTO, "scan": PATH_SCAN, "chunked": PATH_CHUNKED}
+PATHS = {"auto": PATH_AUTO, "scan": PATH_SCAN, "chunked": PATH_CHUNKED, "chunked_tf32": PATH_CHUNKED_TF32}
 
 
 def main(argv=None):

@@ -111,6 +111,9 @@ def test_prefill_flop_counts():
     assert bench.chunked_mma_flops(w, False) == 64 * 4 * 48 * 11 * mib
     # a ragged last chunk still runs whole products
     assert bench.chunked_mma_flops(w.with_(n_tokens=4095), True) == bench.chunked_mma_flops(w, True)
+    # split-bf16 operands: three bf16 products for every one
+    for two in (False, True):
+        assert bench.chunked_mma_flops(w, two, split=True) == 3 * bench.chunked_mma_flops(w, two)
     assert bench.scan_executed_flops(w) == 6 * 128 * 128 * 48 * 4 * 4096
 
 
@@ -118,9 +121,15 @@ def test_prefill_roofline_fields():
     from serving_gdn_decode_gb300.workloads import WORKLOADS
     w = WORKLOADS["long_prefill"]
     peaks = {"hbm_gbs": 6700.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
-    r = bench.prefill_roofline("chunked_two_pass", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
-    assert r["bound"] == "tensor" and r["peak"] == 950.0
+    r = bench.prefill_roofline("chunked_two_pass_tf32", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
+    assert r["bound"] == "tensor" and r["peak"] == 950.0          # TF32: bf16 x 1/2
     assert abs(r["frac"] - r["achieved"] / 950.0) < 2e-3
+    assert r["flops_per_call"] == bench.chunked_mma_flops(w, True)
+    b = bench.prefill_roofline("chunked_two_pass", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
+    assert b["peak"] == 1900.0 and "bf16" in b["flops_counted"]   # split operands: bf16 MMAs
+    assert b["flops_per_call"] == 3 * r["flops_per_call"]
+    o = bench.prefill_roofline("chunked", w, 1e-3, peaks, "measured", None)
+    assert o["flops_per_call"] == bench.chunked_mma_flops(w, False, split=True)
     assert r["hbm_frac"] == round(w.algorithmic_bytes() / 1e-3 / 1e9 / 6700.0, 3)
     s = bench.prefill_roofline("scan", w, 1e-3, peaks, "measured", {"sm_mhz": 2000.0})
     assert s["bound"] == "alu"
