@@ -242,10 +242,22 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   float c = 1.f;          // S = c * (TMEM S)
   uint32_t phase = 0;
   bool failed = false;
+  // Y^T of the chunk starting at token tt0 (ncc tokens) to the output:
+  // thread = d_v, tokens [32*half, +32)
+  auto write_outputs = [&](uint32_t tt0, int ncc) {
+    uint32_t yv[32];
+    GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
+    tmem_wait_ld();
+    float *obase = a.output + ((tok0 + tt0) * a.nv + vh) * D + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int i = 32 * half + j;
+      if (i < ncc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+    }
+  };
 
   for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
     const uint32_t t0 = ch * C;
-    const int nc = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0));
 
     // ---- 0. this chunk's staged inputs (K, V rows, Q half, gates) have landed
     cp_async_wait_all();
@@ -307,9 +319,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // ---- 2. fold c into S if needed (no MMA in flight here)
     if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);
 
-    // ---- 3. operands from the staged rows: the stack's K half (canonical),
-    // its Q half from the staged Q rows, K'^T (smem), V^T (TMEM); split: S~
-    // as hi and lo (TMEM)
+    // ---- 3. the stack from the staged rows: K (canonical) and Q (the staged
+    // Q rows), rounded to TF32 in place or as bf16 hi and lo images
     if constexpr (SPLIT) {
       // the staged Q rows (f32, in the TF32 canonical order of the Q half),
       // read before the bf16 images overwrite them
@@ -331,6 +342,46 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(64 + r, d0, 128)) = h;
         *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(64 + r, d0, 128)) = l;
       }
+    } else {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int ci = tid + NTH * it;        // 16-byte chunk of the K half
+        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
+        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
+        x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
+        *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
+        float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
+        float4 y = *pq;
+        y.x = tf32_rn(y.x); y.y = tf32_rn(y.y); y.z = tf32_rn(y.z); y.w = tf32_rn(y.w);
+        *pq = y;
+      }
+    }
+    fence_async_smem();
+    cta_sync();
+
+    // ---- 4. Gram [K;Q] K^T -> TMEM G.  Meanwhile the other operands from the
+    // staged rows -- K'^T (smem), V^T (TMEM), split: S~ as hi and lo (TMEM) --
+    // and the previous chunk's outputs (its Y^T is read before this chunk's
+    // first batch overwrites it).
+    if (tid == 0) {
+      if constexpr (SPLIT) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t dh = sdesc(sbase + SM_STACK + ks * 256, 2048), dl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
+          mma_ss<true>(tmem + TM::G, dh, dh, idesc_bf16(128, 64), ks > 0);
+          mma_ss<true>(tmem + TM::G, dh, dl, idesc_bf16(128, 64), 1);
+          mma_ss<true>(tmem + TM::G, dl, dh, idesc_bf16(128, 64), 1);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks) {
+          const uint64_t d = sdesc(sbase + SM_STACK + ks * 256, 4096);
+          mma_ss(tmem + TM::G, d, d, idesc_tf32(128, 64), ks > 0);
+        }
+      }
+      mma_commit(mbar);
+    }
+    if constexpr (SPLIT) {
       // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
       const float *kts = sc + SC_KTS * 64;
 #pragma unroll
@@ -365,20 +416,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         GDN_TMEM_ST16(tl + TM::SH + 32 * half + 16 * h, sh);
         GDN_TMEM_ST16(tl + TM::SL + 32 * half + 16 * h, sl);
       }
-      tmem_wait_st();
     } else {
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;        // 16-byte chunk of the K half
-        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
-        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
-        x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
-        *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
-        float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
-        float4 y = *pq;
-        y.x = tf32_rn(y.x); y.y = tf32_rn(y.y); y.z = tf32_rn(y.z); y.w = tf32_rn(y.w);
-        *pq = y;
-      }
       // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
       const float *kts = sc + SC_KTS * 64;
 #pragma unroll
@@ -395,35 +433,10 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 #pragma unroll
       for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rn(sVS[(32 * half + j) * LDS + row]));
       GDN_TMEM_ST32(tl + TM::V + 32 * half, vv);
-      tmem_wait_st();
     }
+    if (ch > 0) write_outputs(t0 - C, C);
+    tmem_wait_st();
     fence_async_smem();
-    cta_sync();
-    // the staging buffers are free: start the next chunk's K and V rows
-    if (ch + 1 < nchunks) {
-      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-      stage_kv_async(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
-    }
-
-    // ---- 4. Gram [K;Q] K^T -> TMEM G
-    if (tid == 0) {
-      if constexpr (SPLIT) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t dh = sdesc(sbase + SM_STACK + ks * 256, 2048), dl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
-          mma_ss<true>(tmem + TM::G, dh, dh, idesc_bf16(128, 64), ks > 0);
-          mma_ss<true>(tmem + TM::G, dh, dl, idesc_bf16(128, 64), 1);
-          mma_ss<true>(tmem + TM::G, dl, dh, idesc_bf16(128, 64), 1);
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) {
-          const uint64_t d = sdesc(sbase + SM_STACK + ks * 256, 4096);
-          mma_ss(tmem + TM::G, d, d, idesc_tf32(128, 64), ks > 0);
-        }
-      }
-      mma_commit(mbar);
-    }
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;
     fence_after();
@@ -503,6 +516,12 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       }
     }
     cta_sync();
+    // the staging buffers are free (every thread took its operands from
+    // them before this barrier): start the next chunk's K and V rows
+    if (ch + 1 < nchunks) {
+      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+      stage_kv_async(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
+    }
 
     // ---- 6. T = (I + A)^-1, then -T' (over A) and T'' (over T), canonical
     tri_inverse(sA, sT, sM, tid);
@@ -603,9 +622,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
                                 sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
       }
-      {
-        // X -> hi | lo over S~ hi; Yt's columns times c q_scale gamma_r
-        const float *qs = sc + SC_QS * 64;
+      {  // X -> hi | lo over S~ hi
         uint32_t xv[32], xh[16], xl[16];
         GDN_TMEM_LD32(tl + TM::X + 32 * half, xv);
         tmem_wait_ld();
@@ -613,11 +630,6 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         for (int j = 0; j < 16; ++j) split2(__uint_as_float(xv[2 * j]), __uint_as_float(xv[2 * j + 1]), xh[j], xl[j]);
         GDN_TMEM_ST16(tl + TM::SH + 16 * half, xh);
         GDN_TMEM_ST16(tl + TM::SH + 32 + 16 * half, xl);
-        GDN_TMEM_LD32(tl + TM::Y + 32 * half, xv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xv[j] = __float_as_uint(__uint_as_float(xv[j]) * qs[32 * half + j]);
-        GDN_TMEM_ST32(tl + TM::Y + 32 * half, xv);
         tmem_wait_st();
       }
       cta_sync();
@@ -630,6 +642,15 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           mma_ts<true>(tmem + TM::U, tmem + TM::SH + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
         }
         mma_commit(mbar);
+      }
+      {  // meanwhile Yt's columns times c q_scale gamma_r (batch 2 adds to them)
+        const float *qs = sc + SC_QS * 64;
+        uint32_t yv[32];
+        GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) yv[j] = __float_as_uint(__uint_as_float(yv[j]) * qs[32 * half + j]);
+        GDN_TMEM_ST32(tl + TM::Y + 32 * half, yv);
       }
       if (!mbar_wait(mbar, phase)) misc->failed = 1;
       phase ^= 1;
@@ -719,23 +740,17 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     phase ^= 1;
     fence_after();
 
-    // ---- 8. outputs: thread = d_v, tokens [32*half, +32)
-    {
-      uint32_t yv[32];
-      GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
-      tmem_wait_ld();
-      float *obase = a.output + ((tok0 + t0) * a.nv + vh) * D + row;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int i = 32 * half + j;
-        if (i < nc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
-      }
-    }
+    // (this chunk's outputs are written during the next chunk's Gram, the
+    // last chunk's after the loop)
     c = misc->c_next;
     cta_sync();
     if (misc->failed) failed = true;
   }
 
+  if (!failed && nchunks > 0) {
+    const uint32_t tl0 = (nchunks - 1) * C;
+    write_outputs(tl0, static_cast<int>(nt - tl0));
+  }
   cp_async_wait_all();  // no copy may still be landing in shared memory at exit
   if (failed && tid == 0) report_wait_timeout();
 
