@@ -548,6 +548,7 @@ struct P2Misc {
   unsigned long long mbar_xy;  // [X | Z] MMA commit
   unsigned long long mbar1;    // U^T MMA commit
   unsigned long long mbar2;    // batch-2 MMA commit
+  unsigned long long mbar2s;   // split operands: batch 2's state update (issued first) done
   unsigned long long bar_kq;   // bulk copy: the [K; Q] image of a chunk
   unsigned long long bar_kt;   // bulk copy: the K^T image of a chunk
   unsigned long long bar_t;    // bulk copy: the T'' image of a chunk
@@ -631,7 +632,7 @@ __global__ void __launch_bounds__(NTH, 1)
   P2Misc *misc = reinterpret_cast<P2Misc *>(smem + P2_MISC);
   const uint32_t sbase = raw_addr + pad;
   const uint32_t mbar_xy = smem_addr(&misc->mbar_xy), mbar1 = smem_addr(&misc->mbar1),
-                 mbar2 = smem_addr(&misc->mbar2);
+                 mbar2 = smem_addr(&misc->mbar2), mbar2s = smem_addr(&misc->mbar2s);
   const uint32_t bar_kq = smem_addr(&misc->bar_kq), bar_kt = smem_addr(&misc->bar_kt),
                  bar_t = smem_addr(&misc->bar_t), bar_v = smem_addr(&misc->bar_v), bar_p = smem_addr(&misc->bar_p);
 
@@ -664,9 +665,9 @@ __global__ void __launch_bounds__(NTH, 1)
   const float *state_src = seg == 0 ? a.state_in : a.state_out;
 
   if (tid == 0) {
-    const uint32_t bars[8] = {mbar_xy, mbar1, mbar2, bar_kq, bar_kt, bar_t, bar_v, bar_p};
+    const uint32_t bars[9] = {mbar_xy, mbar1, mbar2, mbar2s, bar_kq, bar_kt, bar_t, bar_v, bar_p};
 #pragma unroll
-    for (int b = 0; b < 8; ++b) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bars[b]));
+    for (int b = 0; b < 9; ++b) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bars[b]));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
   }
@@ -712,6 +713,20 @@ __global__ void __launch_bounds__(NTH, 1)
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
   const uint32_t tl = tmem + lane_field;
+  // split operands: S~ as the A operand hi (over W's columns) and lo (over
+  // U's) from the state in TMEM; this thread's row, its 64 columns
+  auto split_state = [&]() {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32], sh[16], sl[16];
+      GDN_TMEM_LD32(tl + P2_TM_S + 64 * half + 32 * h, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sh[j], sl[j]);
+      GDN_TMEM_ST16(tl + P2_TM_W + 32 * half + 16 * h, sh);
+      GDN_TMEM_ST16(tl + P2_TM_U + 32 * half + 16 * h, sl);
+    }
+  };
 
   // S <- state_in (c = 1).  Thread: row d_v, columns [64*half, 64*half + 64).
   {
@@ -759,26 +774,11 @@ __global__ void __launch_bounds__(NTH, 1)
       __syncwarp();
       fence_after();
       tmem_scale64(tl + P2_TM_S + 64 * half, misc->c_renorm);
-      cta_sync();
-    }
-    if constexpr (SPLIT) {
-      if (ch > 0) {  // the A operand S~ = hi + lo (batch 2 is done: S~ is final)
-        if (!mbar_wait(mbar2, par ^ 1)) misc->failed = 1;
-        __syncwarp();
-        fence_after();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[32], sh[16], sl[16];
-          GDN_TMEM_LD32(tl + P2_TM_S + 64 * half + 32 * h, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) split2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), sh[j], sl[j]);
-          GDN_TMEM_ST16(tl + P2_TM_W + 32 * half + 16 * h, sh);
-          GDN_TMEM_ST16(tl + P2_TM_U + 32 * half + 16 * h, sl);
-        }
+      if constexpr (SPLIT) {  // and the A operand again from the folded state
+        split_state();
         tmem_wait_st();
-        cta_sync();
       }
+      cta_sync();
     }
     if (tid == 0 && more) {  // V rows are free: the next chunk's
       fence_async_smem();
@@ -938,19 +938,22 @@ __global__ void __launch_bounds__(NTH, 1)
       if (!mbar_wait(bar_p, par)) misc->failed = 1;
       if (!mbar_wait(bar_kt, par)) misc->failed = 1;
       if constexpr (SPLIT) {
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {
-          const uint64_t bh = sdesc(sbase + P2_P + ks * 256, 1024), bl = sdesc(sbase + P2_P + 8192 + ks * 256, 1024);
-          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bh, idesc_bf16(128, 64), 1);
-          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bl, idesc_bf16(128, 64), 1);
-          mma_ts<true>(tmem + tm_y, tmem + tm_x + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
-        }
+        // the state update first, on its own barrier, so that the next
+        // chunk's S~ split runs beside the output product
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks) {
           const uint64_t bh = sdesc(sbase + P2_KT + ks * 256, 1024), bl = sdesc(sbase + P2_KT + 16384 + ks * 256, 1024);
           mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 128), 1);
           mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 128), 1);
           mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        }
+        mma_commit(mbar2s);
+#pragma unroll
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t bh = sdesc(sbase + P2_P + ks * 256, 1024), bl = sdesc(sbase + P2_P + 8192 + ks * 256, 1024);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bh, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 8 * ks, bl, idesc_bf16(128, 64), 1);
+          mma_ts<true>(tmem + tm_y, tmem + tm_x + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
         }
       } else {
 #pragma unroll
@@ -980,6 +983,13 @@ __global__ void __launch_bounds__(NTH, 1)
       if (!mbar_wait(bar_v, par ^ 1)) misc->failed = 1;
 #pragma unroll
       for (int j = 0; j < 32; ++j) vr[j] = sVS[(32 * half + j) * D + row];
+      if constexpr (SPLIT) {  // the next chunk's A operand S~ = hi + lo, once the update is done
+        if (!mbar_wait(mbar2s, par)) misc->failed = 1;
+        __syncwarp();
+        fence_after();
+        split_state();
+        tmem_wait_st();
+      }
     }
     if (tid == 0) {  // batch 2 done: P' and K^T are free for the next chunk's
       if (!mbar_wait(mbar2, par)) misc->failed = 1;
@@ -1021,6 +1031,7 @@ __global__ void __launch_bounds__(NTH, 1)
       (void)mbar_wait(mbar_xy, (n_mma - 1) & 1);
       (void)mbar_wait(mbar1, (n_mma - 1) & 1);
       (void)mbar_wait(mbar2, (n_mma - 1) & 1);
+      if (SPLIT) (void)mbar_wait(mbar2s, (n_mma - 1) & 1);
     }
     const uint32_t pl = (n_ld - 1) & 1;  // every image barrier is armed once per chunk
     (void)mbar_wait(bar_kq, pl);
