@@ -103,11 +103,13 @@ def kernel_traffic(kernel: str, n_tokens: int | None = None):
 
 # ---------------------------------------------------------------- prefill rooflines
 
-def chunked_mma_flops(w, two_pass: bool, split: bool = False) -> int:
+def chunked_mma_flops(w, two_pass: bool, split: bool = False, bf16_in: bool = False) -> int:
     """Tensor-core flops the chunked prefill issues per call (2 per MAC of
     every tcgen05 product, full 64-token chunks even for a ragged last one;
     with split-bf16 operands every product runs as three bf16 MMAs, so three
-    times the TF32 form's count).
+    times the TF32 form's count; with bf16 activations (one-pass form) the
+    products of exact inputs leave out their zero lo terms: the Gram one
+    product, V^T T''^T, X = S K^T and S Q^T two each, the rest three).
     Per (seq, value head, chunk) the one-pass form runs the Gram [K;Q]K^T
     (M 128, N 64, K 128), V^T T''^T, X = S K^T, X(-T')^T, S Q'^T, U^T P'^T
     (each M 128, N 64; K 64, 128, 64, 128, 64) and S += U^T K'^T (M 128,
@@ -119,6 +121,10 @@ def chunked_mma_flops(w, two_pass: bool, split: bool = False) -> int:
     nch = -(-w.n_tokens // 64)
     mm = lambda m, n, k: 2 * m * n * k  # noqa: E731
     gram = mm(128, 64, 128)
+    if bf16_in and not two_pass:
+        per_head = gram + 2 * mm(128, 64, 64) + 2 * mm(128, 64, 128) + 3 * mm(128, 64, 64) \
+            + 2 * mm(128, 64, 128) + 3 * mm(128, 64, 64) + 3 * mm(128, 128, 64)
+        return nch * w.n_seqs * w.n_v_heads * per_head
     if two_pass:
         per_head = mm(128, 128, 128) + 2 * mm(128, 64, 64) + mm(128, 128, 64)
         return terms * nch * w.n_seqs * (w.n_v_heads * per_head + w.n_k_heads * gram)
@@ -158,7 +164,7 @@ def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, 
         tf32 = kind.endswith("_tf32")
         two = kind.startswith("chunked_two_pass")
         src = "bf16_tflops, MEASURED_PEAKS.json" if peak_kind == "measured" else "recipe fallback"
-        ex = chunked_mma_flops(w, two, split=not tf32)
+        ex = chunked_mma_flops(w, two, split=not tf32, bf16_in=act == "bf16")
         if tf32:
             peak = float(peaks["bf16_tflops"]) * 0.5
             out.update(peak_kind=f"of {peak_kind}: bf16 dense tensor peak ({src}) x 1/2, the nominal "
@@ -484,6 +490,7 @@ def extras(torch, nat, peaks, peak_kind, device):
             ("long_prefill_chunked_tf32", wp.params(path=PATH_CHUNKED_TF32), "f32", "chunked_tf32", 300),
             ("long_prefill_chunked_two_pass_tf32", wp.params(path=PATH_CHUNKED_TF32), "ws",
              "chunked_two_pass_tf32", 500),
+            ("long_prefill_auto_bf16", wp.params(), "bf16", None, 300),
             ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16", "scan", 100)):
         sets = make_sets(torch, wp, 1, device, act="f32" if act == "ws" else act)
         if act == "ws":

@@ -48,7 +48,10 @@
 // apart; a split operand is its hi image followed by its lo image.  Every
 // mbarrier wait is bounded; on a timeout the CTA writes NaN to its
 // state_out, frees its TMEM and returns.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "chunked_common.cuh"
 #include "gdn_internal.h"
@@ -92,13 +95,13 @@ constexpr uint32_t SM_TPP = SM_T;                    // T''  canonical (16 KB) o
 enum { SC_G = 0, SC_GAM, SC_GAMP, SC_BETA, SC_KTS, SC_TPS, SC_QS, SC_GPREV, SC_EG, SC_GRAW, SC_BRAW };
 
 struct ChunkArgs {
-  const float *__restrict__ q;
-  const float *__restrict__ k;
-  const float *__restrict__ v;
+  const void *__restrict__ q;  // q, k, v and output: f32, or bf16 with bf16 activations
+  const void *__restrict__ k;
+  const void *__restrict__ v;
   const float *__restrict__ g;
   const float *__restrict__ beta;
   const float *state_in;
-  float *__restrict__ output;
+  void *__restrict__ output;
   float *state_out;
   uint32_t nk, nv, nt, group, khead_div, nchunks;
   float q_scale;
@@ -119,18 +122,36 @@ struct Misc {
   int do_fold;
 };
 
-// Asynchronous copies of one chunk's Q rows into the stack's Q half
-// (canonical layout, rows 64..127), and of its gates and betas into the
-// scalar area; tokens past the chunk's end are zero-filled.
-__device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const float *qbase, size_t kq_tok,
+// bf16 activations: staged rows of 128 bf16 at a stride of 136 (272 bytes)
+constexpr int LDSB = 136;
+
+// Asynchronous copies of one chunk's Q rows and of its gates and betas into
+// the scalar area; tokens past the chunk's end are zero-filled.  f32: into
+// the stack's Q half (rows 64..127) in the TF32 canonical order; bf16
+// activations: straight into the bf16 canonical image of the stack's Q rows
+// (a 16-byte row of a core is 8 consecutive d_k of one token).
+template <bool BF16IN>
+__device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const void *qv, size_t kq_tok,
                                                         const float *g, const float *beta, size_t sc0,
                                                         size_t nv, int nc, int tid) {
+  if constexpr (BF16IN) {
+    const uint16_t *qbase = static_cast<const uint16_t *>(qv);
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int cc = tid + NTH * it;        // 16-byte chunk within the Q half
-    const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
-    cp_async16(sbase + SM_STACK + 32768 + cc * 16, qbase + (r < nc ? r : 0) * kq_tok + 4 * c4,
-               r < nc ? 16u : 0u);
+    for (int it = 0; it < 4; ++it) {
+      const int cc = tid + NTH * it;      // token cc >> 4, d_k 8 (cc & 15) .. +7
+      const int r = cc >> 4, d0 = 8 * (cc & 15);
+      cp_async16(sbase + SM_STACK + canon16(64 + r, d0, 128), qbase + (r < nc ? r : 0) * kq_tok + d0,
+                 r < nc ? 16u : 0u);
+    }
+  } else {
+    const float *qbase = static_cast<const float *>(qv);
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int cc = tid + NTH * it;      // 16-byte chunk within the Q half
+      const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
+      cp_async16(sbase + SM_STACK + 32768 + cc * 16, qbase + (r < nc ? r : 0) * kq_tok + 4 * c4,
+                 r < nc ? 16u : 0u);
+    }
   }
   if (tid < 128) {
     const int i = tid & 63;
@@ -141,26 +162,53 @@ __device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const fl
   cp_async_commit();
 }
 
-// Asynchronous copies of one chunk's K and V rows (natural layout: 64 rows
-// of 512 bytes each) into the staging buffers; rows past the end are zeros.
-__device__ __forceinline__ void stage_kv_async(uint32_t sbase, const float *kbase, size_t kq_tok,
-                                               const float *vbase, size_t v_tok, int nc, int tid) {
+// Asynchronous copies of one chunk's K and V rows (natural layout, row
+// stride LDS floats, or LDSB bf16 with bf16 activations) into the staging
+// buffers; rows past the end are zeros.
+template <bool BF16IN>
+__device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, size_t kq_tok, const void *vv,
+                                               size_t v_tok, int nc, int tid) {
+  if constexpr (BF16IN) {
+    const uint16_t *kbase = static_cast<const uint16_t *>(kv), *vbase = static_cast<const uint16_t *>(vv);
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int ci = tid + NTH * it;        // 16-byte chunk: row ci/32, float4 ci%32
-    const int r = ci >> 5, c4 = ci & 31;
-    const uint32_t n = r < nc ? 16u : 0u;
-    const int rr = r < nc ? r : 0;
-    const uint32_t dst = static_cast<uint32_t>((r * LDS + 4 * c4) * 4);
-    cp_async16(sbase + SM_KS + dst, kbase + rr * kq_tok + 4 * c4, n);
-    cp_async16(sbase + SM_VS + dst, vbase + rr * v_tok + 4 * c4, n);
+    for (int it = 0; it < 4; ++it) {
+      const int ci = tid + NTH * it;      // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
+      const int r = ci >> 4, c8 = ci & 15;
+      const uint32_t n = r < nc ? 16u : 0u;
+      const int rr = r < nc ? r : 0;
+      const uint32_t dst = static_cast<uint32_t>((r * LDSB + 8 * c8) * 2);
+      cp_async16(sbase + SM_KS + dst, kbase + rr * kq_tok + 8 * c8, n);
+      cp_async16(sbase + SM_VS + dst, vbase + rr * v_tok + 8 * c8, n);
+    }
+  } else {
+    const float *kbase = static_cast<const float *>(kv), *vbase = static_cast<const float *>(vv);
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int ci = tid + NTH * it;      // 16-byte chunk: row ci/32, float4 ci%32
+      const int r = ci >> 5, c4 = ci & 31;
+      const uint32_t n = r < nc ? 16u : 0u;
+      const int rr = r < nc ? r : 0;
+      const uint32_t dst = static_cast<uint32_t>((r * LDS + 4 * c4) * 4);
+      cp_async16(sbase + SM_KS + dst, kbase + rr * kq_tok + 4 * c4, n);
+      cp_async16(sbase + SM_VS + dst, vbase + rr * v_tok + 4 * c4, n);
+    }
   }
   cp_async_commit();
 }
 
-template <bool DECAY_AFTER, bool SPLIT>
+// A bf16 bit pattern widened to f32 (exact).
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// BF16IN: q, k, v and output hold bf16 (split operands only): the inputs
+// are exact bf16 values, so K, Q and V^T are their own hi halves with zero
+// lo halves, and the products leave out the terms with a zero lo (the Gram
+// is one bf16 product per K step, X, Y^T and V^T T''^T two); every other
+// step is the f32 form's, and y is rounded to bf16 once when stored.
+template <bool DECAY_AFTER, bool SPLIT, bool BF16IN>
 __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) {
+  static_assert(SPLIT || !BF16IN, "bf16 activations take split operands");
   using TM = Tm<SPLIT>;
+  using In = typename std::conditional<BF16IN, uint16_t, float>::type;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *sA = reinterpret_cast<float *>(smem + SM_A);
   float *sT = reinterpret_cast<float *>(smem + SM_T);
@@ -194,9 +242,11 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   const size_t kq_tok = static_cast<size_t>(a.nk) * D;
   const size_t v_tok = static_cast<size_t>(a.nv) * D;
   const size_t tok0 = static_cast<size_t>(s) * a.nt + tb;  // the segment's first token of this seq
-  const float *kseq = a.k + (tok0 * a.nk + kh) * D;
-  const float *qseq = a.q + (tok0 * a.nk + kh) * D;
-  const float *vseq = a.v + (tok0 * a.nv + vh) * D;
+  const In *kseq = static_cast<const In *>(a.k) + (tok0 * a.nk + kh) * D;
+  const In *qseq = static_cast<const In *>(a.q) + (tok0 * a.nk + kh) * D;
+  const In *vseq = static_cast<const In *>(a.v) + (tok0 * a.nv + vh) * D;
+  const uint16_t *sKSb = reinterpret_cast<const uint16_t *>(smem + SM_KS);  // bf16 staging views
+  const uint16_t *sVSb = reinterpret_cast<const uint16_t *>(smem + SM_VS);
   const size_t sc_first = tok0 * a.nv + vh;
   // the state enters from state_in, or, after an earlier segment, from
   // state_out, where that segment left it (an earlier launch)
@@ -215,8 +265,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   // chunk 0's inputs start arriving while the state is loaded
   {
     const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
-    stage_kv_async(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
-    stage_q_and_gates_async(sbase, qseq, kq_tok, a.g, a.beta, sc_first, a.nv, nc0, tid);
+    stage_kv_async<BF16IN>(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
+    stage_q_and_gates_async<BF16IN>(sbase, qseq, kq_tok, a.g, a.beta, sc_first, a.nv, nc0, tid);
   }
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
@@ -248,11 +298,16 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     uint32_t yv[32];
     GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
     tmem_wait_ld();
-    float *obase = a.output + ((tok0 + tt0) * a.nv + vh) * D + row;
+    In *obase = static_cast<In *>(a.output) + ((tok0 + tt0) * a.nv + vh) * D + row;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int i = 32 * half + j;
-      if (i < ncc) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      if (i < ncc) {
+        if constexpr (BF16IN)
+          obase[static_cast<size_t>(i) * v_tok] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(yv[j])));
+        else
+          obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      }
     }
   };
 
@@ -320,8 +375,17 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);
 
     // ---- 3. the stack from the staged rows: K (canonical) and Q (the staged
-    // Q rows), rounded to TF32 in place or as bf16 hi and lo images
-    if constexpr (SPLIT) {
+    // Q rows), rounded to TF32 in place or as bf16 hi and lo images (bf16
+    // activations: Q is in place already, K's rows are copied)
+    if constexpr (BF16IN) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int ci = tid + NTH * it;        // token ci >> 4, d_k 8 (ci & 15) .. +7
+        const int r = ci >> 4, d0 = 8 * (ci & 15);
+        *reinterpret_cast<uint4 *>(smem + SM_STACK + canon16(r, d0, 128)) =
+            *reinterpret_cast<const uint4 *>(sKSb + r * LDSB + d0);
+      }
+    } else if constexpr (SPLIT) {
       // the staged Q rows (f32, in the TF32 canonical order of the Q half),
       // read before the bf16 images overwrite them
       float4 qv[8];
@@ -364,7 +428,13 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // and the previous chunk's outputs (its Y^T is read before this chunk's
     // first batch overwrites it).
     if (tid == 0) {
-      if constexpr (SPLIT) {
+      if constexpr (BF16IN) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t dh = sdesc(sbase + SM_STACK + ks * 256, 2048);
+          mma_ss<true>(tmem + TM::G, dh, dh, idesc_bf16(128, 64), ks > 0);
+        }
+      } else if constexpr (SPLIT) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t dh = sdesc(sbase + SM_STACK + ks * 256, 2048), dl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
@@ -389,15 +459,24 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         const int i = 32 * half + 8 * j;
         float e[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = sKS[(i + u) * LDS + row] * kts[i + u];
+        for (int u = 0; u < 8; ++u)
+          e[u] = (BF16IN ? bf16_bits_to_f32(sKSb[(i + u) * LDSB + row]) : sKS[(i + u) * LDS + row]) * kts[i + u];
         uint4 h, l;
         split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
         split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
         *reinterpret_cast<uint4 *>(smem + SM_KT + canon16(row, i, 64)) = h;
         *reinterpret_cast<uint4 *>(smem + SM_KT + 16384 + canon16(row, i, 64)) = l;
       }
-      // V^T -> TMEM as hi | lo (lane d_v = row, token pairs of [32*half, +32))
-      {
+      // V^T -> TMEM as hi | lo (lane d_v = row, token pairs of [32*half, +32));
+      // bf16 activations: V^T is its own hi half
+      if constexpr (BF16IN) {
+        uint32_t vh[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          vh[j] = static_cast<uint32_t>(sVSb[(32 * half + 2 * j) * LDSB + row]) |
+                  (static_cast<uint32_t>(sVSb[(32 * half + 2 * j + 1) * LDSB + row]) << 16);
+        GDN_TMEM_ST16(tl + TM::V + 16 * half, vh);
+      } else {
         uint32_t vh[16], vl[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -520,7 +599,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // them before this barrier): start the next chunk's K and V rows
     if (ch + 1 < nchunks) {
       const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-      stage_kv_async(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
+      stage_kv_async<BF16IN>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
     }
 
     // ---- 6. T = (I + A)^-1, then -T' (over A) and T'' (over T), canonical
@@ -592,13 +671,13 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           const uint64_t bh = sdesc(sbase + SM_TPP + ks * 256, 1024), bl = sdesc(sbase + SM_TPP + 8192 + ks * 256, 1024);
           mma_ts<true>(tmem + TM::U, tmem + TM::V + 8 * ks, bh, i64, ks > 0);
           mma_ts<true>(tmem + TM::U, tmem + TM::V + 8 * ks, bl, i64, 1);
-          mma_ts<true>(tmem + TM::U, tmem + TM::V + 32 + 8 * ks, bh, i64, 1);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::U, tmem + TM::V + 32 + 8 * ks, bh, i64, 1);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {  // X = S~ K^T
           const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
           mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
           mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i64, 1);
         }
 #pragma unroll
@@ -606,7 +685,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           const uint64_t bh = sdesc(sbase + SM_STACK + 16384 + ks * 256, 2048),
                          bl = sdesc(sbase + SM_STACK + 49152 + ks * 256, 2048);
           mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
           mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i64, 1);
         }
         mma_commit(mbar);
@@ -619,8 +698,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       // the stack is free now: start the next chunk's Q rows and gates
       if (ch + 1 < nchunks) {
         const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-        stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+        stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                        sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
       }
       {  // X -> hi | lo over S~ hi
         uint32_t xv[32], xh[16], xl[16];
@@ -710,8 +789,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       // the stack's Q half is free now: start the next chunk's Q rows and gates
       if (ch + 1 < nchunks) {
         const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-        stage_q_and_gates_async(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+        stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                        sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
       }
       {
         uint32_t uv[32];
@@ -774,12 +853,11 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TM_COLS));
 }
 
-template <bool DA, bool SPLIT>
+template <bool DA, bool SPLIT, bool BF16IN>
 cudaError_t launch(const Problem &p, cudaStream_t stream) {
   ChunkArgs a;
-  a.q = static_cast<const float *>(p.q); a.k = static_cast<const float *>(p.k);
-  a.v = static_cast<const float *>(p.v); a.g = p.g; a.beta = p.beta;
-  a.state_in = p.state_in; a.output = static_cast<float *>(p.output); a.state_out = p.state_out;
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
+  a.state_in = p.state_in; a.output = p.output; a.state_out = p.state_out;
   a.nk = p.nk; a.nv = p.nv; a.nt = p.nt;
   a.group = p.nv / p.nk;
   a.khead_div = p.khead_div ? 1u : 0u;
@@ -797,7 +875,7 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
   const uint32_t segs = state_segments(heads, nchunks, want);
   a.seg_len = (nchunks + segs - 1) / segs;
   const unsigned long long tasks = heads * ((nchunks + a.seg_len - 1) / a.seg_len);
-  auto kern = gdn_chunked_kernel<DA, SPLIT>;
+  auto kern = gdn_chunked_kernel<DA, SPLIT, BF16IN>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   // one launch per group of up to `want` (one CTA per SM) segments, in the
@@ -817,13 +895,14 @@ cudaError_t launch(const Problem &p, cudaStream_t stream) {
 }  // namespace
 
 bool chunked_supported(const Problem &p) {
-  return p.dk == 128 && p.dv == 128 && p.capture == nullptr && !p.io_bf16;
+  return p.dk == 128 && p.dv == 128 && p.capture == nullptr && !(p.io_bf16 && p.tf32);
 }
 
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream) {
   if (!chunked_supported(p)) return cudaErrorInvalidValue;
-  if (p.tf32) return p.decay_after ? launch<true, false>(p, stream) : launch<false, false>(p, stream);
-  return p.decay_after ? launch<true, true>(p, stream) : launch<false, true>(p, stream);
+  if (p.tf32) return p.decay_after ? launch<true, false, false>(p, stream) : launch<false, false, false>(p, stream);
+  if (p.io_bf16) return p.decay_after ? launch<true, true, true>(p, stream) : launch<false, true, true>(p, stream);
+  return p.decay_after ? launch<true, true, false>(p, stream) : launch<false, true, false>(p, stream);
 }
 
 cudaError_t chunked_wait_status(unsigned int *bits, bool reset, cudaStream_t stream) {

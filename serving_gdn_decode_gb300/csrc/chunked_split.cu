@@ -1170,7 +1170,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 }  // namespace
 
 bool chunked_split_supported(const Problem &p) {
-  return chunked_supported(p) && p.nk > 0 && p.nv / p.nk <= kMaxSplitGroup;
+  return chunked_supported(p) && !p.io_bf16 && p.nk > 0 && p.nv / p.nk <= kMaxSplitGroup;
 }
 
 size_t chunked_split_workspace_bytes(const Problem &p) {

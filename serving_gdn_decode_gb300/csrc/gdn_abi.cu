@@ -139,14 +139,14 @@ gdn_status choose_path(const Decoded &d, bool capture, bool bf16, Path *out) {
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path keeps no per-token state (capture)");
       if (d.prob.dk != 128 || d.prob.dv != 128)
         return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path needs D_k = D_v = 128");
-      if (bf16)
-        return fail(GDN_ERR_UNSUPPORTED, "gdn: the chunked path takes f32 activations only");
+      if (bf16 && d.path == GDN_PATH_CHUNKED_TF32)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn: the TF32 chunked path takes f32 activations only");
       *out = Path::kChunked;
       return GDN_OK;
     default:
       if (d.prob.nt <= kDecodeMaxTokens)
         *out = Path::kDecode;
-      else if (!capture && !bf16 && d.prob.dk == 128 && d.prob.dv == 128 && d.prob.nt >= kChunkedMinTokens)
+      else if (!capture && d.prob.dk == 128 && d.prob.dv == 128 && d.prob.nt >= kChunkedMinTokens)
         *out = Path::kChunked;
       else
         *out = Path::kScan;

@@ -38,7 +38,8 @@ cudaError_t launch_token_loop_layers(const Problem *layers, uint32_t n_layers, c
 // lazy decay; shaped for FP32 issue throughput.
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 
-// Chunked tensor-core prefill (chunked.cu): D_k = D_v = 128, f32 I/O, no capture.
+// Chunked tensor-core prefill (chunked.cu): D_k = D_v = 128, no capture; f32
+// activations, or bf16 ones with split operands (not with tf32).
 bool chunked_supported(const Problem &p);
 cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 
@@ -49,7 +50,7 @@ cudaError_t launch_chunked(const Problem &p, cudaStream_t stream);
 // The chunk pass holds the gate scalars of all value heads of a key head in
 // shared memory, so the form takes at most kMaxSplitGroup of them.
 constexpr uint32_t kMaxSplitGroup = 32;
-bool chunked_split_supported(const Problem &p);  // chunked_supported and n_v / n_k <= kMaxSplitGroup
+bool chunked_split_supported(const Problem &p);  // chunked_supported, f32 activations, n_v / n_k <= kMaxSplitGroup
 size_t chunked_split_workspace_bytes(const Problem &p);
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream);
 

@@ -334,8 +334,11 @@ def test_bf16_unsupported_shapes(L):
     assert "even D_v" in nat.gdn_last_error()
     assert Fake(odd).call() != nat.GDN_ERR_UNSUPPORTED       # f32 takes odd D_v
     w = WORKLOADS["long_prefill"].with_(n_tokens=64, n_seqs=1)
-    assert Fake(w).call(params=w.params(path=PATH_CHUNKED), bf16=True) == nat.GDN_ERR_UNSUPPORTED
+    # bf16 activations take the chunked path with split operands, not with TF32 ones
+    assert Fake(w).call(params=w.params(path=PATH_CHUNKED_TF32), bf16=True) == nat.GDN_ERR_UNSUPPORTED
     assert "f32 activations" in nat.gdn_last_error()
+    assert Fake(w).call(params=w.params(path=PATH_CHUNKED), bf16=True) == nat.GDN_ERR_CUDA  # host checks pass
+    assert Fake(w).call(params=w.params(), bf16=True) == nat.GDN_ERR_CUDA
 
 
 @no_device

@@ -16,13 +16,16 @@ bf16 path, the f32 path and the oracle all read the same values.  Two bars:
 * against the f32 path on the same values: state_out and state_capture bit
   for bit, and output equal, bit for bit, to the f32 path's output rounded to
   nearest-even bf16 -- the header's contract that only the final store of y
-  differs.
+  differs.  This holds on the chunked path too: there the bf16 kernel leaves
+  out the products whose lo half is zero (bf16 inputs are their own hi
+  halves), which add nothing in the f32 kernel.
 """
 import numpy as np
 import pytest
 
-from gpu_helpers import MAXABS_TOL, RELL2_TOL, assert_close, gather_heads, run_gpu, sample_heads
-from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_SCAN
+from gpu_helpers import (MAXABS_TOL, RELL2_TOL, SPLIT_RELL2_TOL, assert_close, assert_rel_l2, gather_heads,
+                         run_gpu, sample_heads)
+from serving_gdn_decode_gb300.params import PATH_CHUNKED, PATH_CHUNKED_TF32, PATH_SCAN
 from serving_gdn_decode_gb300.workloads import Workload, make_inputs, round_to_bf16
 
 pytestmark = pytest.mark.gpu
@@ -101,6 +104,9 @@ CASES = [  # (d_k, d_v, n_k, n_v, n_tokens, n_seqs, capture, path)
     (128, 136, 2, 2, 3, 2, False, 0),       # ragged last row block (136 = 4*32 + 8)
     (128, 128, 2, 4, 40, 2, True, 0),       # auto scan: 2 full 16-token chunks + 8
     (64, 64, 1, 2, 5, 1, True, PATH_SCAN),  # forced scan, one partial chunk
+    (128, 128, 2, 4, 130, 2, False, 0),     # auto chunked: 2 full 64-token chunks + 2
+    (128, 128, 2, 6, 9, 2, False, PATH_CHUNKED),   # forced chunked, one partial chunk
+    (128, 128, 1, 2, 64, 1, False, PATH_CHUNKED),  # exactly one chunk
 ]
 FLAGS = [dict(), dict(decay_after=True), dict(khead_div=True),
          dict(decay_after=True, khead_div=True)]
@@ -140,10 +146,14 @@ def test_bf16_in_place_decode(torch, oracle_mod):
     assert_close("state_out", st, rs, 1)
 
 
-def test_bf16_long_window_sampled(torch, oracle_mod):
-    """A 600-token prefill on the scan path (37 full chunks + 8), sampled heads."""
+@pytest.mark.parametrize("path", [0, PATH_SCAN], ids=["auto-chunked", "scan"])
+def test_bf16_long_window_sampled(torch, oracle_mod, path):
+    """A 600-token prefill (9 full 64-token chunks + 24; 37 full 16-token
+    scan chunks + 8) on the automatic path (the chunked form) and on the
+    forced scan, sampled heads; the chunked state also within the split-bf16
+    bar."""
     w = Workload("bf16", 128, 128, 2, 6, 600, 2, zero_state=True)
-    p = w.params()
+    p = w.params(path=path)
     x = make_inputs(w, 3, act="bf16")
     out, st, _ = run_bf16(torch, w, x, p)
     heads = sample_heads(w, 4, seed=2)
@@ -151,6 +161,8 @@ def test_bf16_long_window_sampled(torch, oracle_mod):
     go, gs, _ = gather_heads(w, out, st, None, heads)
     assert_output_bf16(go, ro, w.n_tokens)
     assert_close("state_out", gs, rs, w.n_tokens)
+    if path == 0:
+        assert_rel_l2("state_out", gs, rs, SPLIT_RELL2_TOL)
 
 
 @pytest.mark.parametrize("capture", [False, True])
@@ -178,9 +190,10 @@ def test_bf16_layers_equal_per_layer_calls(torch, capture):
                                   rc.view(np.uint32))
 
 
-def test_bf16_path_rejects_chunked(torch):
+def test_bf16_path_rejects_tf32_chunked(torch):
+    """bf16 activations take the chunked path with split operands only."""
     from serving_gdn_decode_gb300 import _native as nat
     w = Workload("bf16", 128, 128, 1, 1, 64, 1)
     x = make_inputs(w, 0, act="bf16")
     with pytest.raises(nat.GdnError, match="f32 activations"):
-        run_bf16(torch, w, x, w.params(path=PATH_CHUNKED))
+        run_bf16(torch, w, x, w.params(path=PATH_CHUNKED_TF32))
