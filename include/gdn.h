@@ -238,7 +238,10 @@ gdn_status gdn_commit_capture(const float *state_capture, size_t state_capture_e
  *
  * Extra checks: v 4-byte aligned and output 2-byte aligned (q and k stay
  * 16-byte); UNSUPPORTED when D_v is odd (v is staged two rows at a time) or
- * when the chunked path is forced.
+ * when the TF32 chunked path is forced.  The chunked path (forced, or chosen
+ * by GDN_PATH_AUTO) runs with split operands; bf16 inputs are their own hi
+ * halves, so its products leave out the terms with a zero lo half, which
+ * add nothing in the f32 form: results keep the equalities above.
  */
 typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
 
@@ -292,6 +295,23 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
                           const float *beta, const float *state_in, float *output,
                           float *state_out, const uint32_t *params, size_t n_params,
                           void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * gdn_forward_ws_bf16 -- gdn_forward_ws with bf16 q, k, v and output, as
+ * gdn_forward_bf16 is to gdn_forward (same layouts, f32 g, beta and state;
+ * y rounded once to nearest-even bf16 when stored).  The workspace size is
+ * gdn_workspace_size's for the same params; the two-pass form stores only
+ * the hi halves of K, Q and K^T (bf16 inputs are exact), using part of it.
+ * Results: the state equals gdn_forward_ws's on the same widened inputs bit
+ * for bit, and the output equals its output rounded to bf16.  Checks as
+ * gdn_forward_bf16 plus the workspace checks of gdn_forward_ws; the TF32
+ * chunked path (GDN_PATH_CHUNKED_TF32) is UNSUPPORTED with bf16 activations.
+ */
+gdn_status gdn_forward_ws_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                               const float *g, const float *beta, const float *state_in,
+                               gdn_bf16 *output, float *state_out, const uint32_t *params,
+                               size_t n_params, void *workspace, size_t workspace_bytes,
+                               gdn_stream_t stream);
 
 /*
  * gdn_forward_chunked_noalloc -- the two-pass chunked prefill of

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_forward_layers_bf16.restype = ctypes.c_int
             L.gdn_forward_ws.argtypes = [vp] * 8 + [u32p, sz, vp, sz, vp]
             L.gdn_forward_ws.restype = ctypes.c_int
+            L.gdn_forward_ws_bf16.argtypes = L.gdn_forward_ws.argtypes
+            L.gdn_forward_ws_bf16.restype = ctypes.c_int
             L.gdn_workspace_size.argtypes = [u32p, sz, ctypes.POINTER(ctypes.c_size_t)]
             L.gdn_workspace_size.restype = ctypes.c_int
             L.gdn_forward_chunked_noalloc.argtypes = [vp] * 8 + [u32p, sz, vp]
@@ -156,11 +158,12 @@ def forward_raw(q, k, v, g, beta, state_in, output, state_out, params, stream=0,
 
 
 def forward_ws_raw(q, k, v, g, beta, state_in, output, state_out, params, workspace,
-                   workspace_bytes, stream=0) -> int:
-    """Call gdn_forward_ws with integer device addresses; returns the status."""
+                   workspace_bytes, stream=0, bf16=False) -> int:
+    """Call gdn_forward_ws (gdn_forward_ws_bf16 when ``bf16``) with integer
+    device addresses; returns the status."""
     p, pp, n = _params_arg(params)
-    return lib().gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, pp, n, workspace,
-                                workspace_bytes, stream)
+    fn = lib().gdn_forward_ws_bf16 if bf16 else lib().gdn_forward_ws
+    return fn(q, k, v, g, beta, state_in, output, state_out, pp, n, workspace, workspace_bytes, stream)
 
 
 def forward_chunked_noalloc_raw(q, k, v, g, beta, state_in, output, state_out, params,
@@ -318,12 +321,11 @@ def gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, params, worksp
     """gdn_forward with a device workspace (a contiguous CUDA tensor of any
     dtype holding at least gdn_workspace_size(params) bytes, or None when that
     is 0).  On the chunked path the two-pass form runs; elsewhere as
-    gdn_forward.  f32 activations only."""
+    gdn_forward.  q, k, v and output all f32, or all bf16 (then
+    gdn_forward_ws_bf16 runs)."""
     import torch
     s = _sizes(params)
     ptrs, bf16 = _act_ptrs("", q, k, v, g, beta, state_in, output, state_out, s)
-    if bf16:
-        raise GdnError(GDN_ERR_INVALID_ARGUMENT, "gdn_forward_ws takes f32 activations")
     if workspace is None:
         wp, wb = None, 0
     else:
@@ -331,7 +333,7 @@ def gdn_forward_ws(q, k, v, g, beta, state_in, output, state_out, params, worksp
                 or not workspace.is_contiguous()):
             raise GdnError(GDN_ERR_INVALID_ARGUMENT, "workspace must be a contiguous CUDA tensor")
         wp, wb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    st = forward_ws_raw(*ptrs, params, wp, wb, _stream(stream, q.device))
+    st = forward_ws_raw(*ptrs, params, wp, wb, _stream(stream, q.device), bf16=bf16)
     if st != GDN_OK:
         raise GdnError(st, gdn_last_error())
 

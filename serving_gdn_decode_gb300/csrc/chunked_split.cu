@@ -35,12 +35,17 @@
 //     split: [0, 16384) the stack as blocks hi(d_k 0-63), lo(0-63),
 //            hi(64-127), lo(64-127) of 16 KB (128 rows x 64 bf16, swizzled),
 //            [16384, 20480) K^T hi, [20480, 24576) K^T lo (128 x 64 bf16
-//            canonical).
+//            canonical);
+//     bf16 activations (split operands; K and Q are their own hi halves):
+//            [0, 8192) the stack as hi(d_k 0-63), hi(64-127), [8192, 12288)
+//            K^T; the rest of the slot is unused.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "chunked_common.cuh"
 #include "gdn_internal.h"
@@ -189,8 +194,10 @@ static_assert(sizeof(P1Misc) <= 32, "pass-1 misc area");  // then one int per va
 // once for the key head; the key-head images ([K; Q] stack and K^T) are
 // stored; then, for each value head that reads this key head in turn, its
 // gates turn the Gram into A and P', and T'' follows from T = (I + A)^-1.
-// SPLIT: split-bf16 operands, else TF32.
-template <bool DECAY_AFTER, bool SPLIT>
+// SPLIT: split-bf16 operands, else TF32.  BF16IN: bf16 activations (with
+// SPLIT): the TMA boxes land as the bf16 hi blocks, the Gram is one product
+// per K step, and only hi images are stored.
+template <bool DECAY_AFTER, bool SPLIT, bool BF16IN>
 __global__ void __launch_bounds__(NTH, 3)
     gdn_chunk_prep_kernel(const PrepArgs a, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_q) {
@@ -241,12 +248,13 @@ __global__ void __launch_bounds__(NTH, 3)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(bar_ld));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
-    mbar_expect_tx(bar_ld, 65536);
+    constexpr int kBlocks = BF16IN ? 2 : 4;  // 128-byte column blocks of d_k: 64 bf16 or 32 f32
+    mbar_expect_tx(bar_ld, kBlocks * 16384);
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      tma_load_4d(sbase + P1_STACK + cb * 16384, &tm_k, 32 * cb, static_cast<int>(kh), static_cast<int>(t0),
-                  static_cast<int>(s), bar_ld);
-      tma_load_4d(sbase + P1_STACK + cb * 16384 + 8192, &tm_q, 32 * cb, static_cast<int>(kh),
+    for (int cb = 0; cb < kBlocks; ++cb) {
+      tma_load_4d(sbase + P1_STACK + cb * 16384, &tm_k, (128 / kBlocks) * cb, static_cast<int>(kh),
+                  static_cast<int>(t0), static_cast<int>(s), bar_ld);
+      tma_load_4d(sbase + P1_STACK + cb * 16384 + 8192, &tm_q, (128 / kBlocks) * cb, static_cast<int>(kh),
                   static_cast<int>(t0), static_cast<int>(s), bar_ld);
     }
   }
@@ -262,7 +270,38 @@ __global__ void __launch_bounds__(NTH, 3)
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
 
-  if constexpr (SPLIT) {
+  if constexpr (BF16IN) {
+    // Gram [K;Q] K^T -> TMEM: exact bf16 inputs, one product per K step
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t d = sdesc_sw128(sbase + P1_STACK + (ks >> 2) * 16384 + (ks & 3) * 32);
+        mma_ss<true>(tmem, d, d, idesc_bf16(128, 64), ks > 0);
+      }
+      mma_commit(mbar);
+    }
+    // while it runs (by the first part): the stack as the workspace image,
+    // and K^T (d_k rows x 64 tokens, bf16 canonical) from it
+    if (store_k) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it)
+        __stcg(reinterpret_cast<uint4 *>(wk) + tid + NTH * it,
+               reinterpret_cast<const uint4 *>(smem + P1_STACK)[tid + NTH * it]);
+      unsigned char *wkb = reinterpret_cast<unsigned char *>(wk);
+      for (int oc = tid; oc < 1024; oc += NTH) {  // d_k = oc % 128, tokens 8 (oc / 128) .. +7
+        const int dk = oc & 127, i0 = (oc >> 7) * 8;
+        const unsigned char *kb = smem + P1_STACK + (dk >> 6) * 16384 + (dk & 7) * 2;
+        uint32_t e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          e[u] = *reinterpret_cast<const uint16_t *>(kb + i * 128 + ((((dk & 63) >> 3) ^ (i & 7)) << 4));
+        }
+        __stcg(reinterpret_cast<uint4 *>(wkb + 32768 + canon16(dk, i0, 64)),
+               make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16)));
+      }
+    }
+  } else if constexpr (SPLIT) {
     // K^T (d_k rows x 64 tokens) as bf16 hi and lo canonical images, from
     // the f32 stack (by the first part)
     unsigned char *wkb = reinterpret_cast<unsigned char *>(wk);
@@ -534,7 +573,7 @@ struct StateArgs {
   const float *state_in;
   const float *__restrict__ ws;    // per (head, chunk) images
   const float *__restrict__ ws_k;  // per (seq, key head, chunk) images
-  float *__restrict__ output;
+  void *__restrict__ output;  // f32, or bf16 with bf16 activations
   float *state_out;
   uint32_t nk, nv, nt, group, khead_div, nchunks;
   float q_scale;
@@ -560,6 +599,13 @@ struct P2Misc {
   int do_renorm, do_fold;
 };
 static_assert(sizeof(P2Misc) <= 128, "pass-2 misc area");
+
+// An output value from its f32 bits: f32, or rounded to bf16 (nearest even).
+template <bool BF16>
+__device__ __forceinline__ typename std::conditional<BF16, uint16_t, float>::type to_out(uint32_t bits) {
+  if constexpr (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(bits)));
+  else return __uint_as_float(bits);
+}
 
 // One warp: a chunk's raw g and beta into the scalar area by 4-byte
 // asynchronous copies; tokens past the chunk's end read as zero.
@@ -619,9 +665,18 @@ __device__ __forceinline__ float p2_chunk_setup(float *sc, P2Misc *misc, float c
 // outputs, Z's scaling and the next chunk's V come in beside it.  Thread 32
 // issues the MMAs, thread 0 the copies, warp 2 sets up the next chunk's
 // scalars while batch 2 runs.  Waits are bounded.
-template <bool DECAY_AFTER, bool SPLIT>
+// BF16IN: bf16 activations (with SPLIT): hi-only [K; Q] and K^T images,
+// [X | Z] and the state update two products per K step (the terms with a
+// zero lo half left out), V rows as bf16, y rounded to bf16 when stored.
+template <bool DECAY_AFTER, bool SPLIT, bool BF16IN>
 __global__ void __launch_bounds__(NTH, 1)
     gdn_chunk_state_kernel(const StateArgs a, const __grid_constant__ CUtensorMap tm_v) {
+  static_assert(SPLIT || !BF16IN, "bf16 activations take split operands");
+  using Out = typename std::conditional<BF16IN, uint16_t, float>::type;
+  constexpr uint32_t kKqBytes = BF16IN ? 32768 : 65536;   // the [K; Q] image
+  constexpr uint32_t kKtBytes = BF16IN ? 16384 : 32768;   // the K^T image
+  constexpr uint32_t kKtOff = BF16IN ? 8192 : 16384;      // K^T in the key-head slot (floats)
+  constexpr uint32_t kVBytes = BF16IN ? 16384 : 32768;    // a chunk's V rows
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // operate from a 1024-byte aligned base (the swizzled image needs it)
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -683,13 +738,13 @@ __global__ void __launch_bounds__(NTH, 1)
   __syncthreads();  // barriers initialised and buffers zeroed before anyone uses them
   // chunk 0's inputs start arriving while the state is loaded
   if (tid == 0) {
-    mbar_expect_tx(bar_kq, 65536);
-    bulk_load(sbase + P2_KQ, wkseq, 65536, bar_kq);
-    mbar_expect_tx(bar_kt, kRowsBytes);
-    bulk_load(sbase + P2_KT, wkseq + 16384, kRowsBytes, bar_kt);
+    mbar_expect_tx(bar_kq, kKqBytes);
+    bulk_load(sbase + P2_KQ, wkseq, kKqBytes, bar_kq);
+    mbar_expect_tx(bar_kt, kKtBytes);
+    bulk_load(sbase + P2_KT, wkseq + kKtOff, kKtBytes, bar_kt);
     load_image<SPLIT>(sbase + P2_TPP, wseq, bar_t);
     load_image<SPLIT>(sbase + P2_P, wseq + 4096, bar_p);
-    mbar_expect_tx(bar_v, kRowsBytes);
+    mbar_expect_tx(bar_v, kVBytes);
     tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb), static_cast<int>(s), bar_v);
   }
   // copies armed and MMA batches committed per barrier (uniform over the
@@ -755,7 +810,9 @@ __global__ void __launch_bounds__(NTH, 1)
   float vr[32];
   if (!mbar_wait(bar_v, 0)) misc->failed = 1;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) vr[j] = sVS[(32 * half + j) * D + row];
+  for (int j = 0; j < 32; ++j)
+    vr[j] = BF16IN ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(sVS)[(32 * half + j) * D + row]) << 16)
+                   : sVS[(32 * half + j) * D + row];
 
   bool failed = false;
   for (uint32_t ch = 0; ch < nchunks; ++ch) {
@@ -782,7 +839,7 @@ __global__ void __launch_bounds__(NTH, 1)
     }
     if (tid == 0 && more) {  // V rows are free: the next chunk's
       fence_async_smem();
-      mbar_expect_tx(bar_v, kRowsBytes);
+      mbar_expect_tx(bar_v, kVBytes);
       tma_load_4d(sbase + P2_VS, &tm_v, 0, static_cast<int>(vh), static_cast<int>(tb + t0 + C), static_cast<int>(s),
                   bar_v);
     }
@@ -790,7 +847,14 @@ __global__ void __launch_bounds__(NTH, 1)
     // ---- 1. [X | Z] = S~ [K; Q]^T
     if (tid == ISSUER) {
       if (!mbar_wait(bar_kq, par)) misc->failed = 1;
-      if constexpr (SPLIT) {
+      if constexpr (BF16IN) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t bh = sdesc_sw128(sbase + P2_KQ + (ks >> 2) * 16384 + (ks & 3) * 32);
+          mma_ts<true>(tmem + tm_x, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 128), ks > 0);
+          mma_ts<true>(tmem + tm_x, tmem + P2_TM_U + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        }
+      } else if constexpr (SPLIT) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t b = sbase + P2_KQ + (ks >> 2) * 32768 + (ks & 3) * 32;
@@ -814,14 +878,14 @@ __global__ void __launch_bounds__(NTH, 1)
       __syncwarp();
       fence_after();
       const uint32_t tm_yp = (par ? P2_TM_XY0 : P2_TM_XY1) + 64;
-      float *obase = a.output + ((static_cast<size_t>(s) * a.nt + tb + (t0 - C)) * a.nv + vh) * D + row;
+      Out *obase = static_cast<Out *>(a.output) + ((static_cast<size_t>(s) * a.nt + tb + (t0 - C)) * a.nv + vh) * D + row;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t yv[32];
         GDN_TMEM_LD32(tl + tm_yp + 32 * h, yv);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) obase[static_cast<size_t>(32 * h + j) * v_tok] = __uint_as_float(yv[j]);
+        for (int j = 0; j < 32; ++j) obase[static_cast<size_t>(32 * h + j) * v_tok] = to_out<BF16IN>(yv[j]);
       }
     }
 
@@ -854,8 +918,8 @@ __global__ void __launch_bounds__(NTH, 1)
 
     // ---- 3. U^T = W T''^T; [K; Q] is free for the next chunk's
     if (tid == 0 && more) {
-      mbar_expect_tx(bar_kq, 65536);
-      bulk_load(sbase + P2_KQ, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats, 65536, bar_kq);
+      mbar_expect_tx(bar_kq, kKqBytes);
+      bulk_load(sbase + P2_KQ, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats, kKqBytes, bar_kq);
     }
     if (tid == ISSUER) {
       if (!mbar_wait(bar_t, par)) misc->failed = 1;
@@ -944,7 +1008,7 @@ __global__ void __launch_bounds__(NTH, 1)
         for (int ks = 0; ks < C / 16; ++ks) {
           const uint64_t bh = sdesc(sbase + P2_KT + ks * 256, 1024), bl = sdesc(sbase + P2_KT + 16384 + ks * 256, 1024);
           mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bh, idesc_bf16(128, 128), 1);
-          mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 128), 1);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 8 * ks, bl, idesc_bf16(128, 128), 1);
           mma_ts<true>(tmem + P2_TM_S, tmem + P2_TM_W + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
         }
         mma_commit(mbar2s);
@@ -982,7 +1046,9 @@ __global__ void __launch_bounds__(NTH, 1)
       }
       if (!mbar_wait(bar_v, par ^ 1)) misc->failed = 1;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) vr[j] = sVS[(32 * half + j) * D + row];
+      for (int j = 0; j < 32; ++j)
+        vr[j] = BF16IN ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(sVS)[(32 * half + j) * D + row]) << 16)
+                       : sVS[(32 * half + j) * D + row];
       if constexpr (SPLIT) {  // the next chunk's A operand S~ = hi + lo, once the update is done
         if (!mbar_wait(mbar2s, par)) misc->failed = 1;
         __syncwarp();
@@ -995,8 +1061,8 @@ __global__ void __launch_bounds__(NTH, 1)
       if (!mbar_wait(mbar2, par)) misc->failed = 1;
       if (more) {
         load_image<SPLIT>(sbase + P2_P, wseq + static_cast<size_t>(ch + 1) * kWsFloats + 4096, bar_p);
-        mbar_expect_tx(bar_kt, kRowsBytes);
-        bulk_load(sbase + P2_KT, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats + 16384, kRowsBytes, bar_kt);
+        mbar_expect_tx(bar_kt, kKtBytes);
+        bulk_load(sbase + P2_KT, wkseq + static_cast<size_t>(ch + 1) * kWsKFloats + kKtOff, kKtBytes, bar_kt);
       }
     }
     if (more) { ++n_ld; ++n_v; }
@@ -1014,11 +1080,11 @@ __global__ void __launch_bounds__(NTH, 1)
     uint32_t yv[32];
     GDN_TMEM_LD32(tl + tm_yl + 32 * half, yv);
     tmem_wait_ld();
-    float *obase = a.output + ((static_cast<size_t>(s) * a.nt + tb + cl * C) * a.nv + vh) * D + row;
+    Out *obase = static_cast<Out *>(a.output) + ((static_cast<size_t>(s) * a.nt + tb + cl * C) * a.nv + vh) * D + row;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int i = 32 * half + j;
-      if (i < ncl) obase[static_cast<size_t>(i) * v_tok] = __uint_as_float(yv[j]);
+      if (i < ncl) obase[static_cast<size_t>(i) * v_tok] = to_out<BF16IN>(yv[j]);
     }
   }
 
@@ -1081,23 +1147,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A [128, heads, n_tokens, n_seqs] f32 tensor (128 contiguous) as a 4-D map
-// whose box is `inner` floats x 1 head x 64 tokens x 1 seq.
+// A [128, heads, n_tokens, n_seqs] f32 (or bf16) tensor (128 contiguous) as a
+// 4-D map whose box is `inner` elements x 1 head x 64 tokens x 1 seq.
 cudaError_t rows_map(CUtensorMap *tm, const void *base, uint32_t heads, uint32_t nt, uint32_t ns,
-                     uint32_t inner, CUtensorMapSwizzle swizzle) {
+                     uint32_t inner, CUtensorMapSwizzle swizzle, bool bf16 = false) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t row = bf16 ? 256 : 512;  // bytes of one 128-element row
   const cuuint64_t dims[4] = {128, heads, nt, ns};
-  const cuuint64_t strides[3] = {512, 512ull * heads, 512ull * heads * nt};
+  const cuuint64_t strides[3] = {row, row * heads, row * heads * nt};
   const cuuint32_t box[4] = {inner, 1, 64, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box,
+  const CUresult r = enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                         const_cast<void *>(base), dims, strides, box,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool DA, bool SPLIT>
+template <bool DA, bool SPLIT, bool BF16IN>
 cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t nchunks = (p.nt + C - 1) / C;
   const unsigned long long heads = static_cast<unsigned long long>(p.nv) * p.ns;
@@ -1122,9 +1190,11 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   if (p1_smem(hpc) > 232448u) return cudaErrorInvalidConfiguration;  // raw gates of the heads in a CTA
   if (reinterpret_cast<uintptr_t>(p.v) % 16 != 0) return cudaErrorMisalignedAddress;  // TMA source
   CUtensorMap tm_k, tm_q, tm_v;
-  e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (e == cudaSuccess) e = rows_map(&tm_q, p.q, p.nk, p.nt, p.ns, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (e == cudaSuccess) e = rows_map(&tm_v, p.v, p.nv, p.nt, p.ns, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // K and Q boxes: 128-byte rows (32 f32 or 64 bf16), swizzled like the MMA's operand
+  const uint32_t kq_inner = BF16IN ? 64 : 32;
+  e = rows_map(&tm_k, p.k, p.nk, p.nt, p.ns, kq_inner, CU_TENSOR_MAP_SWIZZLE_128B, BF16IN);
+  if (e == cudaSuccess) e = rows_map(&tm_q, p.q, p.nk, p.nt, p.ns, kq_inner, CU_TENSOR_MAP_SWIZZLE_128B, BF16IN);
+  if (e == cudaSuccess) e = rows_map(&tm_v, p.v, p.nv, p.nt, p.ns, 128, CU_TENSOR_MAP_SWIZZLE_NONE, BF16IN);
   if (e != cudaSuccess) return e;
 
   float *ws_k = ws + static_cast<size_t>(p.nv) * p.ns * nchunks * kWsFloats;
@@ -1133,7 +1203,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   pa.g = p.g; pa.beta = p.beta; pa.ws = ws; pa.ws_k = ws_k;
   pa.nk = p.nk; pa.nv = p.nv; pa.nt = p.nt; pa.group = group; pa.hpc = hpc; pa.parts = parts;
   pa.khead_div = p.khead_div ? 1u : 0u; pa.nchunks = nchunks; pa.q_scale = p.q_scale;
-  auto prep = gdn_chunk_prep_kernel<DA, SPLIT>;
+  auto prep = gdn_chunk_prep_kernel<DA, SPLIT, BF16IN>;
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p1_smem(hpc)));
   if (e != cudaSuccess) return e;
   prep<<<static_cast<unsigned>(prep_blocks), NTH, p1_smem(hpc), stream>>>(pa, tm_k, tm_q);
@@ -1142,7 +1212,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 
   StateArgs sa;
   sa.g = p.g; sa.beta = p.beta;
-  sa.state_in = p.state_in; sa.ws = ws; sa.ws_k = ws_k; sa.output = static_cast<float *>(p.output);
+  sa.state_in = p.state_in; sa.ws = ws; sa.ws_k = ws_k; sa.output = p.output;
   sa.state_out = p.state_out;
   sa.nk = p.nk; sa.nv = p.nv; sa.nt = p.nt; sa.group = pa.group; sa.khead_div = pa.khead_div;
   sa.nchunks = nchunks; sa.q_scale = p.q_scale;
@@ -1150,7 +1220,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
   const uint32_t segs = state_segments(heads, nchunks, want);
   sa.seg_len = (nchunks + segs - 1) / segs;
   const unsigned long long tasks2 = heads * ((nchunks + sa.seg_len - 1) / sa.seg_len);
-  auto state = gdn_chunk_state_kernel<DA, SPLIT>;
+  auto state = gdn_chunk_state_kernel<DA, SPLIT, BF16IN>;
   e = cudaFuncSetAttribute(state, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P2_SMEM));
   if (e != cudaSuccess) return e;
   // one launch per group of up to `want` (one CTA per SM) segments, in the
@@ -1170,7 +1240,7 @@ cudaError_t launch_split(const Problem &p, float *ws, cudaStream_t stream) {
 }  // namespace
 
 bool chunked_split_supported(const Problem &p) {
-  return chunked_supported(p) && !p.io_bf16 && p.nk > 0 && p.nv / p.nk <= kMaxSplitGroup;
+  return chunked_supported(p) && p.nk > 0 && p.nv / p.nk <= kMaxSplitGroup;
 }
 
 size_t chunked_split_workspace_bytes(const Problem &p) {
@@ -1182,10 +1252,13 @@ size_t chunked_split_workspace_bytes(const Problem &p) {
 cudaError_t launch_chunked_split(const Problem &p, float *workspace, cudaStream_t stream) {
   if (!chunked_split_supported(p)) return cudaErrorInvalidValue;
   if (p.tf32)
-    return p.decay_after ? launch_split<true, false>(p, workspace, stream)
-                         : launch_split<false, false>(p, workspace, stream);
-  return p.decay_after ? launch_split<true, true>(p, workspace, stream)
-                       : launch_split<false, true>(p, workspace, stream);
+    return p.decay_after ? launch_split<true, false, false>(p, workspace, stream)
+                         : launch_split<false, false, false>(p, workspace, stream);
+  if (p.io_bf16)
+    return p.decay_after ? launch_split<true, true, true>(p, workspace, stream)
+                         : launch_split<false, true, true>(p, workspace, stream);
+  return p.decay_after ? launch_split<true, true, false>(p, workspace, stream)
+                       : launch_split<false, true, false>(p, workspace, stream);
 }
 
 // ---------------------------------------------------------------- fixed scratch

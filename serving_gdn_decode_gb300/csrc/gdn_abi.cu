@@ -406,6 +406,15 @@ gdn_status gdn_forward_ws(const float *q, const float *k, const float *v, const 
              false, false, stream, true, workspace, workspace_bytes);
 }
 
+gdn_status gdn_forward_ws_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                               const float *g, const float *beta, const float *state_in,
+                               gdn_bf16 *output, float *state_out, const uint32_t *params,
+                               size_t n_params, void *workspace, size_t workspace_bytes,
+                               gdn_stream_t stream) {
+  return run(Buffers{q, k, v, g, beta, state_in, output, state_out, nullptr}, params, n_params, 0,
+             false, true, stream, true, workspace, workspace_bytes);
+}
+
 gdn_status gdn_forward_chunked_noalloc(const float *q, const float *k, const float *v,
                                        const float *g, const float *beta, const float *state_in,
                                        float *output, float *state_out, const uint32_t *params,

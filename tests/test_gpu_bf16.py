@@ -56,8 +56,10 @@ def _dev_bf16(torch, x):
     return d
 
 
-def run_bf16(torch, w, x, params, capture=False, in_place=False):
-    """Run the bf16 path.  Returns numpy (output as f32 values, state_out, capture|None)."""
+def run_bf16(torch, w, x, params, capture=False, in_place=False, workspace=False):
+    """Run the bf16 path (gdn_forward_ws_bf16 with a workspace of
+    gdn_workspace_size's bytes when ``workspace``).  Returns numpy (output as
+    f32 values, state_out, capture|None)."""
     from serving_gdn_decode_gb300 import _native as nat
     d = _dev_bf16(torch, x)
     out = torch.empty(w.v_elems, dtype=torch.bfloat16, device="cuda")
@@ -69,6 +71,10 @@ def run_bf16(torch, w, x, params, capture=False, in_place=False):
         cap = torch.empty(w.capture_elems, dtype=torch.float32, device="cuda")
         nat.gdn_forward_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params,
                                 cap)
+    elif workspace:
+        cap = None
+        ws = torch.empty(max(16, nat.gdn_workspace_size(params)), dtype=torch.uint8, device="cuda")
+        nat.gdn_forward_ws(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params, ws)
     else:
         cap = None
         nat.gdn_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], st_in, out, st, params)
@@ -134,6 +140,34 @@ def test_bf16_parity_and_f32_identity(torch, oracle_mod, case, flags):
             "state_capture differs from f32 path"
     assert np.array_equal(out.view(np.uint32), round_to_bf16(fo).view(np.uint32)), \
         "output is not the f32 path's output rounded to bf16"
+
+
+TWO_PASS = [  # (n_k, n_v, n_tokens, n_seqs, path)
+    (2, 4, 130, 2, 0),             # automatic: the chunked form, 2 full chunks + 2
+    (2, 6, 9, 2, PATH_CHUNKED),    # one partial chunk
+    (1, 8, 64, 1, PATH_CHUNKED),   # exactly one chunk, eight value heads on one key head
+    (4, 4, 70, 1, PATH_CHUNKED),   # one value head per key head
+]
+
+
+@pytest.mark.parametrize("flags", [dict(), dict(decay_after=True, khead_div=True)], ids=["df-mod", "da-div"])
+@pytest.mark.parametrize("case", TWO_PASS, ids=[str(c) for c in TWO_PASS])
+def test_bf16_two_pass_parity_and_f32_identity(torch, oracle_mod, case, flags):
+    """gdn_forward_ws_bf16: the two-pass chunked form with bf16 activations,
+    against the oracle and, bit for bit, against gdn_forward_ws on the same
+    widened values (output: that output rounded to bf16)."""
+    nk, nv, nt, ns, path = case
+    w = Workload("bf16", 128, 128, nk, nv, nt, ns)
+    p = w.params(path=path, **flags)
+    x = make_inputs(w, 13, act="bf16")
+    out, st, _ = run_bf16(torch, w, x, p, workspace=True)
+    ro, rs, _ = oracle_mod.forward(p, **x)
+    assert_output_bf16(out, ro, nt)
+    assert_close("state_out", st, rs, nt)
+    fo, fs, _ = run_gpu(w, x, p, workspace=True)
+    assert np.array_equal(st.view(np.uint32), fs.view(np.uint32)), "state_out differs from the f32 two-pass form"
+    assert np.array_equal(out.view(np.uint32), round_to_bf16(fo).view(np.uint32)), \
+        "output is not the f32 two-pass form's output rounded to bf16"
 
 
 def test_bf16_in_place_decode(torch, oracle_mod):
