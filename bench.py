@@ -109,7 +109,9 @@ def chunked_mma_flops(w, two_pass: bool, split: bool = False, bf16_in: bool = Fa
     with split-bf16 operands every product runs as three bf16 MMAs, so three
     times the TF32 form's count; with bf16 activations (one-pass form) the
     products of exact inputs leave out their zero lo terms: the Gram one
-    product, V^T T''^T, X = S K^T and S Q^T two each, the rest three).
+    product, V^T T''^T, X = S K^T and S Q^T two each, the rest three; in the
+    two-pass form the Gram one, [X | Z] and the state update two, the rest
+    three).
     Per (seq, value head, chunk) the one-pass form runs the Gram [K;Q]K^T
     (M 128, N 64, K 128), V^T T''^T, X = S K^T, X(-T')^T, S Q'^T, U^T P'^T
     (each M 128, N 64; K 64, 128, 64, 128, 64) and S += U^T K'^T (M 128,
@@ -121,6 +123,9 @@ def chunked_mma_flops(w, two_pass: bool, split: bool = False, bf16_in: bool = Fa
     nch = -(-w.n_tokens // 64)
     mm = lambda m, n, k: 2 * m * n * k  # noqa: E731
     gram = mm(128, 64, 128)
+    if bf16_in and two_pass:
+        per_head = 2 * mm(128, 128, 128) + 3 * mm(128, 64, 64) + 3 * mm(128, 64, 64) + 2 * mm(128, 128, 64)
+        return nch * w.n_seqs * (w.n_v_heads * per_head + w.n_k_heads * gram)
     if bf16_in and not two_pass:
         per_head = gram + 2 * mm(128, 64, 64) + 2 * mm(128, 64, 128) + 3 * mm(128, 64, 64) \
             + 2 * mm(128, 64, 128) + 3 * mm(128, 64, 64) + 3 * mm(128, 128, 64)
@@ -159,7 +164,7 @@ def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, 
                    peak_kind=f"derived: {SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop "
                              f"(FMA) x {mhz:.0f} MHz ({mhz_src})",
                    flops_per_call=ex, flops_counted="executed: 3 FMAs per state cell per token")
-        traffic_key = "scan"
+        traffic_key = "scan" + ("_bf16" if act == "bf16" else "")
     else:
         tf32 = kind.endswith("_tf32")
         two = kind.startswith("chunked_two_pass")
@@ -177,7 +182,8 @@ def prefill_roofline(kind: str, w, seconds: float, peaks: dict, peak_kind: str, 
                                      "product of split operands")
         out.update(bound="tensor", achieved=round(ex / seconds / 1e12, 2), peak=round(peak, 1),
                    flops_per_call=ex)
-        traffic_key = ("chunked_split" if two else "chunked") + ("_tf32" if tf32 else "")
+        traffic_key = ("chunked_split" if two else "chunked") + ("_tf32" if tf32 else "") + \
+            ("_bf16" if act == "bf16" else "")
     out["frac"] = round(out["achieved"] / out["peak"], 3)
     out["hbm_achieved_GB_s"] = round(bytes_ / seconds / 1e9, 1)
     out["hbm_frac"] = round(bytes_ / seconds / 1e9 / hbm, 3)
@@ -491,18 +497,21 @@ def extras(torch, nat, peaks, peak_kind, device):
             ("long_prefill_chunked_two_pass_tf32", wp.params(path=PATH_CHUNKED_TF32), "ws",
              "chunked_two_pass_tf32", 500),
             ("long_prefill_auto_bf16", wp.params(), "bf16", None, 300),
+            ("long_prefill_auto_ws_bf16", wp.params(), "ws_bf16", None, 400),
             ("long_prefill_scan_bf16", wp.params(path=PATH_SCAN), "bf16", "scan", 100)):
-        sets = make_sets(torch, wp, 1, device, act="f32" if act == "ws" else act)
-        if act == "ws":
+        ws = act.startswith("ws")
+        act = {"ws": "f32", "ws_bf16": "bf16"}.get(act, act)
+        sets = make_sets(torch, wp, 1, device, act=act)
+        if ws:
             sets[0]["ws"] = torch.empty(nat.gdn_workspace_size(params), dtype=torch.uint8,
                                         device=device)
         path = nat.gdn_path_name(params)
         if kind is None:
-            kind = "scan" if path.startswith("scan") else "chunked" if act != "ws" else "chunked_two_pass"
+            kind = "scan" if path.startswith("scan") else "chunked_two_pass" if ws else "chunked"
         clocks = ClockSampler(device.index or 0, interval_ms=50)
         t, clk = time_graphed(torch, nat, sets, params, steps, 3, clocks=clocks)
         s = t / steps
-        res[key] = {"path": path + (" (two-pass, gdn_forward_ws)" if act == "ws" else ""),
+        res[key] = {"path": path + (" (two-pass, gdn_forward_ws)" if ws else ""),
                     "ms_per_call": round(s * 1e3, 3),
                     "tokens_per_s": round(wp.n_tokens * wp.n_seqs / s, 1),
                     "head_tokens_per_s": round(wp.n_tokens * wp.n_seqs * wp.n_v_heads / s, 1),

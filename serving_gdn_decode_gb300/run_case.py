@@ -31,6 +31,7 @@ def main(argv=None):
                     help="use gdn_forward_ws with a workspace (two-pass form on the chunked path)")
     ap.add_argument("--commit", action="store_true",
                     help="after each capture call, commit a random accepted token per sequence")
+    ap.add_argument("--bf16", action="store_true", help="bf16 activations (q, k, v, output)")
     a = ap.parse_args(argv)
 
     import torch
@@ -42,10 +43,13 @@ def main(argv=None):
     if a.seqs:
         w = w.with_(n_seqs=a.seqs)
     capture = a.capture or w.capture
-    x = make_inputs(w, 0)
+    x = make_inputs(w, 0, act="bf16" if a.bf16 else "f32")
     dev = torch.device("cuda:0")
     d = {k: torch.from_numpy(v).to(dev) for k, v in x.items()}
-    out = torch.empty(w.v_elems, dtype=torch.float32, device=dev)
+    if a.bf16:
+        for n in ("q", "k", "v"):
+            d[n] = d[n].to(torch.bfloat16)
+    out = torch.empty(w.v_elems, dtype=torch.bfloat16 if a.bf16 else torch.float32, device=dev)
     st = torch.empty(w.state_elems, dtype=torch.float32, device=dev)
     cap = torch.empty(w.capture_elems, dtype=torch.float32, device=dev) if capture else None
     p = w.params(decay_after=a.decay_after, khead_div=a.khead_div, path=PATHS[a.path])

@@ -116,6 +116,8 @@ def test_prefill_flop_counts():
         assert bench.chunked_mma_flops(w, two, split=True) == 3 * bench.chunked_mma_flops(w, two)
     # bf16 activations, one pass: per (value head, chunk) 2 + 2 + 4 + 3 + 4 + 3 + 6 = 24 x 2^20
     assert bench.chunked_mma_flops(w, False, split=True, bf16_in=True) == 64 * 4 * 48 * 24 * mib
+    # ... two passes: per (value head, chunk) 8 + 3 + 3 + 4 = 18, per (key head, chunk) 2 x 2^20
+    assert bench.chunked_mma_flops(w, True, split=True, bf16_in=True) == 64 * 4 * (48 * 18 + 16 * 2) * mib
     assert bench.scan_executed_flops(w) == 6 * 128 * 128 * 48 * 4 * 4096
 
 
