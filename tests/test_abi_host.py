@@ -428,6 +428,28 @@ def test_workspace_checks(L):
 
 
 @no_device
+def test_workspace_bf16_checks(L):
+    """gdn_forward_ws_bf16: the workspace checks of gdn_forward_ws with the
+    bf16 checks of gdn_forward_bf16; the TF32 chunked path is refused."""
+    w = WORKLOADS["long_prefill"].with_(n_tokens=100, n_seqs=1)
+    p = w.params(path=PATH_CHUNKED)
+    need = nat.gdn_workspace_size(p)
+    f = Fake(w)
+    args = [f.addr[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+    ws = 10 * GAP
+    assert nat.forward_ws_raw(*args, p, 0, need, bf16=True) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_ws_raw(*args, p, ws, need - 16, bf16=True) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_ws_raw(*args, p, ws, need, bf16=True) == nat.GDN_ERR_CUDA   # host checks pass
+    assert nat.forward_ws_raw(*args, w.params(), ws, need, bf16=True) == nat.GDN_ERR_CUDA
+    assert nat.forward_ws_raw(*args, w.params(path=PATH_CHUNKED_TF32), ws, need, bf16=True) == \
+        nat.GDN_ERR_UNSUPPORTED
+    assert "f32 activations" in nat.gdn_last_error()
+    v2 = list(args)
+    v2[2] += 2                                               # bf16 v 2-byte aligned only
+    assert nat.forward_ws_raw(*v2, p, ws, need, bf16=True) == nat.GDN_ERR_INVALID_ARGUMENT
+
+
+@no_device
 def test_noalloc_host_checks(L):
     """gdn_forward_chunked_noalloc: the fixed 32 MiB scratch holds 16 chunks
     of 16 value and 16 key heads (2 MiB each); one more chunk is refused
