@@ -170,6 +170,23 @@ def test_bf16_two_pass_parity_and_f32_identity(torch, oracle_mod, case, flags):
         "output is not the f32 two-pass form's output rounded to bf16"
 
 
+@pytest.mark.parametrize("workspace", [False, True], ids=["one-pass", "two-pass"])
+def test_bf16_chunked_segments_and_in_place(torch, workspace):
+    """More (seq, value head) chains than SMs (160 chains of 16 chunks): both
+    chunked forms cut the chains into segments over launches.  With bf16
+    activations the state equals the f32 form's on the same values bit for
+    bit and the output equals its output rounded to bf16, out of place and in
+    place (state_in == state_out)."""
+    w = Workload("bf16seg", 128, 128, 2, 40, 1000, 4)
+    p = w.params(path=PATH_CHUNKED, decay_after=True)
+    x = make_inputs(w, 17, act="bf16")
+    fo, fs, _ = run_gpu(w, x, p, workspace=workspace)
+    for in_place in (False, True):
+        out, st, _ = run_bf16(torch, w, x, p, in_place=in_place, workspace=workspace)
+        assert np.array_equal(st.view(np.uint32), fs.view(np.uint32)), f"state_out (in place: {in_place})"
+        assert np.array_equal(out.view(np.uint32), round_to_bf16(fo).view(np.uint32)), f"output (in place: {in_place})"
+
+
 def test_bf16_in_place_decode(torch, oracle_mod):
     w = Workload("bf16", 128, 128, 4, 8, 1, 4)
     p = w.params()
