@@ -602,8 +602,79 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       stage_kv_async<BF16IN>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
     }
 
-    // ---- 6. T = (I + A)^-1, then -T' (over A) and T'' (over T), canonical
-    tri_inverse(sA, sT, sM, tid);
+    // ---- 6. X = S~ K^T and Y^T = S~ Q^T (TF32: S Q'^T), which need no T, run
+    // on the tensor cores while warps 0-3 invert I + A; with split operands
+    // warps 4-7 then split X into hi | lo over S~ hi and scale Y^T's columns
+    // by c q_scale gamma_r.  Warp 4 issues these products (issuing takes
+    // about 44 cycles an instruction), so the inverse starts at once.
+    if (tid == NTH / 2) {
+      if constexpr (SPLIT) {
+        const uint32_t i64 = idesc_bf16(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {  // X = S~ K^T
+          const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i64, 1);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {  // Yt = S~ Q^T
+          const uint64_t bh = sdesc(sbase + SM_STACK + 16384 + ks * 256, 2048),
+                         bl = sdesc(sbase + SM_STACK + 49152 + ks * 256, 2048);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i64, 1);
+        }
+      } else {
+        const uint32_t i64 = idesc_tf32(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
+          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
+          mma_ts(tmem + TM::Y, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
+                 ks > 0);
+      }
+      mma_commit(mbar);
+    }
+    if (warp < 4) {
+      tri_inverse<128>(sA, sT, sM, tid);
+      if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    } else {
+      if (!mbar_wait(mbar, phase)) misc->failed = 1;
+      if constexpr (SPLIT) {
+        __syncwarp();
+        fence_after();
+        const float *qs = sc + SC_QS * 64;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // this warp's lanes, all 64 columns
+          uint32_t xv[32], xh[16], xl[16];
+          GDN_TMEM_LD32(tl + TM::X + 32 * h, xv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) split2(__uint_as_float(xv[2 * j]), __uint_as_float(xv[2 * j + 1]), xh[j], xl[j]);
+          GDN_TMEM_ST16(tl + TM::SH + 16 * h, xh);
+          GDN_TMEM_ST16(tl + TM::SH + 32 + 16 * h, xl);
+          GDN_TMEM_LD32(tl + TM::Y + 32 * h, xv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) xv[j] = __float_as_uint(__uint_as_float(xv[j]) * qs[32 * h + j]);
+          GDN_TMEM_ST32(tl + TM::Y + 32 * h, xv);
+        }
+        tmem_wait_st();
+      }
+    }
+    phase ^= 1;
+    cta_sync();
+    if (misc->failed) { failed = true; break; }
+    // the stack is free (X and Y^T are done): start the next chunk's Q rows and gates
+    if (ch + 1 < nchunks) {
+      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
+      stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                      sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+    }
+
+    // ---- 7. -T' (over A) and T'' (over T), canonical images
     if constexpr (SPLIT) {
       const float *tps = sc + SC_TPS * 64, *bet = sc + SC_BETA * 64;
       float4 t0[2], t1[2];
@@ -654,17 +725,13 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     }
     fence_async_smem();
     cta_sync();
-    if (misc->failed) { failed = true; break; }
 
-    // ---- 7. the state-dependent products.  Batch 1 builds U^T and the
-    // inter-chunk output; then U^T is made an A operand (rounded to TF32 in
-    // place -- the tensor core would otherwise truncate it -- or split) and,
-    // for an extreme-gate chunk, the chunk's decay is folded into S; batch 2
-    // adds the intra-chunk output and updates S.  Split: batch 1 is X = S~ K^T,
-    // Yt = S~ Q^T and Ut = V^T T''^T; X is split and Yt's columns scaled; then
-    // Ut += X (-T')^T runs on its own.
-    if constexpr (SPLIT) {
-      if (tid == 0) {
+    // ---- 8. U^T = V^T T''^T + X (-T')^T; then U^T made an A operand
+    // (rounded to TF32 in place -- the tensor core would otherwise truncate
+    // it -- or split over S~ lo) and, for an extreme-gate chunk, the chunk's
+    // decay folded into S; batch 2 adds the intra-chunk output and updates S.
+    if (tid == 0) {
+      if constexpr (SPLIT) {
         const uint32_t i64 = idesc_bf16(128, 64);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks) {  // Ut = V^T T''^T
@@ -674,66 +741,27 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           if constexpr (!BF16IN) mma_ts<true>(tmem + TM::U, tmem + TM::V + 32 + 8 * ks, bh, i64, 1);
         }
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // X = S~ K^T
-          const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i64, 1);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // Yt = S~ Q^T
-          const uint64_t bh = sdesc(sbase + SM_STACK + 16384 + ks * 256, 2048),
-                         bl = sdesc(sbase + SM_STACK + 49152 + ks * 256, 2048);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i64, 1);
-        }
-        mma_commit(mbar);
-      }
-      if (!mbar_wait(mbar, phase)) misc->failed = 1;
-      phase ^= 1;
-      fence_after();
-      __syncthreads();
-      if (misc->failed) { failed = true; break; }
-      // the stack is free now: start the next chunk's Q rows and gates
-      if (ch + 1 < nchunks) {
-        const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-        stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                        sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
-      }
-      {  // X -> hi | lo over S~ hi
-        uint32_t xv[32], xh[16], xl[16];
-        GDN_TMEM_LD32(tl + TM::X + 32 * half, xv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) split2(__uint_as_float(xv[2 * j]), __uint_as_float(xv[2 * j + 1]), xh[j], xl[j]);
-        GDN_TMEM_ST16(tl + TM::SH + 16 * half, xh);
-        GDN_TMEM_ST16(tl + TM::SH + 32 + 16 * half, xl);
-        tmem_wait_st();
-      }
-      cta_sync();
-      if (tid == 0) {
-#pragma unroll
         for (int ks = 0; ks < C / 16; ++ks) {  // Ut += X (-T')^T
           const uint64_t bh = sdesc(sbase + SM_TP + ks * 256, 1024), bl = sdesc(sbase + SM_TP + 8192 + ks * 256, 1024);
           mma_ts<true>(tmem + TM::U, tmem + TM::SH + 8 * ks, bh, idesc_bf16(128, 64), 1);
           mma_ts<true>(tmem + TM::U, tmem + TM::SH + 8 * ks, bl, idesc_bf16(128, 64), 1);
           mma_ts<true>(tmem + TM::U, tmem + TM::SH + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
         }
-        mma_commit(mbar);
-      }
-      {  // meanwhile Yt's columns times c q_scale gamma_r (batch 2 adds to them)
-        const float *qs = sc + SC_QS * 64;
-        uint32_t yv[32];
-        GDN_TMEM_LD32(tl + TM::Y + 32 * half, yv);
-        tmem_wait_ld();
+      } else {
+        const uint32_t i64 = idesc_tf32(128, 64);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) yv[j] = __float_as_uint(__uint_as_float(yv[j]) * qs[32 * half + j]);
-        GDN_TMEM_ST32(tl + TM::Y + 32 * half, yv);
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
+          mma_ts(tmem + TM::U, tmem + TM::V + 8 * ks, sdesc(sbase + SM_TPP + ks * 256, 2048), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
+          mma_ts(tmem + TM::U, tmem + TM::X + 8 * ks, sdesc(sbase + SM_TP + ks * 256, 2048), i64, 1);
       }
-      if (!mbar_wait(mbar, phase)) misc->failed = 1;
-      phase ^= 1;
-      fence_after();
+      mma_commit(mbar);
+    }
+    if (!mbar_wait(mbar, phase)) misc->failed = 1;
+    phase ^= 1;
+    fence_after();
+    if constexpr (SPLIT) {
       {  // Ut -> hi | lo over S~ lo
         uint32_t uv[32], uh[16], ul[16];
         GDN_TMEM_LD32(tl + TM::U + 32 * half, uv);
@@ -744,9 +772,21 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         GDN_TMEM_ST16(tl + TM::SL + 32 + 16 * half, ul);
         tmem_wait_st();
       }
-      if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
-      cta_sync();
-      if (tid == 0) {
+    } else {
+      {
+        uint32_t uv[32];
+        GDN_TMEM_LD32(tl + TM::U + 32 * half, uv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rn(__uint_as_float(uv[j])));
+        GDN_TMEM_ST32(tl + TM::U + 32 * half, uv);
+        tmem_wait_st();
+      }
+    }
+    if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
+    cta_sync();
+    if (tid == 0) {
+      if constexpr (SPLIT) {
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks) {  // Yt += Ut P'^T
           const uint64_t bh = sdesc(sbase + SM_P + ks * 256, 1024), bl = sdesc(sbase + SM_P + 8192 + ks * 256, 1024);
@@ -761,49 +801,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           mma_ts<true>(tmem + TM::S, tmem + TM::SL + 8 * ks, bl, idesc_bf16(128, 128), 1);
           mma_ts<true>(tmem + TM::S, tmem + TM::SL + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
         }
-        mma_commit(mbar);
-      }
-    } else {
-      if (tid == 0) {
-        const uint32_t i64 = idesc_tf32(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // Ut = V^T T''^T
-          mma_ts(tmem + TM::U, tmem + TM::V + 8 * ks, sdesc(sbase + SM_TPP + ks * 256, 2048), i64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
-          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // Ut += X (-T')^T
-          mma_ts(tmem + TM::U, tmem + TM::X + 8 * ks, sdesc(sbase + SM_TP + ks * 256, 2048), i64, 1);
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
-          mma_ts(tmem + TM::Y, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
-                 ks > 0);
-        mma_commit(mbar);
-      }
-      if (!mbar_wait(mbar, phase)) misc->failed = 1;
-      phase ^= 1;
-      fence_after();
-      __syncthreads();
-      if (misc->failed) { failed = true; break; }
-      // the stack's Q half is free now: start the next chunk's Q rows and gates
-      if (ch + 1 < nchunks) {
-        const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-        stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                        sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
-      }
-      {
-        uint32_t uv[32];
-        GDN_TMEM_LD32(tl + TM::U + 32 * half, uv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) uv[j] = __float_as_uint(tf32_rn(__uint_as_float(uv[j])));
-        GDN_TMEM_ST32(tl + TM::U + 32 * half, uv);
-        tmem_wait_st();
-      }
-      if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
-      cta_sync();
-      if (tid == 0) {
+      } else {
 #pragma unroll
         for (int ks = 0; ks < C / 8; ++ks)   // Yt += Ut P'^T
           mma_ts(tmem + TM::Y, tmem + TM::U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048),
@@ -812,8 +810,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         for (int ks = 0; ks < C / 8; ++ks)   // S += Ut K'^T
           mma_ts(tmem + TM::S, tmem + TM::U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
                  idesc_tf32(128, 128), 1);
-        mma_commit(mbar);
       }
+      mma_commit(mbar);
     }
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;

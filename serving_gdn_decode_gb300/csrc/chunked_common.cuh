@@ -257,16 +257,27 @@ __device__ __forceinline__ void blk_mac(float (&c0)[4], float (&c1)[4], const fl
   }
 }
 
+// Barrier of the NT threads running tri_inverse: the whole CTA, or warps
+// 0-3 alone (named barrier 1) while the other warps do other work.
+template <int NT>
+__device__ __forceinline__ void tri_sync() {
+  if constexpr (NT == NTH) __syncthreads();
+  else asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
+}
+
 // T = (I + A)^-1 for a strictly lower 64 x 64 A (plain, row stride LD), by
 // doubling over 16 x 16 blocks: the four diagonal blocks by forward
 // substitution (one thread per column); then the two 32 x 32 diagonal blocks,
 // T_{j+1,j} = -T_{j+1,j+1} (A_{j+1,j} T_jj) for j = 0, 2; then the lower-left
 // 32 x 32 quarter, -T[hi] (A[hi,lo] T[lo]), as four 16 x 16 output blocks per
 // product, one warp each (2 x 4 register tiles).  M is 4 x 256 floats of
-// scratch for the inner products.
+// scratch for the inner products.  Run by threads 0 .. NT-1 (NT = 128: warps
+// 0-3, which do all the work; NT = NTH: the whole CTA).
+template <int NT = NTH>
 __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
+  static_assert(NT == NTH || NT == 128, "tri_inverse runs on the CTA or on warps 0-3");
   // the six blocks above the diagonal stay zero
-  for (int e = tid; e < 6 * 256; e += NTH) {
+  for (int e = tid; e < 6 * 256; e += NT) {
     const int b = e >> 8, rr = (e & 255) >> 4, cc = e & 15;
     const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2), bj = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
     T[(16 * bi + rr) * LD + 16 * bj + cc] = 0.f;
@@ -284,7 +295,7 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) T[(base + r) * LD + base + cl] = x[r];
   }
-  __syncthreads();
+  tri_sync<NT>();
   const int warp = tid >> 5, lane = tid & 31;
   const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);
   float *mw = M + warp * 256;
@@ -303,7 +314,7 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
     *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
     *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
   }
-  __syncthreads();
+  tri_sync<NT>();
 
   // lower-left quarter, rows r = 2, 3 and columns c = 0, 1 (16-blocks): warp
   // 2(r-2) + c first forms M'_rc = sum_{k=c}^{1} A_rk T_kc ...
@@ -315,7 +326,7 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
     *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
     *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
   }
-  __syncthreads();
+  tri_sync<NT>();
   // ... then T_rc = -sum_{k=2}^{r} T_rk M'_kc (T_rr lower triangular)
   if (warp < 4) {
     float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -326,7 +337,7 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
     *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
     *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
   }
-  __syncthreads();
+  tri_sync<NT>();
 }
 
 }  // namespace
