@@ -112,7 +112,8 @@ struct ChunkArgs {
 };
 
 struct Misc {
-  unsigned long long mbar;
+  unsigned long long mbar;   // MMA commits within a chunk
+  unsigned long long mbar2;  // batch 2 (output and state update), waited in the next chunk
   uint32_t tmem_base;
   int failed;
   float c_renorm;   // factor folded into S at the chunk start (if do_renorm)
@@ -121,6 +122,7 @@ struct Misc {
   int do_renorm;
   int do_fold;
 };
+static_assert(sizeof(Misc) <= 64, "misc area");
 
 // bf16 activations: staged rows of 128 bf16 at a stride of 136 (272 bytes)
 constexpr int LDSB = 136;
@@ -129,16 +131,17 @@ constexpr int LDSB = 136;
 // the scalar area; tokens past the chunk's end are zero-filled.  f32: into
 // the stack's Q half (rows 64..127) in the TF32 canonical order; bf16
 // activations: straight into the bf16 canonical image of the stack's Q rows
-// (a 16-byte row of a core is 8 consecutive d_k of one token).
-template <bool BF16IN>
+// (a 16-byte row of a core is 8 consecutive d_k of one token).  Issued by
+// NT threads, tid counted from the first of them.
+template <bool BF16IN, int NT = NTH>
 __device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const void *qv, size_t kq_tok,
                                                         const float *g, const float *beta, size_t sc0,
                                                         size_t nv, int nc, int tid) {
   if constexpr (BF16IN) {
     const uint16_t *qbase = static_cast<const uint16_t *>(qv);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int cc = tid + NTH * it;      // token cc >> 4, d_k 8 (cc & 15) .. +7
+    for (int it = 0; it < 4 * (NTH / NT); ++it) {
+      const int cc = tid + NT * it;       // token cc >> 4, d_k 8 (cc & 15) .. +7
       const int r = cc >> 4, d0 = 8 * (cc & 15);
       cp_async16(sbase + SM_STACK + canon16(64 + r, d0, 128), qbase + (r < nc ? r : 0) * kq_tok + d0,
                  r < nc ? 16u : 0u);
@@ -146,8 +149,8 @@ __device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const vo
   } else {
     const float *qbase = static_cast<const float *>(qv);
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int cc = tid + NTH * it;      // 16-byte chunk within the Q half
+    for (int it = 0; it < 8 * (NTH / NT); ++it) {
+      const int cc = tid + NT * it;       // 16-byte chunk within the Q half
       const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
       cp_async16(sbase + SM_STACK + 32768 + cc * 16, qbase + (r < nc ? r : 0) * kq_tok + 4 * c4,
                  r < nc ? 16u : 0u);
@@ -164,15 +167,16 @@ __device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const vo
 
 // Asynchronous copies of one chunk's K and V rows (natural layout, row
 // stride LDS floats, or LDSB bf16 with bf16 activations) into the staging
-// buffers; rows past the end are zeros.
-template <bool BF16IN>
+// buffers; rows past the end are zeros.  Issued by NT threads, tid counted
+// from the first of them.
+template <bool BF16IN, int NT = NTH>
 __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, size_t kq_tok, const void *vv,
                                                size_t v_tok, int nc, int tid) {
   if constexpr (BF16IN) {
     const uint16_t *kbase = static_cast<const uint16_t *>(kv), *vbase = static_cast<const uint16_t *>(vv);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int ci = tid + NTH * it;      // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
+    for (int it = 0; it < 4 * (NTH / NT); ++it) {
+      const int ci = tid + NT * it;       // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
       const int r = ci >> 4, c8 = ci & 15;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -183,8 +187,8 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, s
   } else {
     const float *kbase = static_cast<const float *>(kv), *vbase = static_cast<const float *>(vv);
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int ci = tid + NTH * it;      // 16-byte chunk: row ci/32, float4 ci%32
+    for (int it = 0; it < 8 * (NTH / NT); ++it) {
+      const int ci = tid + NT * it;       // 16-byte chunk: row ci/32, float4 ci%32
       const int r = ci >> 5, c4 = ci & 31;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   const float *sVS = reinterpret_cast<const float *>(smem + SM_VS);
   Misc *misc = reinterpret_cast<Misc *>(smem + SM_MISC);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t mbar = smem_addr(&misc->mbar);
+  const uint32_t mbar = smem_addr(&misc->mbar), mbar2 = smem_addr(&misc->mbar2);
 
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -254,6 +258,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar2));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     misc->failed = 0;
   }
@@ -290,7 +295,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   }
 
   float c = 1.f;          // S = c * (TMEM S)
-  uint32_t phase = 0;
+  uint32_t phase = 0, phase2 = 0;
+  bool pending2 = false;  // a batch 2 committed and not yet waited for (uniform over the CTA)
   bool failed = false;
   // Y^T of the chunk starting at token tt0 (ncc tokens) to the output:
   // thread = d_v, tokens [32*half, +32)
@@ -371,9 +377,6 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
     const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
 
-    // ---- 2. fold c into S if needed (no MMA in flight here)
-    if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);
-
     // ---- 3. the stack from the staged rows: K (canonical) and Q (the staged
     // Q rows), rounded to TF32 in place or as bf16 hi and lo images (bf16
     // activations: Q is in place already, K's rows are copied)
@@ -423,10 +426,12 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     fence_async_smem();
     cta_sync();
 
-    // ---- 4. Gram [K;Q] K^T -> TMEM G.  Meanwhile the other operands from the
-    // staged rows -- K'^T (smem), V^T (TMEM), split: S~ as hi and lo (TMEM) --
-    // and the previous chunk's outputs (its Y^T is read before this chunk's
-    // first batch overwrites it).
+    // ---- 4. Gram [K;Q] K^T -> TMEM G.  Meanwhile, once the previous chunk's
+    // batch 2 is done (it ran beside this chunk's first steps): c folded
+    // into S if needed, the other operands from the staged rows -- K'^T
+    // (smem, over the image batch 2 read), V^T (TMEM), split: S~ as hi and lo
+    // (TMEM) -- and the previous chunk's outputs (its Y^T is read before this
+    // chunk's first batch overwrites it).
     if (tid == 0) {
       if constexpr (BF16IN) {
 #pragma unroll
@@ -451,6 +456,13 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       }
       mma_commit(mbar);
     }
+    if (pending2) {
+      if (!mbar_wait(mbar2, phase2)) misc->failed = 1;
+      phase2 ^= 1;
+      pending2 = false;
+      fence_after();
+    }
+    if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);  // c left [2^-30, 2^30] (rare)
     if constexpr (SPLIT) {
       // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
       const float *kts = sc + SC_KTS * 64;
@@ -595,18 +607,14 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       }
     }
     cta_sync();
-    // the staging buffers are free (every thread took its operands from
-    // them before this barrier): start the next chunk's K and V rows
-    if (ch + 1 < nchunks) {
-      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-      stage_kv_async<BF16IN>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok, ncn, tid);
-    }
 
     // ---- 6. X = S~ K^T and Y^T = S~ Q^T (TF32: S Q'^T), which need no T, run
     // on the tensor cores while warps 0-3 invert I + A; with split operands
     // warps 4-7 then split X into hi | lo over S~ hi and scale Y^T's columns
     // by c q_scale gamma_r.  Warp 4 issues these products (issuing takes
-    // about 44 cycles an instruction), so the inverse starts at once.
+    // about 44 cycles an instruction), so the inverse starts at once, and
+    // warps 4-7 stage the next chunk's K and V rows (their copies are issued
+    // off the inverse's path).
     if (tid == NTH / 2) {
       if constexpr (SPLIT) {
         const uint32_t i64 = idesc_bf16(128, 64);
@@ -637,10 +645,18 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       }
       mma_commit(mbar);
     }
+    const bool next = ch + 1 < nchunks;
+    const int ncn = next ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
     if (warp < 4) {
       tri_inverse<128>(sA, sT, sM, tid);
       if (!mbar_wait(mbar, phase)) misc->failed = 1;
     } else {
+      // the staging buffers are free (every thread took its operands from
+      // them before step 5's barrier): the next chunk's K and V rows, issued
+      // here so that warps 0-3 start the inverse at once
+      if (next)
+        stage_kv_async<BF16IN, NTH / 2>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok,
+                                        ncn, tid - NTH / 2);
       if (!mbar_wait(mbar, phase)) misc->failed = 1;
       if constexpr (SPLIT) {
         __syncwarp();
@@ -667,12 +683,6 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     phase ^= 1;
     cta_sync();
     if (misc->failed) { failed = true; break; }
-    // the stack is free (X and Y^T are done): start the next chunk's Q rows and gates
-    if (ch + 1 < nchunks) {
-      const int ncn = static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C));
-      stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                      sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
-    }
 
     // ---- 7. -T' (over A) and T'' (over T), canonical images
     if constexpr (SPLIT) {
@@ -758,6 +768,10 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       }
       mma_commit(mbar);
     }
+    // while U^T runs (the stack is free: X and Y^T are done): the next chunk's Q rows and gates
+    if (next)
+      stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
+                                      sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;
     fence_after();
@@ -811,19 +825,24 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
           mma_ts(tmem + TM::S, tmem + TM::U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
                  idesc_tf32(128, 128), 1);
       }
-      mma_commit(mbar);
+      mma_commit(mbar2);
     }
-    if (!mbar_wait(mbar, phase)) misc->failed = 1;
-    phase ^= 1;
-    fence_after();
+    pending2 = true;
 
-    // (this chunk's outputs are written during the next chunk's Gram, the
-    // last chunk's after the loop)
+    // (batch 2 runs beside the next chunk's first steps, which wait for it
+    // before they touch S, K'^T or Y^T; this chunk's outputs are written
+    // during the next chunk's Gram, the last chunk's after the loop)
     c = misc->c_next;
     cta_sync();
     if (misc->failed) failed = true;
   }
 
+  if (pending2) {
+    if (!mbar_wait(mbar2, phase2)) misc->failed = 1;
+    fence_after();
+  }
+  cta_sync();
+  if (misc->failed) failed = true;
   if (!failed && nchunks > 0) {
     const uint32_t tl0 = (nchunks - 1) * C;
     write_outputs(tl0, static_cast<int>(nt - tl0));

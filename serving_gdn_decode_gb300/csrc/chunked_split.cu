@@ -93,9 +93,6 @@ __device__ __forceinline__ bool chunk_scalars(float *sc, int lane, float *GC_out
 
 // ---------------------------------------------------------------- TMA
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
 // One box of a 4-D tensor map (coordinates innermost first) into shared memory.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, int c2, int c3,
                                             uint32_t bar) {
@@ -103,11 +100,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
-}
-// A contiguous global block into shared memory (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 // K-major SWIZZLE_128B operand descriptor: 8-row x 128-byte atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
