@@ -64,20 +64,28 @@ using namespace chunked;
 
 // TMEM columns
 template <bool SPLIT> struct Tm;
+// X, Y^T and S are adjacent: [X | Y^T] is one N = 128 accumulator and
+// [Y^T | S] one N = 192 accumulator; the Gram takes X's columns, which are
+// dead from the previous chunk's U^T product on
 template <> struct Tm<false> {
-  static constexpr uint32_t S = 0, X = 128, U = 192, Y = 256, G = 320, V = 384;
+  static constexpr uint32_t X = 0, Y = 64, S = 128, G = 0, U = 256, V = 320;
 };
 template <> struct Tm<true> {  // SH / SL: S~ hi and lo, then X hi | lo and Ut hi | lo
-  static constexpr uint32_t S = 0, SH = 128, SL = 192, V = 256, U = 320, Y = 384, G = 448, X = 448;
+  static constexpr uint32_t X = 0, Y = 64, S = 128, G = 0, SH = 256, SL = 320, V = 384, U = 448;
 };
+static_assert(Tm<false>::Y == Tm<false>::X + 64 && Tm<true>::Y == Tm<true>::X + 64 &&
+              Tm<false>::S == Tm<false>::Y + 64 && Tm<true>::S == Tm<true>::Y + 64, "[X | Y^T | S] contiguous");
 constexpr uint32_t TM_COLS = 512;
 
 // shared memory map (bytes)
 constexpr uint32_t SM_STACK = 0;                     // [K;Q] 128 x 128 canonical, 64 KB (split:
                                                      // hi 32 KB, then lo; Q rows from 16 KB on)
-constexpr uint32_t SM_KT = SM_STACK + 65536;         // K'^T 128 x 64 canonical, 32 KB
-constexpr uint32_t SM_P = SM_KT + 32768;             // P'   64 x 64 canonical, 16 KB
-constexpr uint32_t SM_A = SM_P + 16384;              // A plain 64 x LD; then -T' (canonical)
+constexpr uint32_t SM_P = SM_STACK + 65536;          // [P'; K'^T]: P' 64 x 64 canonical, then K'^T
+                                                     // 128 x 64 canonical, rows continuing (one B
+                                                     // operand of 192 rows), 48 KB; split: the hi
+                                                     // images, then the lo images from SM_P + PK_LO
+constexpr uint32_t PK_LO = 24576;
+constexpr uint32_t SM_A = SM_P + 49152;              // A plain 64 x LD; then -T' (canonical)
 constexpr uint32_t SM_T = SM_A + 64 * LD * 4;        // T plain 64 x LD; then T'' (canonical)
 constexpr uint32_t SM_M = SM_T + 64 * LD * 4;        // block products, 4 x 256 f32
 constexpr uint32_t SM_SC = SM_M + 4 * 256 * 4;       // per-token scalars
@@ -212,6 +220,7 @@ template <bool DECAY_AFTER, bool SPLIT, bool BF16IN>
 __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) {
   static_assert(SPLIT || !BF16IN, "bf16 activations take split operands");
   using TM = Tm<SPLIT>;
+  constexpr uint32_t SM_KT = SM_P + (SPLIT ? 8192 : 16384);  // K'^T: after P''s 64 rows
   using In = typename std::conditional<BF16IN, uint16_t, float>::type;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *sA = reinterpret_cast<float *>(smem + SM_A);
@@ -477,7 +486,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
         split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
         *reinterpret_cast<uint4 *>(smem + SM_KT + canon16(row, i, 64)) = h;
-        *reinterpret_cast<uint4 *>(smem + SM_KT + 16384 + canon16(row, i, 64)) = l;
+        *reinterpret_cast<uint4 *>(smem + SM_KT + PK_LO + canon16(row, i, 64)) = l;
       }
       // V^T -> TMEM as hi | lo (lane d_v = row, token pairs of [32*half, +32));
       // bf16 activations: V^T is its own hi half
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
             split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
             split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
             *reinterpret_cast<uint4 *>(smem + SM_P + canon16(r, 32 * half + 8 * j, 64)) = h;
-            *reinterpret_cast<uint4 *>(smem + SM_P + 8192 + canon16(r, 32 * half + 8 * j, 64)) = l;
+            *reinterpret_cast<uint4 *>(smem + SM_P + PK_LO + canon16(r, 32 * half + 8 * j, 64)) = l;
           }
         } else {
 #pragma unroll
@@ -608,7 +617,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     }
     cta_sync();
 
-    // ---- 6. X = S~ K^T and Y^T = S~ Q^T (TF32: S Q'^T), which need no T, run
+    // ---- 6. [X | Y^T] = S~ [K; Q]^T (TF32: S [K; Q']^T), one N = 128
+    // product (the stack's K rows, then its Q rows), which needs no T, runs
     // on the tensor cores while warps 0-3 invert I + A; with split operands
     // warps 4-7 then split X into hi | lo over S~ hi and scale Y^T's columns
     // by c q_scale gamma_r.  Warp 4 issues these products (issuing takes
@@ -617,30 +627,18 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // off the inverse's path).
     if (tid == NTH / 2) {
       if constexpr (SPLIT) {
-        const uint32_t i64 = idesc_bf16(128, 64);
+        const uint32_t i128 = idesc_bf16(128, 128);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // X = S~ K^T
+        for (int ks = 0; ks < D / 16; ++ks) {  // [X | Yt] = S~ [K; Q]^T
           const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i64, 1);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i64, 1);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // Yt = S~ Q^T
-          const uint64_t bh = sdesc(sbase + SM_STACK + 16384 + ks * 256, 2048),
-                         bl = sdesc(sbase + SM_STACK + 49152 + ks * 256, 2048);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bh, i64, ks > 0);
-          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::Y, tmem + TM::SH + 8 * ks, bl, i64, 1);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i64, 1);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i128, ks > 0);
+          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i128, 1);
+          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i128, 1);
         }
       } else {
-        const uint32_t i64 = idesc_tf32(128, 64);
 #pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)   // X = S K^T
-          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), i64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)   // Yt = S Q'^T
-          mma_ts(tmem + TM::Y, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + 32768 + ks * 256, 4096), i64,
+        for (int ks = 0; ks < D / 8; ++ks)   // [X | Yt] = S [K; Q']^T
+          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), idesc_tf32(128, 128),
                  ks > 0);
       }
       mma_commit(mbar);
@@ -799,31 +797,20 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     }
     if (do_fold) tmem_scale64(tl + TM::S + 64 * half, c_fold);  // extreme gates: decay S now
     cta_sync();
-    if (tid == 0) {
+    if (tid == 0) {  // [Yt | S] += Ut [P'; K'^T]^T, one N = 192 product
       if constexpr (SPLIT) {
+        const uint32_t i192 = idesc_bf16(128, 192);
 #pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {  // Yt += Ut P'^T
-          const uint64_t bh = sdesc(sbase + SM_P + ks * 256, 1024), bl = sdesc(sbase + SM_P + 8192 + ks * 256, 1024);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, idesc_bf16(128, 64), 1);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bl, idesc_bf16(128, 64), 1);
-          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 32 + 8 * ks, bh, idesc_bf16(128, 64), 1);
-        }
-#pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {  // S += Ut K'^T
-          const uint64_t bh = sdesc(sbase + SM_KT + ks * 256, 1024), bl = sdesc(sbase + SM_KT + 16384 + ks * 256, 1024);
-          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 8 * ks, bh, idesc_bf16(128, 128), 1);
-          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 8 * ks, bl, idesc_bf16(128, 128), 1);
-          mma_ts<true>(tmem + TM::S, tmem + TM::SL + 32 + 8 * ks, bh, idesc_bf16(128, 128), 1);
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t bh = sdesc(sbase + SM_P + ks * 256, 1024), bl = sdesc(sbase + SM_P + PK_LO + ks * 256, 1024);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bh, i192, 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 8 * ks, bl, i192, 1);
+          mma_ts<true>(tmem + TM::Y, tmem + TM::SL + 32 + 8 * ks, bh, i192, 1);
         }
       } else {
 #pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // Yt += Ut P'^T
-          mma_ts(tmem + TM::Y, tmem + TM::U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048),
-                 idesc_tf32(128, 64), 1);
-#pragma unroll
-        for (int ks = 0; ks < C / 8; ++ks)   // S += Ut K'^T
-          mma_ts(tmem + TM::S, tmem + TM::U + 8 * ks, sdesc(sbase + SM_KT + ks * 256, 2048),
-                 idesc_tf32(128, 128), 1);
+        for (int ks = 0; ks < C / 8; ++ks)
+          mma_ts(tmem + TM::Y, tmem + TM::U + 8 * ks, sdesc(sbase + SM_P + ks * 256, 2048), idesc_tf32(128, 192), 1);
       }
       mma_commit(mbar2);
     }
