@@ -554,51 +554,58 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         // and e^{-G_r} when |G| <= 40, exponentials of differences otherwise
         const float Gr = DECAY_AFTER ? sc[SC_GPREV * 64 + r] : G[r];
         const float bgr = br * (DECAY_AFTER ? sc[SC_GAMP * 64 + r] : sc[SC_GAM * 64 + r]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float e[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = 32 * half + 4 * j + u;
-            const float gam = do_fold ? br * __expf(G[i] - Gr) : bgr * eG[i];
-            e[u] = i < r ? gam * __uint_as_float(gv[4 * j + u]) : 0.f;
-          }
-          *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
-        }
-      } else {
-        const int r = row - 64;
-        const float Gr = G[r];
-        const float qgr = a.q_scale * sc[SC_GAM * 64 + r];
-        if constexpr (SPLIT) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float e[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int i = 32 * half + 8 * j + u;
-              const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-              e[u] = i <= r ? gam * __uint_as_float(gv[8 * j + u]) : 0.f;
-            }
-            uint4 h, l;
-            split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
-            split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
-            *reinterpret_cast<uint4 *>(smem + SM_P + canon16(r, 32 * half + 8 * j, 64)) = h;
-            *reinterpret_cast<uint4 *>(smem + SM_P + PK_LO + canon16(r, 32 * half + 8 * j, 64)) = l;
-          }
-        } else {
+        // the branch on do_fold (uniform) stays outside the loop, so that the
+        // common case evaluates no exponential
+        auto a_row = [&](auto gamf) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             float e[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int i = 32 * half + 4 * j + u;
-              const float gam = do_fold ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-              e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * j + u])) : 0.f;
+              e[u] = i < r ? gamf(i) * __uint_as_float(gv[4 * j + u]) : 0.f;
             }
-            *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
-                make_float4(e[0], e[1], e[2], e[3]);
+            *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * j) = make_float4(e[0], e[1], e[2], e[3]);
           }
-        }
+        };
+        if (do_fold) a_row([&](int i) { return br * __expf(G[i] - Gr); });
+        else a_row([&](int i) { return bgr * eG[i]; });
+      } else {
+        const int r = row - 64;
+        const float Gr = G[r];
+        const float qgr = a.q_scale * sc[SC_GAM * 64 + r];
+        auto p_row = [&](auto gamf) {
+          if constexpr (SPLIT) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float e[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int i = 32 * half + 8 * j + u;
+                e[u] = i <= r ? gamf(i) * __uint_as_float(gv[8 * j + u]) : 0.f;
+              }
+              uint4 h, l;
+              split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+              split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+              *reinterpret_cast<uint4 *>(smem + SM_P + canon16(r, 32 * half + 8 * j, 64)) = h;
+              *reinterpret_cast<uint4 *>(smem + SM_P + PK_LO + canon16(r, 32 * half + 8 * j, 64)) = l;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float e[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i = 32 * half + 4 * j + u;
+                e[u] = i <= r ? tf32_rn(gamf(i) * __uint_as_float(gv[4 * j + u])) : 0.f;
+              }
+              *reinterpret_cast<float4 *>(smem + SM_P + canon(r, 32 * half + 4 * j, 64)) =
+                  make_float4(e[0], e[1], e[2], e[3]);
+            }
+          }
+        };
+        if (do_fold) p_row([&](int i) { return a.q_scale * __expf(G[i] - Gr); });
+        else p_row([&](int i) { return qgr * eG[i]; });
       }
       if constexpr (!SPLIT) {
         // Q' = c q_scale gamma_r Q, in place in the stack's Q half (rows 64..127)

@@ -426,55 +426,62 @@ __global__ void __launch_bounds__(NTH, 3)
       const float br = scj[Q_BETA * 64 + r];
       const float Gr = DECAY_AFTER ? scj[Q_GPREV * 64 + r] : G[r];
       const float bgr = br * (DECAY_AFTER ? scj[Q_GAMP * 64 + r] : scj[Q_GAM * 64 + r]);
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        float e[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 32 * half + 4 * jj + u;
-          const float gam = extreme ? br * __expf(G[i] - Gr) : bgr * eG[i];
-          e[u] = i < r ? gam * __uint_as_float(gv[4 * jj + u]) : 0.f;
-        }
-        *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * jj) = make_float4(e[0], e[1], e[2], e[3]);
-      }
-    } else {
-      const int r = row - 64;
-      const float Gr = G[r];
-      const float qgr = a.q_scale * scj[Q_GAM * 64 + r];
-      float *wp = ws + 4096;
-      if constexpr (SPLIT) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          if (!tri16_used(r >> 3, 4 * half + jj)) continue;  // the rest of the image stays unwritten (zeros)
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = 32 * half + 8 * jj + u;
-            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-            e[u] = i <= r ? gam * __uint_as_float(gv[8 * jj + u]) : 0.f;
-          }
-          uint4 h, l;
-          split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
-          split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
-          unsigned char *wb = reinterpret_cast<unsigned char *>(wp) + canon16(r, 32 * half + 8 * jj, 64);
-          *reinterpret_cast<uint4 *>(wb) = h;
-          *reinterpret_cast<uint4 *>(wb + 8192) = l;
-        }
-      } else {
+      // the branch on extreme (uniform) stays outside the loop, so that the
+      // common case evaluates no exponential
+      auto a_row = [&](auto gamf) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           float e[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i = 32 * half + 4 * jj + u;
-            const float gam = extreme ? a.q_scale * __expf(G[i] - Gr) : qgr * eG[i];
-            e[u] = i <= r ? tf32_rn(gam * __uint_as_float(gv[4 * jj + u])) : 0.f;
+            e[u] = i < r ? gamf(i) * __uint_as_float(gv[4 * jj + u]) : 0.f;
           }
-          if (tri_core_used(r >> 3, 8 * half + jj))  // the rest of the image stays unwritten (zeros)
-            *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) =
-                make_float4(e[0], e[1], e[2], e[3]);
+          *reinterpret_cast<float4 *>(sA + r * LD + 32 * half + 4 * jj) = make_float4(e[0], e[1], e[2], e[3]);
         }
-      }
+      };
+      if (extreme) a_row([&](int i) { return br * __expf(G[i] - Gr); });
+      else a_row([&](int i) { return bgr * eG[i]; });
+    } else {
+      const int r = row - 64;
+      const float Gr = G[r];
+      const float qgr = a.q_scale * scj[Q_GAM * 64 + r];
+      float *wp = ws + 4096;
+      auto p_row = [&](auto gamf) {
+        if constexpr (SPLIT) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            if (!tri16_used(r >> 3, 4 * half + jj)) continue;  // the rest of the image stays unwritten (zeros)
+            float e[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int i = 32 * half + 8 * jj + u;
+              e[u] = i <= r ? gamf(i) * __uint_as_float(gv[8 * jj + u]) : 0.f;
+            }
+            uint4 h, l;
+            split2(e[0], e[1], h.x, l.x); split2(e[2], e[3], h.y, l.y);
+            split2(e[4], e[5], h.z, l.z); split2(e[6], e[7], h.w, l.w);
+            unsigned char *wb = reinterpret_cast<unsigned char *>(wp) + canon16(r, 32 * half + 8 * jj, 64);
+            *reinterpret_cast<uint4 *>(wb) = h;
+            *reinterpret_cast<uint4 *>(wb + 8192) = l;
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            float e[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = 32 * half + 4 * jj + u;
+              e[u] = i <= r ? tf32_rn(gamf(i) * __uint_as_float(gv[4 * jj + u])) : 0.f;
+            }
+            if (tri_core_used(r >> 3, 8 * half + jj))  // the rest of the image stays unwritten (zeros)
+              *reinterpret_cast<float4 *>(wp + canon(r, 32 * half + 4 * jj, 64) / 4) =
+                  make_float4(e[0], e[1], e[2], e[3]);
+          }
+        }
+      };
+      if (extreme) p_row([&](int i) { return a.q_scale * __expf(G[i] - Gr); });
+      else p_row([&](int i) { return qgr * eG[i]; });
     }
   };
   // T'' = T diag(beta) of value head j as canonical images (NaN if a wait
