@@ -437,10 +437,9 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 
     // ---- 4. Gram [K;Q] K^T -> TMEM G.  Meanwhile, once the previous chunk's
     // batch 2 is done (it ran beside this chunk's first steps): c folded
-    // into S if needed, the other operands from the staged rows -- K'^T
+    // into S if needed, and the other operands from the staged rows -- K'^T
     // (smem, over the image batch 2 read), V^T (TMEM), split: S~ as hi and lo
-    // (TMEM) -- and the previous chunk's outputs (its Y^T is read before this
-    // chunk's first batch overwrites it).
+    // (TMEM).  The previous chunk's outputs stay in Y^T until step 6.
     if (tid == 0) {
       if constexpr (BF16IN) {
 #pragma unroll
@@ -534,7 +533,6 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       for (int j = 0; j < 32; ++j) vv[j] = __float_as_uint(tf32_rn(sVS[(32 * half + j) * LDS + row]));
       GDN_TMEM_ST32(tl + TM::V + 32 * half, vv);
     }
-    if (ch > 0) write_outputs(t0 - C, C);
     tmem_wait_st();
     fence_async_smem();
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
@@ -628,34 +626,57 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // product (the stack's K rows, then its Q rows), which needs no T, runs
     // on the tensor cores while warps 0-3 invert I + A; with split operands
     // warps 4-7 then split X into hi | lo over S~ hi and scale Y^T's columns
-    // by c q_scale gamma_r.  Warp 4 issues these products (issuing takes
-    // about 44 cycles an instruction), so the inverse starts at once, and
-    // warps 4-7 stage the next chunk's K and V rows (their copies are issued
-    // off the inverse's path).
-    if (tid == NTH / 2) {
-      if constexpr (SPLIT) {
-        const uint32_t i128 = idesc_bf16(128, 128);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {  // [X | Yt] = S~ [K; Q]^T
-          const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i128, ks > 0);
-          if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i128, 1);
-          mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i128, 1);
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks)   // [X | Yt] = S [K; Q']^T
-          mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), idesc_tf32(128, 128),
-                 ks > 0);
-      }
-      mma_commit(mbar);
-    }
+    // by c q_scale gamma_r.  Warps 4-7 first write the previous chunk's
+    // outputs from Y^T (off the Gram step, where thread 0's issuing held up
+    // its warp); warp 4 then issues the product (issuing takes about 44
+    // cycles an instruction), so the inverse starts at once, and warps 4-7
+    // stage the next chunk's K and V rows (their copies are issued off the
+    // inverse's path).
     const bool next = ch + 1 < nchunks;
     const int ncn = next ? static_cast<int>(min(static_cast<uint32_t>(C), nt - t0 - C)) : 0;
     if (warp < 4) {
       tri_inverse<128>(sA, sT, sM, tid);
       if (!mbar_wait(mbar, phase)) misc->failed = 1;
     } else {
+      // the previous chunk's outputs (this warp's d_v rows, all 64 tokens)
+      // leave Y^T before [X | Y^T] overwrites it
+      if (ch > 0) {
+        In *obase = static_cast<In *>(a.output) + ((tok0 + t0 - C) * a.nv + vh) * D + row;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t yv[32];
+          GDN_TMEM_LD32(tl + TM::Y + 32 * h, yv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if constexpr (BF16IN)
+              obase[static_cast<size_t>(32 * h + j) * v_tok] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(yv[j])));
+            else
+              obase[static_cast<size_t>(32 * h + j) * v_tok] = __uint_as_float(yv[j]);
+          }
+        }
+        fence_before();
+        asm volatile("bar.sync 2, %0;" :: "n"(NTH / 2) : "memory");  // warps 4-7
+        fence_after();
+      }
+      if (tid == NTH / 2) {
+        if constexpr (SPLIT) {
+          const uint32_t i128 = idesc_bf16(128, 128);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {  // [X | Yt] = S~ [K; Q]^T
+            const uint64_t bh = sdesc(sbase + SM_STACK + ks * 256, 2048), bl = sdesc(sbase + SM_STACK + 32768 + ks * 256, 2048);
+            mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bh, i128, ks > 0);
+            if constexpr (!BF16IN) mma_ts<true>(tmem + TM::X, tmem + TM::SH + 8 * ks, bl, i128, 1);
+            mma_ts<true>(tmem + TM::X, tmem + TM::SL + 8 * ks, bh, i128, 1);
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < D / 8; ++ks)   // [X | Yt] = S [K; Q']^T
+            mma_ts(tmem + TM::X, tmem + TM::S + 8 * ks, sdesc(sbase + SM_STACK + ks * 256, 4096), idesc_tf32(128, 128),
+                   ks > 0);
+        }
+        mma_commit(mbar);
+      }
       // the staging buffers are free (every thread took its operands from
       // them before step 5's barrier): the next chunk's K and V rows, issued
       // here so that warps 0-3 start the inverse at once
@@ -825,7 +846,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
 
     // (batch 2 runs beside the next chunk's first steps, which wait for it
     // before they touch S, K'^T or Y^T; this chunk's outputs are written
-    // during the next chunk's Gram, the last chunk's after the loop)
+    // by warps 4-7 in the next chunk's step 6, the last chunk's after the
+    // loop)
     c = misc->c_next;
     cta_sync();
     if (misc->failed) failed = true;
