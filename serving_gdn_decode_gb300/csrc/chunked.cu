@@ -182,9 +182,8 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, s
                                                size_t v_tok, int nc, int tid) {
   if constexpr (BF16IN) {
     const uint16_t *kbase = static_cast<const uint16_t *>(kv), *vbase = static_cast<const uint16_t *>(vv);
-#pragma unroll
-    for (int it = 0; it < 4 * (NTH / NT); ++it) {
-      const int ci = tid + NT * it;       // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
+#pragma unroll 4
+    for (int ci = tid; ci < 64 * 16; ci += NT) {  // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
       const int r = ci >> 4, c8 = ci & 15;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -194,9 +193,8 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, s
     }
   } else {
     const float *kbase = static_cast<const float *>(kv), *vbase = static_cast<const float *>(vv);
-#pragma unroll
-    for (int it = 0; it < 8 * (NTH / NT); ++it) {
-      const int ci = tid + NT * it;       // 16-byte chunk: row ci/32, float4 ci%32
+#pragma unroll 4
+    for (int ci = tid; ci < 64 * 32; ci += NT) {  // 16-byte chunk: row ci/32, float4 ci%32
       const int r = ci >> 5, c4 = ci & 31;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -472,11 +470,15 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     }
     if (do_renorm) tmem_scale64(tl + TM::S + 64 * half, c_renorm);  // c left [2^-30, 2^30] (rare)
     if constexpr (SPLIT) {
-      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
+      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens
+      // [32*hf, +32) for hf = half; warp 0, which issues the Gram, leaves
+      // its share to warp 4
       const float *kts = sc + SC_KTS * 64;
+#pragma unroll 1
+      for (int hf = warp == 4 ? 0 : (warp == 0 ? 2 : half); hf <= (warp == 0 ? 1 : half); ++hf)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int i = 32 * half + 8 * j;
+        const int i = 32 * hf + 8 * j;
         float e[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -516,11 +518,14 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         GDN_TMEM_ST16(tl + TM::SL + 32 * half + 16 * h, sl);
       }
     } else {
-      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens [32*half, +32)
+      // K'^T [d_k][i] (K extent 64): thread owns column d_k = row, tokens
+      // [32*hf, +32) for hf = half; warp 0 leaves its share to warp 4
       const float *kts = sc + SC_KTS * 64;
+#pragma unroll 1
+      for (int hf = warp == 4 ? 0 : (warp == 0 ? 2 : half); hf <= (warp == 0 ? 1 : half); ++hf)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i = 32 * half + 4 * j;
+        const int i = 32 * hf + 4 * j;
         *reinterpret_cast<float4 *>(smem + SM_KT + canon(row, i, 64)) =
             make_float4(tf32_rn(sKS[(i + 0) * LDS + row] * kts[i + 0]),
                         tf32_rn(sKS[(i + 1) * LDS + row] * kts[i + 1]),
@@ -680,9 +685,9 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       // the staging buffers are free (every thread took its operands from
       // them before step 5's barrier): the next chunk's K and V rows, issued
       // here so that warps 0-3 start the inverse at once
-      if (next)
-        stage_kv_async<BF16IN, NTH / 2>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok, v_tok,
-                                        ncn, tid - NTH / 2);
+      if (next && warp > 4)  // warps 5-7 (warp 4 issues the product)
+        stage_kv_async<BF16IN, NTH / 2 - 32>(sbase, kseq + (t0 + C) * kq_tok, kq_tok, vseq + (t0 + C) * v_tok,
+                                             v_tok, ncn, tid - NTH / 2 - 32);
       if (!mbar_wait(mbar, phase)) misc->failed = 1;
       if constexpr (SPLIT) {
         __syncwarp();
