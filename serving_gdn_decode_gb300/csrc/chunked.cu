@@ -135,21 +135,19 @@ static_assert(sizeof(Misc) <= 64, "misc area");
 // bf16 activations: staged rows of 128 bf16 at a stride of 136 (272 bytes)
 constexpr int LDSB = 136;
 
-// Asynchronous copies of one chunk's Q rows and of its gates and betas into
-// the scalar area; tokens past the chunk's end are zero-filled.  f32: into
-// the stack's Q half (rows 64..127) in the TF32 canonical order; bf16
-// activations: straight into the bf16 canonical image of the stack's Q rows
-// (a 16-byte row of a core is 8 consecutive d_k of one token).  Issued by
-// NT threads, tid counted from the first of them.
-template <bool BF16IN, int NT = NTH>
-__device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const void *qv, size_t kq_tok,
-                                                        const float *g, const float *beta, size_t sc0,
-                                                        size_t nv, int nc, int tid) {
+// Asynchronous copies of one chunk's Q rows; tokens past the chunk's end
+// are zero-filled.  f32: into the stack's Q half (rows 64..127) in the TF32
+// canonical order; bf16 activations: straight into the bf16 canonical image
+// of the stack's Q rows (a 16-byte row of a core is 8 consecutive d_k of one
+// token).  Issued by NT threads, tid counted from the first of them.
+template <bool BF16IN, int NT>
+__device__ __forceinline__ void stage_q_async(uint32_t sbase, const void *qv, size_t kq_tok, int nc, int tid) {
   if constexpr (BF16IN) {
     const uint16_t *qbase = static_cast<const uint16_t *>(qv);
 #pragma unroll
-    for (int it = 0; it < 4 * (NTH / NT); ++it) {
+    for (int it = 0; it < (64 * 16 + NT - 1) / NT; ++it) {
       const int cc = tid + NT * it;       // token cc >> 4, d_k 8 (cc & 15) .. +7
+      if ((64 * 16) % NT != 0 && cc >= 64 * 16) break;
       const int r = cc >> 4, d0 = 8 * (cc & 15);
       cp_async16(sbase + SM_STACK + canon16(64 + r, d0, 128), qbase + (r < nc ? r : 0) * kq_tok + d0,
                  r < nc ? 16u : 0u);
@@ -157,18 +155,28 @@ __device__ __forceinline__ void stage_q_and_gates_async(uint32_t sbase, const vo
   } else {
     const float *qbase = static_cast<const float *>(qv);
 #pragma unroll
-    for (int it = 0; it < 8 * (NTH / NT); ++it) {
+    for (int it = 0; it < (64 * 32 + NT - 1) / NT; ++it) {
       const int cc = tid + NT * it;       // 16-byte chunk within the Q half
+      if ((64 * 32) % NT != 0 && cc >= 64 * 32) break;
       const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), c4 = core & 31;
       cp_async16(sbase + SM_STACK + 32768 + cc * 16, qbase + (r < nc ? r : 0) * kq_tok + 4 * c4,
                  r < nc ? 16u : 0u);
     }
   }
-  if (tid < 128) {
-    const int i = tid & 63;
+  cp_async_commit();
+}
+
+// Asynchronous copies of one chunk's gates and betas into the scalar area,
+// by warp 0, which reads them (and waits for them) alone; tokens past the
+// chunk's end are zero-filled.
+__device__ __forceinline__ void stage_gates_async(uint32_t sbase, const float *g, const float *beta, size_t sc0,
+                                                  size_t nv, int nc, int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
     const size_t src = sc0 + static_cast<size_t>(i < nc ? i : 0) * nv;
-    cp_async4(sbase + SM_SC + ((tid < 64 ? SC_GRAW : SC_BRAW) * 64 + i) * 4,
-              (tid < 64 ? g : beta) + src, i < nc ? 4u : 0u);
+    cp_async4(sbase + SM_SC + (SC_GRAW * 64 + i) * 4, g + src, i < nc ? 4u : 0u);
+    cp_async4(sbase + SM_SC + (SC_BRAW * 64 + i) * 4, beta + src, i < nc ? 4u : 0u);
   }
   cp_async_commit();
 }
@@ -182,8 +190,10 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, s
                                                size_t v_tok, int nc, int tid) {
   if constexpr (BF16IN) {
     const uint16_t *kbase = static_cast<const uint16_t *>(kv), *vbase = static_cast<const uint16_t *>(vv);
-#pragma unroll 4
-    for (int ci = tid; ci < 64 * 16; ci += NT) {  // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
+#pragma unroll
+    for (int it = 0; it < (64 * 16 + NT - 1) / NT; ++it) {
+      const int ci = tid + NT * it;       // 16-byte chunk: row ci/16, 8 bf16 at 8 (ci%16)
+      if ((64 * 16) % NT != 0 && ci >= 64 * 16) break;
       const int r = ci >> 4, c8 = ci & 15;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -193,8 +203,10 @@ __device__ __forceinline__ void stage_kv_async(uint32_t sbase, const void *kv, s
     }
   } else {
     const float *kbase = static_cast<const float *>(kv), *vbase = static_cast<const float *>(vv);
-#pragma unroll 4
-    for (int ci = tid; ci < 64 * 32; ci += NT) {  // 16-byte chunk: row ci/32, float4 ci%32
+#pragma unroll
+    for (int it = 0; it < (64 * 32 + NT - 1) / NT; ++it) {
+      const int ci = tid + NT * it;       // 16-byte chunk: row ci/32, float4 ci%32
+      if ((64 * 32) % NT != 0 && ci >= 64 * 32) break;
       const int r = ci >> 5, c4 = ci & 31;
       const uint32_t n = r < nc ? 16u : 0u;
       const int rr = r < nc ? r : 0;
@@ -278,7 +290,8 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   {
     const int nc0 = static_cast<int>(min(nt, static_cast<uint32_t>(C)));
     stage_kv_async<BF16IN>(sbase, kseq, kq_tok, vseq, v_tok, nc0, tid);
-    stage_q_and_gates_async<BF16IN>(sbase, qseq, kq_tok, a.g, a.beta, sc_first, a.nv, nc0, tid);
+    stage_q_async<BF16IN, NTH>(sbase, qseq, kq_tok, nc0, tid);
+    if (warp == 0) stage_gates_async(sbase, a.g, a.beta, sc_first, a.nv, nc0, lane);
   }
   cta_sync();
   const uint32_t tmem = misc->tmem_base;
@@ -301,7 +314,12 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     tmem_wait_st();
   }
 
-  float c = 1.f;          // S = c * (TMEM S)
+  // chunk 0's copies (issued by every thread) have landed; in the loop, warp
+  // 0 waits for its own copies (the gates) and warps 1-7 for theirs (the rows)
+  cp_async_wait_all();
+  __syncthreads();
+
+  float c = 1.f;          // S = c * (TMEM S), carried by warp 0 (the others read c_next at the end)
   uint32_t phase = 0, phase2 = 0;
   bool pending2 = false;  // a batch 2 committed and not yet waited for (uniform over the CTA)
   bool failed = false;
@@ -327,12 +345,12 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   for (uint32_t ch = 0; ch < nchunks && !failed; ++ch) {
     const uint32_t t0 = ch * C;
 
-    // ---- 0. this chunk's staged inputs (K, V rows, Q half, gates) have landed
-    cp_async_wait_all();
-    __syncthreads();
-
-    // ---- 1. per-token scalars (warp 0): prefix sums of g, decays, scalings
+    // ---- 1. per-token scalars (warp 0, once its own copies, the gates, have
+    // landed; it has just issued the previous chunk's batch 2): prefix sums
+    // of g, decays, scalings.  Meanwhile, 3., warps 1-7 build the stack.
     if (warp == 0) {
+      cp_async_wait_all();
+      __syncwarp();
       float g0 = sc[SC_GRAW * 64 + lane], g1 = sc[SC_GRAW * 64 + lane + 32];
       const float b0 = sc[SC_BRAW * 64 + lane], b1 = sc[SC_BRAW * 64 + lane + 32];
 #pragma unroll
@@ -379,59 +397,70 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
         misc->c_renorm = renorm; misc->c_fold = fold; misc->c_next = cnext;
         misc->do_renorm = do_renorm; misc->do_fold = extreme;
       }
-    }
-    __syncthreads();
-    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
-    const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
-
-    // ---- 3. the stack from the staged rows: K (canonical) and Q (the staged
-    // Q rows), rounded to TF32 in place or as bf16 hi and lo images (bf16
-    // activations: Q is in place already, K's rows are copied)
-    if constexpr (BF16IN) {
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int ci = tid + NTH * it;        // token ci >> 4, d_k 8 (ci & 15) .. +7
-        const int r = ci >> 4, d0 = 8 * (ci & 15);
-        *reinterpret_cast<uint4 *>(smem + SM_STACK + canon16(r, d0, 128)) =
-            *reinterpret_cast<const uint4 *>(sKSb + r * LDSB + d0);
-      }
-    } else if constexpr (SPLIT) {
-      // the staged Q rows (f32, in the TF32 canonical order of the Q half),
-      // read before the bf16 images overwrite them
-      float4 qv[8];
-#pragma unroll
-      for (int it = 0; it < 8; ++it)
-        qv[it] = *reinterpret_cast<const float4 *>(smem + SM_STACK + 32768 + (tid + NTH * it) * 16);
-      __syncthreads();
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int cc = tid + NTH * it;        // element group: row r, d_k 4 c4 .. +3
-        const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), d0 = 4 * (core & 31);
-        const float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + d0);
-        uint2 h, l;
-        split2(x.x, x.y, h.x, l.x); split2(x.z, x.w, h.y, l.y);
-        *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(r, d0, 128)) = h;
-        *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(r, d0, 128)) = l;
-        split2(qv[it].x, qv[it].y, h.x, l.x); split2(qv[it].z, qv[it].w, h.y, l.y);
-        *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(64 + r, d0, 128)) = h;
-        *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(64 + r, d0, 128)) = l;
-      }
+      c = cnext;  // warp 0 carries c from chunk to chunk
     } else {
+      // ---- 3. the stack from the staged rows (warps 1-7, once their own
+      // copies -- the K, V and Q rows -- have landed): K (canonical) and Q
+      // (the staged Q rows), rounded to TF32 in place or as bf16 hi and lo
+      // images (bf16 activations: Q is in place already, K's rows are copied)
+      constexpr int NS = NTH - 32;
+      const int vt = tid - 32;
+      cp_async_wait_all();
+      asm volatile("bar.sync 3, %0;" :: "n"(NS) : "memory");  // warps 1-7
+      if constexpr (BF16IN) {
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int ci = tid + NTH * it;        // 16-byte chunk of the K half
-        const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
-        float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
-        x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
-        *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
-        float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
-        float4 y = *pq;
-        y.x = tf32_rn(y.x); y.y = tf32_rn(y.y); y.z = tf32_rn(y.z); y.w = tf32_rn(y.w);
-        *pq = y;
+        for (int it = 0; it < (64 * 16 + NS - 1) / NS; ++it) {
+          const int ci = vt + NS * it;        // token ci >> 4, d_k 8 (ci & 15) .. +7
+          if (ci >= 64 * 16) break;
+          const int r = ci >> 4, d0 = 8 * (ci & 15);
+          *reinterpret_cast<uint4 *>(smem + SM_STACK + canon16(r, d0, 128)) =
+              *reinterpret_cast<const uint4 *>(sKSb + r * LDSB + d0);
+        }
+      } else if constexpr (SPLIT) {
+        // the staged Q rows (f32, in the TF32 canonical order of the Q half),
+        // read before the bf16 images overwrite them
+        constexpr int NIT = (64 * 32 + NS - 1) / NS;
+        float4 qv[NIT];
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+          const int cc = vt + NS * it;
+          if (cc < 64 * 32) qv[it] = *reinterpret_cast<const float4 *>(smem + SM_STACK + 32768 + cc * 16);
+        }
+        asm volatile("bar.sync 3, %0;" :: "n"(NS) : "memory");
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) {
+          const int cc = vt + NS * it;        // element group: row r, d_k 4 c4 .. +3
+          if (cc >= 64 * 32) break;
+          const int core = cc >> 3, r = (core >> 5) * 8 + (cc & 7), d0 = 4 * (core & 31);
+          const float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + d0);
+          uint2 h, l;
+          split2(x.x, x.y, h.x, l.x); split2(x.z, x.w, h.y, l.y);
+          *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(r, d0, 128)) = h;
+          *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(r, d0, 128)) = l;
+          split2(qv[it].x, qv[it].y, h.x, l.x); split2(qv[it].z, qv[it].w, h.y, l.y);
+          *reinterpret_cast<uint2 *>(smem + SM_STACK + canon16(64 + r, d0, 128)) = h;
+          *reinterpret_cast<uint2 *>(smem + SM_STACK + 32768 + canon16(64 + r, d0, 128)) = l;
+        }
+      } else {
+#pragma unroll
+        for (int it = 0; it < (64 * 32 + NS - 1) / NS; ++it) {
+          const int ci = vt + NS * it;        // 16-byte chunk of the K half
+          if (ci >= 64 * 32) break;
+          const int core = ci >> 3, r = (core >> 5) * 8 + (ci & 7), c4 = core & 31;
+          float4 x = *reinterpret_cast<const float4 *>(sKS + r * LDS + 4 * c4);
+          x.x = tf32_rn(x.x); x.y = tf32_rn(x.y); x.z = tf32_rn(x.z); x.w = tf32_rn(x.w);
+          *reinterpret_cast<float4 *>(smem + SM_STACK + ci * 16) = x;
+          float4 *pq = reinterpret_cast<float4 *>(smem + SM_STACK + 32768 + ci * 16);
+          float4 y = *pq;
+          y.x = tf32_rn(y.x); y.y = tf32_rn(y.y); y.z = tf32_rn(y.z); y.w = tf32_rn(y.w);
+          *pq = y;
+        }
       }
     }
     fence_async_smem();
     cta_sync();
+    const float c_renorm = misc->c_renorm, c_fold = misc->c_fold;
+    const bool do_renorm = misc->do_renorm != 0, do_fold = misc->do_fold != 0;
 
     // ---- 4. Gram [K;Q] K^T -> TMEM G.  Meanwhile, once the previous chunk's
     // batch 2 is done (it ran beside this chunk's first steps): c folded
@@ -800,9 +829,12 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
       mma_commit(mbar);
     }
     // while U^T runs (the stack is free: X and Y^T are done): the next chunk's Q rows and gates
-    if (next)
-      stage_q_and_gates_async<BF16IN>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, a.g, a.beta,
-                                      sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, tid);
+    if (next) {
+      if (warp == 0)
+        stage_gates_async(sbase, a.g, a.beta, sc_first + static_cast<size_t>(t0 + C) * a.nv, a.nv, ncn, lane);
+      else
+        stage_q_async<BF16IN, NTH - 32>(sbase, qseq + (t0 + C) * kq_tok, kq_tok, ncn, tid - 32);
+    }
     if (!mbar_wait(mbar, phase)) misc->failed = 1;
     phase ^= 1;
     fence_after();
@@ -853,8 +885,6 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
     // before they touch S, K'^T or Y^T; this chunk's outputs are written
     // by warps 4-7 in the next chunk's step 6, the last chunk's after the
     // loop)
-    c = misc->c_next;
-    cta_sync();
     if (misc->failed) failed = true;
   }
 
@@ -874,7 +904,7 @@ __global__ void __launch_bounds__(NTH, 1) gdn_chunked_kernel(const ChunkArgs a) 
   // ---- state_out = c * S (or NaN if a wait timed out)
   {
     float4 *dst = reinterpret_cast<float4 *>(a.state_out + state_head + row * D + 64 * half);
-    const float f = failed ? __int_as_float(0x7fc00000) : c;
+    const float f = failed ? __int_as_float(0x7fc00000) : (nchunks > 0 ? misc->c_next : 1.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];
