@@ -243,28 +243,71 @@ __device__ __forceinline__ void tmem_scale64(uint32_t taddr, float f) {
   tmem_wait_st();
 }
 
-// One warp accumulates C += L R for 16 x 16 blocks: L rows at stride ldl, R
-// rows at stride ldr; each lane holds a 2 x 4 tile of C (rows tr, tr+1,
-// columns tc..tc+3).  Where L is triangular its other half is stored zeros
-// and is multiplied like the rest: skipping it per lane would save nothing
-// (the lanes of a warp need different lengths) and would keep the loads
-// from being issued ahead of the multiply-adds.
-__device__ __forceinline__ void blk_mac(float (&c0)[4], float (&c1)[4], const float *L, int ldl,
-                                        const float *R, int ldr, int tr, int tc) {
-  const float *l0 = L + tr * ldl;
+// The 16 x 16 block products of the triangular inverse run on the warp's
+// tensor-core MMA (m16n8k8, TF32 operands) with each operand split as
+// x = hi + lo, hi = tf32(x), lo = tf32(x - hi) (both to nearest; x - hi is
+// exact), and C += A_lo B_hi + A_hi B_lo + A_hi B_hi, the small terms first:
+// the three-term split of the same scheme the chunk products use in bf16,
+// here with 11-bit halves, so each product keeps about 22 bits (the dropped
+// A_lo B_lo term is below 2^-22 of it).  Per lane and block product that is
+// 16 four-byte shared loads, one element each, against 24 sixteen-byte
+// loads (each fetched by four or eight lanes) of a 2 x 4 tile of fma.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  const float h = tf32_rn(x);
+  hi = __float_as_uint(h);
+  lo = __float_as_uint(tf32_rn(x - h));
+}
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Column of element (r, c) in the product scratch M (16 x 16 blocks, row
+// stride 16): columns swapped in halves of 8 on rows with bit 1 set, so
+// that the B-fragment loads (rows t, t + 4, columns g) hit distinct banks.
+__device__ __forceinline__ int mcol(int r, int c) { return c ^ (((r >> 1) & 1) << 3); }
+// One warp accumulates C += L R for 16 x 16 blocks (L rows at stride ldl; R
+// rows at stride ldr, or R = a block of M with ldr = 16 and RSWZ); C as two
+// m16n8 accumulator fragments: c[nb] holds rows g, g + 8 and columns
+// 8 nb + 2t, + 1 (g = lane / 4, t = lane % 4).  Where L is triangular its
+// other half is stored zeros and multiplied like the rest.
+template <bool RSWZ>
+__device__ __forceinline__ void blk_mma(float (&c)[2][4], const float *L, int ldl, const float *R, int ldr,
+                                        int lane) {
+  const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int q = 0; q < 16; q += 4) {
-    const float4 x0 = *reinterpret_cast<const float4 *>(l0 + q), x1 = *reinterpret_cast<const float4 *>(l0 + ldl + q);
-    const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+  for (int kb = 0; kb < 2; ++kb) {
+    uint32_t ah[4], al[4];
+    split_tf32(L[g * ldl + 8 * kb + t], ah[0], al[0]);
+    split_tf32(L[(g + 8) * ldl + 8 * kb + t], ah[1], al[1]);
+    split_tf32(L[g * ldl + 8 * kb + t + 4], ah[2], al[2]);
+    split_tf32(L[(g + 8) * ldl + 8 * kb + t + 4], ah[3], al[3]);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float4 b = *reinterpret_cast<const float4 *>(R + (q + u) * ldr + tc);
-      c0[0] = fmaf(a0[u], b.x, c0[0]); c0[1] = fmaf(a0[u], b.y, c0[1]);
-      c0[2] = fmaf(a0[u], b.z, c0[2]); c0[3] = fmaf(a0[u], b.w, c0[3]);
-      c1[0] = fmaf(a1[u], b.x, c1[0]); c1[1] = fmaf(a1[u], b.y, c1[1]);
-      c1[2] = fmaf(a1[u], b.z, c1[2]); c1[3] = fmaf(a1[u], b.w, c1[3]);
+    for (int nb = 0; nb < 2; ++nb) {
+      const int r0 = 8 * kb + t, r1 = 8 * kb + t + 4, cn = 8 * nb + g;
+      uint32_t b0h, b0l, b1h, b1l;
+      split_tf32(R[r0 * ldr + (RSWZ ? mcol(r0, cn) : cn)], b0h, b0l);
+      split_tf32(R[r1 * ldr + (RSWZ ? mcol(r1, cn) : cn)], b1h, b1l);
+      mma_m16n8k8_tf32(c[nb], al, b0h, b1h);
+      mma_m16n8k8_tf32(c[nb], ah, b0l, b1l);
+      mma_m16n8k8_tf32(c[nb], ah, b0h, b1h);
     }
   }
+}
+// sign * C (fragments as above) to the 16 x 16 block at dst (row stride ld,
+// or a block of M with SWZ).
+template <bool SWZ>
+__device__ __forceinline__ void blk_store(float *dst, int ld, const float (&c)[2][4], float sign, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = g + 8 * hh, cn = 8 * nb + 2 * t;
+      *reinterpret_cast<float2 *>(dst + r * ld + (SWZ ? mcol(r, cn) : cn)) =
+          make_float2(sign * c[nb][2 * hh], sign * c[nb][2 * hh + 1]);
+    }
 }
 
 // Barrier of the NT threads running tri_inverse: the whole CTA, or warps
@@ -280,7 +323,7 @@ __device__ __forceinline__ void tri_sync() {
 // substitution (one thread per column); then the two 32 x 32 diagonal blocks,
 // T_{j+1,j} = -T_{j+1,j+1} (A_{j+1,j} T_jj) for j = 0, 2; then the lower-left
 // 32 x 32 quarter, -T[hi] (A[hi,lo] T[lo]), as four 16 x 16 output blocks per
-// product, one warp each (2 x 4 register tiles).  M is 4 x 256 floats of
+// product, one warp each (tensor-core fragments).  M is 4 x 256 floats of
 // scratch for the inner products.  Run by threads 0 .. NT-1 (NT = 128: warps
 // 0-3, which do all the work; NT = NTH: the whole CTA).
 template <int NT = NTH>
@@ -307,22 +350,18 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   }
   tri_sync<NT>();
   const int warp = tid >> 5, lane = tid & 31;
-  const int tr = 2 * (lane >> 2), tc = 4 * (lane & 3);
   float *mw = M + warp * 256;
 
   // 32 x 32 diagonal blocks: warp 0 builds T_10, warp 1 builds T_32
   if (warp < 2) {
     const int j = 2 * warp, i = j + 1;
-    float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
-    blk_mac(m0, m1, A + (16 * i) * LD + 16 * j, LD, T + (16 * j) * LD + 16 * j, LD, tr, tc);
-    *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
-    *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
+    float m[2][4] = {};
+    blk_mma<false>(m, A + (16 * i) * LD + 16 * j, LD, T + (16 * j) * LD + 16 * j, LD, lane);
+    blk_store<true>(mw, 16, m, 1.f, lane);
     __syncwarp();
-    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-    blk_mac(t0, t1, T + (16 * i) * LD + 16 * i, LD, mw, 16, tr, tc);
-    float *to = T + (16 * i + tr) * LD + 16 * j + tc;
-    *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
-    *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
+    float t[2][4] = {};
+    blk_mma<true>(t, T + (16 * i) * LD + 16 * i, LD, mw, 16, lane);
+    blk_store<false>(T + (16 * i) * LD + 16 * j, LD, t, -1.f, lane);
   }
   tri_sync<NT>();
 
@@ -330,22 +369,19 @@ __device__ void tri_inverse(const float *A, float *T, float *M, int tid) {
   // 2(r-2) + c first forms M'_rc = sum_{k=c}^{1} A_rk T_kc ...
   const int r = 2 + (warp >> 1), cb = warp & 1;
   if (warp < 4) {
-    float m0[4] = {0.f, 0.f, 0.f, 0.f}, m1[4] = {0.f, 0.f, 0.f, 0.f};
+    float m[2][4] = {};
     for (int k = cb; k <= 1; ++k)
-      blk_mac(m0, m1, A + (16 * r) * LD + 16 * k, LD, T + (16 * k) * LD + 16 * cb, LD, tr, tc);
-    *reinterpret_cast<float4 *>(mw + tr * 16 + tc) = make_float4(m0[0], m0[1], m0[2], m0[3]);
-    *reinterpret_cast<float4 *>(mw + (tr + 1) * 16 + tc) = make_float4(m1[0], m1[1], m1[2], m1[3]);
+      blk_mma<false>(m, A + (16 * r) * LD + 16 * k, LD, T + (16 * k) * LD + 16 * cb, LD, lane);
+    blk_store<true>(mw, 16, m, 1.f, lane);
   }
   tri_sync<NT>();
   // ... then T_rc = -sum_{k=2}^{r} T_rk M'_kc (T_rr lower triangular)
   if (warp < 4) {
-    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+    float t[2][4] = {};
     if (r == 3)
-      blk_mac(t0, t1, T + (16 * r) * LD + 32, LD, M + cb * 256, 16, tr, tc);  // T_32 M'_2c
-    blk_mac(t0, t1, T + (16 * r) * LD + 16 * r, LD, M + (2 * (r - 2) + cb) * 256, 16, tr, tc);
-    float *to = T + (16 * r + tr) * LD + 16 * cb + tc;
-    *reinterpret_cast<float4 *>(to) = make_float4(-t0[0], -t0[1], -t0[2], -t0[3]);
-    *reinterpret_cast<float4 *>(to + LD) = make_float4(-t1[0], -t1[1], -t1[2], -t1[3]);
+      blk_mma<true>(t, T + (16 * r) * LD + 32, LD, M + cb * 256, 16, lane);  // T_32 M'_2c
+    blk_mma<true>(t, T + (16 * r) * LD + 16 * r, LD, M + (2 * (r - 2) + cb) * 256, 16, lane);
+    blk_store<false>(T + (16 * r) * LD + 16 * cb, LD, t, -1.f, lane);
   }
   tri_sync<NT>();
 }
