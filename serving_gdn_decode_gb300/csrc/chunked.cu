@@ -1,6 +1,6 @@
 // Chunked (WY / UT-transform) prefill of the Gated DeltaNet recurrence on the
-// 5th-generation tensor cores of sm_103a (tcgen05.mma kind::tf32, TMEM
-// accumulators), for D_k = D_v = 128.
+// 5th-generation tensor cores of sm_103a (tcgen05.mma kind::f16 with split
+// operands, or kind::tf32; TMEM accumulators), for D_k = D_v = 128.
 //
 // The recurrence is the token-by-token one of the capture kernel page
 // ("gated_delta_net_decode_capture.metal", mlx-native 0.9.2, decay-first) or
@@ -20,12 +20,11 @@
 // 128 runs on the tensor cores with M = 128 (D_v or the stacked [K;Q]):
 //
 //   G   = [K;Q] K^T              (Gram: rows 0..63 = K K^T, 64..127 = Q K^T)
-//   Ut  = V^T  T''^T              T''= T diag(beta)        (A = V^T from TMEM)
-//   X   = S K^T                                           (A = S from TMEM)
-//   Ut += X (-T')^T               T' = c T diag(beta gamma) (A = X from TMEM)
-//   Yt  = S Q'^T                  Q' = c q_scale diag(gamma) Q
-//   Yt += Ut P'^T                 P' = q_scale (Q K^T o Gam)  (A = Ut from TMEM)
-//   S  += Ut K'^T                 K' = diag(Gam_C / c_next) K
+//   [X | Yt] = S [K; Q']^T        Q' = c q_scale diag(gamma) Q (A = S from TMEM)
+//   Ut  = V^T  T''^T + X (-T')^T  T''= T diag(beta), T' = c T diag(beta gamma)
+//                                 (A = V^T and X from TMEM, one batch)
+//   [Yt | S] += Ut [P'; K'^T]^T   P' = q_scale (Q K^T o Gam), K' = diag(Gam_C /
+//                                 c_next) K (A = Ut from TMEM, one product)
 //
 // where Ut = U^T, Yt = Y^T (D_v x C) live in TMEM, and S is kept lazily as
 // c * S (c = product of the chunk decays since the last fold), so the decay
@@ -35,14 +34,15 @@
 // either rounded to TF32 (round-to-nearest) when staged, or split into bf16
 // hi and lo halves with every product taken as three bf16 MMAs
 // (chunked_common.cuh); the split form computes Yt = S Q^T and scales its
-// columns by c q_scale gamma_r in TMEM instead of scaling Q, and runs
-// Ut += X (-T')^T as a batch of its own once X is split.
-// The triangular inverse (64 x 64) runs on the CUDA cores, blocked 16 x 16.
+// columns by c q_scale gamma_r in TMEM instead of scaling Q, and splits X
+// into hi and lo before the Ut batch.  The triangular inverse (64 x 64) is
+// blocked 16 x 16: the diagonal blocks by substitution on the CUDA cores, the
+// block products on the warp-level MMA with 3xTF32 operands.
 //
-// One CTA (8 warps) owns one (seq, value head) for the whole token range,
-// with 512 TMEM columns: TF32: S 128 cols, X 64, Ut 64, Yt 64, G 64, V^T 64;
-// split: S 128, S hi 64 (then X hi | lo), S lo 64 (then Ut hi | lo), V^T
-// hi | lo 64, Ut 64, Yt 64, G 64 (then X).  Shared-memory operands use the
+// One CTA (8 warps) owns one segment of a (seq, value head) chain, with 512
+// TMEM columns, X, Yt and S adjacent: TF32: X (and G) 0, Yt 64, S 128, Ut 256,
+// V^T 320; split: X (and G) 0, Yt 64, S 128, S hi 256 (then X hi | lo), S lo
+// 320 (then Ut hi | lo), V^T hi | lo 384, Ut 448.  Shared-memory operands use the
 // canonical K-major no-swizzle layout: 8-row x 16-byte core matrices, cores
 // adjacent along K (LBO = 128 B), core rows SBO = (K bytes / 16) * 128 B
 // apart; a split operand is its hi image followed by its lo image.  Every
