@@ -127,7 +127,7 @@ typedef enum gdn_status {
  * Path choice (params[6] bits 2-3).  GDN_PATH_AUTO runs the token-loop
  * kernel for n_tokens <= 16; for longer windows it runs the tensor-core
  * chunked form when that form covers the call (D_k = D_v = 128, f32
- * activations, no capture, v 16-byte aligned) and n_tokens >= 64, and the
+ * activations, no capture, v 16-byte aligned) and n_tokens >= 48, and the
  * token-by-token FP32 scan otherwise.  GDN_PATH_SCAN forces the scan;
  * GDN_PATH_CHUNKED and GDN_PATH_CHUNKED_TF32 force the chunked form
  * (UNSUPPORTED for a shape it does not cover).
@@ -139,7 +139,8 @@ typedef enum gdn_status {
  * window); GDN_PATH_CHUNKED_TF32 rounds the operands to TF32 instead, one
  * product each, about 5e-4 (3e-3 for those negative gates).
  * gdn_forward runs the chunked form in one pass; gdn_forward_ws, given a
- * workspace, in two (faster).
+ * workspace, in two (faster from about 512 tokens on; under GDN_PATH_AUTO it
+ * keeps the one pass below that).
  * Buffer sizes cannot be checked through raw pointers: each buffer must hold
  * the element count its layout above gives.
  */
@@ -273,7 +274,9 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *
  * gdn_workspace_size: *bytes = the workspace gdn_forward_ws needs for
  *   `params` -- on the chunked path (forced, or chosen by GDN_PATH_AUTO for
- *   the shape, assuming a 16-byte-aligned v), per (seq, 64-token chunk),
+ *   the shape, assuming a 16-byte-aligned v, with at least 512 tokens: the
+ *   automatic choice keeps the one-pass form for shorter windows, where it
+ *   is the faster one), per (seq, 64-token chunk),
  *   32 KB per value head plus 96 KB per key head (the K and Q operands and K^T,
  *   shared by the value heads that read the key head); 0 on every other
  *   path, and 0 when a key head has more than 32 value heads (the two-pass
@@ -284,9 +287,9 @@ gdn_status gdn_forward_capture_bf16(const gdn_bf16 *q, const gdn_bf16 *k, const 
  *   at least gdn_workspace_size bytes, 16-byte aligned, overlapping no other
  *   buffer; may be NULL when the size is 0).  The call overwrites the
  *   workspace; its contents afterwards are unspecified.  On the chunked
- *   path (forced, or chosen by GDN_PATH_AUTO) the two-pass form runs; the
- *   other paths run exactly as in gdn_forward and do not touch the
- *   workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
+ *   path (forced, or chosen by GDN_PATH_AUTO for 512 tokens or more) the
+ *   two-pass form runs; otherwise the call runs exactly as gdn_forward and
+ *   does not touch the workspace.  Extra checks: INVALID_ARGUMENT for a NULL, misaligned,
  *   short or overlapping workspace when the size is > 0.
  */
 gdn_status gdn_workspace_size(const uint32_t *params, size_t n_params, size_t *bytes);

@@ -29,7 +29,13 @@ constexpr uint32_t kDecodeMaxTokens = 16;
 // the call.  Measured on GB300 for 16 to 256 (seq, value head) chains: the
 // one-pass and two-pass forms overtake the scan between 32 and 64 tokens
 // (at 64 tokens, 4 x 48 chains: 41.7 / 42.6 against 51.9 us).
-constexpr uint32_t kChunkedMinTokens = 64;
+constexpr uint32_t kChunkedMinTokens = 48;
+// Under GDN_PATH_AUTO a workspace turns the chunked form into two passes from
+// this window length on; below it the one-pass form is the faster one
+// (measured over 48 to 768 chains: at 256 tokens the one pass leads by 2-5 %
+// with 48 or 192 chains, the two passes by 7 % with 768; from 512 tokens on
+// the two passes lead in every case).
+constexpr uint32_t kTwoPassMinTokens = 512;
 // Upper bound on any buffer's element count (keeps byte counts far from
 // 64-bit overflow).
 constexpr unsigned long long kMaxElems = 1ull << 60;
@@ -254,10 +260,12 @@ void fill_problem(gdn::Problem &p, const Buffers &b, bool bf16) {
 
 // Workspace bytes of a decoded, path-checked problem (two-pass chunked only).
 // The two-pass form's workspace; 0 (the one-pass form runs) off the chunked
-// path and for more than kMaxSplitGroup value heads per key head.
+// path, for more than kMaxSplitGroup value heads per key head, and under
+// GDN_PATH_AUTO for windows shorter than kTwoPassMinTokens.
 size_t workspace_bytes_of(const Decoded &d, Path path) {
-  return path == Path::kChunked && gdn::chunked_split_supported(d.prob) ? gdn::chunked_split_workspace_bytes(d.prob)
-                                                                         : 0;
+  const bool two_pass = path == Path::kChunked && gdn::chunked_split_supported(d.prob) &&
+                        (d.path != GDN_PATH_AUTO || d.prob.nt >= kTwoPassMinTokens);
+  return two_pass ? gdn::chunked_split_workspace_bytes(d.prob) : 0;
 }
 
 // with_ws: the caller passed a workspace argument (gdn_forward_ws); the

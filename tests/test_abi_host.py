@@ -77,9 +77,9 @@ def test_path_choice(L):
     assert _path(WORKLOADS["tiny"].params(path=PATH_SCAN), True) == "scan_capture"
     assert _path(WORKLOADS["decode"].with_(n_tokens=16).params()) == "token_loop_decode"
     assert _path(WORKLOADS["decode"].with_(n_tokens=17).params()) == "scan"
-    # the automatic choice takes the chunked form from 64 tokens on, where it covers the shape
-    assert _path(WORKLOADS["decode"].with_(n_tokens=63).params()) == "scan"
-    assert _path(WORKLOADS["decode"].with_(n_tokens=64).params()) == "chunked"
+    # the automatic choice takes the chunked form from 48 tokens on, where it covers the shape
+    assert _path(WORKLOADS["decode"].with_(n_tokens=47).params()) == "scan"
+    assert _path(WORKLOADS["decode"].with_(n_tokens=48).params()) == "chunked"
     assert _path(WORKLOADS["long_prefill"].params(), True) == "scan_capture"
     assert _path(pack_params(64, 64, 2, 4, 4096, 1)) == "scan"
     assert _path(pack_params(128, 64, 2, 4, 4096, 1)) == "scan"
@@ -394,11 +394,16 @@ def test_workspace_size_values(L):
     w = WORKLOADS["long_prefill"].with_(n_tokens=200, n_seqs=3)
     # per (seq, chunk): 32 KB per value head (48) + 96 KB per key head (16); 3 seqs x 4 chunks
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED)) == 3 * 4 * (48 * 32768 + 16 * 98304)
-    # auto: the chunked form from 64 tokens on (two passes given a workspace), else the scan
-    assert nat.gdn_workspace_size(w.params()) == nat.gdn_workspace_size(w.params(path=PATH_CHUNKED))
+    # auto: the chunked form from 48 tokens on, in two passes given a workspace from 512
+    # tokens on (the one pass is the faster form below), else the scan
+    assert nat.gdn_workspace_size(w.params()) == 0
+    w600 = w.with_(n_tokens=600)
+    assert nat.gdn_workspace_size(w600.params()) == nat.gdn_workspace_size(w600.params(path=PATH_CHUNKED))
+    assert nat.gdn_workspace_size(w600.with_(n_tokens=511).params()) == 0
+    assert nat.gdn_workspace_size(w600.with_(n_tokens=512).params()) == 3 * 8 * (48 * 32768 + 16 * 98304)
     assert nat.gdn_workspace_size(w.params(path=PATH_CHUNKED_TF32)) == \
         nat.gdn_workspace_size(w.params(path=PATH_CHUNKED))       # same layout sizes
-    assert nat.gdn_workspace_size(w.with_(n_tokens=63).params()) == 0
+    assert nat.gdn_workspace_size(w.with_(n_tokens=47).params()) == 0
     assert nat.gdn_workspace_size(w.params(path=PATH_SCAN)) == 0
     assert nat.gdn_workspace_size(SMALL.params()) == 0               # decode
     with pytest.raises(nat.GdnError):
@@ -423,8 +428,16 @@ def test_workspace_checks(L):
     assert nat.forward_ws_raw(*args, p, ws, need) == nat.GDN_ERR_CUDA
     # off the chunked path the workspace is not needed
     assert nat.forward_ws_raw(*args, w.params(path=PATH_SCAN), 0, 0) == nat.GDN_ERR_CUDA
-    # the automatic choice at 100 tokens is the chunked form, which needs it
-    assert nat.forward_ws_raw(*args, w.params(), 0, need) == nat.GDN_ERR_INVALID_ARGUMENT
+    # the automatic choice at 100 tokens is the one-pass chunked form (the faster below 512
+    # tokens), which needs none; from 512 tokens on it is the two-pass form, which needs it
+    assert nat.forward_ws_raw(*args, w.params(), 0, 0) == nat.GDN_ERR_CUDA
+    w6 = w.with_(n_tokens=600)
+    f6 = Fake(w6)
+    args6 = [f6.addr[n] for n in ("q", "k", "v", "g", "beta", "state_in", "output", "state_out")]
+    need6 = nat.gdn_workspace_size(w6.params())
+    assert need6 == nat.gdn_workspace_size(w6.params(path=PATH_CHUNKED)) > 0
+    assert nat.forward_ws_raw(*args6, w6.params(), 0, need6) == nat.GDN_ERR_INVALID_ARGUMENT
+    assert nat.forward_ws_raw(*args6, w6.params(), 10 * GAP, need6) == nat.GDN_ERR_CUDA
 
 
 @no_device

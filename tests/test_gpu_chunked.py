@@ -170,19 +170,22 @@ def test_long_prefill_growing_state(torch, oracle_mod, split, gate):
     check("state_out", gs, rs, w.n_tokens, PATH_CHUNKED, tol)
 
 
-def test_auto_is_the_split_chunked_form(torch):
+@pytest.mark.parametrize("n_tokens", [200, 600])
+def test_auto_is_the_split_chunked_form(torch, n_tokens):
     """A long D = 128 window under the automatic choice runs the split-bf16
-    chunked form: one pass through gdn_forward, two through gdn_forward_ws,
-    bit for bit the results of forcing path bits 2."""
+    chunked form, bit for bit the results of forcing path bits 2: one pass
+    through gdn_forward, and through gdn_forward_ws one pass below 512 tokens
+    (where it is the faster form) and two from 512 tokens on."""
     from serving_gdn_decode_gb300 import _native as nat
-    w = Workload("auto", 128, 128, 2, 6, 200, 2)
+    w = Workload("auto", 128, 128, 2, 6, n_tokens, 2)
     x = make_inputs(w, 69)
     assert nat.gdn_path_name(w.params()) == "chunked"
-    for ws in (False, True):
+    one = run_gpu(w, x, w.params(path=PATH_CHUNKED), workspace=False)
+    two = run_gpu(w, x, w.params(path=PATH_CHUNKED), workspace=True)
+    for ws, want in ((False, one), (True, two if n_tokens >= 512 else one)):
         a = run_gpu(w, x, w.params(), workspace=ws)
-        b = run_gpu(w, x, w.params(path=PATH_CHUNKED), workspace=ws)
-        np.testing.assert_array_equal(a[0], b[0])
-        np.testing.assert_array_equal(a[1], b[1])
+        np.testing.assert_array_equal(a[0], want[0])
+        np.testing.assert_array_equal(a[1], want[1])
 
 
 def test_two_pass_chaining_and_workspace_reuse(torch):
