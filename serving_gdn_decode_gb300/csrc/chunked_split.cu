@@ -8,13 +8,15 @@
 // in the 128-byte-swizzled layout the MMA reads (exactly its shared-memory
 // stack), stores K^T as a canonical image, and forms the Gram products K K^T
 // and Q K^T once; then, for each value head that reads the key head, that
-// head's gates give A, T = (I + A)^-1, T'' = T diag(beta) and
+// head's gates give A, T = (I + A)^-1 (chunked_common.cuh), T'' = T diag(beta) and
 // P' = q_scale (Q K^T o Gam)_{i<=r}, stored as canonical images.  The state
 // pass loads every operand ready-made and converts nothing but its own TMEM
 // products.
 //
-// Pass 2, one CTA per (seq, value head), runs the state-dependent chain per
-// chunk with the state in TMEM as S = c * S~ (c a lazy scalar): [X | Z] =
+// Pass 2, one CTA per segment of a (seq, value head) chain (with more chains
+// than SMs the chains are cut into segments run by consecutive launches,
+// which hand the state on through state_out), runs the state-dependent chain
+// per chunk with the state in TMEM as S = c * S~ (c a lazy scalar): [X | Z] =
 // S~ [K; Q]^T, W = V^T - X diag(c gamma), U^T = W T''^T, Y^T = Z diag(c
 // q_scale gamma) + U^T P'^T, S~ += U~^T K^T.  Its loads are bulk copies
 // (images) and one TMA box per chunk (V rows), each on its own mbarrier.
@@ -564,7 +566,6 @@ constexpr uint32_t P2_MISC = P2_SC + Q_NSC * 64 * 4;
 constexpr uint32_t P2_SMEM = P2_MISC + 128 + 1024;  // + room to align the base to 1024
 static_assert(P2_SMEM <= 232448, "pass-2 shared memory");
 constexpr uint32_t kImgBytes = 16384;   // one 64 x 64 workspace image
-constexpr uint32_t kRowsBytes = 32768;  // 64 rows of 128 floats
 
 struct StateArgs {
   const float *__restrict__ g;
