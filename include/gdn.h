@@ -125,7 +125,8 @@ typedef enum gdn_status {
  *     the chunked path forced for a shape it does not cover.
  *
  * Path choice (params[6] bits 2-3).  GDN_PATH_AUTO runs the token-loop
- * kernel for n_tokens <= 16; for longer windows it runs the tensor-core
+ * kernel for n_tokens <= 16 and for every capture call; for longer windows
+ * without capture it runs the tensor-core
  * chunked form when that form covers the call (D_k = D_v = 128, f32
  * activations, no capture, v 16-byte aligned) and n_tokens >= 48, and the
  * token-by-token FP32 scan otherwise.  GDN_PATH_SCAN forces the scan;

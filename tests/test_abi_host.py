@@ -80,7 +80,8 @@ def test_path_choice(L):
     # the automatic choice takes the chunked form from 48 tokens on, where it covers the shape
     assert _path(WORKLOADS["decode"].with_(n_tokens=47).params()) == "scan"
     assert _path(WORKLOADS["decode"].with_(n_tokens=48).params()) == "chunked"
-    assert _path(WORKLOADS["long_prefill"].params(), True) == "scan_capture"
+    # every capture window takes the token loop under the automatic choice
+    assert _path(WORKLOADS["long_prefill"].params(), True) == "token_loop_decode_capture"
     assert _path(pack_params(64, 64, 2, 4, 4096, 1)) == "scan"
     assert _path(pack_params(128, 64, 2, 4, 4096, 1)) == "scan"
 
