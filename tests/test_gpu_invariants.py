@@ -183,6 +183,8 @@ RAGGED = [
     (128, 128, 16, 32, 37, 2, PATH_SCAN),   # 3 token chunks, partial last one
     (64, 70, 2, 4, 100, 1, PATH_SCAN),
     (128, 64, 1, 2, 17, 2, 0),      # auto path just past the decode window
+    (128, 128, 2, 4, 100, 2, 0),    # auto: chunked, or the token loop with capture
+    (64, 64, 2, 4, 60, 1, 0),       # auto: the scan, or the token loop with capture
 ]
 
 
